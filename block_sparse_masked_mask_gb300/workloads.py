@@ -1,0 +1,211 @@
+"""Seeded synthetic inputs for the structured-mask attention forward.
+
+This module only *generates data*: sequence lengths, per-token segment / role /
+turn metadata and random Q, K, V.  It holds none of the method's arithmetic
+(no predicate, no softmax, no tiling), so both the CUDA path and the fp64
+oracle can be fed from it without sharing any code that computes a result.
+
+The five workloads follow the shapes the block-mask pages describe:
+
+* ``causal_s64_d32_fp32`` - one causal sequence, S=64, H=1, D=32, fp32
+  ("Triton from first principles" Ch. 21, Section 21.2, which checks causal
+  flash attention at toy sizes).
+* ``varlen_causal_8seq`` - eight packed sequences of seeded lengths in
+  [128, 2048], causal inside each, nothing across (the cu_seqlens packing of
+  the xorl issue "Block-mask attention: shared-prefix and strip-thinking",
+  Summary).
+* ``shared_prefix_2048_16x512`` - a 2048-token prefix (segment 0) and sixteen
+  512-token suffixes (segments 1..16) (same issue, Mask specifications,
+  "Shared prefix").
+* ``strip_thinking_8turns`` - eight turns of user 128 / think 768 / answer
+  256 tokens, roles USER=0, THINK=1, ANSWER=2, turns numbered from 1 (same
+  issue, "Strip-thinking multi-turn").
+* ``causal_document_32k`` - 32768 tokens cut into twelve documents of seeded
+  lengths (each at least 512), causal inside a document and block-diagonal
+  across (the issue's "Move document boundaries into the mask" decision).
+
+Generation recipe (per workload number ``c`` = 1..5): a CPU
+``torch.Generator`` seeded with ``c``; metadata lengths are drawn first, then
+Q, K and V, each ``torch.randn((T, H, D)) * sigma`` in fp32, then cast to the
+workload dtype.  The inputs are synthetic stand-ins: the pages measure on
+private training data that is not reproduced here.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+ROLE_USER = 0
+ROLE_THINK = 1
+ROLE_ANSWER = 2
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    kind: str                      # "causal" | "causal_document" | "shared_prefix" | "strip_thinking"
+    cu_seqlens: np.ndarray         # int32 [B+1]
+    num_heads: int
+    head_dim: int
+    dtype: torch.dtype
+    sigma: float = 1.0
+    seg: Optional[np.ndarray] = None    # int32 [T]
+    role: Optional[np.ndarray] = None   # int8  [T]
+    turn: Optional[np.ndarray] = None   # int32 [T]
+    role_think: int = ROLE_THINK
+    seed: int = 0
+    q: Optional[torch.Tensor] = None    # [T, H, D] on CPU, workload dtype
+    k: Optional[torch.Tensor] = None
+    v: Optional[torch.Tensor] = None
+
+    @property
+    def total_tokens(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens) - 1
+
+    @property
+    def max_seqlen(self) -> int:
+        lens = np.diff(self.cu_seqlens)
+        return int(lens.max()) if len(lens) else 0
+
+    @property
+    def seqlens(self) -> list:
+        return [int(x) for x in np.diff(self.cu_seqlens)]
+
+    def meta(self) -> dict:
+        return {"seg": self.seg, "role": self.role, "turn": self.turn,
+                "role_think": self.role_think}
+
+
+WORKLOAD_NAMES = {
+    1: "causal_s64_d32_fp32",
+    2: "varlen_causal_8seq",
+    3: "shared_prefix_2048_16x512",
+    4: "strip_thinking_8turns",
+    5: "causal_document_32k",
+}
+
+
+def _cu(lengths) -> np.ndarray:
+    return np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int32)
+
+
+def _randn(g: torch.Generator, T: int, H: int, D: int, sigma: float, dtype: torch.dtype) -> torch.Tensor:
+    x = torch.randn((T, H, D), generator=g, dtype=torch.float32)
+    if sigma != 1.0:
+        x = x * sigma
+    return x.to(dtype)
+
+
+def _fill_tensors(w: Workload, g: torch.Generator) -> None:
+    T, H, D = w.total_tokens, w.num_heads, w.head_dim
+    w.q = _randn(g, T, H, D, w.sigma, w.dtype)
+    w.k = _randn(g, T, H, D, w.sigma, w.dtype)
+    w.v = _randn(g, T, H, D, w.sigma, w.dtype)
+
+
+def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> Workload:
+    """Workload number ``c`` (1..5).
+
+    ``document_form`` only matters for workload 5: ``"mask"`` is one packed
+    sequence with the document index in ``seg`` and kind causal_document;
+    ``"cu_seqlens"`` is the same tokens as twelve sequences under plain causal.
+    Both describe the same set of visible (query, key) pairs.
+    """
+    g = torch.Generator().manual_seed(c)
+    if c == 1:
+        w = Workload(WORKLOAD_NAMES[1], "causal", _cu([64]), 1, 32, torch.float32, seed=c)
+    elif c == 2:
+        lens = torch.randint(128, 2049, (8,), generator=g).tolist()
+        w = Workload(WORKLOAD_NAMES[2], "causal", _cu(lens), 16, 128, torch.bfloat16, seed=c)
+    elif c == 3:
+        seg = np.concatenate([np.zeros(2048, np.int32)] +
+                             [np.full(512, i, np.int32) for i in range(1, 17)])
+        w = Workload(WORKLOAD_NAMES[3], "shared_prefix", _cu([len(seg)]), 32, 128,
+                     torch.bfloat16, seg=seg, seed=c)
+    elif c == 4:
+        role, turn = strip_thinking_layout([(128, 768, 256)] * 8)
+        w = Workload(WORKLOAD_NAMES[4], "strip_thinking", _cu([len(role)]), 32, 128,
+                     torch.bfloat16, sigma=0.5, role=role, turn=turn, seed=c)
+    elif c == 5:
+        cuts = torch.randint(0, 26625, (11,), generator=g).sort().values.tolist()
+        bounds = [0] + cuts + [26624]
+        lens = [bounds[i + 1] - bounds[i] + 512 for i in range(12)]
+        if document_form == "mask":
+            seg = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lens)])
+            w = Workload(WORKLOAD_NAMES[5], "causal_document", _cu([sum(lens)]), 32, 128,
+                         torch.bfloat16, seg=seg, seed=c)
+        elif document_form == "cu_seqlens":
+            w = Workload(WORKLOAD_NAMES[5] + "_cu_seqlens", "causal", _cu(lens), 32, 128,
+                         torch.bfloat16, seed=c)
+        else:
+            raise ValueError(document_form)
+    else:
+        raise ValueError(f"workload number must be 1..5, got {c}")
+    if tensors:
+        _fill_tensors(w, g)
+    return w
+
+
+def strip_thinking_layout(turns):
+    """Role and turn arrays for turns given as (user, think, answer) lengths."""
+    role, turn = [], []
+    for t, (nu, nt, na) in enumerate(turns, start=1):
+        role += [ROLE_USER] * nu + [ROLE_THINK] * nt + [ROLE_ANSWER] * na
+        turn += [t] * (nu + nt + na)
+    return np.asarray(role, np.int8), np.asarray(turn, np.int32)
+
+
+def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: int = ROLE_THINK):
+    """Random per-token metadata for ``kind`` over packed sequences ``lengths``.
+
+    Segment ids are runs (documents / prefix-suffix segments) of random length;
+    roles and turns are random runs too, so tile boundaries cut through runs.
+    """
+    T = int(sum(lengths))
+    seg = role = turn = None
+    if kind in ("causal_document", "shared_prefix"):
+        seg = np.empty(T, np.int32)
+        pos = 0
+        for L in lengths:
+            s, cur = 0, 0
+            while s < L:
+                n = int(rng.integers(1, max(2, L // 2 + 2)))
+                seg[pos + s: pos + min(L, s + n)] = cur
+                s += n
+                cur += 1
+            pos += L
+    if kind == "strip_thinking":
+        role = np.empty(T, np.int8)
+        turn = np.empty(T, np.int32)
+        pos = 0
+        for L in lengths:
+            s, t = 0, 1
+            while s < L:
+                for r in (ROLE_USER, role_think, ROLE_ANSWER):
+                    n = int(rng.integers(1, 200))
+                    role[pos + s: pos + min(L, s + n)] = r
+                    turn[pos + s: pos + min(L, s + n)] = t
+                    s += n
+                    if s >= L:
+                        break
+                t += 1
+            pos += L
+    return seg, role, turn
+
+
+def random_workload(seed: int, kind: str, lengths, num_heads: int, head_dim: int,
+                    dtype: torch.dtype = torch.bfloat16, sigma: float = 1.0) -> Workload:
+    """A small seeded case for parity tests (ragged lengths, any kind)."""
+    rng = np.random.default_rng(seed)
+    seg, role, turn = random_metadata(rng, kind, lengths)
+    w = Workload(f"random_{kind}_{seed}", kind, _cu(lengths), num_heads, head_dim, dtype,
+                 sigma=sigma, seg=seg, role=role, turn=turn, seed=seed)
+    _fill_tensors(w, torch.Generator().manual_seed(10_000 + seed))
+    return w

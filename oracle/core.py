@@ -1,0 +1,262 @@
+"""Plain fp64 CPU oracle for the structured-mask attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this module:
+only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
+It shares no code with the CUDA library (no kernels, headers, helpers or
+constant tables); the two only meet on the seeded inputs.
+
+What it computes, step by step and in the pages' terms:
+
+1. For each packed sequence (cu_seqlens, the xorl issue "Block-mask attention:
+   shared-prefix and strip-thinking", Summary) it materialises the boolean mask
+   M[i, j] by evaluating the mask predicate literally on every (query, key)
+   pair of that sequence.  Pairs from different sequences are never visible.
+2. For each head it forms the scaled scores s = (q . k) / sqrt(d) in fp64,
+   drops masked entries (they get zero weight, the same as exp(-inf)), and
+   takes the three-pass softmax: m = max s, l = sum exp(s - m), LSE = m + ln l,
+   O = sum exp(s - m) v / l  ("Triton from first principles" Ch. 21,
+   Section 21.1, the naive softmax(QK^T/sqrt(d))V the kernel is checked
+   against).  A row with no visible key gets O = 0 and LSE = -inf.
+3. Tile labels by brute force: count the visible in-bounds pairs of every
+   128x128 (q-tile, k-tile) block of M; EMPTY if none, FULL if all, PARTIAL
+   otherwise ("Triton from first principles" Ch. 21, Section 21.2 diagram:
+   all-valid / diagonal / skipped tiles).  Lists are in ascending k order.
+
+Readings of points the pages leave open (each is listed in the design notes):
+* the diagonal is visible under every kind (``j <= i``, Ch. 9, Section 9.1);
+* LSE is the natural log of the sum of exp of the *scaled* scores;
+* roles are USER=0, THINK=1, ANSWER=2 with the THINK code a parameter;
+* a ragged tail tile is labelled from its in-bounds pairs only;
+* tile grids restart at every sequence's first token.
+
+Every input array is widened to fp64 before use; bf16 and fp32 widen exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+KINDS = ("causal", "causal_document", "shared_prefix", "strip_thinking")
+
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+# ----------------------------------------------------------------------------
+# Mask predicates.  qi / ki are global packed token indices of one sequence,
+# so ``qi >= ki`` is the same test as comparing positions inside the sequence.
+# ----------------------------------------------------------------------------
+
+def predicate(kind: str, qi, ki, seg=None, role=None, turn=None, role_think: int = 1):
+    """Visibility of key ``ki`` to query ``qi`` (broadcasting integer arrays).
+
+    * causal          : key at or before the query, diagonal included
+                        ("Triton from first principles" Ch. 9, Section 9.1,
+                        Worked Example 9.1.1: ``cols <= rows``).
+    * causal_document : causal and the same document id (the xorl issue,
+                        "Decisions this settles", item 4: document boundaries
+                        move into the mask).
+    * shared_prefix   : ``(qi >= ki) & ((seg[ki] == 0) | (seg[ki] == seg[qi]))``
+                        (the xorl issue, Mask specifications, "Shared prefix").
+    * strip_thinking  : ``(qi >= ki) & ~((role[ki] == THINK) & (turn[ki] < turn[qi]))``
+                        (the xorl issue, Mask specifications, "Strip-thinking").
+    """
+    qi = np.asarray(qi)
+    ki = np.asarray(ki)
+    causal = qi >= ki
+    if kind == "causal":
+        return causal
+    if kind == "causal_document":
+        return causal & (seg[ki] == seg[qi])
+    if kind == "shared_prefix":
+        return causal & ((seg[ki] == 0) | (seg[ki] == seg[qi]))
+    if kind == "strip_thinking":
+        return causal & ~((role[ki] == role_think) & (turn[ki] < turn[qi]))
+    raise ValueError(f"unknown mask kind {kind!r}")
+
+
+def sequence_mask(kind: str, cu_seqlens, b: int, meta: dict, row_lo: int = 0, row_hi=None,
+                  rows=None):
+    """Rows of sequence ``b``'s full boolean mask, shape [rows, L].
+
+    With the default arguments this is the whole L x L mask.  ``row_lo`` /
+    ``row_hi`` (a range) or ``rows`` (explicit local row indices) only bound
+    memory for long sequences; every entry is the same literal predicate.
+    """
+    start, end = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+    L = end - start
+    if rows is None:
+        if row_hi is None:
+            row_hi = L
+        rows = np.arange(row_lo, row_hi)
+    qi = (start + np.asarray(rows, np.int64))[:, None]
+    ki = np.arange(start, end)[None, :]
+    meta = meta or {}
+    return predicate(kind, qi, ki, meta.get("seg"), meta.get("role"), meta.get("turn"),
+                     meta.get("role_think", 1))
+
+
+# ----------------------------------------------------------------------------
+# Attention by the definition.
+# ----------------------------------------------------------------------------
+
+def masked_attention(q, k, v, mask, scale):
+    """softmax(q k^T * scale, masked) v for one sequence and one head, in fp64.
+
+    q: [M, D], k: [N, D], v: [N, D], mask: bool [M, N].  Returns O [M, D] and
+    LSE [M] (natural log).  Three passes: row max, sum of exponentials, then
+    the normalised weighted sum ("Triton from first principles" Ch. 21,
+    Section 21.1, the naive reference).  Masked entries carry zero weight.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    mask = np.asarray(mask, bool)
+    s = (q @ k.T) * float(scale)
+    s = np.where(mask, s, -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    has_key = np.isfinite(m)
+    m_safe = np.where(has_key, m, 0.0)
+    e = np.where(mask, np.exp(s - m_safe[:, None]), 0.0)
+    l = e.sum(axis=1)
+    o = np.zeros((q.shape[0], v.shape[1]), np.float64)
+    o[has_key] = (e[has_key] @ v) / l[has_key, None]
+    lse = np.full(q.shape[0], -np.inf)
+    lse[has_key] = m[has_key] + np.log(l[has_key])
+    return o, lse
+
+
+def _as_f64(x):
+    """Widen a torch tensor or array to a float64 numpy array (exact for bf16/fp32)."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu()
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        x = x.double().numpy()
+    return np.asarray(x, np.float64)
+
+
+def attention(q, k, v, kind: str, cu_seqlens, meta=None, scale=None, heads=None,
+              rows=None, row_block: int = 512):
+    """O [T, H, D] and LSE [H, T] of the masked attention forward, fp64.
+
+    q, k, v: [T, H, D] (numpy or torch, any float dtype).  ``heads`` selects
+    heads (default all); ``rows`` optionally restricts the computed query rows
+    to a list of global token indices (the others stay NaN), which is how the
+    full-size parity tests sample outputs one by one.
+    """
+    T, H, D = q.shape
+    cu = np.asarray(cu_seqlens, np.int64)
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(D)
+    heads = range(H) if heads is None else heads
+    O = np.full((T, H, D), np.nan)
+    LSE = np.full((H, T), np.nan)
+    row_set = None if rows is None else np.unique(np.asarray(rows, np.int64))
+    for b in range(len(cu) - 1):
+        start, end = int(cu[b]), int(cu[b + 1])
+        L = end - start
+        if L == 0:
+            continue
+        if row_set is None:
+            local_rows = np.arange(L)
+        else:
+            sel = row_set[(row_set >= start) & (row_set < end)]
+            if len(sel) == 0:
+                continue
+            local_rows = sel - start
+        for c0 in range(0, len(local_rows), row_block):
+            lr = local_rows[c0:c0 + row_block]
+            mask = sequence_mask(kind, cu, b, meta, rows=lr)
+            for h in heads:
+                o, lse = masked_attention(_as_f64(q[start + lr, h]), _as_f64(k[start:end, h]),
+                                          _as_f64(v[start:end, h]), mask, scale)
+                O[start + lr, h] = o
+                LSE[h, start + lr] = lse
+    return O, LSE
+
+
+def unmasked_pairs(kind: str, cu_seqlens, meta=None, row_block: int = 1024) -> int:
+    """Number of visible (query, key) pairs per head: the nnz that the
+    effective-FLOP count 4*D*H*nnz is built on."""
+    cu = np.asarray(cu_seqlens, np.int64)
+    total = 0
+    for b in range(len(cu) - 1):
+        L = int(cu[b + 1] - cu[b])
+        for r0 in range(0, L, row_block):
+            total += int(sequence_mask(kind, cu, b, meta, r0, min(L, r0 + row_block)).sum())
+    return total
+
+
+# ----------------------------------------------------------------------------
+# Tile labels and per-q-tile lists by brute-force counting.
+# ----------------------------------------------------------------------------
+
+def tile_labels(kind: str, cu_seqlens, meta=None, block_m: int = 128, block_n: int = 128):
+    """Per sequence, a uint8 matrix [n_q_tiles, n_k_tiles] of EMPTY/PARTIAL/FULL.
+
+    Each label comes from counting the visible pairs of the tile's in-bounds
+    part of the materialised mask: 0 -> EMPTY, all -> FULL, else PARTIAL.
+    """
+    cu = np.asarray(cu_seqlens, np.int64)
+    out = []
+    for b in range(len(cu) - 1):
+        L = int(cu[b + 1] - cu[b])
+        nq = -(-L // block_m)
+        nk = -(-L // block_n)
+        lab = np.zeros((nq, nk), np.uint8)
+        for a in range(nq):
+            r0, r1 = a * block_m, min(L, (a + 1) * block_m)
+            rows = sequence_mask(kind, cu, b, meta, r0, r1)
+            padded = np.zeros((r1 - r0, nk * block_n), bool)
+            padded[:, :L] = rows
+            counts = padded.reshape(r1 - r0, nk, block_n).sum(axis=(0, 2))
+            kn = np.minimum(block_n, L - np.arange(nk) * block_n)
+            inb = (r1 - r0) * kn
+            lab[a] = np.where(counts == 0, EMPTY, np.where(counts == inb, FULL, PARTIAL))
+        out.append(lab)
+    return out
+
+
+def block_lists(labels):
+    """Per-q-tile compacted lists from per-sequence label matrices.
+
+    q-tiles are numbered sequence-major (sequence 0's tiles first, each in
+    ascending order).  Returns a dict with numpy arrays: ``qt_seq``,
+    ``qt_idx`` (q-tile index inside its sequence), ``kcount``, ``koff``
+    (CSR offsets, length n+1), ``kidx`` (ascending k-tile indices) and
+    ``klabel`` (PARTIAL or FULL per list entry).
+    """
+    qt_seq, qt_idx, kcount, kidx, klabel = [], [], [], [], []
+    for b, lab in enumerate(labels):
+        for a in range(lab.shape[0]):
+            nz = np.nonzero(lab[a] != EMPTY)[0]
+            qt_seq.append(b)
+            qt_idx.append(a)
+            kcount.append(len(nz))
+            kidx.extend(nz.tolist())
+            klabel.extend(lab[a, nz].tolist())
+    kcount = np.asarray(kcount, np.int64)
+    return {
+        "qt_seq": np.asarray(qt_seq, np.int64),
+        "qt_idx": np.asarray(qt_idx, np.int64),
+        "kcount": kcount,
+        "koff": np.concatenate([[0], np.cumsum(kcount)]).astype(np.int64),
+        "kidx": np.asarray(kidx, np.int64),
+        "klabel": np.asarray(klabel, np.uint8),
+    }
+
+
+def lpt_order(kcount):
+    """q-tiles by descending work (list length), ties by ascending tile number:
+    the longest-processing-time-first order a one-launch varlen scheduler uses
+    ("Triton from first principles" Ch. 9, Section 9.3: one launch covers the
+    whole ragged batch)."""
+    kcount = np.asarray(kcount, np.int64)
+    return np.lexsort((np.arange(len(kcount)), -kcount)).astype(np.int64)
+
+
+def label_totals(labels):
+    """(FULL, PARTIAL, EMPTY) counts over all sequences."""
+    f = sum(int((l == FULL).sum()) for l in labels)
+    p = sum(int((l == PARTIAL).sum()) for l in labels)
+    e = sum(int((l == EMPTY).sum()) for l in labels)
+    return f, p, e

@@ -1,0 +1,428 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here calls the CUDA path.  Each test names the passage it checks.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import core as oa
+from block_sparse_masked_mask_gb300 import workloads as W
+
+from conftest import GOLDEN
+
+
+def _read_blocks(name):
+    blocks, cur = {}, None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            toks = line.split()
+            if len(toks) == 1 and not toks[0].lstrip("-").replace(".", "").isdigit():
+                cur = toks[0]
+                blocks[cur] = []
+            else:
+                blocks[cur].append(toks)
+    return blocks
+
+
+def _causal_mask(L):
+    return oracle.sequence_mask("causal", np.array([0, L]), 0, {})
+
+
+# ----------------------------------------------------------------------------
+# Causal predicate: Ch. 9, Section 9.1, Worked Examples 9.1.1 and 9.1.2.
+# ----------------------------------------------------------------------------
+
+def test_causal_4x4_matches_page_table():
+    g = _read_blocks("causal_4x4.txt")
+    x = np.array(g["input"], dtype=float)
+    want = np.array(g["causal_masked"], dtype=float)
+    got = np.where(_causal_mask(4), x, 0.0)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got, np.tril(x))
+
+
+def test_strict_lt_trap_is_not_the_oracle():
+    g = _read_blocks("strict_lt_4x4.txt")
+    strict = np.array(g["strict_masked"], dtype=float)
+    x = np.arange(1, 17, dtype=float).reshape(4, 4)
+    got = np.where(_causal_mask(4), x, 0.0)
+    assert not np.array_equal(got, strict)
+    # the page's trap table is exactly the oracle's table minus the diagonal
+    assert np.array_equal(got - np.diag(np.diag(x)), strict)
+
+
+# ----------------------------------------------------------------------------
+# Whole-oracle pin against a printed value: Ch. 21, Worked Example 21.2.2.
+# ----------------------------------------------------------------------------
+
+def _wrong_task_inputs():
+    torch.manual_seed(0)
+    q = torch.randn(20, 8)
+    k = torch.randn(20, 8)
+    v = torch.randn(20, 8)
+    return q.double().numpy(), k.double().numpy(), v.double().numpy()
+
+
+def test_wrong_task_max_diff_matches_page():
+    vals = {}
+    with open(os.path.join(GOLDEN, "wrong_task.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            a, b = line.split()
+            vals[a] = b
+    want = float(vals["max_abs_diff_causal_vs_noncausal"])
+    q, k, v = _wrong_task_inputs()
+    scale = 1.0 / math.sqrt(8)
+    oc, _ = oracle.masked_attention(q, k, v, _causal_mask(20), scale)
+    on, _ = oracle.masked_attention(q, k, v, np.ones((20, 20), bool), scale)
+    diff = np.abs(oc - on).max()
+    # the page computed in fp32; fp64 differs from it by rounding only
+    assert abs(diff - want) < 1e-6, diff
+
+
+# ----------------------------------------------------------------------------
+# Closed forms and special cases.
+# ----------------------------------------------------------------------------
+
+def test_causal_row0_is_v0_and_lse_is_s00():
+    rng = np.random.default_rng(3)
+    q, k, v = (rng.standard_normal((37, 16)) for _ in range(3))
+    scale = 0.25
+    o, lse = oracle.masked_attention(q, k, v, _causal_mask(37), scale)
+    assert np.array_equal(o[0], v[0])
+    assert lse[0] == (q[0] @ k[0]) * scale
+
+
+def test_fully_masked_row_gives_zero_and_minus_inf():
+    rng = np.random.default_rng(4)
+    q, k, v = (rng.standard_normal((5, 8)) for _ in range(3))
+    mask = np.ones((5, 5), bool)
+    mask[2] = False
+    o, lse = oracle.masked_attention(q, k, v, mask, 0.3)
+    assert np.all(o[2] == 0) and lse[2] == -np.inf
+    assert np.all(np.isfinite(o[[0, 1, 3, 4]]))
+
+
+def test_single_key_visible_everywhere_returns_that_value():
+    # softmax over one element is 1 whatever the score
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((6, 4)) for _ in range(3))
+    mask = np.zeros((6, 6), bool)
+    mask[:, 3] = True
+    o, lse = oracle.masked_attention(q, k, v, mask, 1.7)
+    assert np.array_equal(o, np.repeat(v[3:4], 6, axis=0))
+    assert np.allclose(lse, (q @ k[3]) * 1.7, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("kind", oracle.KINDS)
+def test_matches_torch_sdpa_fp64(kind):
+    """The softmax step reduces to a library routine: torch's fp64 SDPA with a
+    boolean mask, and logsumexp for LSE."""
+    rng = np.random.default_rng(11)
+    lens = [70, 1, 33, 150]
+    seg, role, turn = W.random_metadata(rng, kind, lens)
+    cu = W._cu(lens)
+    meta = {"seg": seg, "role": role, "turn": turn, "role_think": 1}
+    T, H, D = sum(lens), 3, 24
+    q, k, v = (torch.randn(T, H, D, dtype=torch.float64) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, kind, cu, meta)
+    scale = 1 / math.sqrt(D)
+    for b in range(len(lens)):
+        s0, s1 = cu[b], cu[b + 1]
+        mask = torch.from_numpy(oracle.sequence_mask(kind, cu, b, meta))
+        for h in range(H):
+            qh, kh, vh = q[s0:s1, h], k[s0:s1, h], v[s0:s1, h]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qh[None], kh[None], vh[None], attn_mask=mask[None], scale=scale)[0]
+            assert np.abs(O[s0:s1, h] - ref.numpy()).max() < 1e-12
+            sc = (qh @ kh.T * scale).masked_fill(~mask, -math.inf)
+            assert np.abs(LSE[h, s0:s1] - torch.logsumexp(sc, -1).numpy()).max() < 1e-12
+
+
+def test_online_softmax_equals_three_pass():
+    """The tiled online update of Ch. 21, Section 21.1 (running max m, running
+    sum l, accumulator rescaled by alpha = exp(m_old - m_new), final acc / l),
+    restated here in fp64, equals the oracle's three-pass definition for every
+    tile width: the tile size is a performance knob, never a correctness one."""
+    rng = np.random.default_rng(7)
+    M, N, D = 17, 23, 8
+    q, k, v = rng.standard_normal((M, D)), rng.standard_normal((N, D)), rng.standard_normal((N, D))
+    mask = rng.random((M, N)) < 0.6
+    mask[:, 0] = True
+    scale = 1 / math.sqrt(D)
+    want_o, want_lse = oracle.masked_attention(q, k, v, mask, scale)
+    for bn in (1, 3, 4, 64, 128):
+        m = np.full(M, -np.inf)
+        l = np.zeros(M)
+        acc = np.zeros((M, D))
+        for n0 in range(0, N, bn):
+            s = (q @ k[n0:n0 + bn].T) * scale
+            s = np.where(mask[:, n0:n0 + bn], s, -np.inf)
+            m_new = np.maximum(m, s.max(axis=1))
+            m_safe = np.where(np.isfinite(m_new), m_new, 0.0)
+            alpha = np.exp(m - m_safe)
+            p = np.exp(s - m_safe[:, None])
+            l = alpha * l + p.sum(axis=1)
+            acc = alpha[:, None] * acc + p @ v[n0:n0 + bn]
+            m = m_new
+        assert np.abs(acc / l[:, None] - want_o).max() < 1e-12
+        assert np.abs(m + np.log(l) - want_lse).max() < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# Structured masks equal the separate computations they replace.
+# ----------------------------------------------------------------------------
+
+def test_shared_prefix_equals_separate_runs():
+    """xorl issue, "Shared prefix": each suffix attends prefix + own suffix, which
+    must equal running causal attention on P || S_i alone, and the prefix rows
+    must equal causal attention over P alone."""
+    rng = np.random.default_rng(21)
+    P, sufs = 37, [20, 33, 9]
+    seg = np.concatenate([np.zeros(P, np.int32)] + [np.full(n, i + 1, np.int32) for i, n in enumerate(sufs)])
+    T, H, D = len(seg), 2, 16
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, "shared_prefix", np.array([0, T]), {"seg": seg})
+    Op, Lp = oracle.attention(q[:P], k[:P], v[:P], "causal", np.array([0, P]))
+    assert np.abs(O[:P] - Op).max() < 1e-12 and np.abs(LSE[:, :P] - Lp).max() < 1e-12
+    pos = P
+    for n in sufs:
+        idx = np.r_[0:P, pos:pos + n]
+        Oi, Li = oracle.attention(q[idx], k[idx], v[idx], "causal", np.array([0, P + n]))
+        assert np.abs(O[pos:pos + n] - Oi[P:]).max() < 1e-12
+        assert np.abs(LSE[:, pos:pos + n] - Li[:, P:]).max() < 1e-12
+        pos += n
+
+
+def test_strip_thinking_equals_per_turn_recomputation():
+    """xorl issue, "Strip-thinking multi-turn": turn t sees earlier turns' user
+    and answer tokens plus all of its own turn; the naive alternative is one
+    causal pass per turn over exactly those tokens."""
+    rng = np.random.default_rng(22)
+    turns = [(5, 9, 4), (3, 11, 6), (7, 2, 5), (4, 6, 3)]
+    role, turn = W.strip_thinking_layout(turns)
+    T, H, D = len(role), 2, 8
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, "strip_thinking", np.array([0, T]),
+                              {"role": role, "turn": turn, "role_think": W.ROLE_THINK})
+    for t in range(1, len(turns) + 1):
+        keep = np.nonzero((turn < t) & (role != W.ROLE_THINK) | (turn == t))[0]
+        Ot, Lt = oracle.attention(q[keep], k[keep], v[keep], "causal", np.array([0, len(keep)]))
+        rows = np.nonzero(turn[keep] == t)[0]
+        assert np.abs(O[keep[rows]] - Ot[rows]).max() < 1e-12
+        assert np.abs(LSE[:, keep[rows]] - Lt[:, rows]).max() < 1e-12
+
+
+def test_varlen_equals_independent_sequences():
+    """cu_seqlens packing (xorl issue, Summary): a causal square per sequence and
+    nothing across, i.e. each sequence alone."""
+    rng = np.random.default_rng(23)
+    lens = [13, 1, 40, 7]
+    cu = W._cu(lens)
+    T, H, D = sum(lens), 2, 8
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, "causal", cu)
+    for b, n in enumerate(lens):
+        s = slice(cu[b], cu[b + 1])
+        Ob, Lb = oracle.attention(q[s], k[s], v[s], "causal", np.array([0, n]))
+        assert np.array_equal(O[s], Ob) and np.array_equal(LSE[:, s], Lb)
+
+
+def test_predicate_truth_tables():
+    text = "\n".join(l for l in open(os.path.join(GOLDEN, "predicate_tables.txt"))
+                     .read().splitlines() if not l.startswith("#"))
+    blocks = text.split("table ")[1:]
+    seen = set()
+    for blk in blocks:
+        lines = [l.split() for l in blk.strip().splitlines() if l.strip() and not l.startswith("#")]
+        kind = lines[0][0]
+        meta, rows = {"role_think": 1}, []
+        for toks in lines[1:]:
+            if toks[0] in ("seg", "turn"):
+                meta[toks[0]] = np.array(toks[1:], np.int32)
+            elif toks[0] == "role":
+                meta["role"] = np.array(toks[1:], np.int8)
+            elif toks[0] == "len":
+                pass
+            else:
+                rows.append([int(x) for x in toks])
+        want = np.array(rows, bool)
+        L = want.shape[0]
+        got = oracle.sequence_mask(kind, np.array([0, L]), 0, meta)
+        assert np.array_equal(got, want), kind
+        seen.add(kind)
+    assert seen == set(oracle.KINDS)
+
+
+# ----------------------------------------------------------------------------
+# Tile labels and counts: closed forms derived from the workload structure.
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 257, 300, 513])
+def test_causal_tile_labels_closed_form(L):
+    lab = oracle.tile_labels("causal", np.array([0, L]))[0]
+    n = -(-L // 128)
+    for a in range(n):
+        for b in range(n):
+            if b > a:
+                want = oracle.EMPTY
+            elif b < a:
+                want = oracle.FULL
+            else:
+                rows = min(128, L - 128 * a)
+                want = oracle.FULL if rows == 1 else oracle.PARTIAL
+            assert lab[a, b] == want
+
+
+def test_shared_prefix_workload_counts_closed_form():
+    w = W.make_workload(3, tensors=False)
+    P, n, s = 2048, 16, 512
+    tp, ts = P // 128, s // 128
+    full = tp * (tp - 1) // 2 + n * (tp * ts + ts * (ts - 1) // 2)
+    partial = tp + n * ts
+    ntiles = (P + n * s) // 128
+    lab = oracle.tile_labels(w.kind, w.cu_seqlens, w.meta())
+    assert oracle.label_totals(lab) == (full, partial, ntiles * ntiles - full - partial)
+    assert (full, partial) == (1240, 80)
+    nnz = P * (P + 1) // 2 + n * (s * P + s * (s + 1) // 2)
+    assert oracle.unmasked_pairs(w.kind, w.cu_seqlens, w.meta()) == nnz == 20_976_640
+
+
+def test_strip_thinking_workload_counts_closed_form():
+    w = W.make_workload(4, tensors=False)
+    nturn, u, th, a = 8, 128, 768, 256
+    per = (u + th + a) // 128                       # 9 tiles per turn
+    own_full = per * (per - 1) // 2                 # strictly-lower tiles of a turn
+    hist_full = per * ((u + a) // 128)              # q-tiles x (user + answer) tiles of an earlier turn
+    full = nturn * own_full + hist_full * sum(range(nturn))
+    partial = nturn * per
+    nt = nturn * per
+    lab = oracle.tile_labels(w.kind, w.cu_seqlens, w.meta())
+    assert oracle.label_totals(lab) == (full, partial, nt * nt - full - partial)
+    assert (full, partial) == (1044, 72)
+    L = u + th + a
+    nnz = nturn * L * (L + 1) // 2 + L * (u + a) * sum(range(nturn))
+    assert oracle.unmasked_pairs(w.kind, w.cu_seqlens, w.meta()) == nnz == 17_699_328
+
+
+def test_varlen_and_document_workload_counts_closed_form():
+    w2 = W.make_workload(2, tensors=False)
+    assert w2.seqlens == [860, 289, 1664, 1816, 272, 1814, 1638, 1843]
+    lab2 = oracle.tile_labels("causal", w2.cu_seqlens)
+    nts = [-(-L // 128) for L in w2.seqlens]
+    ones = sum(1 for L in w2.seqlens if L % 128 == 1)   # a 1x1 diagonal tile is FULL
+    f = sum(n * (n - 1) // 2 for n in nts) + ones
+    p = sum(nts) - ones
+    assert oracle.label_totals(lab2) == (f, p, sum(n * n for n in nts) - f - p) == (498, 84, 498)
+    assert oracle.unmasked_pairs("causal", w2.cu_seqlens) == sum(L * (L + 1) // 2 for L in w2.seqlens)
+
+    w5 = W.make_workload(5, tensors=False, document_form="cu_seqlens")
+    w5d = W.make_workload(5, tensors=False, document_form="mask")
+    nnz = sum(L * (L + 1) // 2 for L in w5.seqlens)
+    assert nnz == 67_979_834
+    assert oracle.unmasked_pairs(w5.kind, w5.cu_seqlens) == nnz
+    assert oracle.unmasked_pairs(w5d.kind, w5d.cu_seqlens, w5d.meta()) == nnz
+    nts = [-(-L // 128) for L in w5.seqlens]
+    f = sum(n * (n - 1) // 2 for n in nts)
+    assert oracle.label_totals(oracle.tile_labels("causal", w5.cu_seqlens)) == (f, sum(nts), f)
+
+
+def test_document_form_labels_match_interval_reasoning():
+    """For documents that are contiguous runs, a global tile pair is EMPTY iff no
+    (q, k) pair is both causal and inside one document; checked by interval
+    arithmetic on the document spans instead of counting the mask."""
+    w = W.make_workload(5, tensors=False)
+    lab = oracle.tile_labels(w.kind, w.cu_seqlens, w.meta())[0]
+    bounds = np.concatenate([[0], np.cumsum(W.make_workload(5, tensors=False,
+                                                           document_form="cu_seqlens").seqlens)])
+    nt = lab.shape[0]
+    for a in range(nt):
+        q0, q1 = 128 * a, 128 * a + 127
+        for b in range(nt):
+            k0, k1 = 128 * b, 128 * b + 127
+            any_vis = False
+            all_vis = True
+            for d in range(len(bounds) - 1):
+                s, e = bounds[d], bounds[d + 1] - 1
+                qa, qb = max(q0, s), min(q1, e)
+                ka, kb = max(k0, s), min(k1, e)
+                if qa <= qb and ka <= kb and ka <= qb:
+                    any_vis = True
+            # FULL iff every q row and k column share one document and k1 <= q0
+            docs_q = set(np.searchsorted(bounds, [q0, q1], side="right"))
+            docs_k = set(np.searchsorted(bounds, [k0, k1], side="right"))
+            all_vis = k1 <= q0 and len(docs_q | docs_k) == 1
+            want = oracle.FULL if all_vis else (oracle.PARTIAL if any_vis else oracle.EMPTY)
+            assert lab[a, b] == want, (a, b)
+
+
+def test_block_lists_and_lpt_order():
+    lab = oracle.tile_labels("causal", np.array([0, 300, 300, 301]))
+    bl = oracle.block_lists(lab)
+    assert bl["qt_seq"].tolist() == [0, 0, 0, 2]
+    assert bl["kcount"].tolist() == [1, 2, 3, 1]
+    assert bl["kidx"].tolist() == [0, 0, 1, 0, 1, 2, 0]
+    assert bl["klabel"].tolist() == [1, 2, 1, 2, 2, 1, 2]
+    assert oracle.lpt_order(bl["kcount"]).tolist() == [2, 1, 0, 3]
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: each plausible slip in the oracle must fail a pin above.
+# ----------------------------------------------------------------------------
+
+def _pins_pass():
+    try:
+        test_causal_4x4_matches_page_table()
+        test_causal_row0_is_v0_and_lse_is_s00()
+        test_predicate_truth_tables()
+        test_shared_prefix_equals_separate_runs()
+        test_strip_thinking_equals_per_turn_recomputation()
+        test_wrong_task_max_diff_matches_page()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_pins_pass_on_the_real_oracle():
+    assert _pins_pass()
+
+
+@pytest.mark.parametrize("mutant", ["strict_diagonal", "prefix_drops_seg0", "think_le_turn",
+                                    "no_scale", "transposed_scores"])
+def test_pins_catch_planted_mistakes(monkeypatch, mutant):
+    real_pred, real_attn = oa.predicate, oa.masked_attention
+
+    def pred(kind, qi, ki, seg=None, role=None, turn=None, role_think=1):
+        qi, ki = np.asarray(qi), np.asarray(ki)
+        if mutant == "strict_diagonal":
+            c = qi > ki
+            return c if kind == "causal" else c & real_pred(kind, qi, ki, seg, role, turn, role_think)
+        if mutant == "prefix_drops_seg0" and kind == "shared_prefix":
+            return (qi >= ki) & (seg[ki] == seg[qi])
+        if mutant == "think_le_turn" and kind == "strip_thinking":
+            return (qi >= ki) & ~((role[ki] == role_think) & (turn[ki] <= turn[qi]))
+        return real_pred(kind, qi, ki, seg, role, turn, role_think)
+
+    def attn(q, k, v, mask, scale):
+        if mutant == "no_scale":
+            return real_attn(q, k, v, mask, 1.0)
+        if mutant == "transposed_scores":
+            q2 = np.asarray(q, float)
+            if q2.shape[0] == np.asarray(k).shape[0]:
+                # scores k q^T instead of q k^T
+                return real_attn(k, q, v, mask, scale)
+        return real_attn(q, k, v, mask, scale)
+
+    monkeypatch.setattr(oa, "predicate", pred)
+    monkeypatch.setattr(oa, "masked_attention", attn)
+    monkeypatch.setattr(oracle, "masked_attention", attn)
+    assert not _pins_pass()
