@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of the structured-mask attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch: build the block
+mask (tile summaries, exact classification, compacted lists, longest-first
+order) and run the attention forward, on inputs already resident in HBM.
+Metric: effective TFLOP/s counting only unmasked score FLOPs, 4*D*H*nnz per
+step (2*D for q.k and 2*D for p.v per visible pair), and its fraction of the
+measured dense bf16 tensor peak.
+
+Default workload: the 32768-token causal+document mask (12 documents, H=32,
+D=128, bf16), the largest configuration.  ``--impl reference`` times the fp64
+CPU oracle on the host cores on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(weak scaling); the forward has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "masked attn fwd TFLOP/s (unmasked FLOPs) & % of GB300 bf16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int) -> float:
+    """Max over ranks (the job finishes when the slowest rank does)."""
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(flops_per_step_per_rank: float, ws: int, seconds_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank's units divided by the slowest rank's time."""
+    return flops_per_step_per_rank * ws / seconds_per_step / 1e12
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_config(w, nnz, extra=None):
+    cfg = {"workload": w.name, "kind": w.kind, "total_tokens": w.total_tokens,
+           "batch": w.batch, "seqlens": w.seqlens, "num_heads": w.num_heads,
+           "head_dim": w.head_dim, "unmasked_pairs_per_head": nnz,
+           "flops_per_step": 4 * w.head_dim * w.num_heads * nnz,
+           "l2": "inputs larger than L2 (Q+K+V = %.0f MB)" %
+                 (3 * w.total_tokens * w.num_heads * w.head_dim * 2 / 1e6)}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# Visible (query, key) pairs per head of each workload: the nnz of the metric's
+# 4*D*H*nnz.  Closed forms: workload 2 and 5 are sums of L(L+1)/2 over the
+# (seeded) sequence / document lengths; workload 3 is P(P+1)/2 + n(sP + s(s+1)/2)
+# with P=2048, n=16, s=512; workload 4 is 8 L(L+1)/2 + L*384*(0+1+...+7) with
+# L=1152.  tests/test_bench_host.py checks each against the oracle's count.
+UNMASKED_PAIRS = {1: 2080, 2: 8_172_171, 3: 20_976_640, 4: 17_699_328, 5: 67_979_834}
+
+
+def count_pairs(w, c):
+    return UNMASKED_PAIRS[c]
+
+
+def cpu_baseline(w, budget_s: float, seed: int = 0):
+    """The fp64 oracle on the host cores over a bounded sample of rows of head 0."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    T = w.total_tokens
+    t0 = time.perf_counter()
+    flops = 0
+    rows_done = 0
+    block = 256
+    qh, kh, vh = w.q[:, :1], w.k[:, :1], w.v[:, :1]
+    while time.perf_counter() - t0 < budget_s:
+        r0 = int(rng.integers(0, max(1, T - block)))
+        rows = np.arange(r0, min(T, r0 + block))
+        oracle.attention(qh, kh, vh, w.kind, w.cu_seqlens, w.meta(), rows=rows)
+        # visible pairs of the sampled rows
+        for b in range(w.batch):
+            s0, s1 = int(w.cu_seqlens[b]), int(w.cu_seqlens[b + 1])
+            sel = rows[(rows >= s0) & (rows < s1)]
+            if len(sel):
+                m = oracle.sequence_mask(w.kind, w.cu_seqlens, b, w.meta(), rows=sel - s0)
+                flops += 4 * w.head_dim * int(m.sum())
+        rows_done += len(rows)
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows_done} query rows of head 0 in random {block}-row blocks, "
+                      f"{el:.1f} s of fp64 numpy work (BLAS thread pool over all cores)"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from block_sparse_masked_mask_gb300 import workloads as W
+    w = W.make_workload(args.workload, tensors=True)
+    nnz = count_pairs(w, args.workload)
+    import oracle
+    rng = np.random.default_rng(0)
+    block = 256
+    qh, kh, vh = w.q[:, :1], w.k[:, :1], w.v[:, :1]
+
+    def step():
+        r0 = int(rng.integers(0, max(1, w.total_tokens - block)))
+        rows = np.arange(r0, min(w.total_tokens, r0 + block))
+        oracle.attention(qh, kh, vh, w.kind, w.cu_seqlens, w.meta(), rows=rows)
+        f = 0
+        for b in range(w.batch):
+            s0, s1 = int(w.cu_seqlens[b]), int(w.cu_seqlens[b + 1])
+            sel = rows[(rows >= s0) & (rows < s1)]
+            if len(sel):
+                f += 4 * w.head_dim * int(oracle.sequence_mask(w.kind, w.cu_seqlens, b, w.meta(),
+                                                                rows=sel - s0).sum())
+        return f
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    flops = sum(step() for _ in range(args.steps))
+    el = time.perf_counter() - t0
+    val = flops / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(w, nnz, {"sample": f"each step: {block} random query rows of head 0"}),
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{args.steps} steps of {block} query rows of head 0"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_sparse_masked_mask_gb300 import api
+    from block_sparse_masked_mask_gb300 import workloads as W
+
+    w = W.make_workload(args.workload, tensors=True)
+    nnz = count_pairs(w, args.workload)
+    flops = 4 * w.head_dim * w.num_heads * nnz
+    dm = w.device_meta(dev)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    T, H, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    ws_bytes = api.attn_block_mask_workspace_size(w.batch, T, w.max_seqlen)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], T, w.max_seqlen,
+                                       seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"],
+                                       role_think=w.role_think, workspace=workspace)
+        if ev is not None:
+            ev.record(stream)
+        api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, seg_id=dm["seg_id"],
+                     role=dm["role"], turn=dm["turn"], role_think=w.role_think, out=out, lse=lse)
+        return bm
+
+    for _ in range(args.warmup):
+        bm = step()
+    status = api.attn_get_status(bm)
+    if status != 0:
+        raise RuntimeError(f"device status {api.attn_status_string(status)}")
+    hdr = bm.header().tolist()
+
+    # ---- timed region: K steps, events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        time.sleep(0.2)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(mids[i])
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(ws)
+    total_ms = starts[0].elapsed_time(ends[-1])
+    fwd_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    build_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    sec_per_step = reduce_max(total_ms / 1e3 / args.steps, ws)
+    value = aggregate_throughput(flops, ws, sec_per_step)
+    status = api.attn_get_status(bm)
+    if status != 0:
+        raise RuntimeError(f"device status {api.attn_status_string(status)}")
+
+    peaks, peak_kind = load_peaks()
+    fwd_avg_s = sum(fwd_ms) / len(fwd_ms) / 1e3
+    achieved = flops / fwd_avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "kernel": "attn_fwd_bf16_kernel<128>", "achieved": achieved,
+                "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "traffic": None}
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv = pin(w.q), pin(w.k), pin(w.v)
+    hmeta = {k2: (None if t is None else pin(t.cpu())) for k2, t in dm.items()}
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv] + [t for t in hmeta.values() if t is not None])
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dmeta = {k2: (None if t is None else torch.empty_like(t, device=dev)) for k2, t in hmeta.items()}
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        for k2, t in hmeta.items():
+            if t is not None:
+                dmeta[k2].copy_(t, non_blocking=True)
+        bm2 = api.attn_block_mask_build(w.kind, dmeta["cu_seqlens"], T, w.max_seqlen,
+                                        seg_id=dmeta["seg_id"], role=dmeta["role"],
+                                        turn=dmeta["turn"], role_think=w.role_think,
+                                        workspace=workspace)
+        api.attn_fwd(dq, dk, dv, bm2, w.kind, dmeta["cu_seqlens"], w.max_seqlen,
+                     seg_id=dmeta["seg_id"], role=dmeta["role"], turn=dmeta["turn"],
+                     role_think=w.role_think, out=out, lse=lse)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_sec = reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, ws)
+    e2e = {"value": aggregate_throughput(flops, ws, e2e_sec), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, nnz, {
+                "parallelism": f"replicas{ws}",
+                "tiles_empty_partial_full": hdr[4:7],
+                "skipped_tile_ratio": hdr[4] / max(1, sum(hdr[4:7])),
+                "fwd_ms_mean": sum(fwd_ms) / len(fwd_ms), "fwd_ms_min": min(fwd_ms),
+                "build_ms_mean": sum(build_ms) / len(build_ms),
+                "fwd_tflops": achieved, "pct_of_peak_fwd": 100 * achieved / peak}),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "gpu_launches": 6 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5],
+                    help="workload number (2-5 are the bf16 block-mask workloads)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="time budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    from block_sparse_masked_mask_gb300 import build as _b
+    _b.ensure_built()
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

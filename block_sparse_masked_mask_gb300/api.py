@@ -1,0 +1,155 @@
+"""Python binding of the C ABI, with the same names.
+
+Tensors are PyTorch CUDA tensors (device memory and streams only); each call
+hands raw pointers and the current stream to libattnmask.  The binding does
+no arithmetic of the method.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _native
+
+ATTN_OK = 0
+STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+    3: "ATTN_ERR_WORKSPACE_TOO_SMALL", 4: "ATTN_ERR_MASK_MISMATCH", 5: "ATTN_ERR_CUDA",
+    6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_DEVICE_INVALID_INPUT",
+}
+MASK_KINDS = {"causal": 0, "causal_document": 1, "shared_prefix": 2, "strip_thinking": 3}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
+BLOCK_M = BLOCK_N = 128
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({attn_status_string(status)})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _kind(kind) -> int:
+    return MASK_KINDS[kind] if isinstance(kind, str) else int(kind)
+
+
+def attn_status_string(status: int) -> str:
+    return _native.lib().attn_status_string(int(status)).decode()
+
+
+def attn_version() -> int:
+    return int(_native.lib().attn_version())
+
+
+def attn_block_mask_workspace_size(batch: int, total_tokens: int, max_seqlen: int,
+                                   block_m: int = BLOCK_M, block_n: int = BLOCK_N) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_native.lib().attn_block_mask_workspace_size(batch, total_tokens, max_seqlen, block_m,
+                                                        block_n, ctypes.byref(out)),
+           "attn_block_mask_workspace_size")
+    return int(out.value)
+
+
+class BlockMask:
+    """A built block mask: the C struct plus the tensors it points into."""
+
+    def __init__(self, struct: _native.AttnBlockMask, workspace: torch.Tensor, keep: tuple):
+        self.struct = struct
+        self.workspace = workspace
+        self._keep = keep  # metadata tensors must outlive the mask
+
+    # -- read-back helpers (copy device arrays to the host; synchronising) --
+    def _array(self, off: int, count: int, dtype) -> torch.Tensor:
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        raw = self.workspace[off: off + nbytes]
+        return raw.view(dtype).cpu()
+
+    def header(self) -> torch.Tensor:
+        return self._array(self.struct.off_header, 8, torch.int32)
+
+    @property
+    def n_qtiles(self) -> int:
+        return int(self.header()[0])
+
+    def lists(self) -> dict:
+        """Device arrays copied back: q-tile descriptors, labels, CSR lists, order."""
+        s = self.struct
+        n = self.n_qtiles
+        hdr = self.header()
+        nent = int(hdr[1])
+        koff = self._array(s.off_koff, n + 1, torch.int32)
+        return {
+            "header": hdr,
+            "qt_seq": self._array(s.off_qt_seq, n, torch.int32),
+            "qt_idx": self._array(s.off_qt_idx, n, torch.int32),
+            "labels": self._array(s.off_labels, s.max_qtiles * s.max_ktiles, torch.uint8)
+                          .view(s.max_qtiles, s.max_ktiles)[:n],
+            "kcount": self._array(s.off_kcount, n, torch.int32),
+            "koff": koff,
+            "kidx": self._array(s.off_kidx, nent, torch.int32),
+            "klabel": self._array(s.off_klabel, nent, torch.uint8),
+            "order": self._array(s.off_order, n, torch.int32),
+            "qt_off": self._array(s.off_qt_off, s.batch + 1, torch.int32),
+        }
+
+
+def attn_block_mask_build(kind, cu_seqlens: torch.Tensor, total_tokens: int, max_seqlen: int,
+                          seg_id: Optional[torch.Tensor] = None, role: Optional[torch.Tensor] = None,
+                          turn: Optional[torch.Tensor] = None, role_think: int = 1,
+                          workspace: Optional[torch.Tensor] = None, stream=None) -> BlockMask:
+    """Build the block mask on the device (asynchronous on ``stream``)."""
+    batch = cu_seqlens.numel() - 1
+    need = attn_block_mask_workspace_size(batch, total_tokens, max_seqlen)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=cu_seqlens.device)
+    params = _native.AttnMaskParams(role_think)
+    out = _native.AttnBlockMask()
+    _check(_native.lib().attn_block_mask_build(
+        _kind(kind), ctypes.byref(params), _ptr(cu_seqlens), batch, total_tokens, max_seqlen,
+        _ptr(seg_id), _ptr(role), _ptr(turn), BLOCK_M, BLOCK_N, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(out), _stream(stream)),
+        "attn_block_mask_build")
+    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn))
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, kind,
+             cu_seqlens: torch.Tensor, max_seqlen: int, seg_id=None, role=None, turn=None,
+             role_think: int = 1, scale: float = 0.0, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, stream=None):
+    """Masked attention forward; returns (O [T, H, D], LSE [H, T] fp32)."""
+    T, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if q.dtype not in DTYPES:
+        raise AttnError(1, "attn_fwd: dtype must be bfloat16 or float32")
+    params = _native.AttnMaskParams(role_think)
+    _check(_native.lib().attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), DTYPES[q.dtype], T, H, D, float(scale),
+        _ptr(cu_seqlens), cu_seqlens.numel() - 1, max_seqlen, _kind(kind), ctypes.byref(params),
+        _ptr(seg_id), _ptr(role), _ptr(turn), ctypes.byref(bm.struct), _stream(stream)),
+        "attn_fwd")
+    return out, lse
+
+
+def attn_get_status(bm: BlockMask, stream=None) -> int:
+    """Synchronise and return the device status code of the mask's error word."""
+    return int(_native.lib().attn_get_status(ctypes.byref(bm.struct), _stream(stream)))

@@ -1,0 +1,342 @@
+// Block-mask builder: tile summaries, exact FULL/PARTIAL/EMPTY classification
+// of every (q-tile, k-tile) pair of each sequence, compacted per-q-tile k-tile
+// lists (forward, q-major orientation) and a longest-first q-tile order.
+//
+// "Triton from first principles" Ch. 9, Section 9.2 skips whole tiles on a
+// per-tile scalar flag, and Ch. 21, Section 21.2 names the three tile classes
+// (all-valid, diagonal/partial, skipped).  The xorl issue "Block-mask
+// attention: shared-prefix and strip-thinking" builds such a mask once from
+// per-token segment / role / turn tensors and reuses it (Proposed work,
+// item 3); its forward metadata is per-q-block lists of k-blocks.
+//
+// Exactness: a label is decided from per-tile metadata summaries only when the
+// summaries prove it (interval reasoning below); every other pair is counted
+// pair by pair with the predicate, so labels always equal brute-force counts.
+#include "common.cuh"
+
+namespace attnmask {
+namespace {
+
+constexpr int kUnknown = -1;
+
+__device__ __forceinline__ int warp_sum(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ int warp_min(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = min(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ int warp_max(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// 1 CTA: validate cu_seqlens, per-sequence q-tile offsets, q-tile -> (seq, idx).
+__global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
+  __shared__ int s_err;
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  if (tid == 0) { s_err = 0; s_carry = 0; }
+  __syncthreads();
+  const int B = v.batch;
+  int err = 0;
+  for (int b = tid; b < B; b += blockDim.x) {
+    const int c0 = v.cu[b], c1 = v.cu[b + 1];
+    if (c1 < c0) err |= kErrCuOrder;
+    else if (c1 - c0 > v.max_seqlen) err |= kErrSeqTooLong;
+  }
+  if (tid == 0) {
+    if (v.cu[0] != 0) err |= kErrCuFirst;
+    if (v.cu[B] != v.total_tokens) err |= kErrCuLast;
+  }
+  if (err) atomicOr(&s_err, err);
+  __syncthreads();
+  const int bad = s_err;
+
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + tid;
+    int nt = 0;
+    if (!bad && b < B) nt = (v.cu[b + 1] - v.cu[b] + kTile - 1) / kTile;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nw) s_warp[lane] = w;  // inclusive warp prefix
+    }
+    __syncthreads();
+    const int before = (warp ? s_warp[warp - 1] : 0) + incl - nt;
+    if (b < B) v.qt_off[b] = s_carry + before;
+    __syncthreads();
+    if (tid == 0) s_carry += s_warp[nw - 1];
+    __syncthreads();
+  }
+  const int n_qt = s_carry;
+  if (tid == 0) {
+    v.qt_off[B] = n_qt;
+    v.header[kHdrQtiles] = n_qt;
+    v.header[kHdrEntries] = 0;
+    v.header[kHdrError] = bad;
+    v.header[3] = 0;
+    v.header[kHdrEmpty] = 0;
+    v.header[kHdrPartial] = 0;
+    v.header[kHdrFull] = 0;
+    v.header[7] = 0;
+  }
+  __syncthreads();
+  for (int g = tid; g < n_qt; g += blockDim.x) {
+    // sequence b with qt_off[b] <= g < qt_off[b+1] (empty sequences own no tile)
+    int lo = 0, hi = B;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (v.qt_off[mid] <= g) lo = mid; else hi = mid;
+    }
+    v.qt_seq[g] = lo;
+    v.qt_idx[g] = g - v.qt_off[lo];
+  }
+}
+
+// Per 128-token tile: the metadata summary the classifier reasons with.
+//   causal_document / shared_prefix: [0] min seg, [1] max seg, [2] any seg == 0
+//   strip_thinking: [0] min turn, [1] max turn, [2] #THINK tokens,
+//                   [3] min THINK turn, [4] max THINK turn, [5] #tokens
+__global__ void __launch_bounds__(128) bm_summary_kernel(BmView v, MaskArgs m) {
+  const int g = blockIdx.x;
+  if (g >= v.header[kHdrQtiles] || m.kind == ATTN_MASK_CAUSAL) return;
+  __shared__ int s_red[4][6];
+  const int b = v.qt_seq[g], a = v.qt_idx[g];
+  const int s0 = v.cu[b], L = v.cu[b + 1] - s0;
+  const int n = min(kTile, L - a * kTile);
+  const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+  const bool in = r < n;
+  const int tok = s0 + a * kTile + r;
+  int x[6];
+  if (m.kind == ATTN_MASK_STRIP_THINKING) {
+    const int t = in ? m.turn[tok] : 0;
+    const bool th = in && (int)m.role[tok] == m.role_think;
+    x[0] = warp_min(in ? t : INT_MAX);
+    x[1] = warp_max(in ? t : INT_MIN);
+    x[2] = warp_sum(th ? 1 : 0);
+    x[3] = warp_min(th ? t : INT_MAX);
+    x[4] = warp_max(th ? t : INT_MIN);
+    x[5] = warp_sum(in ? 1 : 0);
+  } else {
+    const int sg = in ? m.seg[tok] : 0;
+    x[0] = warp_min(in ? sg : INT_MAX);
+    x[1] = warp_max(in ? sg : INT_MIN);
+    x[2] = warp_sum(in && sg == 0 ? 1 : 0);
+    x[3] = x[4] = x[5] = 0;
+  }
+  if (lane == 0)
+    for (int i = 0; i < 6; ++i) s_red[warp][i] = x[i];
+  __syncthreads();
+  if (r == 0) {
+    int* out = v.summary + size_t(g) * kSumInts;
+    int mn0 = INT_MAX, mx1 = INT_MIN, c2 = 0, mn3 = INT_MAX, mx4 = INT_MIN, c5 = 0;
+    for (int w = 0; w < 4; ++w) {
+      mn0 = min(mn0, s_red[w][0]);
+      mx1 = max(mx1, s_red[w][1]);
+      c2 += s_red[w][2];
+      mn3 = min(mn3, s_red[w][3]);
+      mx4 = max(mx4, s_red[w][4]);
+      c5 += s_red[w][5];
+    }
+    out[0] = mn0; out[1] = mx1; out[2] = c2; out[3] = mn3; out[4] = mx4; out[5] = c5;
+    out[6] = 0; out[7] = 0;
+  }
+}
+
+// Label of the pair (q rows i0..i1, k columns j0..j1, local positions) when the
+// summaries prove it, else kUnknown.  Every rule is a sufficient condition.
+__device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
+                                      const int* sq, const int* sk) {
+  if (j0 > i1) return ATTN_TILE_EMPTY;           // every key after every query
+  const bool all_causal = j1 <= i0;              // every key at or before every query
+  switch (kind) {
+    case ATTN_MASK_CAUSAL:
+      // j0 <= i1 gives a visible pair (i1, j0); j1 > i0 a hidden one (i0, j1)
+      return all_causal ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL;
+    case ATTN_MASK_CAUSAL_DOCUMENT:
+      if (sq[1] < sk[0] || sk[1] < sq[0]) return ATTN_TILE_EMPTY;  // no shared document id
+      if (all_causal && sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0]) return ATTN_TILE_FULL;
+      return kUnknown;
+    case ATTN_MASK_SHARED_PREFIX:
+      if (sk[2] == 0 && (sq[1] < sk[0] || sk[1] < sq[0])) return ATTN_TILE_EMPTY;
+      if (all_causal && sk[0] == 0 && sk[1] == 0) return ATTN_TILE_FULL;       // all prefix keys
+      if (all_causal && sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0]) return ATTN_TILE_FULL;
+      return kUnknown;
+    case ATTN_MASK_STRIP_THINKING:
+      // hidden iff key is THINK with an earlier turn than the query
+      if (all_causal && (sk[2] == 0 || sk[3] >= sq[1])) return ATTN_TILE_FULL;
+      if (sk[2] == sk[5] && sk[4] < sq[0]) return ATTN_TILE_EMPTY;
+      return kUnknown;
+  }
+  return kUnknown;
+}
+
+// One CTA per q-tile: labels of its whole row, and its non-EMPTY count.
+__global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) {
+  const int g = blockIdx.x;
+  if (g >= v.header[kHdrQtiles]) return;
+  __shared__ int s_kcode[kTile];
+  __shared__ int s_red[4];
+  const int b = v.qt_seq[g], a = v.qt_idx[g];
+  const int s0 = v.cu[b], L = v.cu[b + 1] - s0;
+  const int nt = (L + kTile - 1) / kTile;
+  const int i0 = a * kTile, i1 = min(L, i0 + kTile) - 1, qn = i1 - i0 + 1;
+  const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+  const bool row_in = r < qn;
+  const int qcode = row_in ? query_code(m, s0 + i0 + r) : 0;
+  int sq[kSumInts], sk[kSumInts];
+  const int* qsum = v.summary + size_t(g) * kSumInts;
+  for (int i = 0; i < kSumInts; ++i) sq[i] = m.kind == ATTN_MASK_CAUSAL ? 0 : qsum[i];
+  const int gbase = v.qt_off[b];
+  uint8_t* row = v.labels + size_t(g) * v.max_nt;
+  int n_empty = 0, n_partial = 0, n_full = 0;
+  for (int bt = 0; bt < nt; ++bt) {
+    const int j0 = bt * kTile, j1 = min(L, j0 + kTile) - 1, kn = j1 - j0 + 1;
+    if (m.kind != ATTN_MASK_CAUSAL) {
+      const int* ks = v.summary + size_t(gbase + bt) * kSumInts;
+      for (int i = 0; i < kSumInts; ++i) sk[i] = ks[i];
+    } else {
+      for (int i = 0; i < kSumInts; ++i) sk[i] = 0;
+    }
+    int lab = decide(m.kind, i0, i1, j0, j1, sq, sk);
+    if (lab == kUnknown) {
+      __syncthreads();
+      if (r < kn) s_kcode[r] = key_code(m, s0 + j0 + r);
+      __syncthreads();
+      int cnt = 0;
+      if (row_in) {
+        const int lim = min(kn, i0 + r - j0 + 1);  // keys with j <= i
+        for (int c = 0; c < lim; ++c) cnt += code_visible(m.kind, qcode, s_kcode[c]) ? 1 : 0;
+      }
+      cnt = warp_sum(cnt);
+      if (lane == 0) s_red[warp] = cnt;
+      __syncthreads();
+      const int total = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+      lab = total == 0 ? ATTN_TILE_EMPTY : (total == qn * kn ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL);
+    }
+    n_empty += lab == ATTN_TILE_EMPTY;
+    n_partial += lab == ATTN_TILE_PARTIAL;
+    n_full += lab == ATTN_TILE_FULL;
+    if (r == 0) row[bt] = uint8_t(lab);
+  }
+  if (r == 0) {
+    v.kcount[g] = n_partial + n_full;
+    atomicAdd(v.header + kHdrEmpty, n_empty);
+    atomicAdd(v.header + kHdrPartial, n_partial);
+    atomicAdd(v.header + kHdrFull, n_full);
+  }
+}
+
+// 1 CTA: CSR offsets koff = exclusive prefix sum of kcount.
+__global__ void __launch_bounds__(1024) bm_scan_kernel(BmView v) {
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int n = v.header[kHdrQtiles];
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int g = base + tid;
+    const int x = g < n ? v.kcount[g] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nw) s_warp[lane] = w;
+    }
+    __syncthreads();
+    if (g < n) v.koff[g] = s_carry + (warp ? s_warp[warp - 1] : 0) + incl - x;
+    __syncthreads();
+    if (tid == 0) s_carry += s_warp[nw - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    v.koff[n] = s_carry;
+    v.header[kHdrEntries] = s_carry;
+  }
+}
+
+// One CTA per q-tile: compact its row into ascending (kidx, klabel) entries,
+// and place it in the longest-first order (descending kcount, ties by number).
+__global__ void __launch_bounds__(128) bm_fill_kernel(BmView v) {
+  const int g = blockIdx.x;
+  const int n_qt = v.header[kHdrQtiles];
+  if (g >= n_qt) return;
+  __shared__ int s_warp[4];
+  const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
+  const int b = v.qt_seq[g];
+  const int L = v.cu[b + 1] - v.cu[b];
+  const int nt = (L + kTile - 1) / kTile;
+  const uint8_t* row = v.labels + size_t(g) * v.max_nt;
+  int pos = v.koff[g];
+  for (int c0 = 0; c0 < nt; c0 += kTile) {
+    const int bt = c0 + r;
+    const int lab = bt < nt ? row[bt] : ATTN_TILE_EMPTY;
+    const bool keep = lab != ATTN_TILE_EMPTY;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s_warp[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    before += __popc(bal & ((1u << lane) - 1u));
+    if (keep) {
+      v.kidx[pos + before] = bt;
+      v.klabel[pos + before] = uint8_t(lab);
+    }
+    pos += s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3];
+    __syncthreads();
+  }
+  const int mine = v.kcount[g];
+  int ahead = 0;
+  for (int g2 = r; g2 < n_qt; g2 += blockDim.x) {
+    const int k2 = v.kcount[g2];
+    ahead += (k2 > mine) || (k2 == mine && g2 < g);
+  }
+  ahead = warp_sum(ahead);
+  if (lane == 0) s_warp[warp] = ahead;
+  __syncthreads();
+  if (r == 0) v.order[s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3]] = g;
+}
+
+}  // namespace
+
+cudaError_t launch_block_mask_build(const BmView& v, const MaskArgs& m, cudaStream_t s) {
+  const int grid = v.max_qt > 0 ? v.max_qt : 1;
+  bm_prepare_kernel<<<1, 1024, 0, s>>>(v);
+  bm_summary_kernel<<<grid, 128, 0, s>>>(v, m);
+  bm_classify_kernel<<<grid, 128, 0, s>>>(v, m);
+  bm_scan_kernel<<<1, 1024, 0, s>>>(v);
+  bm_fill_kernel<<<grid, 128, 0, s>>>(v);
+  return cudaGetLastError();
+}
+
+}  // namespace attnmask

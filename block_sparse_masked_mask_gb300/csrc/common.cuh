@@ -1,0 +1,123 @@
+// Internal declarations shared by the translation units of libattnmask.
+// Not installed; the public interface is include/attn_block_mask.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <climits>
+
+#include <cuda_runtime.h>
+
+#include "attn_block_mask.h"
+
+namespace attnmask {
+
+constexpr uint32_t kMaskMagic = 0x4B53414Du;  // "MASK"
+constexpr int kTile = 128;                    // q-tile rows = k-tile columns
+
+// Device error bits, kept in header[kHdrError] of the block-mask workspace.
+enum : int32_t {
+  kErrCuFirst = 1 << 0,      // cu_seqlens[0] != 0
+  kErrCuOrder = 1 << 1,      // cu_seqlens decreases somewhere
+  kErrCuLast = 1 << 2,       // cu_seqlens[batch] != total_tokens
+  kErrSeqTooLong = 1 << 3,   // a sequence is longer than max_seqlen
+  kErrTimeout = 1 << 8,      // a pipeline wait gave up (bits 9.. hold the wait site)
+  kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong,
+};
+
+enum : int { kHdrQtiles = 0, kHdrEntries = 1, kHdrError = 2, kHdrEmpty = 4, kHdrPartial = 5,
+             kHdrFull = 6, kHdrInts = 8 };
+
+enum : int { kSumInts = 8 };  // ints per tile summary
+
+// Byte layout of the block-mask workspace.
+struct BmLayout {
+  int max_qt = 0, max_nt = 0;
+  uint64_t header = 0, qt_seq = 0, qt_idx = 0, labels = 0, kcount = 0, koff = 0, kidx = 0,
+           klabel = 0, order = 0, qt_off = 0, summary = 0, total = 0;
+};
+
+// Returns false on overflow / invalid sizes.
+bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out);
+
+// Device-side view of a built block mask.
+struct BmView {
+  int32_t* header;
+  int32_t* qt_seq;
+  int32_t* qt_idx;
+  uint8_t* labels;
+  int32_t* kcount;
+  int32_t* koff;
+  int32_t* kidx;
+  uint8_t* klabel;
+  int32_t* order;
+  int32_t* qt_off;
+  int32_t* summary;
+  const int32_t* cu;
+  int max_qt, max_nt, batch, total_tokens, max_seqlen;
+};
+
+// Per-token mask metadata as the kernels see it.
+struct MaskArgs {
+  int kind;
+  int role_think;
+  const int32_t* seg;
+  const int8_t* role;
+  const int32_t* turn;
+};
+
+// The four predicates factor as  (ki <= qi) && code_visible(qcode(qi), kcode(ki)):
+//   causal          : always true
+//   causal_document : seg[k] == seg[q]
+//   shared_prefix   : seg[k] == 0 || seg[k] == seg[q]
+//   strip_thinking  : !(role[k] == THINK && turn[k] < turn[q]); the key code is
+//                     turn[k] for THINK keys and INT_MAX otherwise, so the test
+//                     becomes kcode >= turn[q].
+__device__ __forceinline__ int query_code(const MaskArgs& m, int qi) {
+  switch (m.kind) {
+    case ATTN_MASK_CAUSAL_DOCUMENT:
+    case ATTN_MASK_SHARED_PREFIX: return m.seg[qi];
+    case ATTN_MASK_STRIP_THINKING: return m.turn[qi];
+    default: return 0;
+  }
+}
+
+__device__ __forceinline__ int key_code(const MaskArgs& m, int ki) {
+  switch (m.kind) {
+    case ATTN_MASK_CAUSAL_DOCUMENT:
+    case ATTN_MASK_SHARED_PREFIX: return m.seg[ki];
+    case ATTN_MASK_STRIP_THINKING:
+      return (int)m.role[ki] == m.role_think ? m.turn[ki] : INT_MAX;
+    default: return 0;
+  }
+}
+
+__device__ __forceinline__ bool code_visible(int kind, int qcode, int kcode) {
+  switch (kind) {
+    case ATTN_MASK_CAUSAL_DOCUMENT: return kcode == qcode;
+    case ATTN_MASK_SHARED_PREFIX: return kcode == 0 || kcode == qcode;
+    case ATTN_MASK_STRIP_THINKING: return kcode >= qcode;
+    default: return true;
+  }
+}
+
+// Launchers (return a cudaError_t of the launch).
+cudaError_t launch_block_mask_build(const BmView& v, const MaskArgs& m, cudaStream_t s);
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int total_tokens, num_heads, head_dim;
+  float scale;
+  BmView bm;
+  MaskArgs mask;
+};
+
+// Returns ATTN_OK or an error status (tensor-map encoding or launch failure).
+attn_status launch_attn_fwd_bf16(const FwdArgs& a, cudaStream_t s);
+attn_status launch_attn_fwd_f32(const FwdArgs& a, cudaStream_t s);
+
+}  // namespace attnmask

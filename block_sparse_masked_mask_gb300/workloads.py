@@ -82,6 +82,13 @@ class Workload:
         return {"seg": self.seg, "role": self.role, "turn": self.turn,
                 "role_think": self.role_think}
 
+    def device_meta(self, device="cuda") -> dict:
+        """cu_seqlens and the per-token metadata as device tensors."""
+        def dev(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return {"cu_seqlens": dev(self.cu_seqlens), "seg_id": dev(self.seg),
+                "role": dev(self.role), "turn": dev(self.turn)}
+
 
 WORKLOAD_NAMES = {
     1: "causal_s64_d32_fp32",
