@@ -235,6 +235,9 @@ def run_ours(args):
     from block_sparse_masked_mask_gb300 import workloads as W
 
     w = W.make_workload(args.workload, tensors=True)
+    if args.heads:
+        w.num_heads = args.heads
+        w.q, w.k, w.v = (t[:, :args.heads].contiguous() for t in (w.q, w.k, w.v))
     nnz = count_pairs(w, args.workload)
     flops = 4 * w.head_dim * w.num_heads * nnz
     dm = w.device_meta(dev)
@@ -379,6 +382,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (a smaller case of the same mask for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -46,6 +46,9 @@ class AttnBlockMask(ctypes.Structure):
         ("off_order", ctypes.c_uint64),
         ("off_qt_off", ctypes.c_uint64),
         ("off_summary", ctypes.c_uint64),
+        ("off_pair_off", ctypes.c_uint64),
+        ("off_pair_q0", ctypes.c_uint64),
+        ("off_pair_order", ctypes.c_uint64),
     ]
 
 
@@ -81,6 +84,8 @@ def lib() -> ctypes.CDLL:
     L.attn_get_status.restype = ctypes.c_int
     L.attn_status_string.argtypes = [ctypes.c_int]
     L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_last_error_message.argtypes = []
+    L.attn_last_error_message.restype = ctypes.c_char_p
     L.attn_version.argtypes = []
     L.attn_version.restype = c_int32
     _lib = L

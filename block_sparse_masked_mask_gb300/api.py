@@ -28,7 +28,10 @@ BLOCK_M = BLOCK_N = 128
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({attn_status_string(status)})")
+        msg = f"{where}: {STATUS.get(status, status)} ({attn_status_string(status)})"
+        if status == 5:
+            msg += f": {attn_last_error_message()}"
+        super().__init__(msg)
 
 
 def _check(status: int, where: str) -> None:
@@ -52,6 +55,10 @@ def _kind(kind) -> int:
 
 def attn_status_string(status: int) -> str:
     return _native.lib().attn_status_string(int(status)).decode()
+
+
+def attn_last_error_message() -> str:
+    return _native.lib().attn_last_error_message().decode()
 
 
 def attn_version() -> int:
@@ -107,6 +114,9 @@ class BlockMask:
             "klabel": self._array(s.off_klabel, nent, torch.uint8),
             "order": self._array(s.off_order, n, torch.int32),
             "qt_off": self._array(s.off_qt_off, s.batch + 1, torch.int32),
+            "pair_off": self._array(s.off_pair_off, s.batch + 1, torch.int32),
+            "pair_q0": self._array(s.off_pair_q0, int(hdr[3]), torch.int32),
+            "pair_order": self._array(s.off_pair_order, int(hdr[3]), torch.int32),
         }
 
 

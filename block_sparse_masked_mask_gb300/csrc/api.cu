@@ -1,10 +1,19 @@
 // C ABI of libattnmask: argument checks, workspace layout and dispatch.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 
 #include "common.cuh"
 
 namespace attnmask {
+
+static thread_local char g_last_error[256] = "";
+
+attn_status record_cuda_error(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return ATTN_ERR_CUDA;
+}
 
 static uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255u); }
 
@@ -29,6 +38,9 @@ bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out) {
   l.order = take(4 * nq);
   l.qt_off = take(4 * (uint64_t(batch) + 1));
   l.summary = take(4 * kSumInts * nq);
+  l.pair_off = take(4 * (uint64_t(batch) + 1));
+  l.pair_q0 = take(4 * nq);
+  l.pair_order = take(4 * nq);
   l.total = p;
   *out = l;
   return true;
@@ -48,6 +60,9 @@ static BmView make_view(const attn_block_mask* bm) {
   v.order = reinterpret_cast<int32_t*>(base + bm->off_order);
   v.qt_off = reinterpret_cast<int32_t*>(base + bm->off_qt_off);
   v.summary = reinterpret_cast<int32_t*>(base + bm->off_summary);
+  v.pair_off = reinterpret_cast<int32_t*>(base + bm->off_pair_off);
+  v.pair_q0 = reinterpret_cast<int32_t*>(base + bm->off_pair_q0);
+  v.pair_order = reinterpret_cast<int32_t*>(base + bm->off_pair_order);
   v.cu = bm->cu_seqlens;
   v.max_qt = bm->max_qtiles;
   v.max_nt = bm->max_ktiles;
@@ -75,6 +90,8 @@ using namespace attnmask;
 extern "C" {
 
 int32_t attn_version(void) { return 100; }
+
+const char* attn_last_error_message(void) { return g_last_error; }
 
 const char* attn_status_string(attn_status s) {
   switch (s) {
@@ -143,10 +160,13 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   bm.off_order = l.order;
   bm.off_qt_off = l.qt_off;
   bm.off_summary = l.summary;
+  bm.off_pair_off = l.pair_off;
+  bm.off_pair_q0 = l.pair_q0;
+  bm.off_pair_order = l.pair_order;
 
   MaskArgs m{kind, bm.role_think, seg_id, role, turn};
   cudaError_t e = launch_block_mask_build(make_view(&bm), m, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_block_mask_build launch");
   *out = bm;
   return ATTN_OK;
 }
@@ -195,13 +215,15 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 attn_status attn_get_status(const attn_block_mask* bm, attn_stream_t stream) {
   if (bm == nullptr || bm->magic != kMaskMagic) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_get_status synchronize");
   int32_t err = 0;
   const char* base = static_cast<const char*>(bm->workspace);
-  if (cudaMemcpy(&err, base + bm->off_header + sizeof(int32_t) * kHdrError, sizeof(err),
-                 cudaMemcpyDeviceToHost) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  e = cudaMemcpy(&err, base + bm->off_header + sizeof(int32_t) * kHdrError, sizeof(err),
+                 cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_get_status read");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_get_status");
   if (err & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
   if (err & kErrInputMask) return ATTN_ERR_DEVICE_INVALID_INPUT;
   return ATTN_OK;

@@ -2,26 +2,32 @@
 //
 // The loop is the online-softmax flash attention of "Triton from first
 // principles" Ch. 21, Section 21.1 (running max m, running sum l, accumulator
-// rescaled by alpha = exp(m_old - m_new), one division at the end), with the
-// causal / structured mask applied inside the loop as in Section 21.2, and
-// only the k-tiles the block mask lists for a q-tile are visited (Ch. 9,
-// Section 9.2: a skipped tile is never loaded).
+// rescaled by exp(m_old - m_new), one division at the end), with the causal /
+// structured mask applied inside the loop as in Section 21.2, and only the
+// k-tiles the block mask lists are visited (Ch. 9, Section 9.2: a skipped
+// tile is never loaded).
 //
-// One CTA handles one (q-tile of 128 rows, head) work item.  Warp roles:
-//   warp 0     TMA producer: Q once, then K and V tiles of the listed k-tiles
-//              into a 2-stage shared-memory ring; key mask codes for PARTIAL
-//              tiles.
-//   warp 1     tcgen05 issuer (one thread): S = Q K^T into one of two TMEM
-//              score buffers, then O += P V with P read from TMEM.
-//   warps 2-5  softmax: one thread per query row.  Each thread reads its row
-//              of S from TMEM, applies the mask (PARTIAL tiles: predicate and
-//              bounds; FULL tiles: bounds only on a ragged last tile), updates
-//              m and l, rescales its row of O in TMEM when m grew, writes P as
-//              bf16 over the first half of its S row, and finally writes
-//              O / l and LSE.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
-// Every mbarrier wait is bounded: on timeout the CTA records kErrTimeout in
-// the block-mask error word, drains what it issued, frees TMEM and exits.
+// One CTA handles one work item: a pair of adjacent 128-row q-tiles of one
+// sequence (the second may be absent) and one head.  The pair walks the
+// ascending union of its two k-tile lists; each K and V tile is loaded once
+// and serves both q-tiles, and a q-tile skips the entries its own list does
+// not hold (EMPTY for it).  Warp roles:
+//   warps 0-3  softmax of q-tile 0, one thread per query row
+//   warps 4-7  softmax of q-tile 1
+//   warp 8     TMA producer: Q0/Q1 once, then K(j), V(j) into a ring of
+//              four 128 x D slots; zeroes V rows past a sequence end
+//   warps 10-11 idle
+//   warp 9     tcgen05 issuer (one thread) and TMEM owner.  Order per entry
+//              j: PV0(j), S0(j+1), PV1(j), S1(j+1), so one softmax group works
+//              while the tensor cores serve the other (ping-pong).
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
+// P (bf16) overwrites the first 64 columns of its S buffer.
+//
+// The row maximum used as the exponent reference only moves when a new tile
+// raises it by more than 2^8 (factor 256 in p); O and l are then rescaled
+// together, so the final O / l and LSE are unchanged in exact arithmetic.
+// Every mbarrier wait is bounded: on timeout the CTA records kErrTimeout in the
+// block-mask error word, drains what it issued, frees TMEM and exits.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -32,11 +38,21 @@ namespace attnmask {
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // bound on waiting for in-flight copies
+constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // bound on waiting for in-flight work
+constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 256
+// 384 threads = 3 warpgroups, one warp of each on every SM sub-partition.
+// Launched at kLaunchRegs per thread; the two softmax warpgroups then take
+// kSoftmaxRegs and the producer / MMA warpgroup keeps kOtherRegs:
+// 2 * 216 + 72 = 504 = 3 * 168, the launch budget of a sub-partition's warps.
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 216;
+constexpr uint32_t kOtherRegs = 72;
+static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
 
 template <int D>
 struct Cfg {
-  static constexpr int NST = 2;                       // K/V ring stages
+  static constexpr int NSLOT = 4;                     // K/V ring slots (one tile each)
   static constexpr int CE = D >= 64 ? 64 : 32;        // bf16 elements per swizzled row chunk
   static constexpr int ROWB = CE * 2;                 // bytes per row chunk (128 or 64)
   static constexpr int NCH = D / CE;                  // row chunks per tile
@@ -44,30 +60,28 @@ struct Cfg {
   static constexpr int TILE = NCH * CHUNK;            // 128 x D bf16
   static constexpr uint32_t SW = D >= 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
   static constexpr int SBO = 8 * ROWB;                // 8-row core-matrix group stride
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + NST * TILE;
-  static constexpr int OFF_KCODE = OFF_V + NST * TILE;
-  // barriers: q, kfull[NST], vfull[NST], empty[NST], sfull[2], pfull[2], odone, drain
-  static constexpr int B_Q = 0, B_KFULL = 1, B_VFULL = 1 + NST, B_EMPTY = 1 + 2 * NST,
-                       B_SFULL = 1 + 3 * NST, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-                       B_DRAIN = B_ODONE + 1, NBAR = B_DRAIN + 1;
-  static constexpr int OFF_BAR = OFF_KCODE + NST * kTile * 4;
+  static constexpr int OFF_Q0 = 0, OFF_Q1 = TILE, OFF_RING = 2 * TILE;
+  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_VTMA = 1 + 2 * NSLOT,
+                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
+                       B_DRAIN = B_ODONE + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_O = 256;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, D, false, true);
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return uint32_t(t) * 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
   int32_t* header;
-  const int32_t* order;
+  const int32_t* pair_order;
+  const int32_t* pair_q0;
   const int32_t* qt_seq;
   const int32_t* qt_idx;
   const int32_t* koff;
@@ -79,6 +93,24 @@ struct FwdParams {
   float* lse;
   int H, T;
   float scale_log2;  // scale * log2(e)
+};
+
+// Ascending union of the two q-tiles' k-tile lists, with each q-tile's label
+// (EMPTY where its own list lacks the k-tile).  Every role walks it alike.
+// Entries are positions in the CSR arrays: e0 .. end0 (q-tile 0), e1 .. end1.
+struct PairWalk {
+  int e0, end0, e1, end1;
+  __device__ bool next(const int32_t* kidx, const uint8_t* klabel, int& kt, int& a, int& b) {
+    const int x0 = e0 < end0 ? __ldg(kidx + e0) : INT_MAX;
+    const int x1 = e1 < end1 ? __ldg(kidx + e1) : INT_MAX;
+    kt = min(x0, x1);
+    if (kt == INT_MAX) return false;
+    a = ATTN_TILE_EMPTY;
+    b = ATTN_TILE_EMPTY;
+    if (x0 == kt) a = __ldg(klabel + e0++);
+    if (x1 == kt) b = __ldg(klabel + e1++);
+    return true;
+  }
 };
 
 // Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting.
@@ -122,15 +154,20 @@ __device__ __forceinline__ uint32_t prefix_bits(int n) {
   return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
 }
 
-// Visibility bits of 32 consecutive keys (codes in shared memory) for one query code.
+// Visibility bits of keys [32q, 32q+32) of a k-tile starting at global token
+// `k0tok` (kn keys in bounds) for one query code, read from the metadata.
 template <int KIND>
-__device__ __forceinline__ uint32_t code_word(const int* kc, int qcode) {
+__device__ __forceinline__ uint32_t code_word(const MaskArgs& m, int k0tok, int q, int kn, int qcode) {
   uint32_t w = 0;
 #pragma unroll
-  for (int c = 0; c < 32; c += 4) {
-    const int4 k = *reinterpret_cast<const int4*>(kc + c);
-    w |= (uint32_t(code_visible(KIND, qcode, k.x)) << c) | (uint32_t(code_visible(KIND, qcode, k.y)) << (c + 1)) |
-         (uint32_t(code_visible(KIND, qcode, k.z)) << (c + 2)) | (uint32_t(code_visible(KIND, qcode, k.w)) << (c + 3));
+  for (int c = 0; c < 32; ++c) {
+    const int idx = min(32 * q + c, kn - 1);  // clamped: out-of-bounds bits are cleared anyway
+    int kc;
+    if (KIND == ATTN_MASK_STRIP_THINKING)
+      kc = int(__ldg(m.role + k0tok + idx)) == m.role_think ? __ldg(m.turn + k0tok + idx) : INT_MAX;
+    else
+      kc = __ldg(m.seg + k0tok + idx);
+    w |= uint32_t(code_visible(KIND, qcode, kc)) << c;
   }
   return w;
 }
@@ -153,7 +190,24 @@ __device__ __forceinline__ uint64_t v_desc(uint32_t tile_addr, int kk) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    ptx::mma_ss(d_tmem, kmajor_desc<D>(q_addr, kk), kmajor_desc<D>(k_addr, kk), C::IDESC_S, kk > 0);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool acc) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc<D>(v_addr, kk), C::IDESC_PV,
+                (acc || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -162,23 +216,28 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_qt = p.header[kHdrQtiles];
+  const int n_pairs = p.header[kHdrPairs];
   const int item = blockIdx.x;
-  if (item >= n_qt * p.H) return;
+  if (item >= n_pairs * p.H) return;
   int32_t* err = p.header + kHdrError;
 
-  const int h = item / n_qt;
-  const int g = p.order[item % n_qt];
-  const int b = p.qt_seq[g], qa = p.qt_idx[g];
+  const int h = item / n_pairs;
+  const int pr = p.pair_order[item % n_pairs];
+  const int g0 = p.pair_q0[pr];
+  const int b = p.qt_seq[g0];
+  const bool has1 = g0 + 1 < n_qt && p.qt_seq[g0 + 1] == b;
   const int s0 = p.cu[b], L = p.cu[b + 1] - s0;
-  const int i0 = qa * kTile;                  // first query row, local to the sequence
-  const int qn = min(kTile, L - i0);
-  const int e0 = p.koff[g], n = p.koff[g + 1] - e0;
+  const int qi0 = p.qt_idx[g0] * kTile;  // first query row of q-tile 0, local to the sequence
+  PairWalk walk0;
+  walk0.e0 = p.koff[g0];
+  walk0.end0 = p.koff[g0 + 1];
+  walk0.e1 = walk0.end0;
+  walk0.end1 = has1 ? p.koff[g0 + 2] : walk0.end0;
 
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
-  int* kcode = reinterpret_cast<int*>(sbase + C::OFF_KCODE);
+  const uint32_t sQ0 = base + C::OFF_Q0, sQ1 = base + C::OFF_Q1, sRing = base + C::OFF_RING;
   const uint32_t bars = base + C::OFF_BAR;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
@@ -186,22 +245,22 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_Q), 1);
-    for (int s = 0; s < C::NST; ++s) {
-      ptx::mbar_init(bar(C::B_KFULL + s), 1);
-      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(bar(C::B_FULL + s), 1);
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(C::B_SFULL + s), 1);
-      ptx::mbar_init(bar(C::B_PFULL + s), 128);
+    ptx::mbar_init(bar(C::B_VTMA), 1);
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(C::B_SFULL + t), 1);
+      ptx::mbar_init(bar(C::B_PFULL + t), 128);
+      ptx::mbar_init(bar(C::B_ODONE + t), 1);
     }
-    ptx::mbar_init(bar(C::B_ODONE), 1);
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -211,116 +270,190 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = misc[0];
   const bool skip = *abort_flag != 0u;
 
-  if (skip) {
+  if (warp >= 8) {
+   ptx::regs_dec<kOtherRegs>();
+   if (skip) {
     // nothing issued, nothing to drain
-  } else if (warp == 0) {
+   } else if (warp == 8) {
     // ------------------------------------------------------------ producer
-    int n_issued = 0;
-    const bool need_codes = p.mask.kind != ATTN_MASK_CAUSAL;
+    PairWalk walk = walk0;
+    int nload = 0, ntail = 0;
+    bool tail_pending = false;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
       ptx::prefetch_tensormap(&tmK);
       ptx::prefetch_tensormap(&tmV);
-      ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
+      ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE * (has1 ? 2 : 1));
       for (int c = 0; c < C::NCH; ++c)
-        ptx::tma_load_3d(sQ + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, h, s0 + i0);
+        ptx::tma_load_3d(sQ0 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, h, s0 + qi0);
+      if (has1)
+        for (int c = 0; c < C::NCH; ++c)
+          ptx::tma_load_3d(sQ1 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, h, s0 + qi0 + kTile);
     }
-    for (int it = 0; it < n; ++it) {
-      const int st = it % C::NST;
-      const uint32_t ph = uint32_t(it / C::NST) & 1u;
-      if (it >= C::NST && !warp_wait(bar(C::B_EMPTY + st), ph ^ 1u, abort_flag, err, 1)) break;
-      const int kt = p.kidx[e0 + it];
-      const int lab = p.klabel[e0 + it];
-      const int j0 = kt * kTile;
-      if (need_codes && lab == ATTN_TILE_PARTIAL) {
-        for (int c = lane; c < kTile; c += 32)
-          kcode[st * kTile + c] = (j0 + c < L) ? key_code(p.mask, s0 + j0 + c) : 0;
-      }
-      __syncwarp();
+    int kt, la, lb;
+    while (walk.next(p.kidx, p.klabel, kt, la, lb)) {
+      const int j0 = kt * kTile, kn = min(kTile, L - j0);
+      // K(j)
+      int slot = nload % C::NSLOT;
+      if (nload >= C::NSLOT &&
+          !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1))
+        break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::TILE);
+        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sK + st * C::TILE + c * C::CHUNK, &tmK, bar(C::B_KFULL + st), c * C::CE,
-                           h, s0 + j0);
-        ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sV + st * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VFULL + st), c * C::CE,
-                           h, s0 + j0);
+          ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmK, bar(C::B_FULL + slot),
+                           c * C::CE, h, s0 + j0);
       }
-      n_issued = it + 1;
+      ++nload;
+      // V(j)
+      slot = nload % C::NSLOT;
+      if (nload >= C::NSLOT &&
+          !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1))
+        break;
+      if (kn < kTile) {
+        // Rows past the sequence end come from the next sequence (or are zero
+        // past the tensor).  Their P is exactly 0, but 0 * inf is NaN, so they
+        // are zeroed before the P.V product may read them.
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(bar(C::B_VTMA), C::TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VTMA), c * C::CE,
+                             h, s0 + j0);
+        }
+        tail_pending = true;
+        if (!warp_wait(bar(C::B_VTMA), uint32_t(ntail) & 1u, abort_flag, err, 2)) break;
+        tail_pending = false;
+        ++ntail;
+        for (int rr = kn + lane; rr < kTile; rr += 32) {
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK +
+                                                  rr * C::ROWB);
+#pragma unroll
+            for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(C::B_FULL + slot));
+      } else if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_FULL + slot),
+                           c * C::CE, h, s0 + j0);
+      }
+      ++nload;
     }
     // Do not leave while a load this CTA issued may still be writing shared memory.
     if (lane == 0) {
-      for (int s = 0; s < C::NST; ++s) {
-        if (n_issued <= s) continue;
-        const int last = s + C::NST * ((n_issued - 1 - s) / C::NST);  // last load into stage s
-        const uint32_t ph = uint32_t(last / C::NST) & 1u;
-        drain_bar(bar(C::B_KFULL + s), ph, err);
-        drain_bar(bar(C::B_VFULL + s), ph, err);
+      for (int s = 0; s < C::NSLOT; ++s) {
+        if (nload <= s) continue;
+        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);  // last load into slot s
+        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
       }
+      if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
       drain_bar(bar(C::B_Q), 0, err);
     }
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, err, 3);
-      for (int it = 0; ok && it <= n; ++it) {
-        if (it < n) {
-          const int st = it % C::NST;
-          if (!wait_bar(bar(C::B_KFULL + st), uint32_t(it / C::NST) & 1u, abort_flag, err, 4)) break;
+      PairWalk walk = walk0;
+      int kt, a, bl;
+      bool have = wait_bar(bar(C::B_Q), 0, abort_flag, err, 3) && walk.next(p.kidx, p.klabel, kt, a, bl);
+      int nload = 0, c0 = 0, c1 = 0;
+      if (have) {
+        if (!wait_bar(bar(C::B_FULL + 0), 0, abort_flag, err, 4)) {
+          have = false;
+        } else {
           ptx::tc_fence_after();
-          const uint32_t dS = tmem + C::COL_S0 + uint32_t(it & 1) * 128u;
-          const uint32_t kb = sK + st * C::TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            ptx::mma_ss(dS, kmajor_desc<D>(sQ, kk), kmajor_desc<D>(kb, kk), C::IDESC_S, kk > 0);
-          ptx::mma_commit(bar(C::B_SFULL + (it & 1)));
+          if (a) { issue_s<D>(tmem + C::col_s(0), sQ0, sRing); ptx::mma_commit(bar(C::B_SFULL + 0)); }
+          if (bl) { issue_s<D>(tmem + C::col_s(1), sQ1, sRing); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          ptx::mma_commit(bar(C::B_EMPTY + 0));
+          nload = 1;
         }
-        if (it >= 1) {
-          const int j = it - 1, st = j % C::NST;
-          if (!wait_bar(bar(C::B_PFULL + (j & 1)), uint32_t(j >> 1) & 1u, abort_flag, err, 5)) break;
-          if (!wait_bar(bar(C::B_VFULL + st), uint32_t(j / C::NST) & 1u, abort_flag, err, 6)) break;
+      }
+      while (have) {
+        int kt2, a2, b2;
+        const bool nxt = walk.next(p.kidx, p.klabel, kt2, a2, b2);
+        const int vslot = nload % C::NSLOT, kslot = (nload + 1) % C::NSLOT;
+        const uint32_t vph = uint32_t(nload / C::NSLOT) & 1u;
+        const uint32_t kph = uint32_t((nload + 1) / C::NSLOT) & 1u;
+        const uint32_t vaddr = sRing + vslot * C::TILE, kaddr = sRing + kslot * C::TILE;
+        bool vready = false, kready = false;
+        if (a) {
+          if (!wait_bar(bar(C::B_PFULL + 0), uint32_t(c0) & 1u, abort_flag, err, 5)) break;
+          if (!wait_bar(bar(C::B_FULL + vslot), vph, abort_flag, err, 6)) break;
+          vready = true;
           ptx::tc_fence_after();
-          const uint32_t aP = tmem + C::COL_S0 + uint32_t(j & 1) * 128u;
-          const uint32_t vb = sV + st * C::TILE;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            ptx::mma_ts(tmem + C::COL_O, aP + uint32_t(kk) * 8u, v_desc<D>(vb, kk), C::IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(C::B_EMPTY + st));
-          ptx::mma_commit(bar(C::B_ODONE));
+          issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vaddr, c0 > 0);
+          ptx::mma_commit(bar(C::B_ODONE + 0));
+          ++c0;
         }
+        if (nxt) {
+          if (!wait_bar(bar(C::B_FULL + kslot), kph, abort_flag, err, 4)) break;
+          kready = true;
+          ptx::tc_fence_after();
+          if (a2) { issue_s<D>(tmem + C::col_s(0), sQ0, kaddr); ptx::mma_commit(bar(C::B_SFULL + 0)); }
+        }
+        if (bl) {
+          if (!wait_bar(bar(C::B_PFULL + 1), uint32_t(c1) & 1u, abort_flag, err, 5)) break;
+          if (!vready && !wait_bar(bar(C::B_FULL + vslot), vph, abort_flag, err, 6)) break;
+          ptx::tc_fence_after();
+          issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vaddr, c1 > 0);
+          ptx::mma_commit(bar(C::B_ODONE + 1));
+          ++c1;
+        }
+        ptx::mma_commit(bar(C::B_EMPTY + vslot));
+        ++nload;
+        if (nxt && kready) {
+          if (b2) { issue_s<D>(tmem + C::col_s(1), sQ1, kaddr); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          ptx::mma_commit(bar(C::B_EMPTY + kslot));
+          ++nload;
+        }
+        a = a2;
+        bl = b2;
+        have = nxt;
       }
       // Every MMA issued above has finished once this commit arrives.
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-  } else {
+   }  // warps 10-11 idle
+  } else if (!skip) {
+    ptx::regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                   // which q-tile of the pair
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;         // query row inside the tile
+    const bool present = t == 0 || has1;
+    const int it0 = qi0 + t * kTile;           // first row of this q-tile (local)
+    const int qn = present ? min(kTile, L - it0) : 0;
     const bool row_in = r < qn;
-    const int il = i0 + r;                     // local query index
-    const int qcode = (row_in && p.mask.kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
+    const int il = it0 + r;                    // local query index
+    const int kind = p.mask.kind;
+    const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
     const float c2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;
+    int cnt = 0;
     bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int sb = it & 1, st = it % C::NST;
-      const int kt = p.kidx[e0 + it];
-      const int lab = p.klabel[e0 + it];
+    PairWalk walk = walk0;
+    int kt, la, lb;
+    while (present && walk.next(p.kidx, p.klabel, kt, la, lb)) {
+      const int lab = t == 0 ? la : lb;
+      if (lab == ATTN_TILE_EMPTY) continue;
       const int j0 = kt * kTile;
-      if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(it >> 1) & 1u, abort_flag, err, 8)) { ok = false; break; }
-      ptx::tc_fence_after();
       const int kn = min(kTile, L - j0);
+      if (!warp_wait(bar(C::B_SFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 8)) { ok = false; break; }
+      ptx::tc_fence_after();
       float s[128];
       {
         uint32_t v[4][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(lane_base + C::COL_S0 + sb * 128 + q * 32, v[q]);
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(lane_base + colS + q * 32, v[q]);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -329,100 +462,97 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
         // bit c of vis[c / 32]: key column c is visible to this row.  Causal part
-        // and bounds together: columns c < upto.  PARTIAL tiles of the
-        // metadata kinds also AND in the per-key predicate.
+        // and bounds: columns c < upto; PARTIAL tiles of the metadata kinds also
+        // AND in the per-key predicate.
         const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
         uint32_t vis[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
-        if (lab == ATTN_TILE_PARTIAL && p.mask.kind != ATTN_MASK_CAUSAL) {
-          if (!warp_wait(bar(C::B_KFULL + st), uint32_t(it / C::NST) & 1u, abort_flag, err, 9)) { ok = false; break; }
-          const int* kc = kcode + st * kTile;
-          switch (p.mask.kind) {
-            case ATTN_MASK_CAUSAL_DOCUMENT:
+        if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+          const int k0tok = s0 + j0;
+          if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(kc + 32 * q, qcode);
-              break;
-            case ATTN_MASK_SHARED_PREFIX:
+            for (int q = 0; q < 4; ++q)
+              if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(p.mask, k0tok, q, kn, qcode);
+          } else if (kind == ATTN_MASK_SHARED_PREFIX) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(kc + 32 * q, qcode);
-              break;
-            default:
+            for (int q = 0; q < 4; ++q)
+              if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(p.mask, k0tok, q, kn, qcode);
+          } else {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(kc + 32 * q, qcode);
-              break;
+            for (int q = 0; q < 4; ++q)
+              if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(p.mask, k0tok, q, kn, qcode);
           }
         }
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (vis[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
       }
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float mx4[4];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], s[c]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float m_new = fmaxf(m, mx * c2);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ptx::ex2(m - m_use);
-      float sum2[2] = {0.f, 0.f};
-      uint32_t pk[2][32];
+      for (int u = 0; u < 4; ++u) {
+        float mv = s[32 * u];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = ptx::ex2(fmaf(s[c], c2, -m_use));
-        const float p1 = ptx::ex2(fmaf(s[c + 1], c2, -m_use));
-        sum2[(c >> 1) & 1] += p0 + p1;
-        pk[c >> 6][(c & 63) >> 1] = ptx::pack_bf16(p0, p1);
+        for (int c = 1; c < 31; c += 2) mv = ptx::fmax3(mv, s[32 * u + c], s[32 * u + c + 1]);
+        mx4[u] = fmaxf(mv, s[32 * u + 31]);
       }
-      const float sum = sum2[0] + sum2[1];
-      l = l * alpha + sum;
-      m = m_new;
-      if (it > 0) {
-        // O must hold exactly PV of tiles < it before it is rescaled.
-        if (!warp_wait(bar(C::B_ODONE), uint32_t(it - 1) & 1u, abort_flag, err, 10)) { ok = false; break; }
+      const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+      const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
+      const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
+      const float m_new = raise ? mxs : m_ref;
+      const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
+      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O must hold exactly the P.V of earlier entries before it is rescaled.
+        if (!warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 10)) { ok = false; break; }
         ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          ptx::tmem_ld32(lane_base + colO + q * 32, v);
+          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t v[32];
-            ptx::tmem_ld32(lane_base + C::COL_O + q * 32, v);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-            ptx::tmem_st32(lane_base + C::COL_O + q * 32, v);
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = ptx::fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), a2);
+            v[c] = __float_as_uint(x.x);
+            v[c + 1] = __float_as_uint(x.y);
           }
+          ptx::tmem_st32(lane_base + colO + q * 32, v);
         }
       }
-      ptx::tmem_st32(lane_base + C::COL_S0 + sb * 128, pk[0]);
-      ptx::tmem_st32(lane_base + C::COL_S0 + sb * 128 + 32, pk[1]);
-      if (kn < kTile) {
-        // Rows past the sequence end were loaded from the next sequence (or
-        // zero-filled past the tensor).  Their P is exactly 0, but 0 * inf is
-        // NaN, so the V rows are zeroed before the P.V product reads them.
-        if (!warp_wait(bar(C::B_VFULL + st), uint32_t(it / C::NST) & 1u, abort_flag, err, 12)) { ok = false; break; }
-        if (r >= kn) {
+      l *= alpha;
+      m_ref = m_new;
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
-            uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_V + st * C::TILE + c * C::CHUNK + r * C::ROWB);
+      for (int hh = 0; hh < 4; ++hh) {
+        uint32_t pk[16];
 #pragma unroll
-            for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
-          }
+        for (int c = 0; c < 32; c += 2) {
+          const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
+          const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+          sum2 = ptx::fadd2(sum2, e);
+          pk[c >> 1] = ptx::pack_bf16(e.x, e.y);
         }
-        ptx::fence_proxy_async_smem();
+        ptx::tmem_st16(lane_base + colS + hh * 16, pk);
       }
+      l += sum2.x + sum2.y;
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_PFULL + sb));
+      ptx::mbar_arrive(bar(C::B_PFULL + t));
+      ++cnt;
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && n > 0) ok = warp_wait(bar(C::B_ODONE), uint32_t(n - 1) & 1u, abort_flag, err, 11);
-    if (ok) {
+    if (present && ok && cnt > 0) ok = warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 11);
+    if (present && ok) {
       ptx::tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + h) * D;
-#pragma unroll
+#pragma unroll 1
       for (int q = 0; q < D / 32; ++q) {
         uint32_t v[32];
-        if (n > 0) {
-          ptx::tmem_ld32(lane_base + C::COL_O + q * 32, v);
+        if (cnt > 0) {
+          ptx::tmem_ld32(lane_base + colO + q * 32, v);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
@@ -439,13 +569,13 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (row_in)
-        p.lse[size_t(h) * p.T + s0 + il] = l > 0.f ? (m + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[size_t(h) * p.T + s0 + il] = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -487,17 +617,23 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   if (!make_map<D>(&mq, a.q, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mk, a.k, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads))
-    return ATTN_ERR_CUDA;
+    return record_cuda_error(cudaErrorInvalidValue, "attn_fwd tensor map encoding");
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_ALLOC) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    // The warpgroups' register split assumes the kernel launches with exactly
+    // kLaunchRegs per thread; anything else could leave setmaxnreg.inc waiting.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_bf16_kernel<D>);
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
+    if (fa.numRegs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+    e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
     configured = true;
   }
   FwdParams p;
   p.header = a.bm.header;
-  p.order = a.bm.order;
+  p.pair_order = a.bm.pair_order;
+  p.pair_q0 = a.bm.pair_q0;
   p.qt_seq = a.bm.qt_seq;
   p.qt_idx = a.bm.qt_idx;
   p.koff = a.bm.koff;
@@ -510,10 +646,12 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  // the pair count is only known on the device; max_qt bounds it
   const long long grid = (long long)a.bm.max_qt * a.num_heads;
   if (grid <= 0 || grid > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  attn_fwd_bf16_kernel<D><<<unsigned(grid), 192, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  attn_fwd_bf16_kernel<D><<<unsigned(grid), kThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");
 }
 
 }  // namespace

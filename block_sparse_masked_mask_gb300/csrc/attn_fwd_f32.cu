@@ -126,9 +126,9 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
                       kChunk * sizeof(int);
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(attn_fwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem)) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_fwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
     configured = true;
   }
   F32Params p;
@@ -152,7 +152,8 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   const long long grid = (long long)a.bm.max_qt * a.num_heads;
   if (grid <= 0 || grid > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   attn_fwd_f32_kernel<D><<<unsigned(grid), 128, smem, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");
 }
 
 }  // namespace

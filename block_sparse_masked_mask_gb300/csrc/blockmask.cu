@@ -35,13 +35,44 @@ __device__ __forceinline__ int warp_max(int x) {
   return x;
 }
 
-// 1 CTA: validate cu_seqlens, per-sequence q-tile offsets, q-tile -> (seq, idx).
+// Block-wide exclusive prefix sum of one value per thread (blockDim.x a
+// multiple of 32, at most 1024); returns the prefix and sets *total.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int before = (warp ? s_warp[warp - 1] : 0) + incl - x;
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return before;
+}
+
+// 1 CTA: validate cu_seqlens; per-sequence q-tile and q-tile-pair offsets;
+// q-tile -> (seq, idx); pair -> first q-tile.  A pair is q-tiles (2j, 2j+1)
+// of one sequence (the second is absent when the sequence has an odd count).
 __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
   __shared__ int s_err;
   __shared__ int s_warp[32];
   __shared__ int s_carry;
+  __shared__ int s_pcarry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  if (tid == 0) { s_err = 0; s_carry = 0; }
+  if (tid == 0) { s_err = 0; s_carry = 0; s_pcarry = 0; }
   __syncthreads();
   const int B = v.batch;
   int err = 0;
@@ -62,37 +93,25 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
     const int b = base + tid;
     int nt = 0;
     if (!bad && b < B) nt = (v.cu[b + 1] - v.cu[b] + kTile - 1) / kTile;
-    int incl = nt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int w = lane < nw ? s_warp[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
-      }
-      if (lane < nw) s_warp[lane] = w;  // inclusive warp prefix
+    int tot_t, tot_p;
+    const int bt = block_exclusive_scan(nt, s_warp, &tot_t);
+    const int bp = block_exclusive_scan((nt + 1) / 2, s_warp, &tot_p);
+    if (b < B) {
+      v.qt_off[b] = s_carry + bt;
+      v.pair_off[b] = s_pcarry + bp;
     }
     __syncthreads();
-    const int before = (warp ? s_warp[warp - 1] : 0) + incl - nt;
-    if (b < B) v.qt_off[b] = s_carry + before;
-    __syncthreads();
-    if (tid == 0) s_carry += s_warp[nw - 1];
+    if (tid == 0) { s_carry += tot_t; s_pcarry += tot_p; }
     __syncthreads();
   }
-  const int n_qt = s_carry;
+  const int n_qt = s_carry, n_pairs = s_pcarry;
   if (tid == 0) {
     v.qt_off[B] = n_qt;
+    v.pair_off[B] = n_pairs;
     v.header[kHdrQtiles] = n_qt;
     v.header[kHdrEntries] = 0;
     v.header[kHdrError] = bad;
-    v.header[3] = 0;
+    v.header[kHdrPairs] = n_pairs;
     v.header[kHdrEmpty] = 0;
     v.header[kHdrPartial] = 0;
     v.header[kHdrFull] = 0;
@@ -108,6 +127,14 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
     }
     v.qt_seq[g] = lo;
     v.qt_idx[g] = g - v.qt_off[lo];
+  }
+  for (int p = tid; p < n_pairs; p += blockDim.x) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (v.pair_off[mid] <= p) lo = mid; else hi = mid;
+    }
+    v.pair_q0[p] = v.qt_off[lo] + 2 * (p - v.pair_off[lo]);
   }
 }
 
@@ -190,11 +217,16 @@ __device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
 }
 
 // One CTA per q-tile: labels of its whole row, and its non-EMPTY count.
+// Each thread decides one k-tile from the summaries; only the pairs the
+// summaries leave undecided are counted pair by pair, one at a time.
 __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) {
   const int g = blockIdx.x;
   if (g >= v.header[kHdrQtiles]) return;
   __shared__ int s_kcode[kTile];
   __shared__ int s_red[4];
+  __shared__ int s_unknown[kTile];
+  __shared__ int s_nunk;
+  __shared__ uint8_t s_lab[kTile];
   const int b = v.qt_seq[g], a = v.qt_idx[g];
   const int s0 = v.cu[b], L = v.cu[b + 1] - s0;
   const int nt = (L + kTile - 1) / kTile;
@@ -202,23 +234,31 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
   const bool row_in = r < qn;
   const int qcode = row_in ? query_code(m, s0 + i0 + r) : 0;
-  int sq[kSumInts], sk[kSumInts];
+  int sq[kSumInts];
   const int* qsum = v.summary + size_t(g) * kSumInts;
   for (int i = 0; i < kSumInts; ++i) sq[i] = m.kind == ATTN_MASK_CAUSAL ? 0 : qsum[i];
   const int gbase = v.qt_off[b];
   uint8_t* row = v.labels + size_t(g) * v.max_nt;
-  int n_empty = 0, n_partial = 0, n_full = 0;
-  for (int bt = 0; bt < nt; ++bt) {
-    const int j0 = bt * kTile, j1 = min(L, j0 + kTile) - 1, kn = j1 - j0 + 1;
-    if (m.kind != ATTN_MASK_CAUSAL) {
+  int n_empty = 0, n_partial = 0, n_full = 0;  // meaningful in thread 0
+  for (int c0 = 0; c0 < nt; c0 += kTile) {
+    const int bt = c0 + r;
+    int lab = ATTN_TILE_EMPTY;
+    if (r == 0) s_nunk = 0;
+    __syncthreads();
+    if (bt < nt) {
+      int sk[kSumInts];
       const int* ks = v.summary + size_t(gbase + bt) * kSumInts;
-      for (int i = 0; i < kSumInts; ++i) sk[i] = ks[i];
-    } else {
-      for (int i = 0; i < kSumInts; ++i) sk[i] = 0;
+      for (int i = 0; i < kSumInts; ++i) sk[i] = m.kind == ATTN_MASK_CAUSAL ? 0 : ks[i];
+      const int j0 = bt * kTile, j1 = min(L, j0 + kTile) - 1;
+      lab = decide(m.kind, i0, i1, j0, j1, sq, sk);
+      if (lab == kUnknown) s_unknown[atomicAdd(&s_nunk, 1)] = r;
     }
-    int lab = decide(m.kind, i0, i1, j0, j1, sq, sk);
-    if (lab == kUnknown) {
-      __syncthreads();
+    s_lab[r] = uint8_t(lab < 0 ? 0 : lab);
+    __syncthreads();
+    const int nunk = s_nunk;
+    for (int u = 0; u < nunk; ++u) {
+      const int bu = c0 + s_unknown[u];
+      const int j0 = bu * kTile, kn = min(L, j0 + kTile) - j0;
       if (r < kn) s_kcode[r] = key_code(m, s0 + j0 + r);
       __syncthreads();
       int cnt = 0;
@@ -229,13 +269,28 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
       cnt = warp_sum(cnt);
       if (lane == 0) s_red[warp] = cnt;
       __syncthreads();
-      const int total = s_red[0] + s_red[1] + s_red[2] + s_red[3];
-      lab = total == 0 ? ATTN_TILE_EMPTY : (total == qn * kn ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL);
+      if (r == 0) {
+        const int total = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+        s_lab[s_unknown[u]] = uint8_t(total == 0 ? ATTN_TILE_EMPTY
+                                                 : (total == qn * kn ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL));
+      }
+      __syncthreads();
     }
-    n_empty += lab == ATTN_TILE_EMPTY;
-    n_partial += lab == ATTN_TILE_PARTIAL;
-    n_full += lab == ATTN_TILE_FULL;
-    if (r == 0) row[bt] = uint8_t(lab);
+    if (bt < nt) row[bt] = s_lab[r];
+    const int fl = bt < nt ? s_lab[r] : -1;
+    const int e = warp_sum(fl == ATTN_TILE_EMPTY), pa = warp_sum(fl == ATTN_TILE_PARTIAL),
+              fu = warp_sum(fl == ATTN_TILE_FULL);
+    __syncthreads();
+    if (lane == 0) { s_red[warp] = e | (pa << 10) | (fu << 20); }
+    __syncthreads();
+    if (r == 0) {
+      for (int w = 0; w < 4; ++w) {
+        n_empty += s_red[w] & 1023;
+        n_partial += (s_red[w] >> 10) & 1023;
+        n_full += (s_red[w] >> 20) & 1023;
+      }
+    }
+    __syncthreads();
   }
   if (r == 0) {
     v.kcount[g] = n_partial + n_full;
@@ -325,6 +380,27 @@ __global__ void __launch_bounds__(128) bm_fill_kernel(BmView v) {
   if (lane == 0) s_warp[warp] = ahead;
   __syncthreads();
   if (r == 0) v.order[s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3]] = g;
+  // The CTA of a pair's first q-tile places the pair in the longest-first
+  // pair order (work = kcount of both q-tiles, ties by pair number).
+  const int qa = v.qt_idx[g];
+  if (qa & 1) return;
+  auto pair_work = [&](int g0) {
+    const bool two = g0 + 1 < n_qt && v.qt_seq[g0 + 1] == v.qt_seq[g0];
+    return v.kcount[g0] + (two ? v.kcount[g0 + 1] : 0);
+  };
+  const int n_pairs = v.header[kHdrPairs];
+  const int p = v.pair_off[b] + qa / 2;
+  const int wp = pair_work(g);
+  int pahead = 0;
+  for (int p2 = r; p2 < n_pairs; p2 += blockDim.x) {
+    const int w2 = pair_work(v.pair_q0[p2]);
+    pahead += (w2 > wp) || (w2 == wp && p2 < p);
+  }
+  pahead = warp_sum(pahead);
+  __syncthreads();
+  if (lane == 0) s_warp[warp] = pahead;
+  __syncthreads();
+  if (r == 0) v.pair_order[s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3]] = p;
 }
 
 }  // namespace

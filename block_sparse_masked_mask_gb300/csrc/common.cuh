@@ -25,8 +25,8 @@ enum : int32_t {
   kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong,
 };
 
-enum : int { kHdrQtiles = 0, kHdrEntries = 1, kHdrError = 2, kHdrEmpty = 4, kHdrPartial = 5,
-             kHdrFull = 6, kHdrInts = 8 };
+enum : int { kHdrQtiles = 0, kHdrEntries = 1, kHdrError = 2, kHdrPairs = 3, kHdrEmpty = 4,
+             kHdrPartial = 5, kHdrFull = 6, kHdrInts = 8 };
 
 enum : int { kSumInts = 8 };  // ints per tile summary
 
@@ -34,7 +34,8 @@ enum : int { kSumInts = 8 };  // ints per tile summary
 struct BmLayout {
   int max_qt = 0, max_nt = 0;
   uint64_t header = 0, qt_seq = 0, qt_idx = 0, labels = 0, kcount = 0, koff = 0, kidx = 0,
-           klabel = 0, order = 0, qt_off = 0, summary = 0, total = 0;
+           klabel = 0, order = 0, qt_off = 0, summary = 0, pair_off = 0, pair_q0 = 0,
+           pair_order = 0, total = 0;
 };
 
 // Returns false on overflow / invalid sizes.
@@ -53,6 +54,9 @@ struct BmView {
   int32_t* order;
   int32_t* qt_off;
   int32_t* summary;
+  int32_t* pair_off;
+  int32_t* pair_q0;
+  int32_t* pair_order;
   const int32_t* cu;
   int max_qt, max_nt, batch, total_tokens, max_seqlen;
 };
@@ -100,6 +104,9 @@ __device__ __forceinline__ bool code_visible(int kind, int qcode, int kcode) {
     default: return true;
   }
 }
+
+// Remember a CUDA failure for attn_last_error_message(); returns ATTN_ERR_CUDA.
+attn_status record_cuda_error(cudaError_t e, const char* where);
 
 // Launchers (return a cudaError_t of the launch).
 cudaError_t launch_block_mask_build(const BmView& v, const MaskArgs& m, cudaStream_t s);

@@ -107,8 +107,8 @@ typedef struct attn_mask_params {
  * Byte offsets (off_*) are from the workspace base; array sizes are in the
  * comments, with NQ = max_qtiles and NK = max_ktiles.
  *   off_header  int32[8]: [0] n_qtiles, [1] n_entries (sum of kcount),
- *               [2] error bits, [3] reserved, [4] EMPTY, [5] PARTIAL,
- *               [6] FULL pair totals, [7] reserved
+ *               [2] error bits, [3] n_qpairs, [4] EMPTY, [5] PARTIAL,
+ *               [6] FULL tile-pair totals, [7] reserved
  *   off_qt_seq  int32[NQ]       sequence of each q-tile (q-tiles are numbered
  *                               sequence-major, ascending inside a sequence)
  *   off_qt_idx  int32[NQ]       index of the q-tile inside its sequence
@@ -121,6 +121,12 @@ typedef struct attn_mask_params {
  *   off_order   int32[NQ]       q-tiles by descending kcount, ties by index
  *   off_qt_off  int32[batch+1]  first q-tile number of each sequence
  *   off_summary int32[NQ * 8]   per-tile metadata summary used by the classifier
+ *   off_pair_off   int32[batch+1]  first q-tile-pair number of each sequence
+ *   off_pair_q0    int32[NQ]       first q-tile of each q-tile pair; a pair is
+ *                                  q-tiles (2j, 2j+1) of one sequence, the second
+ *                                  absent when the sequence has an odd count
+ *   off_pair_order int32[NQ]       q-tile pairs by descending summed kcount,
+ *                                  ties by pair number (the forward's schedule)
  */
 typedef struct attn_block_mask {
   uint32_t magic;          /* set by the builder; checked by attn_fwd */
@@ -137,7 +143,8 @@ typedef struct attn_block_mask {
   void* workspace;
   size_t workspace_bytes;
   uint64_t off_header, off_qt_seq, off_qt_idx, off_labels, off_kcount, off_koff,
-      off_kidx, off_klabel, off_order, off_qt_off, off_summary;
+      off_kidx, off_klabel, off_order, off_qt_off, off_summary, off_pair_off, off_pair_q0,
+      off_pair_order;
 } attn_block_mask;
 
 /*
@@ -209,6 +216,14 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  * next attn_block_mask_build() on the same workspace.
  */
 ATTN_API attn_status attn_get_status(const attn_block_mask* bm, attn_stream_t stream);
+
+/*
+ * The CUDA runtime's message for the last CUDA failure this library saw on the
+ * calling thread (the one behind the most recent ATTN_ERR_CUDA), or "" if none.
+ * The string is owned by the library and stays valid until the next call on
+ * this thread.
+ */
+ATTN_API const char* attn_last_error_message(void);
 
 /* Static, NUL-terminated description of a status code. */
 ATTN_API const char* attn_status_string(attn_status status);

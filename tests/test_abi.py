@@ -19,7 +19,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = set(declared_functions())
     assert {"attn_block_mask_workspace_size", "attn_block_mask_build", "attn_fwd",
-            "attn_get_status", "attn_status_string", "attn_version"} <= names
+            "attn_get_status", "attn_status_string", "attn_version",
+            "attn_last_error_message"} <= names
 
 
 def test_library_exports_every_declared_symbol(native_lib):

@@ -42,6 +42,13 @@ def assert_matches_oracle(w, bm):
     f, p, e = oracle.label_totals(labels)
     assert got["header"][4:7].tolist() == [e, p, f]
     assert int(got["header"][1]) == int(want["koff"][-1])
+    # q-tile pairs: tiles (2j, 2j+1) of one sequence, ordered by summed work
+    q0 = [g for g in range(n) if want["qt_idx"][g] % 2 == 0]
+    assert int(got["header"][3]) == len(q0)
+    assert got["pair_q0"].tolist() == q0
+    work = [int(want["kcount"][g]) + (int(want["kcount"][g + 1])
+            if g + 1 < n and want["qt_seq"][g + 1] == want["qt_seq"][g] else 0) for g in q0]
+    assert got["pair_order"].tolist() == oracle.lpt_order(work).tolist()
 
 
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
