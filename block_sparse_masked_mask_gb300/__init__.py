@@ -5,6 +5,7 @@ in ``include/attn_block_mask.h``); this package is its thin Python binding
 plus the seeded synthetic workloads used by the tests and the benchmark.
 """
 from .api import (AttnError, BlockMask, MASK_KINDS, TILE_EMPTY, TILE_FULL,  # noqa: F401
-                  TILE_PARTIAL, attn_block_mask_build, attn_block_mask_workspace_size,
+                  TILE_PARTIAL, attn_block_mask_build, attn_block_mask_build_noalloc,
+                  attn_block_mask_workspace_size,
                   attn_fwd, attn_get_status, attn_last_error_message, attn_status_string,
                   attn_version)

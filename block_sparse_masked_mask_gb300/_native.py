@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, ctypes.c_size_t,
         P(AttnBlockMask), c_void_p]
     L.attn_block_mask_build.restype = ctypes.c_int
+    L.attn_block_mask_build_noalloc.argtypes = L.attn_block_mask_build.argtypes
+    L.attn_block_mask_build_noalloc.restype = ctypes.c_int
     L.attn_fwd.argtypes = [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, ctypes.c_int, c_int32, c_int32,
         c_int32, ctypes.c_float, c_void_p, c_int32, c_int32, ctypes.c_int, P(AttnMaskParams),

@@ -139,6 +139,32 @@ def attn_block_mask_build(kind, cu_seqlens: torch.Tensor, total_tokens: int, max
     return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn))
 
 
+def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: int,
+                                  max_seqlen: int, workspace: torch.Tensor,
+                                  seg_id: Optional[torch.Tensor] = None,
+                                  role: Optional[torch.Tensor] = None,
+                                  turn: Optional[torch.Tensor] = None, role_think: int = 1,
+                                  stream=None) -> BlockMask:
+    """Block-mask build that allocates nothing, for callers that cannot.
+
+    The caller passes the output buffer ``workspace`` (at least
+    ``attn_block_mask_workspace_size`` bytes); the builder's temporaries use a
+    fixed 4 MiB array inside the library, shared by every call on the device,
+    so calls must not overlap on the GPU.  The first call on a device does a
+    one-time address lookup and should come before any stream capture.  Only
+    the arrays the forward reads are stored (``labels`` is not).
+    """
+    batch = cu_seqlens.numel() - 1
+    params = _native.AttnMaskParams(role_think)
+    out = _native.AttnBlockMask()
+    _check(_native.lib().attn_block_mask_build_noalloc(
+        _kind(kind), ctypes.byref(params), _ptr(cu_seqlens), batch, total_tokens, max_seqlen,
+        _ptr(seg_id), _ptr(role), _ptr(turn), BLOCK_M, BLOCK_N, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(out), _stream(stream)),
+        "attn_block_mask_build_noalloc")
+    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn))
+
+
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, kind,
              cu_seqlens: torch.Tensor, max_seqlen: int, seg_id=None, role=None, turn=None,
              role_think: int = 1, scale: float = 0.0, out: Optional[torch.Tensor] = None,

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libattnmask.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["api.cu", "blockmask.cu", "attn_fwd_bf16.cu", "attn_fwd_f32.cu"]
+SOURCES = ["api.cu", "blockmask.cu", "blockmask_noalloc.cu", "attn_fwd_bf16.cu", "attn_fwd_f32.cu"]
 HEADERS = ["common.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = [

@@ -210,6 +210,34 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_stream_t stream);
 
 /*
+ * Same as attn_block_mask_build(), for callers that cannot allocate device
+ * memory (a host memory manager that owns every device byte, or a loop where
+ * an allocation and its implicit synchronisation are not allowed).  The pages
+ * have no counterpart: this is a deployment variant of the builder.
+ *   - Same arguments and the same output: the block-mask arrays attn_fwd()
+ *     reads (header, q-tile descriptors, kcount, koff, kidx, klabel, order,
+ *     q-tile pairs) are written to `workspace` at the usual offsets
+ *     (workspace_bytes >= attn_block_mask_workspace_size()).
+ *   - The builder's temporary arrays (tile summaries, the dense tile-label
+ *     matrix, per-sequence offsets) live in a fixed 4 MiB device array inside
+ *     the library instead; they are not kept, so off_labels, off_summary,
+ *     off_qt_off and off_pair_off name unwritten workspace regions.
+ *   - Needs max_qtiles * max_ktiles + 32 * max_qtiles + 8 * (batch + 1) bytes
+ *     of that array (each part rounded up to 256); larger problems return
+ *     ATTN_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on a device looks up the array's address with that device
+ *     current; make that first call before any stream capture.
+ *   - All calls on a device share the array: calls whose kernels overlap on the
+ *     GPU race and must be serialised by the caller.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+ATTN_API attn_status attn_block_mask_build_noalloc(
+    attn_mask_kind kind, const attn_mask_params* params, const int32_t* cu_seqlens, int32_t batch,
+    int32_t total_tokens, int32_t max_seqlen, const int32_t* seg_id, const int8_t* role,
+    const int32_t* turn, int32_t block_m, int32_t block_n, void* workspace, size_t workspace_bytes,
+    attn_block_mask* out, attn_stream_t stream);
+
+/*
  * Synchronise `stream`, then report the device error word of `bm` (and any
  * pending CUDA error): ATTN_OK, ATTN_ERR_DEVICE_INVALID_INPUT,
  * ATTN_ERR_DEVICE_TIMEOUT or ATTN_ERR_CUDA.  The error word is cleared by the
