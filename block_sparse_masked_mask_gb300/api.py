@@ -89,7 +89,7 @@ class BlockMask:
         return raw.view(dtype).cpu()
 
     def header(self) -> torch.Tensor:
-        return self._array(self.struct.off_header, 8, torch.int32)
+        return self._array(self.struct.off_header, 16, torch.int32)
 
     @property
     def n_qtiles(self) -> int:

@@ -7,8 +7,9 @@
 // k-tiles the block mask lists are visited (Ch. 9, Section 9.2: a skipped
 // tile is never loaded).
 //
-// One CTA handles one work item: a pair of adjacent 128-row q-tiles of one
-// sequence (the second may be absent) and one head.  The pair walks the
+// A work item is a pair of adjacent 128-row q-tiles of one sequence (the
+// second may be absent) and one head; persistent CTAs (one per SM) loop over
+// the items.  The pair walks the
 // ascending union of its two k-tile lists; each K and V tile is loaded once
 // and serves both q-tiles, and a q-tile skips the entries its own list does
 // not hold (EMPTY for it).  Warp roles:
@@ -61,12 +62,15 @@ struct Cfg {
   static constexpr uint32_t SW = D >= 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
   static constexpr int SBO = 8 * ROWB;                // 8-row core-matrix group stride
   static constexpr int OFF_Q0 = 0, OFF_Q1 = TILE, OFF_RING = 2 * TILE;
-  static constexpr int B_Q = 0, B_FULL = 1, B_EMPTY = 1 + NSLOT, B_VTMA = 1 + 2 * NSLOT,
+  static constexpr int B_Q = 0, B_QFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
                        B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-                       B_DRAIN = B_ODONE + 2, NBAR = B_DRAIN + 1;
+                       B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
+                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int OFF_RINGI = OFF_MISC + 16;    // two decoded work items, 8 ints each
+  static constexpr int OFF_SINFO = OFF_RINGI + 2 * 8 * 4;  // per ring slot: labels / has-next
+  static constexpr int SMEM_USED = OFF_SINFO + NSLOT * 4;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
@@ -172,40 +176,130 @@ __device__ __forceinline__ uint32_t code_word(const MaskArgs& m, int k0tok, int 
   return w;
 }
 
+// Shared-memory descriptors: one base per tile; each k-step adds a constant to
+// the start-address field (addresses stay below 2^18, so no carry leaves it).
 // K-major operand (Q or K): k-step kk covers elements [16kk, 16kk+16) of D.
 template <int D>
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile_addr, int kk) {
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile_addr) {
   using C = Cfg<D>;
-  const uint32_t e = uint32_t(kk) * 16u;
-  const uint32_t addr = tile_addr + (e / C::CE) * C::CHUNK + (e % C::CE) * 2u;
-  return ptx::smem_desc(addr, 16u, C::SBO, C::SW);
+  return ptx::smem_desc(tile_addr, 16u, C::SBO, C::SW);
 }
-
+template <int D>
+__host__ __device__ constexpr uint64_t kmajor_step(int kk) {
+  using C = Cfg<D>;
+  return uint64_t(((16 * kk) / C::CE) * C::CHUNK + ((16 * kk) % C::CE) * 2) >> 4;
+}
 // MN-major operand V (N = D across chunks, K = keys): k-step kk covers keys [16kk, 16kk+16).
 template <int D>
-__device__ __forceinline__ uint64_t v_desc(uint32_t tile_addr, int kk) {
+__device__ __forceinline__ uint64_t v_base(uint32_t tile_addr) {
   using C = Cfg<D>;
-  const uint32_t addr = tile_addr + uint32_t(kk) * 16u * C::ROWB;
-  return ptx::smem_desc(addr, C::CHUNK, C::SBO, C::SW);
+  return ptx::smem_desc(tile_addr, C::CHUNK, C::SBO, C::SW);
+}
+template <int D>
+__host__ __device__ constexpr uint64_t v_step(int kk) {
+  using C = Cfg<D>;
+  return uint64_t(kk * 16 * C::ROWB) >> 4;
 }
 
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Cfg<D>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
-    ptx::mma_ss(d_tmem, kmajor_desc<D>(q_addr, kk), kmajor_desc<D>(k_addr, kk), C::IDESC_S, kk > 0);
+    ptx::mma_ss(d_tmem, q_desc + kmajor_step<D>(kk), k_desc + kmajor_step<D>(kk), C::IDESC_S, kk > 0);
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool acc) {
   using C = Cfg<D>;
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk)
-    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc<D>(v_addr, kk), C::IDESC_PV,
+    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc + v_step<D>(kk), C::IDESC_PV,
                 (acc || kk > 0) ? 1u : 0u);
 }
 
+// Per-slot note the producer leaves for the MMA issuer with every load:
+// K loads carry the two q-tiles' labels, V loads whether the item has another entry.
+constexpr uint32_t kInfoHasNext = 1u << 5;
+
+// One work item: a q-tile pair of one sequence and one head.
+struct Item {
+  int h, s0, L, qi0;
+  bool has1;
+  PairWalk walk;
+};
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_pairs, int n_qt) {
+  Item it;
+  it.h = item / n_pairs;
+  const int g0 = p.pair_q0[p.pair_order[item % n_pairs]];
+  const int b = p.qt_seq[g0];
+  it.has1 = g0 + 1 < n_qt && p.qt_seq[g0 + 1] == b;
+  it.s0 = p.cu[b];
+  it.L = p.cu[b + 1] - it.s0;
+  it.qi0 = p.qt_idx[g0] * kTile;  // first query row of q-tile 0, local to the sequence
+  it.walk.e0 = p.koff[g0];
+  it.walk.end0 = p.koff[g0 + 1];
+  it.walk.e1 = it.walk.end0;
+  it.walk.end1 = it.has1 ? p.koff[g0 + 2] : it.walk.end0;
+  return it;
+}
+
+// The producer publishes decoded items to the other roles as 8 ints.
+__device__ __forceinline__ void store_item(volatile int* d, const Item& it, bool valid) {
+  d[0] = valid ? 1 : 0;
+  d[1] = it.h;
+  d[2] = it.s0;
+  d[3] = it.L;
+  d[4] = it.qi0 | (it.has1 ? int(0x80000000) : 0);
+  d[5] = it.walk.e0;
+  d[6] = it.walk.end0;
+  d[7] = it.walk.end1;
+}
+__device__ __forceinline__ bool load_item(const volatile int* d, Item& it) {
+  if (!d[0]) return false;
+  it.h = d[1];
+  it.s0 = d[2];
+  it.L = d[3];
+  const int q = d[4];
+  it.has1 = q < 0;
+  it.qi0 = q & 0x7fffffff;
+  it.walk.e0 = d[5];
+  it.walk.end0 = d[6];
+  it.walk.e1 = it.walk.end0;
+  it.walk.end1 = d[7];
+  return true;
+}
+
+// Producer warp: take a ticket, decode it and publish item k in ring slot k & 1
+// (barriers iempty0 / ifull0 and the next ones 8 bytes on).  Returns 1 for an
+// item, 0 when no work is left (an end marker is published), -1 on abort.
+__device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane, int n_items, int n_pairs,
+                                            int n_qt, Item& it, volatile int* item_ring, uint32_t iempty0,
+                                            uint32_t ifull0, volatile uint32_t* abort_flag, int32_t* err) {
+  int ticket = 0;
+  if (lane == 0) ticket = atomicAdd(p.header + kHdrTicket, 1);
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  const bool valid = ticket < n_items;
+  if (valid) it = decode_item(p, ticket, n_pairs, n_qt);
+  const int slot_i = k & 1;
+  if (k >= 2 && !warp_wait(iempty0 + 8u * slot_i, uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 15))
+    return -1;
+  if (lane == 0) {
+    store_item(item_ring + 8 * slot_i, it, valid);
+    ptx::mbar_arrive(ifull0 + 8u * slot_i);
+  }
+  return valid ? 1 : 0;
+}
+
+// Persistent: each CTA takes work items from a global ticket counter (items
+// are head-major, longest q-tile pair first inside a head, so tickets hand
+// out the longest work first).  The producer takes the tickets, decodes them
+// one item ahead and passes them to the MMA warp and the softmax groups
+// through a two-slot ring in shared memory.  Barrier phases run on across
+// items; the next item's Q load and first S MMAs overlap the current item's
+// last P.V and O epilogue.  The last CTA to finish returns the counters to
+// zero for the next launch.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -217,22 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_qt = p.header[kHdrQtiles];
   const int n_pairs = p.header[kHdrPairs];
-  const int item = blockIdx.x;
-  if (item >= n_pairs * p.H) return;
+  const int n_items = n_pairs * p.H;
   int32_t* err = p.header + kHdrError;
-
-  const int h = item / n_pairs;
-  const int pr = p.pair_order[item % n_pairs];
-  const int g0 = p.pair_q0[pr];
-  const int b = p.qt_seq[g0];
-  const bool has1 = g0 + 1 < n_qt && p.qt_seq[g0 + 1] == b;
-  const int s0 = p.cu[b], L = p.cu[b + 1] - s0;
-  const int qi0 = p.qt_idx[g0] * kTile;  // first query row of q-tile 0, local to the sequence
-  PairWalk walk0;
-  walk0.e0 = p.koff[g0];
-  walk0.end0 = p.koff[g0 + 1];
-  walk0.e1 = walk0.end0;
-  walk0.end1 = has1 ? p.koff[g0 + 2] : walk0.end0;
 
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -242,9 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
+  volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);  // 2 x 8 ints
+  volatile uint32_t* slot_info = reinterpret_cast<volatile uint32_t*>(sbase + C::OFF_SINFO);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar(C::B_IFULL + s), 1);
+      ptx::mbar_init(bar(C::B_IEMPTY + s), 1 + 256);  // MMA thread + both softmax groups
+    }
+    ptx::mbar_init(bar(C::B_QFREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
@@ -254,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::B_SFULL + t), 1);
       ptx::mbar_init(bar(C::B_PFULL + t), 128);
       ptx::mbar_init(bar(C::B_ODONE + t), 1);
+      ptx::mbar_init(bar(C::B_OFREE + t), 128);
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
@@ -276,73 +364,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing issued, nothing to drain
    } else if (warp == 8) {
     // ------------------------------------------------------------ producer
-    PairWalk walk = walk0;
-    int nload = 0, ntail = 0;
-    bool tail_pending = false;
+    int nload = 0, ntail = 0, nq = 0;
+    bool tail_pending = false, ok = true;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
       ptx::prefetch_tensormap(&tmK);
       ptx::prefetch_tensormap(&tmV);
-      ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE * (has1 ? 2 : 1));
-      for (int c = 0; c < C::NCH; ++c)
-        ptx::tma_load_3d(sQ0 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, h, s0 + qi0);
-      if (has1)
-        for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sQ1 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, h, s0 + qi0 + kTile);
     }
-    int kt, la, lb;
-    while (walk.next(p.kidx, p.klabel, kt, la, lb)) {
-      const int j0 = kt * kTile, kn = min(kTile, L - j0);
-      // K(j)
-      int slot = nload % C::NSLOT;
-      if (nload >= C::NSLOT &&
-          !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1))
-        break;
+    // Take a ticket, decode it and publish it in ring slot k & 1, one item
+    // ahead of the loads, so the other roles never wait on the decoding.
+    Item it_next;
+    int st_next = publish_item(p, 0, lane, n_items, n_pairs, n_qt, it_next, item_ring,
+                               bar(C::B_IEMPTY), bar(C::B_IFULL), abort_flag, err);
+    for (int k = 0; ok && st_next == 1; ++k) {
+      Item it = it_next;
+      st_next = publish_item(p, k + 1, lane, n_items, n_pairs, n_qt, it_next, item_ring,
+                             bar(C::B_IEMPTY), bar(C::B_IFULL), abort_flag, err);
+      if (st_next < 0) break;
+      // Q of this item, once the previous item's S MMAs no longer read Q.
+      if (nq > 0 && !warp_wait(bar(C::B_QFREE), uint32_t(nq - 1) & 1u, abort_flag, err, 13)) break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+        ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE * (it.has1 ? 2 : 1));
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmK, bar(C::B_FULL + slot),
-                           c * C::CE, h, s0 + j0);
-      }
-      ++nload;
-      // V(j)
-      slot = nload % C::NSLOT;
-      if (nload >= C::NSLOT &&
-          !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1))
-        break;
-      if (kn < kTile) {
-        // Rows past the sequence end come from the next sequence (or are zero
-        // past the tensor).  Their P is exactly 0, but 0 * inf is NaN, so they
-        // are zeroed before the P.V product may read them.
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(bar(C::B_VTMA), C::TILE);
+          ptx::tma_load_3d(sQ0 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h, it.s0 + it.qi0);
+        if (it.has1)
           for (int c = 0; c < C::NCH; ++c)
-            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VTMA), c * C::CE,
-                             h, s0 + j0);
-        }
-        tail_pending = true;
-        if (!warp_wait(bar(C::B_VTMA), uint32_t(ntail) & 1u, abort_flag, err, 2)) break;
-        tail_pending = false;
-        ++ntail;
-        for (int rr = kn + lane; rr < kTile; rr += 32) {
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
-            uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK +
-                                                  rr * C::ROWB);
-#pragma unroll
-            for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(C::B_FULL + slot));
-      } else if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_FULL + slot),
-                           c * C::CE, h, s0 + j0);
+            ptx::tma_load_3d(sQ1 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h,
+                             it.s0 + it.qi0 + kTile);
       }
-      ++nload;
+      ++nq;
+      int kt, la, lb;
+      bool have = it.walk.next(p.kidx, p.klabel, kt, la, lb);
+      while (have) {
+        int kt2, la2, lb2;
+        const bool nxt = it.walk.next(p.kidx, p.klabel, kt2, la2, lb2);
+        const int j0 = kt * kTile, kn = min(kTile, it.L - j0);
+        // K(j)
+        int slot = nload % C::NSLOT;
+        if (nload >= C::NSLOT &&
+            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          slot_info[slot] = uint32_t(la) | (uint32_t(lb) << 2);
+          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmK, bar(C::B_FULL + slot),
+                             c * C::CE, it.h, it.s0 + j0);
+        }
+        ++nload;
+        // V(j)
+        slot = nload % C::NSLOT;
+        if (nload >= C::NSLOT &&
+            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
+          ok = false;
+          break;
+        }
+        if (kn < kTile) {
+          // Rows past the sequence end come from the next sequence (or are zero
+          // past the tensor).  Their P is exactly 0, but 0 * inf is NaN, so they
+          // are zeroed before the P.V product may read them.
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::B_VTMA), C::TILE);
+            for (int c = 0; c < C::NCH; ++c)
+              ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VTMA), c * C::CE,
+                               it.h, it.s0 + j0);
+          }
+          tail_pending = true;
+          if (!warp_wait(bar(C::B_VTMA), uint32_t(ntail) & 1u, abort_flag, err, 2)) {
+            ok = false;
+            break;
+          }
+          tail_pending = false;
+          ++ntail;
+          for (int rr = kn + lane; rr < kTile; rr += 32) {
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK +
+                                                    rr * C::ROWB);
+#pragma unroll
+              for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            slot_info[slot] = nxt ? kInfoHasNext : 0u;
+            ptx::mbar_arrive(bar(C::B_FULL + slot));
+          }
+        } else if (lane == 0) {
+          slot_info[slot] = nxt ? kInfoHasNext : 0u;
+          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+          for (int c = 0; c < C::NCH; ++c)
+            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_FULL + slot),
+                             c * C::CE, it.h, it.s0 + j0);
+        }
+        ++nload;
+        kt = kt2;
+        la = la2;
+        lb = lb2;
+        have = nxt;
+      }
     }
     // Do not leave while a load this CTA issued may still be writing shared memory.
     if (lane == 0) {
@@ -352,68 +475,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
       }
       if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
-      drain_bar(bar(C::B_Q), 0, err);
+      if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
     }
     __syncwarp();
    } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      PairWalk walk = walk0;
-      int kt, a, bl;
-      bool have = wait_bar(bar(C::B_Q), 0, abort_flag, err, 3) && walk.next(p.kidx, p.klabel, kt, a, bl);
       int nload = 0, c0 = 0, c1 = 0;
-      if (have) {
-        if (!wait_bar(bar(C::B_FULL + 0), 0, abort_flag, err, 4)) {
-          have = false;
-        } else {
-          ptx::tc_fence_after();
-          if (a) { issue_s<D>(tmem + C::col_s(0), sQ0, sRing); ptx::mma_commit(bar(C::B_SFULL + 0)); }
-          if (bl) { issue_s<D>(tmem + C::col_s(1), sQ1, sRing); ptx::mma_commit(bar(C::B_SFULL + 1)); }
-          ptx::mma_commit(bar(C::B_EMPTY + 0));
-          nload = 1;
+      bool ok = true;
+      const uint64_t qdesc0 = kmajor_base<D>(sQ0), qdesc1 = kmajor_base<D>(sQ1);
+      const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
+      for (int k = 0; ok; ++k) {
+        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+        Item it;
+        const bool valid = load_item(item_ring + 8 * (k & 1), it);
+        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        if (!valid) break;
+        if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
+        bool first0 = true, first1 = true;  // first P.V of this item for each q-tile
+        if (it.walk.e0 == it.walk.end0 && it.walk.e1 == it.walk.end1) {  // no entries
+          ptx::mma_commit(bar(C::B_QFREE));
+          continue;
         }
-      }
-      while (have) {
-        int kt2, a2, b2;
-        const bool nxt = walk.next(p.kidx, p.klabel, kt2, a2, b2);
-        const int vslot = nload % C::NSLOT, kslot = (nload + 1) % C::NSLOT;
-        const uint32_t vph = uint32_t(nload / C::NSLOT) & 1u;
-        const uint32_t kph = uint32_t((nload + 1) / C::NSLOT) & 1u;
-        const uint32_t vaddr = sRing + vslot * C::TILE, kaddr = sRing + kslot * C::TILE;
-        bool vready = false, kready = false;
-        if (a) {
-          if (!wait_bar(bar(C::B_PFULL + 0), uint32_t(c0) & 1u, abort_flag, err, 5)) break;
-          if (!wait_bar(bar(C::B_FULL + vslot), vph, abort_flag, err, 6)) break;
-          vready = true;
+        // entry 0: S of both q-tiles from K(0)
+        int a, bl;
+        {
+          const int slot = nload % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
-          issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vaddr, c0 > 0);
-          ptx::mma_commit(bar(C::B_ODONE + 0));
-          ++c0;
-        }
-        if (nxt) {
-          if (!wait_bar(bar(C::B_FULL + kslot), kph, abort_flag, err, 4)) break;
-          kready = true;
-          ptx::tc_fence_after();
-          if (a2) { issue_s<D>(tmem + C::col_s(0), sQ0, kaddr); ptx::mma_commit(bar(C::B_SFULL + 0)); }
-        }
-        if (bl) {
-          if (!wait_bar(bar(C::B_PFULL + 1), uint32_t(c1) & 1u, abort_flag, err, 5)) break;
-          if (!vready && !wait_bar(bar(C::B_FULL + vslot), vph, abort_flag, err, 6)) break;
-          ptx::tc_fence_after();
-          issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vaddr, c1 > 0);
-          ptx::mma_commit(bar(C::B_ODONE + 1));
-          ++c1;
-        }
-        ptx::mma_commit(bar(C::B_EMPTY + vslot));
-        ++nload;
-        if (nxt && kready) {
-          if (b2) { issue_s<D>(tmem + C::col_s(1), sQ1, kaddr); ptx::mma_commit(bar(C::B_SFULL + 1)); }
-          ptx::mma_commit(bar(C::B_EMPTY + kslot));
+          const uint32_t info = slot_info[slot];
+          a = int(info & 3u);
+          bl = int((info >> 2) & 3u);
+          const uint64_t kdesc = kdesc0 + uint64_t(slot) * (C::TILE >> 4);
+          if (a) { issue_s<D>(tmem + C::col_s(0), qdesc0, kdesc); ptx::mma_commit(bar(C::B_SFULL + 0)); }
+          if (bl) { issue_s<D>(tmem + C::col_s(1), qdesc1, kdesc); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          ptx::mma_commit(bar(C::B_EMPTY + slot));
           ++nload;
         }
-        a = a2;
-        bl = b2;
-        have = nxt;
+        for (;;) {
+          // V(j): its note says whether entry j+1 exists
+          const int vslot = nload % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + vslot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 6)) {
+            ok = false;
+            break;
+          }
+          const bool nxt = (slot_info[vslot] & kInfoHasNext) != 0u;
+          // every S of this item has been issued: Q may be replaced once they finish
+          if (!nxt) ptx::mma_commit(bar(C::B_QFREE));
+          const uint64_t vdesc = vdesc0 + uint64_t(vslot) * (C::TILE >> 4);
+          if (a) {
+            if (!wait_bar(bar(C::B_PFULL + 0), uint32_t(c0) & 1u, abort_flag, err, 5)) { ok = false; break; }
+            if (first0 && k > 0 &&
+                !wait_bar(bar(C::B_OFREE + 0), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vdesc, !first0);
+            ptx::mma_commit(bar(C::B_ODONE + 0));
+            first0 = false;
+            ++c0;
+          }
+          int a2 = 0, b2 = 0;
+          const int kslot = (nload + 1) % C::NSLOT;
+          const uint64_t kdesc = kdesc0 + uint64_t(kslot) * (C::TILE >> 4);
+          if (nxt) {
+            if (!wait_bar(bar(C::B_FULL + kslot), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t info = slot_info[kslot];
+            a2 = int(info & 3u);
+            b2 = int((info >> 2) & 3u);
+            if (a2) { issue_s<D>(tmem + C::col_s(0), qdesc0, kdesc); ptx::mma_commit(bar(C::B_SFULL + 0)); }
+          }
+          if (bl) {
+            if (!wait_bar(bar(C::B_PFULL + 1), uint32_t(c1) & 1u, abort_flag, err, 5)) { ok = false; break; }
+            if (first1 && k > 0 &&
+                !wait_bar(bar(C::B_OFREE + 1), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vdesc, !first1);
+            ptx::mma_commit(bar(C::B_ODONE + 1));
+            first1 = false;
+            ++c1;
+          }
+          ptx::mma_commit(bar(C::B_EMPTY + vslot));
+          ++nload;
+          if (!nxt) break;
+          if (b2) { issue_s<D>(tmem + C::col_s(1), qdesc1, kdesc); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          ptx::mma_commit(bar(C::B_EMPTY + kslot));
+          ++nload;
+          a = a2;
+          bl = b2;
+        }
       }
       // Every MMA issued above has finished once this commit arrives.
       ptx::mma_commit(bar(C::B_DRAIN));
@@ -427,149 +582,170 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;                   // which q-tile of the pair
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;         // query row inside the tile
-    const bool present = t == 0 || has1;
-    const int it0 = qi0 + t * kTile;           // first row of this q-tile (local)
-    const int qn = present ? min(kTile, L - it0) : 0;
-    const bool row_in = r < qn;
-    const int il = it0 + r;                    // local query index
     const int kind = p.mask.kind;
-    const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     const uint32_t colS = C::col_s(t), colO = C::col_o(t);
     const float c2 = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
-    int cnt = 0;
+    int cnt = 0;  // entries processed by this q-tile slot over all items (barrier phases)
     bool ok = true;
-    PairWalk walk = walk0;
-    int kt, la, lb;
-    while (present && walk.next(p.kidx, p.klabel, kt, la, lb)) {
-      const int lab = t == 0 ? la : lb;
-      if (lab == ATTN_TILE_EMPTY) continue;
-      const int j0 = kt * kTile;
-      const int kn = min(kTile, L - j0);
-      if (!warp_wait(bar(C::B_SFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 8)) { ok = false; break; }
-      ptx::tc_fence_after();
-      float s[128];
-      {
-        uint32_t v[4][32];
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      Item it;
+      const bool valid = load_item(item_ring + 8 * (k & 1), it);
+      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      const bool present = t == 0 || it.has1;
+      const int it0 = it.qi0 + t * kTile;      // first row of this q-tile (local)
+      const int qn = present ? min(kTile, it.L - it0) : 0;
+      const bool row_in = r < qn;
+      const int il = it0 + r;                  // local query index
+      const int s0 = it.s0, L = it.L;
+      const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
+      float m_ref = -INFINITY, l = 0.f;
+      int cnt_item = 0;
+      int kt, la, lb;
+      bool have = present && it.walk.next(p.kidx, p.klabel, kt, la, lb);
+      while (have) {
+        const int lab = t == 0 ? la : lb;
+        const int j0 = kt * kTile;
+        // fetch the next entry now; its loads complete under this entry's work
+        have = it.walk.next(p.kidx, p.klabel, kt, la, lb);
+        if (lab == ATTN_TILE_EMPTY) continue;
+        const int kn = min(kTile, L - j0);
+        if (!warp_wait(bar(C::B_SFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 8)) { ok = false; break; }
+        ptx::tc_fence_after();
+        float s[128];
+        {
+          uint32_t v[4][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(lane_base + colS + q * 32, v[q]);
-        ptx::tmem_wait_ld();
+          for (int q = 0; q < 4; ++q) ptx::tmem_ld32(lane_base + colS + q * 32, v[q]);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[q][c]);
-      }
-      if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
-        // bit c of vis[c / 32]: key column c is visible to this row.  Causal part
-        // and bounds: columns c < upto; PARTIAL tiles of the metadata kinds also
-        // AND in the per-key predicate.
-        const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
-        uint32_t vis[4];
+            for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[q][c]);
+        }
+        if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
+          // bit c of vis[c / 32]: key column c is visible to this row.  Causal part
+          // and bounds: columns c < upto; PARTIAL tiles of the metadata kinds also
+          // AND in the per-key predicate.
+          const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
+          uint32_t vis[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
-        if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-          const int k0tok = s0 + j0;
-          if (kind == ATTN_MASK_STRIP_THINKING) {
+          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
+          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+            const int k0tok = s0 + j0;
+            if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(p.mask, k0tok, q, kn, qcode);
-          } else if (kind == ATTN_MASK_SHARED_PREFIX) {
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(p.mask, k0tok, q, kn, qcode);
+            } else if (kind == ATTN_MASK_SHARED_PREFIX) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(p.mask, k0tok, q, kn, qcode);
-          } else {
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(p.mask, k0tok, q, kn, qcode);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(p.mask, k0tok, q, kn, qcode);
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(p.mask, k0tok, q, kn, qcode);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (vis[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
+        }
+        float mx4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float mv = s[32 * u];
+#pragma unroll
+          for (int c = 1; c < 31; c += 2) mv = ptx::fmax3(mv, s[32 * u + c], s[32 * u + c + 1]);
+          mx4[u] = fmaxf(mv, s[32 * u + 31]);
+        }
+        const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+        const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
+        const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
+        const float m_new = raise ? mxs : m_ref;
+        const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
+        if (cnt_item > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O must hold exactly the P.V of earlier entries before it is rescaled.
+          if (!warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 10)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            ptx::tmem_ld32(lane_base + colO + q * 32, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 x = ptx::fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), a2);
+              v[c] = __float_as_uint(x.x);
+              v[c + 1] = __float_as_uint(x.y);
+            }
+            ptx::tmem_st32(lane_base + colO + q * 32, v);
           }
         }
+        l *= alpha;
+        m_ref = m_new;
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
+        float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (vis[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
+        for (int hh = 0; hh < 4; ++hh) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
+            const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            sum2 = ptx::fadd2(sum2, e);
+            pk[c >> 1] = ptx::pack_bf16(e.x, e.y);
+          }
+          ptx::tmem_st16(lane_base + colS + hh * 16, pk);
+        }
+        l += sum2.x + sum2.y;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL + t));
+        ++cnt;
+        ++cnt_item;
       }
-      float mx4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float mv = s[32 * u];
-#pragma unroll
-        for (int c = 1; c < 31; c += 2) mv = ptx::fmax3(mv, s[32 * u + c], s[32 * u + c + 1]);
-        mx4[u] = fmaxf(mv, s[32 * u + 31]);
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (present && cnt_item > 0 &&
+          !warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 11)) {
+        ok = false;
+        break;
       }
-      const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
-      const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
-      const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
-      const float m_new = raise ? mxs : m_ref;
-      const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
-      if (cnt > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O must hold exactly the P.V of earlier entries before it is rescaled.
-        if (!warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 10)) { ok = false; break; }
+      if (present) {
         ptx::tc_fence_after();
-        const float2 a2 = make_float2(alpha, alpha);
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + it.h) * D;
 #pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
           uint32_t v[32];
-          ptx::tmem_ld32(lane_base + colO + q * 32, v);
-          ptx::tmem_wait_ld();
+          if (cnt_item > 0) {
+            ptx::tmem_ld32(lane_base + colO + q * 32, v);
+            ptx::tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 x = ptx::fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), a2);
-            v[c] = __float_as_uint(x.x);
-            v[c + 1] = __float_as_uint(x.y);
+            for (int c = 0; c < 32; ++c) v[c] = 0u;
           }
-          ptx::tmem_st32(lane_base + colO + q * 32, v);
-        }
-      }
-      l *= alpha;
-      m_ref = m_new;
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
-      float2 sum2 = make_float2(0.f, 0.f);
+          uint32_t w[16];
 #pragma unroll
-      for (int hh = 0; hh < 4; ++hh) {
-        uint32_t pk[16];
+          for (int c = 0; c < 16; ++c)
+            w[c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * inv_l, __uint_as_float(v[2 * c + 1]) * inv_l);
+          if (row_in) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
-          const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-          sum2 = ptx::fadd2(sum2, e);
-          pk[c >> 1] = ptx::pack_bf16(e.x, e.y);
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          }
         }
-        ptx::tmem_st16(lane_base + colS + hh * 16, pk);
+        if (row_in)
+          p.lse[size_t(it.h) * p.T + s0 + il] =
+              l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
       }
-      l += sum2.x + sum2.y;
-      ptx::tmem_wait_st();
+      // This q-tile slot's O columns may now take the next item's P.V.
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_PFULL + t));
-      ++cnt;
-    }
-    // ------------------------------------------------------------ epilogue
-    if (present && ok && cnt > 0) ok = warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 11);
-    if (present && ok) {
-      ptx::tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + h) * D;
-#pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        if (cnt > 0) {
-          ptx::tmem_ld32(lane_base + colO + q * 32, v);
-          ptx::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          w[c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * inv_l, __uint_as_float(v[2 * c + 1]) * inv_l);
-        if (row_in) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-      }
-      if (row_in)
-        p.lse[size_t(h) * p.T + s0 + il] = l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
+      ptx::mbar_arrive(bar(C::B_OFREE + t));
     }
   }
 
@@ -578,6 +754,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // Every CTA has taken its last ticket before it counts itself finished, so
+    // the last one can return both counters to zero for the next launch.
+    __threadfence();
+    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
+      atomicExch(p.header + kHdrTicket, 0);
+      atomicExch(p.header + kHdrFinished, 0);
+    }
   }
 }
 
@@ -646,9 +831,18 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  // the pair count is only known on the device; max_qt bounds it
-  const long long grid = (long long)a.bm.max_qt * a.num_heads;
-  if (grid <= 0 || grid > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  // Persistent: one CTA per SM (the pair count is only known on the device;
+  // max_qt * H bounds it).
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd device query");
+  }
+  const long long items = (long long)a.bm.max_qt * a.num_heads;
+  if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const long long grid = items < num_sms ? items : num_sms;
   attn_fwd_bf16_kernel<D><<<unsigned(grid), kThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");

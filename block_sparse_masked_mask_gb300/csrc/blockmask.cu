@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
     v.header[kHdrEmpty] = 0;
     v.header[kHdrPartial] = 0;
     v.header[kHdrFull] = 0;
-    v.header[7] = 0;
+    for (int i = 7; i < kHdrInts; ++i) v.header[i] = 0;
   }
   __syncthreads();
   for (int g = tid; g < n_qt; g += blockDim.x) {

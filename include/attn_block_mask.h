@@ -106,9 +106,12 @@ typedef struct attn_mask_params {
  * caller, describing arrays that live in the caller's device workspace.
  * Byte offsets (off_*) are from the workspace base; array sizes are in the
  * comments, with NQ = max_qtiles and NK = max_ktiles.
- *   off_header  int32[8]: [0] n_qtiles, [1] n_entries (sum of kcount),
+ *   off_header  int32[16]: [0] n_qtiles, [1] n_entries (sum of kcount),
  *               [2] error bits, [3] n_qpairs, [4] EMPTY, [5] PARTIAL,
- *               [6] FULL tile-pair totals, [7] reserved
+ *               [6] FULL tile-pair totals, [8] [9] the forward's work
+ *               counters (zero between launches), others reserved.
+ *               Because of [8] and [9], attn_fwd calls that share one block
+ *               mask must not run concurrently (same stream, or ordered).
  *   off_qt_seq  int32[NQ]       sequence of each q-tile (q-tiles are numbered
  *                               sequence-major, ascending inside a sequence)
  *   off_qt_idx  int32[NQ]       index of the q-tile inside its sequence

@@ -228,3 +228,23 @@ def test_mask_mismatch_and_metadata_errors():
     with pytest.raises(api.AttnError) as e:
         api.attn_fwd(q, q, q, bm, w.kind, other_cu, w.max_seqlen, seg_id=dm["seg_id"])
     assert e.value.status == 4
+
+
+def test_repeated_forwards_on_one_mask():
+    """The forward's work counters return to zero after every launch, so a
+    mask serves any number of forwards with different inputs."""
+    w = W.random_workload(12, "causal_document", [900, 1300], num_heads=3, head_dim=128)
+    dm = w.device_meta()
+    bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], w.total_tokens, w.max_seqlen,
+                                   seg_id=dm["seg_id"])
+    for i in range(3):
+        g = torch.Generator().manual_seed(100 + i)
+        q, k, v = (torch.randn(w.total_tokens, 3, 128, generator=g).bfloat16() for _ in range(3))
+        o, lse = api.attn_fwd(q.cuda(), k.cuda(), v.cuda(), bm, w.kind, dm["cu_seqlens"],
+                              w.max_seqlen, seg_id=dm["seg_id"])
+        assert api.attn_get_status(bm) == api.ATTN_OK
+        rows = list(range(0, w.total_tokens, 7))
+        O, L = oracle.attention(q, k, v, w.kind, w.cu_seqlens, w.meta(), rows=rows)
+        assert np.abs(o.float().cpu().numpy()[rows] - O[rows]).max() <= 2e-2
+        assert np.abs(lse.cpu().numpy()[:, rows] - L[:, rows]).max() <= 1e-3
+        assert bm.header()[8:10].tolist() == [0, 0]
