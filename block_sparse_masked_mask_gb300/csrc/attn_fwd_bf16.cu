@@ -17,10 +17,12 @@
 //   warps 4-7  softmax of q-tile 1
 //   warp 8     TMA producer: Q0/Q1 once, then K(j), V(j) into a ring of
 //              four 128 x D slots; zeroes V rows past a sequence end
-//   warps 10-11 idle
-//   warp 9     tcgen05 issuer (one thread) and TMEM owner.  Order per entry
-//              j: PV0(j), S0(j+1), PV1(j), S1(j+1), so one softmax group works
-//              while the tensor cores serve the other (ping-pong).
+//   warps 9-10 tcgen05 issuers, one thread each: warp 9 for q-tile 0, warp 10
+//              for q-tile 1 (warp 9 also owns the TMEM allocation).  Each
+//              issues PV(j) then S(j+1) for its q-tile, so one softmax group
+//              works while the tensor cores serve the other (ping-pong), and
+//              one issuer's barrier waits hide behind the other's MMAs.
+//   warp 11    idle
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
 // P (bf16) overwrites the first 64 columns of its S buffer.
 //
@@ -329,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(C::B_Q), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(C::B_IFULL + s), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + s), 1 + 256);  // MMA thread + both softmax groups
+      ptx::mbar_init(bar(C::B_IEMPTY + s), 2 + 256);  // both MMA issuers + both softmax groups
     }
-    ptx::mbar_init(bar(C::B_QFREE), 1);
+    ptx::mbar_init(bar(C::B_QFREE), 2);  // both MMA issuers
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
-      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_EMPTY + s), 2);  // both MMA issuers
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
     for (int t = 0; t < 2; ++t) {
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::B_ODONE + t), 1);
       ptx::mbar_init(bar(C::B_OFREE + t), 128);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 2);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
@@ -478,12 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
     }
     __syncwarp();
-   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+   } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 9 issues q-tile 0's MMAs, warp 10 q-tile 1's (one thread each), so
+    // one issuer's barrier waits hide behind the other's MMAs.
     if (lane == 0) {
-      int nload = 0, c0 = 0, c1 = 0;
+      const int t = warp - 9;
+      const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+      int nload = 0, cnt = 0;
       bool ok = true;
-      const uint64_t qdesc0 = kmajor_base<D>(sQ0), qdesc1 = kmajor_base<D>(sQ1);
+      const uint64_t qdesc = kmajor_base<D>(t == 0 ? sQ0 : sQ1);
       const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -492,13 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
         if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
-        bool first0 = true, first1 = true;  // first P.V of this item for each q-tile
+        bool first = true;  // first P.V of this item
         if (it.walk.e0 == it.walk.end0 && it.walk.e1 == it.walk.end1) {  // no entries
           ptx::mma_commit(bar(C::B_QFREE));
           continue;
         }
-        // entry 0: S of both q-tiles from K(0)
-        int a, bl;
+        // entry 0: S from K(0)
+        int lab;
         {
           const int slot = nload % C::NSLOT;
           if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
@@ -506,12 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t info = slot_info[slot];
-          a = int(info & 3u);
-          bl = int((info >> 2) & 3u);
-          const uint64_t kdesc = kdesc0 + uint64_t(slot) * (C::TILE >> 4);
-          if (a) { issue_s<D>(tmem + C::col_s(0), qdesc0, kdesc); ptx::mma_commit(bar(C::B_SFULL + 0)); }
-          if (bl) { issue_s<D>(tmem + C::col_s(1), qdesc1, kdesc); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          lab = int((slot_info[slot] >> (2 * t)) & 3u);
+          if (lab) {
+            issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(slot) * (C::TILE >> 4));
+            ptx::mma_commit(bar(C::B_SFULL + t));
+          }
           ptx::mma_commit(bar(C::B_EMPTY + slot));
           ++nload;
         }
@@ -525,57 +530,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool nxt = (slot_info[vslot] & kInfoHasNext) != 0u;
           // every S of this item has been issued: Q may be replaced once they finish
           if (!nxt) ptx::mma_commit(bar(C::B_QFREE));
-          const uint64_t vdesc = vdesc0 + uint64_t(vslot) * (C::TILE >> 4);
-          if (a) {
-            if (!wait_bar(bar(C::B_PFULL + 0), uint32_t(c0) & 1u, abort_flag, err, 5)) { ok = false; break; }
-            if (first0 && k > 0 &&
-                !wait_bar(bar(C::B_OFREE + 0), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
+          if (lab) {
+            if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 5)) { ok = false; break; }
+            if (first && k > 0 &&
+                !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
             ptx::tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), vdesc, !first0);
-            ptx::mma_commit(bar(C::B_ODONE + 0));
-            first0 = false;
-            ++c0;
+            issue_pv<D>(tmem + colO, tmem + colS, vdesc0 + uint64_t(vslot) * (C::TILE >> 4), !first);
+            first = false;
+            ++cnt;
           }
-          int a2 = 0, b2 = 0;
-          const int kslot = (nload + 1) % C::NSLOT;
-          const uint64_t kdesc = kdesc0 + uint64_t(kslot) * (C::TILE >> 4);
-          if (nxt) {
-            if (!wait_bar(bar(C::B_FULL + kslot), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t info = slot_info[kslot];
-            a2 = int(info & 3u);
-            b2 = int((info >> 2) & 3u);
-            if (a2) { issue_s<D>(tmem + C::col_s(0), qdesc0, kdesc); ptx::mma_commit(bar(C::B_SFULL + 0)); }
-          }
-          if (bl) {
-            if (!wait_bar(bar(C::B_PFULL + 1), uint32_t(c1) & 1u, abort_flag, err, 5)) { ok = false; break; }
-            if (first1 && k > 0 &&
-                !wait_bar(bar(C::B_OFREE + 1), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
-            ptx::tc_fence_after();
-            issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1), vdesc, !first1);
-            ptx::mma_commit(bar(C::B_ODONE + 1));
-            first1 = false;
-            ++c1;
-          }
+          // The item's last P.V: O is final once this arrives.
+          if (!nxt && !first) ptx::mma_commit(bar(C::B_ODONE + t));
           ptx::mma_commit(bar(C::B_EMPTY + vslot));
           ++nload;
           if (!nxt) break;
-          if (b2) { issue_s<D>(tmem + C::col_s(1), qdesc1, kdesc); ptx::mma_commit(bar(C::B_SFULL + 1)); }
+          // K(j+1)
+          const int kslot = nload % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + kslot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          lab = int((slot_info[kslot] >> (2 * t)) & 3u);
+          if (lab) {
+            issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
+            ptx::mma_commit(bar(C::B_SFULL + t));
+          }
           ptx::mma_commit(bar(C::B_EMPTY + kslot));
           ++nload;
-          a = a2;
-          bl = b2;
         }
       }
-      // Every MMA issued above has finished once this commit arrives.
+      // Every MMA this thread issued has finished once this commit arrives.
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-   }  // warps 10-11 idle
+   }  // warp 11 idle
   } else if (!skip) {
     ptx::regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
@@ -586,7 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     const uint32_t colS = C::col_s(t), colO = C::col_o(t);
     const float c2 = p.scale_log2;
-    int cnt = 0;  // entries processed by this q-tile slot over all items (barrier phases)
+    int cnt = 0;     // entries processed by this q-tile slot over all items (barrier phases)
+    int nodone = 0;  // items whose final O this slot has waited for
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -652,23 +643,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (vis[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
         }
-        float mx4[4];
+        float mx8[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float mv = s[32 * u];
+        for (int u = 0; u < 8; ++u) {
+          float mv = s[16 * u];
 #pragma unroll
-          for (int c = 1; c < 31; c += 2) mv = ptx::fmax3(mv, s[32 * u + c], s[32 * u + c + 1]);
-          mx4[u] = fmaxf(mv, s[32 * u + 31]);
+          for (int c = 1; c < 15; c += 2) mv = ptx::fmax3(mv, s[16 * u + c], s[16 * u + c + 1]);
+          mx8[u] = fmaxf(mv, s[16 * u + 15]);
         }
-        const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+        const float mxs = ptx::fmax3(ptx::fmax3(mx8[0], mx8[1], mx8[2]), ptx::fmax3(mx8[3], mx8[4], mx8[5]),
+                                     fmaxf(mx8[6], mx8[7])) * c2;
         const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
         const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
         const float m_new = raise ? mxs : m_ref;
         const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
         if (cnt_item > 0 && __any_sync(0xffffffffu, rescale)) {
-          // O must hold exactly the P.V of earlier entries before it is rescaled.
-          if (!warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 10)) { ok = false; break; }
-          ptx::tc_fence_after();
+          // O holds exactly the P.V of earlier entries: this S was issued after
+          // them by the same thread, and its commit arrives only once they are done.
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
@@ -710,10 +701,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (present && cnt_item > 0 &&
-          !warp_wait(bar(C::B_ODONE + t), uint32_t(cnt - 1) & 1u, abort_flag, err, 11)) {
-        ok = false;
-        break;
+      if (present && cnt_item > 0) {
+        if (!warp_wait(bar(C::B_ODONE + t), uint32_t(nodone) & 1u, abort_flag, err, 11)) {
+          ok = false;
+          break;
+        }
+        ++nodone;
       }
       if (present) {
         ptx::tc_fence_after();
