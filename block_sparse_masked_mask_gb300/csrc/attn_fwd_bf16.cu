@@ -72,7 +72,8 @@ struct Cfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;    // two decoded work items, 8 ints each
   static constexpr int OFF_SINFO = OFF_RINGI + 2 * 8 * 4;  // per ring slot: labels / has-next
-  static constexpr int SMEM_USED = OFF_SINFO + NSLOT * 4;
+  static constexpr int OFF_CODES = (OFF_SINFO + NSLOT * 4 + 15) & ~15;  // per slot: 128 key codes
+  static constexpr int SMEM_USED = OFF_CODES + NSLOT * kTile * 4;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
@@ -160,20 +161,19 @@ __device__ __forceinline__ uint32_t prefix_bits(int n) {
   return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
 }
 
-// Visibility bits of keys [32q, 32q+32) of a k-tile starting at global token
-// `k0tok` (kn keys in bounds) for one query code, read from the metadata.
+// Visibility bits of keys [32q, 32q+32) of a k-tile for one query code, from
+// the keys' codes the producer staged in shared memory.
 template <int KIND>
-__device__ __forceinline__ uint32_t code_word(const MaskArgs& m, int k0tok, int q, int kn, int qcode) {
+__device__ __forceinline__ uint32_t code_word(const int* codes, int q, int qcode) {
   uint32_t w = 0;
+  const int4* c4 = reinterpret_cast<const int4*>(codes + 32 * q);
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const int idx = min(32 * q + c, kn - 1);  // clamped: out-of-bounds bits are cleared anyway
-    int kc;
-    if (KIND == ATTN_MASK_STRIP_THINKING)
-      kc = int(__ldg(m.role + k0tok + idx)) == m.role_think ? __ldg(m.turn + k0tok + idx) : INT_MAX;
-    else
-      kc = __ldg(m.seg + k0tok + idx);
-    w |= uint32_t(code_visible(KIND, qcode, kc)) << c;
+  for (int c = 0; c < 8; ++c) {
+    const int4 k = c4[c];
+    w |= (uint32_t(code_visible(KIND, qcode, k.x)) << (4 * c)) |
+         (uint32_t(code_visible(KIND, qcode, k.y)) << (4 * c + 1)) |
+         (uint32_t(code_visible(KIND, qcode, k.z)) << (4 * c + 2)) |
+         (uint32_t(code_visible(KIND, qcode, k.w)) << (4 * c + 3));
   }
   return w;
 }
@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = misc + 1;
   volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);  // 2 x 8 ints
   volatile uint32_t* slot_info = reinterpret_cast<volatile uint32_t*>(sbase + C::OFF_SINFO);
+  int* slot_codes = reinterpret_cast<int*>(sbase + C::OFF_CODES);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_Q), 1);
@@ -422,6 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
           ok = false;
           break;
+        }
+        // Keys' mask codes for the softmax of PARTIAL tiles; they live as long
+        // as V(j), i.e. until both q-tiles' P.V(j) are done.
+        if (p.mask.kind != ATTN_MASK_CAUSAL && (la == ATTN_TILE_PARTIAL || lb == ATTN_TILE_PARTIAL)) {
+          for (int c = lane; c < kTile; c += 32)
+            slot_codes[slot * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
+          __syncwarp();
         }
         if (kn < kTile) {
           // Rows past the sequence end come from the next sequence (or are zero
@@ -578,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c2 = p.scale_log2;
     int cnt = 0;     // entries processed by this q-tile slot over all items (barrier phases)
     int nodone = 0;  // items whose final O this slot has waited for
+    int ue_next = 0; // union entries walked (both q-tiles), = K/V ring loads / 2
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -595,10 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       int cnt_item = 0;
       int kt, la, lb;
+      // an absent second q-tile does not walk, but the ring still advanced by
+      // the item's union entries (q-tile 0's list)
+      if (!present) ue_next += it.walk.end0 - it.walk.e0;
       bool have = present && it.walk.next(p.kidx, p.klabel, kt, la, lb);
       while (have) {
         const int lab = t == 0 ? la : lb;
         const int j0 = kt * kTile;
+        const int ue = ue_next++;  // union entry number over all items (ring position)
         // fetch the next entry now; its loads complete under this entry's work
         have = it.walk.next(p.kidx, p.klabel, kt, la, lb);
         if (lab == ATTN_TILE_EMPTY) continue;
@@ -625,19 +638,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
           if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-            const int k0tok = s0 + j0;
+            // the codes arrive with V(j): load 2 * ue + 1 of the ring
+            const int vload = 2 * ue + 1, vslot = vload % C::NSLOT;
+            if (!warp_wait(bar(C::B_FULL + vslot), uint32_t(vload / C::NSLOT) & 1u, abort_flag, err, 9)) {
+              ok = false;
+              break;
+            }
+            const int* codes = slot_codes + vslot * kTile;
             if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(p.mask, k0tok, q, kn, qcode);
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(codes, q, qcode);
             } else if (kind == ATTN_MASK_SHARED_PREFIX) {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(p.mask, k0tok, q, kn, qcode);
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(codes, q, qcode);
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(p.mask, k0tok, q, kn, qcode);
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
             }
           }
 #pragma unroll
@@ -679,7 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
-        float2 sum2 = make_float2(0.f, 0.f);
+        // four independent partial sums keep the additions off one serial chain
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh) {
           uint32_t pk[16];
@@ -687,12 +708,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; c += 2) {
             const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
             const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-            sum2 = ptx::fadd2(sum2, e);
+            sum2[(c >> 1) & 3] = ptx::fadd2(sum2[(c >> 1) & 3], e);
             pk[c >> 1] = ptx::pack_bf16(e.x, e.y);
           }
           ptx::tmem_st16(lane_base + colS + hh * 16, pk);
         }
-        l += sum2.x + sum2.y;
+        const float2 sa = ptx::fadd2(sum2[0], sum2[1]), sb = ptx::fadd2(sum2[2], sum2[3]);
+        l += (sa.x + sb.x) + (sa.y + sb.y);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(C::B_PFULL + t));
