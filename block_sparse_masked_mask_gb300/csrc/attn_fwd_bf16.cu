@@ -17,12 +17,10 @@
 //   warps 4-7  softmax of q-tile 1
 //   warp 8     TMA producer: Q0/Q1 once, then K(j), V(j) into a ring of
 //              four 128 x D slots; zeroes V rows past a sequence end
-//   warps 9-10 tcgen05 issuers, one thread each: warp 9 for q-tile 0, warp 10
-//              for q-tile 1 (warp 9 also owns the TMEM allocation).  Each
-//              issues PV(j) then S(j+1) for its q-tile, so one softmax group
-//              works while the tensor cores serve the other (ping-pong), and
-//              one issuer's barrier waits hide behind the other's MMAs.
-//   warp 11    idle
+//   warp 9     tcgen05 issuer (one thread; also owns the TMEM allocation):
+//              PV0(j), S0(j+1), PV1(j), S1(j+1), ... so the tensor cores
+//              serve one q-tile while the other's softmax runs (ping-pong)
+//   warps 10-11 idle
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
 // P (bf16) overwrites the first 64 columns of its S buffer.
 //
@@ -46,11 +44,11 @@ constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 25
 // 384 threads = 3 warpgroups, one warp of each on every SM sub-partition.
 // Launched at kLaunchRegs per thread; the two softmax warpgroups then take
 // kSoftmaxRegs and the producer / MMA warpgroup keeps kOtherRegs:
-// 2 * 216 + 72 = 504 = 3 * 168, the launch budget of a sub-partition's warps.
+// 2 * 208 + 88 = 504 = 3 * 168, the launch budget of a sub-partition's warps.
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 216;
-constexpr uint32_t kOtherRegs = 72;
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kOtherRegs = 88;
 static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
 
 template <int D>
@@ -332,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(C::B_Q), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(C::B_IFULL + s), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + s), 2 + 256);  // both MMA issuers + both softmax groups
+      ptx::mbar_init(bar(C::B_IEMPTY + s), 1 + 256);  // the MMA issuer + both softmax groups
     }
-    ptx::mbar_init(bar(C::B_QFREE), 2);  // both MMA issuers
+    ptx::mbar_init(bar(C::B_QFREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
-      ptx::mbar_init(bar(C::B_EMPTY + s), 2);  // both MMA issuers
+      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
     for (int t = 0; t < 2; ++t) {
@@ -346,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::B_ODONE + t), 1);
       ptx::mbar_init(bar(C::B_OFREE + t), 128);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 2);
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
@@ -488,16 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
     }
     __syncwarp();
-   } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------------------ MMA issuers
-    // Warp 9 issues q-tile 0's MMAs, warp 10 q-tile 1's (one thread each), so
-    // one issuer's barrier waits hide behind the other's MMAs.
+   } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    // One thread issues every MMA, strictly alternating between the q-tiles:
+    // PV0(j), S0(j+1), PV1(j), S1(j+1), ...  The tensor pipe executes them in
+    // that order, so one q-tile's S is ready while the other's P.V and S are
+    // still running, and the two softmax groups take turns instead of running
+    // (and contending) at the same time.
     if (lane == 0) {
-      const int t = warp - 9;
-      const uint32_t colS = C::col_s(t), colO = C::col_o(t);
-      int nload = 0, cnt = 0;
+      int nload = 0;
+      int cnt[2] = {0, 0};  // P.V products issued per q-tile slot (its PFULL phases)
       bool ok = true;
-      const uint64_t qdesc = kmajor_base<D>(t == 0 ? sQ0 : sQ1);
+      const uint64_t qdesc[2] = {kmajor_base<D>(sQ0), kmajor_base<D>(sQ1)};
       const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -506,13 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
         if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
-        bool first = true;  // first P.V of this item
         if (it.walk.e0 == it.walk.end0 && it.walk.e1 == it.walk.end1) {  // no entries
           ptx::mma_commit(bar(C::B_QFREE));
           continue;
         }
+        bool first[2] = {true, true};  // no P.V of this item issued yet
+        int lab[2];
         // entry 0: S from K(0)
-        int lab;
         {
           const int slot = nload % C::NSLOT;
           if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
@@ -520,10 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          lab = int((slot_info[slot] >> (2 * t)) & 3u);
-          if (lab) {
-            issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(slot) * (C::TILE >> 4));
-            ptx::mma_commit(bar(C::B_SFULL + t));
+          const uint32_t info = slot_info[slot];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            lab[t] = int((info >> (2 * t)) & 3u);
+            if (lab[t]) {
+              issue_s<D>(tmem + C::col_s(t), qdesc[t], kdesc0 + uint64_t(slot) * (C::TILE >> 4));
+              ptx::mma_commit(bar(C::B_SFULL + t));
+            }
           }
           ptx::mma_commit(bar(C::B_EMPTY + slot));
           ++nload;
@@ -536,36 +540,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const bool nxt = (slot_info[vslot] & kInfoHasNext) != 0u;
-          // every S of this item has been issued: Q may be replaced once they finish
-          if (!nxt) ptx::mma_commit(bar(C::B_QFREE));
-          if (lab) {
-            if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 5)) { ok = false; break; }
-            if (first && k > 0 &&
-                !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
-            ptx::tc_fence_after();
-            issue_pv<D>(tmem + colO, tmem + colS, vdesc0 + uint64_t(vslot) * (C::TILE >> 4), !first);
-            first = false;
-            ++cnt;
+          int nlab[2] = {0, 0};
+          const int kslot = (nload + 1) % C::NSLOT;
+          if (nxt) {
+            // K(j+1), so that S(j+1) follows each P.V(j) without a gap
+            if (!wait_bar(bar(C::B_FULL + kslot), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+              ok = false;
+              break;
+            }
+            const uint32_t info = slot_info[kslot];
+            nlab[0] = int(info & 3u);
+            nlab[1] = int((info >> 2) & 3u);
+          } else {
+            // every S of this item has been issued: Q may be replaced once they finish
+            ptx::mma_commit(bar(C::B_QFREE));
           }
-          // The item's last P.V: O is final once this arrives.
-          if (!nxt && !first) ptx::mma_commit(bar(C::B_ODONE + t));
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (lab[t]) {
+              if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt[t]) & 1u, abort_flag, err, 5)) { ok = false; break; }
+              if (first[t] && k > 0 &&
+                  !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
+              ptx::tc_fence_after();
+              issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), vdesc0 + uint64_t(vslot) * (C::TILE >> 4),
+                          !first[t]);
+              first[t] = false;
+              ++cnt[t];
+            }
+            // The item's last P.V: O is final once this arrives.
+            if (!nxt && !first[t]) ptx::mma_commit(bar(C::B_ODONE + t));
+            if (nlab[t]) {
+              issue_s<D>(tmem + C::col_s(t), qdesc[t], kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
+              ptx::mma_commit(bar(C::B_SFULL + t));
+            }
+          }
+          if (!ok) break;
           ptx::mma_commit(bar(C::B_EMPTY + vslot));
           ++nload;
           if (!nxt) break;
-          // K(j+1)
-          const int kslot = nload % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + kslot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          lab = int((slot_info[kslot] >> (2 * t)) & 3u);
-          if (lab) {
-            issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
-            ptx::mma_commit(bar(C::B_SFULL + t));
-          }
           ptx::mma_commit(bar(C::B_EMPTY + kslot));
           ++nload;
+          lab[0] = nlab[0];
+          lab[1] = nlab[1];
         }
       }
       // Every MMA this thread issued has finished once this commit arrives.
@@ -573,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-   }  // warp 11 idle
+   }  // warps 10-11 idle
   } else if (!skip) {
     ptx::regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
