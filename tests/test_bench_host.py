@@ -61,3 +61,26 @@ def test_reduce_max_over_two_gloo_ranks():
         assert p.exitcode == 0
     assert [r[1] for r in res] == [pytest.approx(0.02)] * 2
     assert [r[2] for r in res] == [pytest.approx(2e12 * 2 / 0.02 / 1e12)] * 2
+
+
+def test_profiled_traffic_only_for_the_profiled_kernel_source(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from the committed ncu summary, scaled by
+    heads, and is dropped (None) once the kernel source differs from the one
+    that was captured."""
+    import hashlib
+    fields = {}
+    for line in open(bench.TRAFFIC_PROFILE):
+        if ":" in line and not line.startswith(("|", "#", " ", "*")):
+            k, _, v = line.partition(":")
+            fields[k.strip()] = v.strip()
+    src = tmp_path / "kernel.cu"
+    src.write_bytes(b"// some other kernel\n")
+    monkeypatch.setattr(bench, "FWD_SOURCE", str(src))
+    assert bench.profiled_traffic(5, 32) == (None, None)
+    # a source whose hash matches the capture: traffic scales with the head count
+    monkeypatch.setattr(hashlib, "sha256", lambda b: type("H", (), {
+        "hexdigest": lambda self: fields["source_sha256"]})())
+    t, note = bench.profiled_traffic(5, 32)
+    assert t == int(fields["traffic_bytes_per_launch_h8"]) * 32 / int(fields["heads"])
+    assert "scaled" in note
+    assert bench.profiled_traffic(3, 32) == (None, None)
