@@ -17,10 +17,12 @@
 //   warps 4-7  softmax of q-tile 1
 //   warp 8     TMA producer: Q0/Q1 once, then K(j), V(j) into a ring of
 //              four 128 x D slots; zeroes V rows past a sequence end
-//   warp 9     tcgen05 issuer (one thread; also owns the TMEM allocation):
-//              PV0(j), S0(j+1), PV1(j), S1(j+1), ... so the tensor cores
-//              serve one q-tile while the other's softmax runs (ping-pong)
-//   warps 10-11 idle
+//   warps 9-10 tcgen05 issuers, one thread each: warp 9 for q-tile 0, warp 10
+//              for q-tile 1 (warp 9 also owns the TMEM allocation).  They
+//              take turns, PV0(j), S0(j+1) | PV1(j), S1(j+1) | ..., so the
+//              tensor cores serve one q-tile while the other's softmax runs
+//              (ping-pong), and each does its waits while the other issues.
+//   warp 11    idle
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
 // P (bf16) overwrites the first 64 columns of its S buffer.
 //
@@ -65,7 +67,7 @@ struct Cfg {
   static constexpr int B_Q = 0, B_QFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
                        B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                        B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_IEMPTY + 2, B_TURN = B_DRAIN + 1, NBAR = B_TURN + 2;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;    // two decoded work items, 8 ints each
@@ -330,12 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(C::B_Q), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(C::B_IFULL + s), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + s), 1 + 256);  // the MMA issuer + both softmax groups
+      ptx::mbar_init(bar(C::B_IEMPTY + s), 2 + 256);  // both MMA issuers + both softmax groups
     }
-    ptx::mbar_init(bar(C::B_QFREE), 1);
+    ptx::mbar_init(bar(C::B_QFREE), 2);  // both MMA issuers
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
-      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+      ptx::mbar_init(bar(C::B_EMPTY + s), 2);  // both MMA issuers
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
     for (int t = 0; t < 2; ++t) {
@@ -344,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::B_ODONE + t), 1);
       ptx::mbar_init(bar(C::B_OFREE + t), 128);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::mbar_init(bar(C::B_DRAIN), 2);
+    for (int t = 0; t < 2; ++t) ptx::mbar_init(bar(C::B_TURN + t), 1);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
@@ -486,19 +489,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
     }
     __syncwarp();
-   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread issues every MMA, strictly alternating between the q-tiles:
-    // PV0(j), S0(j+1), PV1(j), S1(j+1), ...  The tensor pipe executes them in
-    // that order, so one q-tile's S is ready while the other's P.V and S are
-    // still running, and the two softmax groups take turns instead of running
-    // (and contending) at the same time.
+   } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread of warp 9 issues q-tile 0's MMAs, one of warp 10 q-tile 1's.
+    // They take turns: PV0(j), S0(j+1) | PV1(j), S1(j+1) | PV0(j+1), ... so the
+    // tensor pipe serves the q-tiles alternately (one softmax group works while
+    // the pipe runs the other's products).  An MMA issue blocks while the
+    // pipe's short queue is full, so each issuer does its barrier waits and
+    // commits while the other one is issuing, and the queue does not run dry.
     if (lane == 0) {
-      int nload = 0;
-      int cnt[2] = {0, 0};  // P.V products issued per q-tile slot (its PFULL phases)
+      const int t = warp - 9;
+      const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+      int nload = 0, cnt = 0, nturn = 0;
       bool ok = true;
-      const uint64_t qdesc[2] = {kmajor_base<D>(sQ0), kmajor_base<D>(sQ1)};
+      const uint64_t qdesc = kmajor_base<D>(t == 0 ? sQ0 : sQ1);
       const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
+      // Turn n of issuer 0 follows turn n-1 of issuer 1; turn n of issuer 1
+      // follows turn n of issuer 0.
+      auto take_turn = [&]() -> bool {
+        if (t == 0 && nturn == 0) return true;
+        return wait_bar(bar(C::B_TURN + t), uint32_t(t == 0 ? nturn - 1 : nturn) & 1u, abort_flag, err, 18);
+      };
+      auto pass_turn = [&]() {
+        ptx::mbar_arrive(bar(C::B_TURN + (1 - t)));
+        ++nturn;
+      };
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
         Item it;
@@ -510,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(bar(C::B_QFREE));
           continue;
         }
-        bool first[2] = {true, true};  // no P.V of this item issued yet
-        int lab[2];
+        bool first = true;  // no P.V of this item issued yet
+        int lab;
         // entry 0: S from K(0)
         {
           const int slot = nload % C::NSLOT;
@@ -520,15 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t info = slot_info[slot];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            lab[t] = int((info >> (2 * t)) & 3u);
-            if (lab[t]) {
-              issue_s<D>(tmem + C::col_s(t), qdesc[t], kdesc0 + uint64_t(slot) * (C::TILE >> 4));
-              ptx::mma_commit(bar(C::B_SFULL + t));
-            }
-          }
+          lab = int((slot_info[slot] >> (2 * t)) & 3u);
+          if (!take_turn()) { ok = false; break; }
+          if (lab) issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(slot) * (C::TILE >> 4));
+          pass_turn();
+          if (lab) ptx::mma_commit(bar(C::B_SFULL + t));
           ptx::mma_commit(bar(C::B_EMPTY + slot));
           ++nload;
         }
@@ -540,49 +551,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const bool nxt = (slot_info[vslot] & kInfoHasNext) != 0u;
-          int nlab[2] = {0, 0};
           const int kslot = (nload + 1) % C::NSLOT;
+          int nlab = 0;
           if (nxt) {
-            // K(j+1), so that S(j+1) follows each P.V(j) without a gap
+            // K(j+1), so that S(j+1) follows P.V(j) in the same turn
             if (!wait_bar(bar(C::B_FULL + kslot), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
               ok = false;
               break;
             }
-            const uint32_t info = slot_info[kslot];
-            nlab[0] = int(info & 3u);
-            nlab[1] = int((info >> 2) & 3u);
+            nlab = int((slot_info[kslot] >> (2 * t)) & 3u);
           } else {
             // every S of this item has been issued: Q may be replaced once they finish
             ptx::mma_commit(bar(C::B_QFREE));
           }
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (lab[t]) {
-              if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt[t]) & 1u, abort_flag, err, 5)) { ok = false; break; }
-              if (first[t] && k > 0 &&
-                  !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
-              ptx::tc_fence_after();
-              issue_pv<D>(tmem + C::col_o(t), tmem + C::col_s(t), vdesc0 + uint64_t(vslot) * (C::TILE >> 4),
-                          !first[t]);
-              first[t] = false;
-              ++cnt[t];
-            }
-            // The item's last P.V: O is final once this arrives.
-            if (!nxt && !first[t]) ptx::mma_commit(bar(C::B_ODONE + t));
-            if (nlab[t]) {
-              issue_s<D>(tmem + C::col_s(t), qdesc[t], kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
-              ptx::mma_commit(bar(C::B_SFULL + t));
-            }
+          if (lab) {
+            if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 5)) { ok = false; break; }
+            if (first && k > 0 &&
+                !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
           }
-          if (!ok) break;
+          ptx::tc_fence_after();
+          if (!take_turn()) { ok = false; break; }
+          if (lab) issue_pv<D>(tmem + colO, tmem + colS, vdesc0 + uint64_t(vslot) * (C::TILE >> 4), !first);
+          if (nlab) issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
+          pass_turn();
+          if (lab) {
+            first = false;
+            ++cnt;
+          }
+          // The item's last P.V: O is final once this arrives.
+          if (!nxt && !first) ptx::mma_commit(bar(C::B_ODONE + t));
+          if (nlab) ptx::mma_commit(bar(C::B_SFULL + t));
           ptx::mma_commit(bar(C::B_EMPTY + vslot));
           ++nload;
           if (!nxt) break;
           ptx::mma_commit(bar(C::B_EMPTY + kslot));
           ++nload;
-          lab[0] = nlab[0];
-          lab[1] = nlab[1];
+          lab = nlab;
         }
       }
       // Every MMA this thread issued has finished once this commit arrives.
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-   }  // warps 10-11 idle
+   }  // warp 11 idle
   } else if (!skip) {
     ptx::regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
