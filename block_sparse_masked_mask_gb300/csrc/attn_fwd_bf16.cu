@@ -56,6 +56,7 @@ static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split 
 template <int D>
 struct Cfg {
   static constexpr int NSLOT = 4;                     // K/V ring slots (one tile each)
+  static constexpr int NCODE = 3;                     // key-code buffers, one per ring entry in flight
   static constexpr int CE = D >= 64 ? 64 : 32;        // bf16 elements per swizzled row chunk
   static constexpr int ROWB = CE * 2;                 // bytes per row chunk (128 or 64)
   static constexpr int NCH = D / CE;                  // row chunks per tile
@@ -67,13 +68,13 @@ struct Cfg {
   static constexpr int B_Q = 0, B_QFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
                        B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
                        B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, B_TURN = B_DRAIN + 1, NBAR = B_TURN + 2;
+                       B_DRAIN = B_IEMPTY + 2, B_TURN = B_DRAIN + 1, B_CODE = B_TURN + 2, NBAR = B_CODE + NCODE;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;    // two decoded work items, 8 ints each
   static constexpr int OFF_SINFO = OFF_RINGI + 2 * 8 * 4;  // per ring slot: labels / has-next
-  static constexpr int OFF_CODES = (OFF_SINFO + NSLOT * 4 + 15) & ~15;  // per slot: 128 key codes
-  static constexpr int SMEM_USED = OFF_CODES + NSLOT * kTile * 4;
+  static constexpr int OFF_CODES = (OFF_SINFO + NSLOT * 4 + 15) & ~15;  // per buffer: 128 key codes
+  static constexpr int SMEM_USED = OFF_CODES + NCODE * kTile * 4;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
@@ -348,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar(C::B_DRAIN), 2);
     for (int t = 0; t < 2; ++t) ptx::mbar_init(bar(C::B_TURN + t), 1);
+    for (int c = 0; c < C::NCODE; ++c) ptx::mbar_init(bar(C::B_CODE + c), 1);
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
@@ -410,6 +412,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // Keys' mask codes for the softmax of PARTIAL tiles, in buffer j % 3,
+        // ready when S(j) is.  The buffer's previous entry, j - 3, is done with
+        // it: K(j-2)'s slot is freed by each MMA thread after its P.V(j-3),
+        // which it issues only once that q-tile's softmax of entry j-3 is over.
+        {
+          const int cb = (nload / 2) % C::NCODE;
+          if (p.mask.kind != ATTN_MASK_CAUSAL && (la == ATTN_TILE_PARTIAL || lb == ATTN_TILE_PARTIAL)) {
+            for (int c = lane; c < kTile; c += 32)
+              slot_codes[cb * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
+            __syncwarp();
+          }
+          if (lane == 0) ptx::mbar_arrive(bar(C::B_CODE + cb));
+        }
         if (lane == 0) {
           slot_info[slot] = uint32_t(la) | (uint32_t(lb) << 2);
           ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
@@ -424,13 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
           ok = false;
           break;
-        }
-        // Keys' mask codes for the softmax of PARTIAL tiles; they live as long
-        // as V(j), i.e. until both q-tiles' P.V(j) are done.
-        if (p.mask.kind != ATTN_MASK_CAUSAL && (la == ATTN_TILE_PARTIAL || lb == ATTN_TILE_PARTIAL)) {
-          for (int c = lane; c < kTile; c += 32)
-            slot_codes[slot * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
-          __syncwarp();
         }
         if (kn < kTile) {
           // Rows past the sequence end come from the next sequence (or are zero
@@ -622,6 +630,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int il = it0 + r;                  // local query index
       const int s0 = it.s0, L = it.L;
       const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
+      // The rows of a warp usually share one query code (one document, one
+      // turn).  A key's visibility is then the same for all of them, and one
+      // ballot over the keys' codes replaces 32 tests per row.
+      const int qcode_w = __shfl_sync(0xffffffffu, qcode, 0);
+      const bool uniform_q = __all_sync(0xffffffffu, !row_in || qcode == qcode_w);
       float m_ref = -INFINITY, l = 0.f;
       int cnt_item = 0;
       int kt, la, lb;
@@ -659,14 +672,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
           if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-            // the codes arrive with V(j): load 2 * ue + 1 of the ring
-            const int vload = 2 * ue + 1, vslot = vload % C::NSLOT;
-            if (!warp_wait(bar(C::B_FULL + vslot), uint32_t(vload / C::NSLOT) & 1u, abort_flag, err, 9)) {
+            // the producer wrote this entry's key codes before loading K(j)
+            if (!warp_wait(bar(C::B_CODE + ue % C::NCODE), uint32_t(ue / C::NCODE) & 1u, abort_flag, err, 9)) {
               ok = false;
               break;
             }
-            const int* codes = slot_codes + vslot * kTile;
-            if (kind == ATTN_MASK_STRIP_THINKING) {
+            const int* codes = slot_codes + (ue % C::NCODE) * kTile;
+            if (uniform_q) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                vis[q] &= __ballot_sync(0xffffffffu, code_visible(kind, qcode_w, codes[32 * q + lane]));
+            } else if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(codes, q, qcode);
