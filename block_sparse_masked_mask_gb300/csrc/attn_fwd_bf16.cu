@@ -679,9 +679,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int* codes = slot_codes + (ue % C::NCODE) * kTile;
             if (uniform_q) {
+              int kc[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                vis[q] &= __ballot_sync(0xffffffffu, code_visible(kind, qcode_w, codes[32 * q + lane]));
+              for (int q = 0; q < 4; ++q) kc[q] = codes[32 * q + lane];
+              if (kind == ATTN_MASK_STRIP_THINKING) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_STRIP_THINKING, qcode_w, kc[q]));
+              } else if (kind == ATTN_MASK_SHARED_PREFIX) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc[q]));
+              } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc[q]));
+              }
             } else if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
@@ -696,8 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
             }
           }
+          // A word the whole warp sees needs no select (on a diagonal tile, the
+          // words left of the warp's own rows).
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (vis[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
+          for (int q = 0; q < 4; ++q) {
+            if (__all_sync(0xffffffffu, vis[q] == 0xffffffffu)) continue;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) s[32 * q + c] = (vis[q] >> c) & 1u ? s[32 * q + c] : -INFINITY;
+          }
         }
         float mx8[8];
 #pragma unroll
