@@ -7,24 +7,26 @@
 // k-tiles the block mask lists are visited (Ch. 9, Section 9.2: a skipped
 // tile is never loaded).
 //
-// A work item is a pair of adjacent 128-row q-tiles of one sequence (the
-// second may be absent) and one head; persistent CTAs (one per SM) loop over
-// the items.  The pair walks the
-// ascending union of its two k-tile lists; each K and V tile is loaded once
-// and serves both q-tiles, and a q-tile skips the entries its own list does
-// not hold (EMPTY for it).  Warp roles:
-//   warps 0-3  softmax of q-tile 0, one thread per query row
-//   warps 4-7  softmax of q-tile 1
-//   warp 8     TMA producer: Q0/Q1 once, then K(j), V(j) into a ring of
-//              four 128 x D slots; zeroes V rows past a sequence end
-//   warps 9-10 tcgen05 issuers, one thread each: warp 9 for q-tile 0, warp 10
-//              for q-tile 1 (warp 9 also owns the TMEM allocation).  They
-//              take turns, PV0(j), S0(j+1) | PV1(j), S1(j+1) | ..., so the
-//              tensor cores serve one q-tile while the other's softmax runs
-//              (ping-pong), and each does its waits while the other issues.
-//   warp 11    idle
-// TMEM columns: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).
-// P (bf16) overwrites the first 64 columns of its S buffer.
+// A work item is one 128-row q-tile of one sequence and one head; persistent
+// CTAs (one per SM) take the items longest first and walk each q-tile's k-tile
+// list in ascending order.  Warp roles (384 threads):
+//   warps 0-7  softmax, two threads per query row: warps 0-3 take score
+//              columns 0-63 of every k-tile, warps 4-7 columns 64-127
+//   warp 8     TMA producer of Q and of the K ring (three slots); stages the
+//              keys' mask codes of PARTIAL tiles; takes the work tickets
+//   warp 9     tcgen05 issuer of the P.V products (one thread; also owns the
+//              TMEM allocation)
+//   warp 10    TMA producer of the V ring (two slots); zeroes V rows past a
+//              sequence end
+//   warp 11    tcgen05 issuer of the S = Q K^T products (one thread)
+// The two issuers work independently: an MMA issue blocks while the tensor
+// pipe's short queue is full, and with two threads one waits on its barriers
+// while the other keeps the queue fed.
+// TMEM columns: S0 [0,128) and S1 [128,256) hold S of alternate k-tiles,
+// O_A [256, 256+D) and O_B [384, 384+D) the two column halves' accumulators.
+// Each half writes its bf16 P over the first 32 of its own 64 S columns.  With
+// S double-buffered, the tensor cores compute S(j+1) and P(j-1).V while the
+// softmax works on S(j).
 //
 // The row maximum used as the exponent reference only moves when a new tile
 // raises it by more than 2^8 (factor 256 in p); O and l are then rescaled
@@ -43,20 +45,14 @@ namespace {
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: far above any legitimate wait
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // bound on waiting for in-flight work
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 256
-// 384 threads = 3 warpgroups, one warp of each on every SM sub-partition.
-// Launched at kLaunchRegs per thread; the two softmax warpgroups then take
-// kSoftmaxRegs and the producer / MMA warpgroup keeps kOtherRegs:
-// 2 * 208 + 88 = 504 = 3 * 168, the launch budget of a sub-partition's warps.
 constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 208;
-constexpr uint32_t kOtherRegs = 88;
-static_assert(2 * kSoftmaxRegs + kOtherRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
+constexpr int kWarpKLoad = 8, kWarpPV = 9, kWarpVLoad = 10, kWarpS = 11;
 
 template <int D>
 struct Cfg {
-  static constexpr int NSLOT = 4;                     // K/V ring slots (one tile each)
-  static constexpr int NCODE = 3;                     // key-code buffers, one per ring entry in flight
+  static constexpr int NK = 3;                        // K ring slots
+  static constexpr int NV = 2;                        // V ring slots
+  static constexpr int NCODE = 6;                     // key-code buffers (entries in flight)
   static constexpr int CE = D >= 64 ? 64 : 32;        // bf16 elements per swizzled row chunk
   static constexpr int ROWB = CE * 2;                 // bytes per row chunk (128 or 64)
   static constexpr int NCH = D / CE;                  // row chunks per tile
@@ -64,32 +60,34 @@ struct Cfg {
   static constexpr int TILE = NCH * CHUNK;            // 128 x D bf16
   static constexpr uint32_t SW = D >= 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
   static constexpr int SBO = 8 * ROWB;                // 8-row core-matrix group stride
-  static constexpr int OFF_Q0 = 0, OFF_Q1 = TILE, OFF_RING = 2 * TILE;
-  static constexpr int B_Q = 0, B_QFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
-                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-                       B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, B_TURN = B_DRAIN + 1, B_CODE = B_TURN + 2, NBAR = B_CODE + NCODE;
-  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
+  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = OFF_K + NK * TILE;
+  // PFULL / PDONE: [half][S buffer]; XCH: [item parity]
+  static constexpr int B_Q = 0, B_QFREE = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
+                       B_VEMPTY = B_VFULL + NV, B_VTMA = B_VEMPTY + NV, B_SFULL = B_VTMA + 1,
+                       B_PFULL = B_SFULL + 2, B_PDONE = B_PFULL + 4, B_ODONE = B_PDONE + 4,
+                       B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
+                       B_CODE = B_IEMPTY + 2, B_CODEFREE = B_CODE + NCODE, B_XCH = B_CODEFREE + NCODE,
+                       B_DRAIN = B_XCH + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_BAR = OFF_V + NV * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_RINGI = OFF_MISC + 16;    // two decoded work items, 8 ints each
-  static constexpr int OFF_SINFO = OFF_RINGI + 2 * 8 * 4;  // per ring slot: labels / has-next
-  static constexpr int OFF_CODES = (OFF_SINFO + NSLOT * 4 + 15) & ~15;  // per buffer: 128 key codes
-  static constexpr int SMEM_USED = OFF_CODES + NCODE * kTile * 4;
+  static constexpr int OFF_RINGI = OFF_MISC + 16;            // two decoded work items, 8 ints each
+  static constexpr int OFF_CODES = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;  // per buffer: 128 key codes
+  static constexpr int OFF_XCH = OFF_CODES + NCODE * kTile * 4;  // [item parity][m, l][half][row] floats
+  static constexpr int SMEM_USED = OFF_XCH + 2 * 2 * 2 * kTile * 4;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, D, false, true);
-  __host__ __device__ static constexpr uint32_t col_s(int t) { return uint32_t(t) * 128u; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
+  __host__ __device__ static constexpr uint32_t col_s(int i) { return uint32_t(i) * 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int h) { return 256u + uint32_t(h) * 128u; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
 struct FwdParams {
   int32_t* header;
-  const int32_t* pair_order;
-  const int32_t* pair_q0;
+  const int32_t* order;
   const int32_t* qt_seq;
   const int32_t* qt_idx;
   const int32_t* koff;
@@ -101,24 +99,6 @@ struct FwdParams {
   float* lse;
   int H, T;
   float scale_log2;  // scale * log2(e)
-};
-
-// Ascending union of the two q-tiles' k-tile lists, with each q-tile's label
-// (EMPTY where its own list lacks the k-tile).  Every role walks it alike.
-// Entries are positions in the CSR arrays: e0 .. end0 (q-tile 0), e1 .. end1.
-struct PairWalk {
-  int e0, end0, e1, end1;
-  __device__ bool next(const int32_t* kidx, const uint8_t* klabel, int& kt, int& a, int& b) {
-    const int x0 = e0 < end0 ? __ldg(kidx + e0) : INT_MAX;
-    const int x1 = e1 < end1 ? __ldg(kidx + e1) : INT_MAX;
-    kt = min(x0, x1);
-    if (kt == INT_MAX) return false;
-    a = ATTN_TILE_EMPTY;
-    b = ATTN_TILE_EMPTY;
-    if (x0 == kt) a = __ldg(klabel + e0++);
-    if (x1 == kt) b = __ldg(klabel + e1++);
-    return true;
-  }
 };
 
 // Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting.
@@ -204,6 +184,7 @@ __host__ __device__ constexpr uint64_t v_step(int kk) {
   return uint64_t(kk * 16 * C::ROWB) >> 4;
 }
 
+
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = Cfg<D>;
@@ -212,79 +193,68 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64
     ptx::mma_ss(d_tmem, q_desc + kmajor_step<D>(kk), k_desc + kmajor_step<D>(kk), C::IDESC_S, kk > 0);
 }
 
+// O_h += P_h V over keys [64h, 64h + 64): P_h is 128 x 64 bf16 in TMEM (32
+// columns), four k-steps of 16 keys.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool acc) {
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool acc, int h) {
   using C = Cfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc + v_step<D>(kk), C::IDESC_PV,
+  for (int kk = 0; kk < 4; ++kk)
+    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc + v_step<D>(4 * h + kk), C::IDESC_PV,
                 (acc || kk > 0) ? 1u : 0u);
 }
 
-// Per-slot note the producer leaves for the MMA issuer with every load:
-// K loads carry the two q-tiles' labels, V loads whether the item has another entry.
-constexpr uint32_t kInfoHasNext = 1u << 5;
-
-// One work item: a q-tile pair of one sequence and one head.
+// One work item: a q-tile of one sequence and one head; its k-tile list is
+// entries e0 .. e1 of the CSR arrays.
 struct Item {
-  int h, s0, L, qi0;
-  bool has1;
-  PairWalk walk;
+  int h, s0, L, qi0, e0, e1;
 };
 
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_pairs, int n_qt) {
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_qt) {
   Item it;
-  it.h = item / n_pairs;
-  const int g0 = p.pair_q0[p.pair_order[item % n_pairs]];
-  const int b = p.qt_seq[g0];
-  it.has1 = g0 + 1 < n_qt && p.qt_seq[g0 + 1] == b;
+  it.h = item / n_qt;
+  const int g = p.order[item % n_qt];
+  const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
   it.L = p.cu[b + 1] - it.s0;
-  it.qi0 = p.qt_idx[g0] * kTile;  // first query row of q-tile 0, local to the sequence
-  it.walk.e0 = p.koff[g0];
-  it.walk.end0 = p.koff[g0 + 1];
-  it.walk.e1 = it.walk.end0;
-  it.walk.end1 = it.has1 ? p.koff[g0 + 2] : it.walk.end0;
+  it.qi0 = p.qt_idx[g] * kTile;  // first query row of the q-tile, local to the sequence
+  it.e0 = p.koff[g];
+  it.e1 = p.koff[g + 1];
   return it;
 }
 
-// The producer publishes decoded items to the other roles as 8 ints.
+// The K producer publishes decoded items to the other roles as 8 ints.
 __device__ __forceinline__ void store_item(volatile int* d, const Item& it, bool valid) {
   d[0] = valid ? 1 : 0;
   d[1] = it.h;
   d[2] = it.s0;
   d[3] = it.L;
-  d[4] = it.qi0 | (it.has1 ? int(0x80000000) : 0);
-  d[5] = it.walk.e0;
-  d[6] = it.walk.end0;
-  d[7] = it.walk.end1;
+  d[4] = it.qi0;
+  d[5] = it.e0;
+  d[6] = it.e1;
 }
 __device__ __forceinline__ bool load_item(const volatile int* d, Item& it) {
   if (!d[0]) return false;
   it.h = d[1];
   it.s0 = d[2];
   it.L = d[3];
-  const int q = d[4];
-  it.has1 = q < 0;
-  it.qi0 = q & 0x7fffffff;
-  it.walk.e0 = d[5];
-  it.walk.end0 = d[6];
-  it.walk.e1 = it.walk.end0;
-  it.walk.end1 = d[7];
+  it.qi0 = d[4];
+  it.e0 = d[5];
+  it.e1 = d[6];
   return true;
 }
 
-// Producer warp: take a ticket, decode it and publish item k in ring slot k & 1
-// (barriers iempty0 / ifull0 and the next ones 8 bytes on).  Returns 1 for an
-// item, 0 when no work is left (an end marker is published), -1 on abort.
-__device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane, int n_items, int n_pairs,
-                                            int n_qt, Item& it, volatile int* item_ring, uint32_t iempty0,
+// Take a ticket, decode it and publish item k in ring slot k & 1 (barriers
+// iempty0 / ifull0 and the next ones 8 bytes on).  Returns 1 for an item, 0
+// when no work is left (an end marker is published), -1 on abort.
+__device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane, int n_items, int n_qt,
+                                            Item& it, volatile int* item_ring, uint32_t iempty0,
                                             uint32_t ifull0, volatile uint32_t* abort_flag, int32_t* err) {
   int ticket = 0;
   if (lane == 0) ticket = atomicAdd(p.header + kHdrTicket, 1);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   const bool valid = ticket < n_items;
-  if (valid) it = decode_item(p, ticket, n_pairs, n_qt);
+  if (valid) it = decode_item(p, ticket, n_qt);
   const int slot_i = k & 1;
   if (k >= 2 && !warp_wait(iempty0 + 8u * slot_i, uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 15))
     return -1;
@@ -296,13 +266,12 @@ __device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane,
 }
 
 // Persistent: each CTA takes work items from a global ticket counter (items
-// are head-major, longest q-tile pair first inside a head, so tickets hand
-// out the longest work first).  The producer takes the tickets, decodes them
-// one item ahead and passes them to the MMA warp and the softmax groups
-// through a two-slot ring in shared memory.  Barrier phases run on across
-// items; the next item's Q load and first S MMAs overlap the current item's
-// last P.V and O epilogue.  The last CTA to finish returns the counters to
-// zero for the next launch.
+// are head-major, longest q-tile first inside a head, so tickets hand out the
+// longest work first).  The K producer takes the tickets, decodes them one item
+// ahead and passes them to the other roles through a two-slot ring in shared
+// memory.  Barrier phases run on across items: the next item's Q load and
+// first S MMAs overlap the current item's last P.V and O epilogue.  The last
+// CTA to finish returns the counters to zero for the next launch.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -313,48 +282,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int n_qt = p.header[kHdrQtiles];
-  const int n_pairs = p.header[kHdrPairs];
-  const int n_items = n_pairs * p.H;
+  const int n_items = n_qt * p.H;
   int32_t* err = p.header + kHdrError;
 
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sQ0 = base + C::OFF_Q0, sQ1 = base + C::OFF_Q1, sRing = base + C::OFF_RING;
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
   const uint32_t bars = base + C::OFF_BAR;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
   volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);  // 2 x 8 ints
-  volatile uint32_t* slot_info = reinterpret_cast<volatile uint32_t*>(sbase + C::OFF_SINFO);
-  int* slot_codes = reinterpret_cast<int*>(sbase + C::OFF_CODES);
+  int* key_codes = reinterpret_cast<int*>(sbase + C::OFF_CODES);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_Q), 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(C::B_IFULL + s), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + s), 2 + 256);  // both MMA issuers + both softmax groups
+    ptx::mbar_init(bar(C::B_QFREE), 1);
+    for (int s = 0; s < C::NK; ++s) {
+      ptx::mbar_init(bar(C::B_KFULL + s), 1);
+      ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
     }
-    ptx::mbar_init(bar(C::B_QFREE), 2);  // both MMA issuers
-    for (int s = 0; s < C::NSLOT; ++s) {
-      ptx::mbar_init(bar(C::B_FULL + s), 1);
-      ptx::mbar_init(bar(C::B_EMPTY + s), 2);  // both MMA issuers
+    for (int s = 0; s < C::NV; ++s) {
+      ptx::mbar_init(bar(C::B_VFULL + s), 1);
+      ptx::mbar_init(bar(C::B_VEMPTY + s), 1);
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
-    for (int t = 0; t < 2; ++t) {
-      ptx::mbar_init(bar(C::B_SFULL + t), 1);
-      ptx::mbar_init(bar(C::B_PFULL + t), 128);
-      ptx::mbar_init(bar(C::B_ODONE + t), 1);
-      ptx::mbar_init(bar(C::B_OFREE + t), 128);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(C::B_SFULL + i), 1);
+      ptx::mbar_init(bar(C::B_IFULL + i), 1);
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 3);  // softmax threads, both MMA threads, V producer
+      ptx::mbar_init(bar(C::B_XCH + i), 256);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 2);
-    for (int t = 0; t < 2; ++t) ptx::mbar_init(bar(C::B_TURN + t), 1);
-    for (int c = 0; c < C::NCODE; ++c) ptx::mbar_init(bar(C::B_CODE + c), 1);
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(bar(C::B_PFULL + i), 128);
+      ptx::mbar_init(bar(C::B_PDONE + i), 1);
+    }
+    ptx::mbar_init(bar(C::B_ODONE), 1);
+    ptx::mbar_init(bar(C::B_OFREE), 256);
+    for (int c = 0; c < C::NCODE; ++c) {
+      ptx::mbar_init(bar(C::B_CODE + c), 1);
+      ptx::mbar_init(bar(C::B_CODEFREE + c), 256);
+    }
+    ptx::mbar_init(bar(C::B_DRAIN), 2);  // both MMA threads
     // An earlier CTA that gave up on a wait makes every later one skip its work.
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpPV) {
     ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -364,79 +339,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = misc[0];
   const bool skip = *abort_flag != 0u;
 
-  if (warp >= 8) {
-   ptx::regs_dec<kOtherRegs>();
-   if (skip) {
+  if (skip) {
     // nothing issued, nothing to drain
-   } else if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    int nload = 0, ntail = 0, nq = 0;
-    bool tail_pending = false, ok = true;
+  } else if (warp == kWarpKLoad) {
+    // ------------------------------------------------------------ Q, K, key codes
+    int nk = 0, nq = 0, ue = 0;
+    bool ok = true;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
       ptx::prefetch_tensormap(&tmK);
-      ptx::prefetch_tensormap(&tmV);
     }
     // Take a ticket, decode it and publish it in ring slot k & 1, one item
     // ahead of the loads, so the other roles never wait on the decoding.
     Item it_next;
-    int st_next = publish_item(p, 0, lane, n_items, n_pairs, n_qt, it_next, item_ring,
-                               bar(C::B_IEMPTY), bar(C::B_IFULL), abort_flag, err);
+    int st_next = publish_item(p, 0, lane, n_items, n_qt, it_next, item_ring, bar(C::B_IEMPTY),
+                               bar(C::B_IFULL), abort_flag, err);
     for (int k = 0; ok && st_next == 1; ++k) {
-      Item it = it_next;
-      st_next = publish_item(p, k + 1, lane, n_items, n_pairs, n_qt, it_next, item_ring,
-                             bar(C::B_IEMPTY), bar(C::B_IFULL), abort_flag, err);
+      const Item it = it_next;
+      st_next = publish_item(p, k + 1, lane, n_items, n_qt, it_next, item_ring, bar(C::B_IEMPTY),
+                             bar(C::B_IFULL), abort_flag, err);
       if (st_next < 0) break;
       // Q of this item, once the previous item's S MMAs no longer read Q.
       if (nq > 0 && !warp_wait(bar(C::B_QFREE), uint32_t(nq - 1) & 1u, abort_flag, err, 13)) break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE * (it.has1 ? 2 : 1));
+        ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sQ0 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h, it.s0 + it.qi0);
-        if (it.has1)
-          for (int c = 0; c < C::NCH; ++c)
-            ptx::tma_load_3d(sQ1 + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h,
-                             it.s0 + it.qi0 + kTile);
+          ptx::tma_load_3d(sQ + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h, it.s0 + it.qi0);
       }
       ++nq;
-      int kt, la, lb;
-      bool have = it.walk.next(p.kidx, p.klabel, kt, la, lb);
-      while (have) {
-        int kt2, la2, lb2;
-        const bool nxt = it.walk.next(p.kidx, p.klabel, kt2, la2, lb2);
-        const int j0 = kt * kTile, kn = min(kTile, it.L - j0);
-        // K(j)
-        int slot = nload % C::NSLOT;
-        if (nload >= C::NSLOT &&
-            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
+      for (int e = it.e0; e < it.e1; ++e) {
+        const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, it.L - j0);
+        const int lab = __ldg(p.klabel + e);
+        // Keys' mask codes for the softmax of a PARTIAL tile, in buffer ue % NCODE
+        // once the softmax is done with the buffer's previous entry.
+        const int cb = ue % C::NCODE;
+        if (ue >= C::NCODE &&
+            !warp_wait(bar(C::B_CODEFREE + cb), uint32_t(ue / C::NCODE - 1) & 1u, abort_flag, err, 10)) {
           ok = false;
           break;
         }
-        // Keys' mask codes for the softmax of PARTIAL tiles, in buffer j % 3,
-        // ready when S(j) is.  The buffer's previous entry, j - 3, is done with
-        // it: K(j-2)'s slot is freed by each MMA thread after its P.V(j-3),
-        // which it issues only once that q-tile's softmax of entry j-3 is over.
-        {
-          const int cb = (nload / 2) % C::NCODE;
-          if (p.mask.kind != ATTN_MASK_CAUSAL && (la == ATTN_TILE_PARTIAL || lb == ATTN_TILE_PARTIAL)) {
-            for (int c = lane; c < kTile; c += 32)
-              slot_codes[cb * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
-            __syncwarp();
-          }
-          if (lane == 0) ptx::mbar_arrive(bar(C::B_CODE + cb));
+        if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL) {
+          for (int c = lane; c < kTile; c += 32)
+            key_codes[cb * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
+          __syncwarp();
+        }
+        if (lane == 0) ptx::mbar_arrive(bar(C::B_CODE + cb));
+        ++ue;
+        // K(j)
+        const int slot = nk % C::NK;
+        if (nk >= C::NK &&
+            !warp_wait(bar(C::B_KEMPTY + slot), uint32_t(nk / C::NK - 1) & 1u, abort_flag, err, 1)) {
+          ok = false;
+          break;
         }
         if (lane == 0) {
-          slot_info[slot] = uint32_t(la) | (uint32_t(lb) << 2);
-          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+          ptx::mbar_arrive_expect_tx(bar(C::B_KFULL + slot), C::TILE);
           for (int c = 0; c < C::NCH; ++c)
-            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmK, bar(C::B_FULL + slot),
-                             c * C::CE, it.h, it.s0 + j0);
+            ptx::tma_load_3d(sK + slot * C::TILE + c * C::CHUNK, &tmK, bar(C::B_KFULL + slot), c * C::CE,
+                             it.h, it.s0 + j0);
         }
-        ++nload;
-        // V(j)
-        slot = nload % C::NSLOT;
-        if (nload >= C::NSLOT &&
-            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
+        ++nk;
+      }
+    }
+    // Do not leave while a load this CTA issued may still be writing shared memory.
+    if (lane == 0) {
+      for (int s = 0; s < C::NK; ++s) {
+        if (nk <= s) continue;
+        const int last = s + C::NK * ((nk - 1 - s) / C::NK);  // last load into slot s
+        drain_bar(bar(C::B_KFULL + s), uint32_t(last / C::NK) & 1u, err);
+      }
+      if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpVLoad) {
+    // ------------------------------------------------------------ V
+    int nv = 0, ntail = 0;
+    bool tail_pending = false, ok = true;
+    if (lane == 0) ptx::prefetch_tensormap(&tmV);
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      Item it;
+      const bool valid = load_item(item_ring + 8 * (k & 1), it);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      for (int e = it.e0; e < it.e1; ++e) {
+        const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, it.L - j0);
+        const int slot = nv % C::NV;
+        if (nv >= C::NV &&
+            !warp_wait(bar(C::B_VEMPTY + slot), uint32_t(nv / C::NV - 1) & 1u, abort_flag, err, 1)) {
           ok = false;
           break;
         }
@@ -447,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             ptx::mbar_arrive_expect_tx(bar(C::B_VTMA), C::TILE);
             for (int c = 0; c < C::NCH; ++c)
-              ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VTMA), c * C::CE,
-                               it.h, it.s0 + j0);
+              ptx::tma_load_3d(sV + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VTMA), c * C::CE, it.h,
+                               it.s0 + j0);
           }
           tail_pending = true;
           if (!warp_wait(bar(C::B_VTMA), uint32_t(ntail) & 1u, abort_flag, err, 2)) {
@@ -460,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int rr = kn + lane; rr < kTile; rr += 32) {
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-              uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_RING + slot * C::TILE + c * C::CHUNK +
+              uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_V + slot * C::TILE + c * C::CHUNK +
                                                     rr * C::ROWB);
 #pragma unroll
               for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
@@ -468,154 +459,127 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            slot_info[slot] = nxt ? kInfoHasNext : 0u;
-            ptx::mbar_arrive(bar(C::B_FULL + slot));
-          }
+          if (lane == 0) ptx::mbar_arrive(bar(C::B_VFULL + slot));
         } else if (lane == 0) {
-          slot_info[slot] = nxt ? kInfoHasNext : 0u;
-          ptx::mbar_arrive_expect_tx(bar(C::B_FULL + slot), C::TILE);
+          ptx::mbar_arrive_expect_tx(bar(C::B_VFULL + slot), C::TILE);
           for (int c = 0; c < C::NCH; ++c)
-            ptx::tma_load_3d(sRing + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_FULL + slot),
-                             c * C::CE, it.h, it.s0 + j0);
+            ptx::tma_load_3d(sV + slot * C::TILE + c * C::CHUNK, &tmV, bar(C::B_VFULL + slot), c * C::CE,
+                             it.h, it.s0 + j0);
         }
-        ++nload;
-        kt = kt2;
-        la = la2;
-        lb = lb2;
-        have = nxt;
+        ++nv;
       }
     }
-    // Do not leave while a load this CTA issued may still be writing shared memory.
     if (lane == 0) {
-      for (int s = 0; s < C::NSLOT; ++s) {
-        if (nload <= s) continue;
-        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);  // last load into slot s
-        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
+      for (int s = 0; s < C::NV; ++s) {
+        if (nv <= s) continue;
+        const int last = s + C::NV * ((nv - 1 - s) / C::NV);
+        drain_bar(bar(C::B_VFULL + s), uint32_t(last / C::NV) & 1u, err);
       }
       if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
-      if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
     }
     __syncwarp();
-   } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------------------ MMA issuers
-    // One thread of warp 9 issues q-tile 0's MMAs, one of warp 10 q-tile 1's.
-    // They take turns: PV0(j), S0(j+1) | PV1(j), S1(j+1) | PV0(j+1), ... so the
-    // tensor pipe serves the q-tiles alternately (one softmax group works while
-    // the pipe runs the other's products).  An MMA issue blocks while the
-    // pipe's short queue is full, so each issuer does its barrier waits and
-    // commits while the other one is issuing, and the queue does not run dry.
+  } else if (warp == kWarpS) {
+    // ------------------------------------------------------------ S issuer
+    // S(j) into S buffer j % 2 once both halves' P.V(j-2) have read the P
+    // written over S(j-2) there.
     if (lane == 0) {
-      const int t = warp - 9;
-      const uint32_t colS = C::col_s(t), colO = C::col_o(t);
-      int nload = 0, cnt = 0, nturn = 0;
+      int nkc = 0, ns = 0;  // K loads consumed, S issued (all items)
       bool ok = true;
-      const uint64_t qdesc = kmajor_base<D>(t == 0 ? sQ0 : sQ1);
-      const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
-      // Turn n of issuer 0 follows turn n-1 of issuer 1; turn n of issuer 1
-      // follows turn n of issuer 0.
-      auto take_turn = [&]() -> bool {
-        if (t == 0 && nturn == 0) return true;
-        return wait_bar(bar(C::B_TURN + t), uint32_t(t == 0 ? nturn - 1 : nturn) & 1u, abort_flag, err, 18);
-      };
-      auto pass_turn = [&]() {
-        ptx::mbar_arrive(bar(C::B_TURN + (1 - t)));
-        ++nturn;
-      };
+      const uint64_t qdesc = kmajor_base<D>(sQ), kdesc0 = kmajor_base<D>(sK);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
         Item it;
         const bool valid = load_item(item_ring + 8 * (k & 1), it);
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
-        if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
-        if (it.walk.e0 == it.walk.end0 && it.walk.e1 == it.walk.end1) {  // no entries
-          ptx::mma_commit(bar(C::B_QFREE));
-          continue;
-        }
-        bool first = true;  // no P.V of this item issued yet
-        int lab;
-        // entry 0: S from K(0)
-        {
-          const int slot = nload % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
+        if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) break;
+        for (int e = it.e0; e < it.e1; ++e) {
+          const int sb = ns & 1, ks = nkc % C::NK;
+          if (ns >= 2 && !wait_bar(bar(C::B_PDONE + 2 + sb), uint32_t((ns - 2) >> 1) & 1u, abort_flag, err, 7)) {
             ok = false;
             break;
           }
+          if (!wait_bar(bar(C::B_KFULL + ks), uint32_t(nkc / C::NK) & 1u, abort_flag, err, 4)) { ok = false; break; }
           ptx::tc_fence_after();
-          lab = int((slot_info[slot] >> (2 * t)) & 3u);
-          if (!take_turn()) { ok = false; break; }
-          if (lab) issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(slot) * (C::TILE >> 4));
-          pass_turn();
-          if (lab) ptx::mma_commit(bar(C::B_SFULL + t));
-          ptx::mma_commit(bar(C::B_EMPTY + slot));
-          ++nload;
+          issue_s<D>(tmem + C::col_s(sb), qdesc, kdesc0 + uint64_t(ks) * (C::TILE >> 4));
+          ptx::mma_commit(bar(C::B_SFULL + sb));
+          ptx::mma_commit(bar(C::B_KEMPTY + ks));
+          ++ns;
+          ++nkc;
         }
-        for (;;) {
-          // V(j): its note says whether entry j+1 exists
-          const int vslot = nload % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + vslot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 6)) {
-            ok = false;
-            break;
-          }
-          const bool nxt = (slot_info[vslot] & kInfoHasNext) != 0u;
-          const int kslot = (nload + 1) % C::NSLOT;
-          int nlab = 0;
-          if (nxt) {
-            // K(j+1), so that S(j+1) follows P.V(j) in the same turn
-            if (!wait_bar(bar(C::B_FULL + kslot), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
-              ok = false;
-              break;
-            }
-            nlab = int((slot_info[kslot] >> (2 * t)) & 3u);
-          } else {
-            // every S of this item has been issued: Q may be replaced once they finish
-            ptx::mma_commit(bar(C::B_QFREE));
-          }
-          if (lab) {
-            if (!wait_bar(bar(C::B_PFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 5)) { ok = false; break; }
-            if (first && k > 0 &&
-                !wait_bar(bar(C::B_OFREE + t), uint32_t(k - 1) & 1u, abort_flag, err, 14)) { ok = false; break; }
-          }
-          ptx::tc_fence_after();
-          if (!take_turn()) { ok = false; break; }
-          if (lab) issue_pv<D>(tmem + colO, tmem + colS, vdesc0 + uint64_t(vslot) * (C::TILE >> 4), !first);
-          if (nlab) issue_s<D>(tmem + colS, qdesc, kdesc0 + uint64_t(kslot) * (C::TILE >> 4));
-          pass_turn();
-          if (lab) {
-            first = false;
-            ++cnt;
-          }
-          // The item's last P.V: O is final once this arrives.
-          if (!nxt && !first) ptx::mma_commit(bar(C::B_ODONE + t));
-          if (nlab) ptx::mma_commit(bar(C::B_SFULL + t));
-          ptx::mma_commit(bar(C::B_EMPTY + vslot));
-          ++nload;
-          if (!nxt) break;
-          ptx::mma_commit(bar(C::B_EMPTY + kslot));
-          ++nload;
-          lab = nlab;
-        }
+        // every S of this item has been issued: Q may be replaced once they finish
+        ptx::mma_commit(bar(C::B_QFREE));
       }
       // Every MMA this thread issued has finished once this commit arrives.
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-   }  // warp 11 idle
-  } else if (!skip) {
-    ptx::regs_inc<kSoftmaxRegs>();
+  } else if (warp == kWarpPV) {
+    // ------------------------------------------------------------ P.V issuer
+    if (lane == 0) {
+      int nvc = 0, np = 0;  // V loads consumed, P.V issued (all items)
+      bool ok = true;
+      const uint64_t vdesc0 = v_base<D>(sV);
+      for (int k = 0; ok; ++k) {
+        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+        Item it;
+        const bool valid = load_item(item_ring + 8 * (k & 1), it);
+        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        if (!valid) break;
+        const int n = it.e1 - it.e0;
+        for (int j = 0; j < n; ++j) {
+          const int pb = np & 1, vs = nvc % C::NV;
+          const uint64_t vd = vdesc0 + uint64_t(vs) * (C::TILE >> 4);
+          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
+            ok = false;
+            break;
+          }
+          if (!wait_bar(bar(C::B_VFULL + vs), uint32_t(nvc / C::NV) & 1u, abort_flag, err, 6)) { ok = false; break; }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // half h: O_h += P_h V[64h, 64h + 64)
+            if (!wait_bar(bar(C::B_PFULL + 2 * h + pb), uint32_t(np >> 1) & 1u, abort_flag, err, 5)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv_half<D>(tmem + C::col_o(h), tmem + C::col_s(pb) + 64u * h, vd, j > 0, h);
+            ptx::mma_commit(bar(C::B_PDONE + 2 * h + pb));
+          }
+          if (!ok) break;
+          // V(j) is read by no later MMA
+          ptx::mma_commit(bar(C::B_VEMPTY + vs));
+          ++np;
+          ++nvc;
+        }
+        // The item's last P.V: O is final once this arrives.
+        if (ok && n > 0) ptx::mma_commit(bar(C::B_ODONE));
+      }
+      ptx::mma_commit(bar(C::B_DRAIN));
+      drain_bar(bar(C::B_DRAIN), 0, err);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;                   // which q-tile of the pair
+    // Two threads per query row: warps 0-3 take score columns 0-63 of every
+    // k-tile (half A), warps 4-7 columns 64-127 (half B).  Each half is its
+    // own online softmax over its columns, with its own reference m, sum l
+    // and accumulator O_A or O_B (its P.V covers only its 64 keys), so the
+    // halves never wait for each other inside the loop; the two partial
+    // results are merged once per item:
+    //   O = (2^(mA-m) O_A + 2^(mB-m) O_B) / (2^(mA-m) lA + 2^(mB-m) lB),  m = max(mA, mB).
+    const int hf = warp >> 2;                  // 0: half A, 1: half B
     const int quarter = warp & 3;              // TMEM lanes this warp may access
-    const int r = quarter * 32 + lane;         // query row inside the tile
+    const int r = quarter * 32 + lane;         // query row inside the tile = TMEM lane
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+    const uint32_t col_o = C::col_o(hf);
     const float c2 = p.scale_log2;
-    int cnt = 0;     // entries processed by this q-tile slot over all items (barrier phases)
-    int nodone = 0;  // items whose final O this slot has waited for
-    int ue_next = 0; // union entries walked (both q-tiles), = K/V ring loads / 2
+    float* xch = reinterpret_cast<float*>(sbase + C::OFF_XCH);  // [item parity][m, l][half][row]
+    int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % 2
+    int ue = 0;      // the same count for the code buffers
+    int nodone = 0;  // items whose final O this warp has waited for
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -623,11 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = load_item(item_ring + 8 * (k & 1), it);
       ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
       if (!valid) break;
-      const bool present = t == 0 || it.has1;
-      const int it0 = it.qi0 + t * kTile;      // first row of this q-tile (local)
-      const int qn = present ? min(kTile, it.L - it0) : 0;
+      const int qn = min(kTile, it.L - it.qi0);
       const bool row_in = r < qn;
-      const int il = it0 + r;                  // local query index
+      const int il = it.qi0 + r;               // local query index
       const int s0 = it.s0, L = it.L;
       const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
       // The rows of a warp usually share one query code (one document, one
@@ -637,109 +599,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool uniform_q = __all_sync(0xffffffffu, !row_in || qcode == qcode_w);
       float m_ref = -INFINITY, l = 0.f;
       int cnt_item = 0;
-      int kt, la, lb;
-      // an absent second q-tile does not walk, but the ring still advanced by
-      // the item's union entries (q-tile 0's list)
-      if (!present) ue_next += it.walk.end0 - it.walk.e0;
-      bool have = present && it.walk.next(p.kidx, p.klabel, kt, la, lb);
-      while (have) {
-        const int lab = t == 0 ? la : lb;
-        const int j0 = kt * kTile;
-        const int ue = ue_next++;  // union entry number over all items (ring position)
-        // fetch the next entry now; its loads complete under this entry's work
-        have = it.walk.next(p.kidx, p.klabel, kt, la, lb);
-        if (lab == ATTN_TILE_EMPTY) continue;
-        const int kn = min(kTile, L - j0);
-        if (!warp_wait(bar(C::B_SFULL + t), uint32_t(cnt) & 1u, abort_flag, err, 8)) { ok = false; break; }
+      for (int e = it.e0; e < it.e1; ++e) {
+        const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, L - j0);
+        const int lab = __ldg(p.klabel + e);
+        const int sb = nsf & 1;
+        const uint32_t col_s = C::col_s(sb) + 64u * hf;  // this half's 64 score columns; its P goes
+                                                         // over the first 32 of them
+        if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(nsf >> 1) & 1u, abort_flag, err, 8)) { ok = false; break; }
         ptx::tc_fence_after();
-        float s[128];
+        float s[64];
         {
-          uint32_t v[4][32];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) ptx::tmem_ld32(lane_base + colS + q * 32, v[q]);
+          uint32_t v[2][32];
+          ptx::tmem_ld32(lane_base + col_s, v[0]);
+          ptx::tmem_ld32(lane_base + col_s + 32, v[1]);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[q][c]);
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(v[c >> 5][c & 31]);
         }
+        const int cb = ue % C::NCODE;
         if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
-          // bit c of vis[c / 32]: key column c is visible to this row.  Causal part
-          // and bounds: columns c < upto; PARTIAL tiles of the metadata kinds also
-          // AND in the per-key predicate.
-          const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
-          uint32_t vis[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
+          // bit c of vis[c / 32]: key column 64 * hf + c is visible to this row.
+          // Causal part and bounds: columns below upto; PARTIAL tiles of the
+          // metadata kinds also AND in the per-key predicate.
+          const int upto = (lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn) - 64 * hf;
+          uint32_t vis[2] = {prefix_bits(upto), prefix_bits(upto - 32)};
           if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-            // the producer wrote this entry's key codes before loading K(j)
-            if (!warp_wait(bar(C::B_CODE + ue % C::NCODE), uint32_t(ue / C::NCODE) & 1u, abort_flag, err, 9)) {
+            // the K producer staged this entry's key codes
+            if (!warp_wait(bar(C::B_CODE + cb), uint32_t(ue / C::NCODE) & 1u, abort_flag, err, 9)) {
               ok = false;
               break;
             }
-            const int* codes = slot_codes + (ue % C::NCODE) * kTile;
+            const int* codes = key_codes + cb * kTile + 64 * hf;
             if (uniform_q) {
-              int kc[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) kc[q] = codes[32 * q + lane];
+              const int kc0 = codes[lane], kc1 = codes[32 + lane];
               if (kind == ATTN_MASK_STRIP_THINKING) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_STRIP_THINKING, qcode_w, kc[q]));
+                vis[0] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_STRIP_THINKING, qcode_w, kc0));
+                vis[1] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_STRIP_THINKING, qcode_w, kc1));
               } else if (kind == ATTN_MASK_SHARED_PREFIX) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc[q]));
+                vis[0] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc0));
+                vis[1] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc1));
               } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  vis[q] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc[q]));
+                vis[0] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc0));
+                vis[1] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc1));
               }
             } else if (kind == ATTN_MASK_STRIP_THINKING) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
+              for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(codes, q, qcode);
             } else if (kind == ATTN_MASK_SHARED_PREFIX) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
+              for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(codes, q, qcode);
             } else {
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
+              for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
             }
           }
-          // A word the whole warp sees needs no select (on a diagonal tile, the
-          // words left of the warp's own rows).
+          // A word the whole warp sees needs no select.
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             if (__all_sync(0xffffffffu, vis[q] == 0xffffffffu)) continue;
 #pragma unroll
             for (int c = 0; c < 32; ++c) s[32 * q + c] = (vis[q] >> c) & 1u ? s[32 * q + c] : -INFINITY;
           }
         }
-        float mx8[8];
+        // done with this entry's code buffer (used or not)
+        ptx::mbar_arrive(bar(C::B_CODEFREE + cb));
+        ++ue;
+        float mx4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
           float mv = s[16 * u];
 #pragma unroll
           for (int c = 1; c < 15; c += 2) mv = ptx::fmax3(mv, s[16 * u + c], s[16 * u + c + 1]);
-          mx8[u] = fmaxf(mv, s[16 * u + 15]);
+          mx4[u] = fmaxf(mv, s[16 * u + 15]);
         }
-        const float mxs = ptx::fmax3(ptx::fmax3(mx8[0], mx8[1], mx8[2]), ptx::fmax3(mx8[3], mx8[4], mx8[5]),
-                                     fmaxf(mx8[6], mx8[7])) * c2;
+        const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
         const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
         const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
         const float m_new = raise ? mxs : m_ref;
         const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
         if (cnt_item > 0 && __any_sync(0xffffffffu, rescale)) {
-          // O holds exactly the P.V of earlier entries: this S was issued after
-          // them by the same thread, and its commit arrives only once they are done.
+          // This half's O must hold exactly its P.V of the earlier entries: wait
+          // for the last of them.
+          const int pl = nsf - 1;
+          if (!warp_wait(bar(C::B_PDONE + 2 * hf + (pl & 1)), uint32_t(pl >> 1) & 1u, abort_flag, err, 12)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t v[32];
-            ptx::tmem_ld32(lane_base + colO + q * 32, v);
+            ptx::tmem_ld32(lane_base + col_o + q * 32, v);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -747,82 +701,97 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[c] = __float_as_uint(x.x);
               v[c + 1] = __float_as_uint(x.y);
             }
-            ptx::tmem_st32(lane_base + colO + q * 32, v);
+            ptx::tmem_st32(lane_base + col_o + q * 32, v);
           }
         }
         l *= alpha;
         m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
-        // four independent partial sums keep the additions off one serial chain
         float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
-            const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-            sum2[(c >> 1) & 3] = ptx::fadd2(sum2[(c >> 1) & 3], e);
-            pk[c >> 1] = ptx::pack_bf16(e.x, e.y);
+            const float2 e2 = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            sum2[(c >> 1) & 3] = ptx::fadd2(sum2[(c >> 1) & 3], e2);
+            pk[c >> 1] = ptx::pack_bf16(e2.x, e2.y);
           }
-          ptx::tmem_st16(lane_base + colS + hh * 16, pk);
+          ptx::tmem_st16(lane_base + col_s + hh * 16, pk);
         }
-        const float2 sa = ptx::fadd2(sum2[0], sum2[1]), sb = ptx::fadd2(sum2[2], sum2[3]);
-        l += (sa.x + sb.x) + (sa.y + sb.y);
+        const float2 sa = ptx::fadd2(sum2[0], sum2[1]), sb2 = ptx::fadd2(sum2[2], sum2[3]);
+        l += (sa.x + sb2.x) + (sa.y + sb2.y);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_PFULL + t));
-        ++cnt;
+        ptx::mbar_arrive(bar(C::B_PFULL + 2 * hf + sb));
+        ++nsf;
         ++cnt_item;
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      if (present && cnt_item > 0) {
-        if (!warp_wait(bar(C::B_ODONE + t), uint32_t(nodone) & 1u, abort_flag, err, 11)) {
-          ok = false;
-          break;
-        }
+      // Swap (m, l) with the other half of the row, then each half writes half
+      // of the output columns from both accumulators.
+      {
+        float* xb = xch + (k & 1) * (2 * 2 * kTile);
+        xb[(0 * 2 + hf) * kTile + r] = m_ref;
+        xb[(1 * 2 + hf) * kTile + r] = l;
+        ptx::mbar_arrive(bar(C::B_XCH + (k & 1)));
+        if (!warp_wait(bar(C::B_XCH + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 17)) break;
+      }
+      const float* xb = xch + (k & 1) * (2 * 2 * kTile);
+      const float mA = xb[0 * kTile + r], mB = xb[1 * kTile + r];
+      const float lA = xb[2 * kTile + r], lB = xb[3 * kTile + r];
+      const float m = fmaxf(mA, mB);
+      const float aA = mA == -INFINITY ? 0.f : ptx::ex2(mA - m);
+      const float aB = mB == -INFINITY ? 0.f : ptx::ex2(mB - m);
+      const float lt = lA * aA + lB * aB;
+      if (cnt_item > 0) {
+        if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
         ++nodone;
       }
-      if (present) {
-        ptx::tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + it.h) * D;
+      ptx::tc_fence_after();
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+      const float2 wA = make_float2(aA * inv_l, aA * inv_l), wB = make_float2(aB * inv_l, aB * inv_l);
+      constexpr int DH = D / 2;  // output columns per half
+      __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + it.h) * D + DH * hf;
 #pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          if (cnt_item > 0) {
-            ptx::tmem_ld32(lane_base + colO + q * 32, v);
-            ptx::tmem_wait_ld();
-          } else {
+      for (int q = 0; q < DH / 16; ++q) {
+        uint32_t va[16], vb[16];
+        if (cnt_item > 0) {
+          ptx::tmem_ld16(lane_base + C::col_o(0) + DH * hf + q * 16, va);
+          ptx::tmem_ld16(lane_base + C::col_o(1) + DH * hf + q * 16, vb);
+          ptx::tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = 0u;
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            w[c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * inv_l, __uint_as_float(v[2 * c + 1]) * inv_l);
-          if (row_in) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-          }
+          for (int c = 0; c < 16; ++c) va[c] = vb[c] = 0u;
         }
-        if (row_in)
-          p.lse[size_t(it.h) * p.T + s0 + il] =
-              l > 0.f ? (m_ref + ptx::lg2(l)) * 0.69314718055994531f : -INFINITY;
+        uint32_t w[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float2 x = ptx::ffma2(make_float2(__uint_as_float(va[2 * c]), __uint_as_float(va[2 * c + 1])), wA,
+                                      ptx::fmul2(make_float2(__uint_as_float(vb[2 * c]), __uint_as_float(vb[2 * c + 1])), wB));
+          w[c] = ptx::pack_bf16(x.x, x.y);
+        }
+        if (row_in) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + q * 16);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
-      // This q-tile slot's O columns may now take the next item's P.V.
+      if (row_in && hf == 0)
+        p.lse[size_t(it.h) * p.T + s0 + il] = lt > 0.f ? (m + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
+      // O may now take the next item's P.V.
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE + t));
+      ptx::mbar_arrive(bar(C::B_OFREE));
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpPV) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -866,6 +835,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int T, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+
 template <int D>
 attn_status launch(const FwdArgs& a, cudaStream_t s) {
   using C = Cfg<D>;
@@ -876,20 +846,14 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
     return record_cuda_error(cudaErrorInvalidValue, "attn_fwd tensor map encoding");
   static bool configured = false;
   if (!configured) {
-    // The warpgroups' register split assumes the kernel launches with exactly
-    // kLaunchRegs per thread; anything else could leave setmaxnreg.inc waiting.
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_fwd_bf16_kernel<D>);
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
-    if (fa.numRegs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
-    e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    const cudaError_t e =
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
     configured = true;
   }
   FwdParams p;
   p.header = a.bm.header;
-  p.pair_order = a.bm.pair_order;
-  p.pair_q0 = a.bm.pair_q0;
+  p.order = a.bm.order;
   p.qt_seq = a.bm.qt_seq;
   p.qt_idx = a.bm.qt_idx;
   p.koff = a.bm.koff;
@@ -902,8 +866,8 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  // Persistent: one CTA per SM (the pair count is only known on the device;
-  // max_qt * H bounds it).
+  // Persistent: one CTA per SM (the q-tile count is only known on the device;
+  // max_qt * H bounds the item count).
   static int num_sms = 0;
   if (num_sms == 0) {
     int dev = 0;
