@@ -22,11 +22,10 @@
 // The two issuers work independently: an MMA issue blocks while the tensor
 // pipe's short queue is full, and with two threads one waits on its barriers
 // while the other keeps the queue fed.
-// TMEM columns: S0 [0,128) and S1 [128,256) hold S of alternate k-tiles,
-// O_A [256, 256+D) and O_B [384, 384+D) the two column halves' accumulators.
-// Each half writes its bf16 P over the first 32 of its own 64 S columns.  With
-// S double-buffered, the tensor cores compute S(j+1) and P(j-1).V while the
-// softmax works on S(j).
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384) hold S of three
+// consecutive k-tiles, O [384, 384+D).  Each half of a row writes its bf16 P
+// over the first 32 of its own 64 S columns.  With three S buffers the tensor
+// cores compute S(j+1), S(j+2) and P(j-1).V while the softmax works on S(j).
 //
 // The row maximum used as the exponent reference only moves when a new tile
 // raises it by more than 2^8 (factor 256 in p); O and l are then rescaled
@@ -61,27 +60,29 @@ struct Cfg {
   static constexpr uint32_t SW = D >= 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
   static constexpr int SBO = 8 * ROWB;                // 8-row core-matrix group stride
   static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = OFF_K + NK * TILE;
-  // PFULL / PDONE: [half][S buffer]; XCH: [item parity]
+  static constexpr int NS = 3;                        // S buffers in TMEM
+  // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; XSUM: per item parity
   static constexpr int B_Q = 0, B_QFREE = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
                        B_VEMPTY = B_VFULL + NV, B_VTMA = B_VEMPTY + NV, B_SFULL = B_VTMA + 1,
-                       B_PFULL = B_SFULL + 2, B_PDONE = B_PFULL + 4, B_ODONE = B_PDONE + 4,
+                       B_PFULL = B_SFULL + NS, B_PDONE = B_PFULL + NS, B_ODONE = B_PDONE + NS,
                        B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
-                       B_CODE = B_IEMPTY + 2, B_CODEFREE = B_CODE + NCODE, B_XCH = B_CODEFREE + NCODE,
-                       B_DRAIN = B_XCH + 2, NBAR = B_DRAIN + 1;
+                       B_CODE = B_IEMPTY + 2, B_CODEFREE = B_CODE + NCODE, B_XMAX = B_CODEFREE + NCODE,
+                       B_XSUM = B_XMAX + 2, B_DRAIN = B_XSUM + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_BAR = OFF_V + NV * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;            // two decoded work items, 8 ints each
   static constexpr int OFF_CODES = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;  // per buffer: 128 key codes
-  static constexpr int OFF_XCH = OFF_CODES + NCODE * kTile * 4;  // [item parity][m, l][half][row] floats
-  static constexpr int SMEM_USED = OFF_XCH + 2 * 2 * 2 * kTile * 4;
+  static constexpr int OFF_XMAX = OFF_CODES + NCODE * kTile * 4;  // [entry parity][half][row] floats
+  static constexpr int OFF_XSUM = OFF_XMAX + 2 * 2 * kTile * 4;    // [item parity][half][row] floats
+  static constexpr int SMEM_USED = OFF_XSUM + 2 * 2 * kTile * 4;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, D, false, true);
+  static constexpr uint32_t COL_O = 384;
   __host__ __device__ static constexpr uint32_t col_s(int i) { return uint32_t(i) * 128u; }
-  __host__ __device__ static constexpr uint32_t col_o(int h) { return 256u + uint32_t(h) * 128u; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
@@ -193,15 +194,16 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64
     ptx::mma_ss(d_tmem, q_desc + kmajor_step<D>(kk), k_desc + kmajor_step<D>(kk), C::IDESC_S, kk > 0);
 }
 
-// O_h += P_h V over keys [64h, 64h + 64): P_h is 128 x 64 bf16 in TMEM (32
-// columns), four k-steps of 16 keys.
+// O += P V over the 128 keys of a k-tile: P (bf16) of keys 0-63 sits over the
+// first 32 columns of the S buffer, P of keys 64-127 over columns 64-95 (each
+// half writes P over its own score columns); eight k-steps of 16 keys.
 template <int D>
-__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, bool acc, int h) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t s_tmem, uint64_t v_desc, bool acc) {
   using C = Cfg<D>;
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    ptx::mma_ts(d_tmem, p_tmem + uint32_t(kk) * 8u, v_desc + v_step<D>(4 * h + kk), C::IDESC_PV,
-                (acc || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    ptx::mma_ts(d_tmem, s_tmem + uint32_t(kk >> 2) * 64u + uint32_t(kk & 3) * 8u, v_desc + v_step<D>(kk),
+                C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
 }
 
 // One work item: a q-tile of one sequence and one head; its k-tile list is
@@ -309,13 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar(C::B_SFULL + i), 1);
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
       ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 3);  // softmax threads, both MMA threads, V producer
-      ptx::mbar_init(bar(C::B_XCH + i), 256);
+      ptx::mbar_init(bar(C::B_XMAX + i), 256);
+      ptx::mbar_init(bar(C::B_XSUM + i), 256);
     }
-    for (int i = 0; i < 4; ++i) {
-      ptx::mbar_init(bar(C::B_PFULL + i), 128);
+    for (int i = 0; i < C::NS; ++i) {
+      ptx::mbar_init(bar(C::B_SFULL + i), 1);
+      ptx::mbar_init(bar(C::B_PFULL + i), 256);
       ptx::mbar_init(bar(C::B_PDONE + i), 1);
     }
     ptx::mbar_init(bar(C::B_ODONE), 1);
@@ -480,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
-    // S(j) into S buffer j % 2 once both halves' P.V(j-2) have read the P
-    // written over S(j-2) there.
+    // S(j) into S buffer j % 3 once P.V(j-3) has read the P written over
+    // S(j-3) there.
     if (lane == 0) {
       int nkc = 0, ns = 0;  // K loads consumed, S issued (all items)
       bool ok = true;
@@ -494,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid) break;
         if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) break;
         for (int e = it.e0; e < it.e1; ++e) {
-          const int sb = ns & 1, ks = nkc % C::NK;
-          if (ns >= 2 && !wait_bar(bar(C::B_PDONE + 2 + sb), uint32_t((ns - 2) >> 1) & 1u, abort_flag, err, 7)) {
+          const int sb = ns % C::NS, ks = nkc % C::NK;
+          if (ns >= C::NS && !wait_bar(bar(C::B_PDONE + sb), uint32_t(ns / C::NS - 1) & 1u, abort_flag, err, 7)) {
             ok = false;
             break;
           }
@@ -529,26 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!valid) break;
         const int n = it.e1 - it.e0;
         for (int j = 0; j < n; ++j) {
-          const int pb = np & 1, vs = nvc % C::NV;
-          const uint64_t vd = vdesc0 + uint64_t(vs) * (C::TILE >> 4);
+          const int pb = np % C::NS, vs = nvc % C::NV;
           if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
             ok = false;
             break;
           }
           if (!wait_bar(bar(C::B_VFULL + vs), uint32_t(nvc / C::NV) & 1u, abort_flag, err, 6)) { ok = false; break; }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            // half h: O_h += P_h V[64h, 64h + 64)
-            if (!wait_bar(bar(C::B_PFULL + 2 * h + pb), uint32_t(np >> 1) & 1u, abort_flag, err, 5)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_pv_half<D>(tmem + C::col_o(h), tmem + C::col_s(pb) + 64u * h, vd, j > 0, h);
-            ptx::mma_commit(bar(C::B_PDONE + 2 * h + pb));
-          }
-          if (!ok) break;
-          // V(j) is read by no later MMA
+          if (!wait_bar(bar(C::B_PFULL + pb), uint32_t(np / C::NS) & 1u, abort_flag, err, 5)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_pv<D>(tmem + C::COL_O, tmem + C::col_s(pb), vdesc0 + uint64_t(vs) * (C::TILE >> 4), j > 0);
+          // P(j) and V(j) are read by no later MMA
+          ptx::mma_commit(bar(C::B_PDONE + pb));
           ptx::mma_commit(bar(C::B_VEMPTY + vs));
           ++np;
           ++nvc;
@@ -563,21 +557,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     // Two threads per query row: warps 0-3 take score columns 0-63 of every
-    // k-tile (half A), warps 4-7 columns 64-127 (half B).  Each half is its
-    // own online softmax over its columns, with its own reference m, sum l
-    // and accumulator O_A or O_B (its P.V covers only its 64 keys), so the
-    // halves never wait for each other inside the loop; the two partial
-    // results are merged once per item:
-    //   O = (2^(mA-m) O_A + 2^(mB-m) O_B) / (2^(mA-m) lA + 2^(mB-m) lB),  m = max(mA, mB).
-    const int hf = warp >> 2;                  // 0: half A, 1: half B
+    // k-tile, warps 4-7 columns 64-127.  Both halves keep the same exponent
+    // reference m (and each its own part of the row sum l); O is shared.  Per
+    // k-tile each half posts its maximum for the other and takes its
+    // exponentials with the current reference right away; only when the row
+    // maximum rises by more than the threshold (rare after the first k-tile)
+    // are they taken again with the new reference.
+    const int hf = warp >> 2;                  // which half of the columns
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;         // query row inside the tile = TMEM lane
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const uint32_t col_o = C::col_o(hf);
+    constexpr int DH = D / 2;                  // O columns this half rescales and writes
+    const uint32_t col_oh = C::COL_O + uint32_t(DH * hf);
     const float c2 = p.scale_log2;
-    float* xch = reinterpret_cast<float*>(sbase + C::OFF_XCH);  // [item parity][m, l][half][row]
-    int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % 2
+    const float2 c22 = make_float2(c2, c2);
+    float* xmax = reinterpret_cast<float*>(sbase + C::OFF_XMAX);  // [entry parity][half][row]
+    float* xsum = reinterpret_cast<float*>(sbase + C::OFF_XSUM);  // [item parity][half][row]
+    int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % 3
     int ue = 0;      // the same count for the code buffers
     int nodone = 0;  // items whose final O this warp has waited for
     bool ok = true;
@@ -602,10 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = it.e0; e < it.e1; ++e) {
         const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, L - j0);
         const int lab = __ldg(p.klabel + e);
-        const int sb = nsf & 1;
+        const int sb = nsf % 3, xb = nsf & 1;
         const uint32_t col_s = C::col_s(sb) + 64u * hf;  // this half's 64 score columns; its P goes
                                                          // over the first 32 of them
-        if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(nsf >> 1) & 1u, abort_flag, err, 8)) { ok = false; break; }
+        if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(nsf / 3) & 1u, abort_flag, err, 8)) { ok = false; break; }
         ptx::tc_fence_after();
         float s[64];
         {
@@ -675,106 +672,109 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 1; c < 15; c += 2) mv = ptx::fmax3(mv, s[16 * u + c], s[16 * u + c + 1]);
           mx4[u] = fmaxf(mv, s[16 * u + 15]);
         }
-        const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
-        const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
-        const bool rescale = raise && m_ref != -INFINITY;   // O and l hold an older reference
-        const float m_new = raise ? mxs : m_ref;
-        const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
-        if (cnt_item > 0 && __any_sync(0xffffffffu, rescale)) {
-          // This half's O must hold exactly its P.V of the earlier entries: wait
-          // for the last of them.
-          const int pl = nsf - 1;
-          if (!warp_wait(bar(C::B_PDONE + 2 * hf + (pl & 1)), uint32_t(pl >> 1) & 1u, abort_flag, err, 12)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t v[32];
-            ptx::tmem_ld32(lane_base + col_o + q * 32, v);
-            ptx::tmem_wait_ld();
+        const float mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;
+        // post this half's maximum for the other half of the row
+        xmax[(xb * 2 + hf) * kTile + r] = mh;
+        ptx::mbar_arrive(bar(C::B_XMAX + xb));
+        // p = 2^(s c2 - m) for the 64 columns, written as bf16 over this half's
+        // first 32 S columns; returns the partial row sum.
+        auto exp_pass = [&](float m) -> float {
+          const float2 nm2 = make_float2(-m, -m);
+          float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const float2 x = ptx::fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), a2);
-              v[c] = __float_as_uint(x.x);
-              v[c + 1] = __float_as_uint(x.y);
+              const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
+              const float2 e2 = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+              sum2[(c >> 1) & 3] = ptx::fadd2(sum2[(c >> 1) & 3], e2);
+              pk[c >> 1] = ptx::pack_bf16(e2.x, e2.y);
             }
-            ptx::tmem_st32(lane_base + col_o + q * 32, v);
+            ptx::tmem_st16(lane_base + col_s + hh * 16, pk);
           }
-        }
-        l *= alpha;
-        m_ref = m_new;
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m_use, -m_use);
-        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
+          const float2 sa = ptx::fadd2(sum2[0], sum2[1]), sb2 = ptx::fadd2(sum2[2], sum2[3]);
+          return (sa.x + sb2.x) + (sa.y + sb2.y);
+        };
+        // With a reference in every row of the warp, the exponentials need not
+        // wait for the other half's maximum.
+        const bool early = !__any_sync(0xffffffffu, m_ref == -INFINITY);
+        float psum = early ? exp_pass(m_ref) : 0.f;
+        if (!warp_wait(bar(C::B_XMAX + xb), uint32_t(nsf >> 1) & 1u, abort_flag, err, 17)) { ok = false; break; }
+        const float mxs = fmaxf(mh, xmax[(xb * 2 + (1 - hf)) * kTile + r]);  // the same in both halves
+        const bool raise = mxs > m_ref + kRescaleThreshold;  // always true on the first visible key
+        if (!early || __any_sync(0xffffffffu, raise)) {
+          const bool rescale = raise && m_ref != -INFINITY;  // O and l hold an older reference
+          const float m_new = raise ? mxs : m_ref;
+          const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.f;
+          if (cnt_item > 0 && __any_sync(0xffffffffu, rescale)) {
+            // O must hold exactly the P.V of the earlier entries: wait for the
+            // last of them.  Each half rescales its half of the O columns.
+            const int pl = nsf - 1;
+            if (!warp_wait(bar(C::B_PDONE + pl % 3), uint32_t(pl / 3) & 1u, abort_flag, err, 12)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+            for (int q = 0; q < DH / 16; ++q) {
+              uint32_t v[16];
+              ptx::tmem_ld16(lane_base + col_oh + q * 16, v);
+              ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float2 x = ptx::ffma2(make_float2(s[32 * hh + c], s[32 * hh + c + 1]), c22, nm2);
-            const float2 e2 = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-            sum2[(c >> 1) & 3] = ptx::fadd2(sum2[(c >> 1) & 3], e2);
-            pk[c >> 1] = ptx::pack_bf16(e2.x, e2.y);
+              for (int c = 0; c < 16; c += 2) {
+                const float2 x = ptx::fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), a2);
+                v[c] = __float_as_uint(x.x);
+                v[c + 1] = __float_as_uint(x.y);
+              }
+              ptx::tmem_st16(lane_base + col_oh + q * 16, v);
+            }
           }
-          ptx::tmem_st16(lane_base + col_s + hh * 16, pk);
+          l *= alpha;
+          m_ref = m_new;
+          psum = exp_pass(m_ref == -INFINITY ? 0.f : m_ref);
         }
-        const float2 sa = ptx::fadd2(sum2[0], sum2[1]), sb2 = ptx::fadd2(sum2[2], sum2[3]);
-        l += (sa.x + sb2.x) + (sa.y + sb2.y);
+        l += psum;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_PFULL + 2 * hf + sb));
+        ptx::mbar_arrive(bar(C::B_PFULL + sb));
         ++nsf;
         ++cnt_item;
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      // Swap (m, l) with the other half of the row, then each half writes half
-      // of the output columns from both accumulators.
+      // Swap the partial row sums; each half writes its half of the O columns.
       {
-        float* xb = xch + (k & 1) * (2 * 2 * kTile);
-        xb[(0 * 2 + hf) * kTile + r] = m_ref;
-        xb[(1 * 2 + hf) * kTile + r] = l;
-        ptx::mbar_arrive(bar(C::B_XCH + (k & 1)));
-        if (!warp_wait(bar(C::B_XCH + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 17)) break;
+        float* xs = xsum + (k & 1) * (2 * kTile);
+        xs[hf * kTile + r] = l;
+        ptx::mbar_arrive(bar(C::B_XSUM + (k & 1)));
+        if (!warp_wait(bar(C::B_XSUM + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 17)) break;
       }
-      const float* xb = xch + (k & 1) * (2 * 2 * kTile);
-      const float mA = xb[0 * kTile + r], mB = xb[1 * kTile + r];
-      const float lA = xb[2 * kTile + r], lB = xb[3 * kTile + r];
-      const float m = fmaxf(mA, mB);
-      const float aA = mA == -INFINITY ? 0.f : ptx::ex2(mA - m);
-      const float aB = mB == -INFINITY ? 0.f : ptx::ex2(mB - m);
-      const float lt = lA * aA + lB * aB;
+      const float* xs = xsum + (k & 1) * (2 * kTile);
+      const float lt = xs[r] + xs[kTile + r];  // the same order in both halves
       if (cnt_item > 0) {
         if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
         ++nodone;
       }
       ptx::tc_fence_after();
       const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      const float2 wA = make_float2(aA * inv_l, aA * inv_l), wB = make_float2(aB * inv_l, aB * inv_l);
-      constexpr int DH = D / 2;  // output columns per half
       __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + it.h) * D + DH * hf;
 #pragma unroll 1
       for (int q = 0; q < DH / 16; ++q) {
-        uint32_t va[16], vb[16];
+        uint32_t v[16];
         if (cnt_item > 0) {
-          ptx::tmem_ld16(lane_base + C::col_o(0) + DH * hf + q * 16, va);
-          ptx::tmem_ld16(lane_base + C::col_o(1) + DH * hf + q * 16, vb);
+          ptx::tmem_ld16(lane_base + col_oh + q * 16, v);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) va[c] = vb[c] = 0u;
+          for (int c = 0; c < 16; ++c) v[c] = 0u;
         }
         uint32_t w[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float2 x = ptx::ffma2(make_float2(__uint_as_float(va[2 * c]), __uint_as_float(va[2 * c + 1])), wA,
-                                      ptx::fmul2(make_float2(__uint_as_float(vb[2 * c]), __uint_as_float(vb[2 * c + 1])), wB));
-          w[c] = ptx::pack_bf16(x.x, x.y);
-        }
+        for (int c = 0; c < 8; ++c)
+          w[c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * inv_l, __uint_as_float(v[2 * c + 1]) * inv_l);
         if (row_in) {
           uint4* dst = reinterpret_cast<uint4*>(orow + q * 16);
           dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -782,7 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_in && hf == 0)
-        p.lse[size_t(it.h) * p.T + s0 + il] = lt > 0.f ? (m + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
+        p.lse[size_t(it.h) * p.T + s0 + il] =
+            lt > 0.f ? (m_ref + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
       // O may now take the next item's P.V.
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE));
