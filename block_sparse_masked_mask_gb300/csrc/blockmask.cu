@@ -200,12 +200,23 @@ __device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
       return all_causal ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL;
     case ATTN_MASK_CAUSAL_DOCUMENT:
       if (sq[1] < sk[0] || sk[1] < sq[0]) return ATTN_TILE_EMPTY;  // no shared document id
-      if (all_causal && sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0]) return ATTN_TILE_FULL;
+      if (sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0])       // one document throughout
+        return all_causal ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL;      // else (i1, j0) seen, (i0, j1) not
+      // Every key precedes every query and all keys share one id, held by the
+      // first or last query id (so some query row has it): that row sees every
+      // key, a row with another id (the ids differ) sees none.
+      if (all_causal && sk[0] == sk[1] && sq[0] != sq[1] && (sk[0] == sq[0] || sk[0] == sq[1]))
+        return ATTN_TILE_PARTIAL;
       return kUnknown;
     case ATTN_MASK_SHARED_PREFIX:
       if (sk[2] == 0 && (sq[1] < sk[0] || sk[1] < sq[0])) return ATTN_TILE_EMPTY;
       if (all_causal && sk[0] == 0 && sk[1] == 0) return ATTN_TILE_FULL;       // all prefix keys
-      if (all_causal && sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0]) return ATTN_TILE_FULL;
+      if (sq[0] == sq[1] && sk[0] == sk[1] && sq[0] == sk[0])                  // one segment throughout
+        return all_causal ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL;
+      // As for documents, with suffix keys (id != 0) only: the query row holding
+      // their id sees them all, a row with another id sees none.
+      if (all_causal && sk[0] == sk[1] && sk[0] != 0 && sq[0] != sq[1] && (sk[0] == sq[0] || sk[0] == sq[1]))
+        return ATTN_TILE_PARTIAL;
       return kUnknown;
     case ATTN_MASK_STRIP_THINKING:
       // hidden iff key is THINK with an earlier turn than the query
