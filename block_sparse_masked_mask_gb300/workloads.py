@@ -169,11 +169,15 @@ def strip_thinking_layout(turns):
     return np.asarray(role, np.int8), np.asarray(turn, np.int32)
 
 
-def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: int = ROLE_THINK):
+def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: int = ROLE_THINK,
+                    id_alphabet: int = 0):
     """Random per-token metadata for ``kind`` over packed sequences ``lengths``.
 
     Segment ids are runs (documents / prefix-suffix segments) of random length;
     roles and turns are random runs too, so tile boundaries cut through runs.
+    By default ids count up run by run (0, 1, 2, ...) and turns count up from 1.
+    With ``id_alphabet`` = n > 0 every run draws its segment id from 0..n-1 and
+    every turn its number from 1..n instead, so ids repeat, fall and skip.
     """
     T = int(sum(lengths))
     seg = role = turn = None
@@ -184,7 +188,7 @@ def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: in
             s, cur = 0, 0
             while s < L:
                 n = int(rng.integers(1, max(2, L // 2 + 2)))
-                seg[pos + s: pos + min(L, s + n)] = cur
+                seg[pos + s: pos + min(L, s + n)] = cur if id_alphabet <= 0 else int(rng.integers(0, id_alphabet))
                 s += n
                 cur += 1
             pos += L
@@ -195,10 +199,11 @@ def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: in
         for L in lengths:
             s, t = 0, 1
             while s < L:
+                tt = t if id_alphabet <= 0 else int(rng.integers(1, id_alphabet + 1))
                 for r in (ROLE_USER, role_think, ROLE_ANSWER):
                     n = int(rng.integers(1, 200))
                     role[pos + s: pos + min(L, s + n)] = r
-                    turn[pos + s: pos + min(L, s + n)] = t
+                    turn[pos + s: pos + min(L, s + n)] = tt
                     s += n
                     if s >= L:
                         break
@@ -208,10 +213,12 @@ def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: in
 
 
 def random_workload(seed: int, kind: str, lengths, num_heads: int, head_dim: int,
-                    dtype: torch.dtype = torch.bfloat16, sigma: float = 1.0) -> Workload:
-    """A small seeded case for parity tests (ragged lengths, any kind)."""
+                    dtype: torch.dtype = torch.bfloat16, sigma: float = 1.0,
+                    id_alphabet: int = 0) -> Workload:
+    """A small seeded case for parity tests (ragged lengths, any kind); see
+    random_metadata for ``id_alphabet``."""
     rng = np.random.default_rng(seed)
-    seg, role, turn = random_metadata(rng, kind, lengths)
+    seg, role, turn = random_metadata(rng, kind, lengths, id_alphabet=id_alphabet)
     w = Workload(f"random_{kind}_{seed}", kind, _cu(lengths), num_heads, head_dim, dtype,
                  sigma=sigma, seg=seg, role=role, turn=turn, seed=seed)
     _fill_tensors(w, torch.Generator().manual_seed(10_000 + seed))

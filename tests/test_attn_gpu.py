@@ -67,6 +67,17 @@ def test_small_all_elements(kind, D, dtype):
     compare(w, o, lse)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking"])
+def test_small_repeating_ids_all_elements(kind, D):
+    """Ids and turns drawn from a small alphabet: the rows of a warp often hold
+    different query codes, so PARTIAL tiles take the per-row predicate path
+    rather than the per-warp ballot."""
+    w = W.random_workload(70 + D, kind, [700, 255, 1000], num_heads=2, head_dim=D, id_alphabet=4)
+    o, lse = run_gpu(w)
+    compare(w, o, lse)
+
+
 @pytest.mark.parametrize("lens", [[1], [2], [127], [128], [129], [255, 257], [1000]])
 def test_ragged_shapes_causal(lens):
     w = W.random_workload(sum(lens), "causal", lens, num_heads=3, head_dim=128)

@@ -113,3 +113,18 @@ def test_last_entry_must_equal_total_tokens():
     cu_t = torch.tensor([0, 10, 20], dtype=torch.int32, device="cuda")
     bm = api.attn_block_mask_build("causal", cu_t, 25, 64)
     assert api.attn_get_status(bm) == 7
+
+
+@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking"])
+@pytest.mark.parametrize("li", [4, 5, 7])
+def test_random_metadata_repeating_ids_bit_exact(kind, li):
+    """Ids drawn from a small alphabet (they repeat, fall and skip), so the
+    classifier's interval reasoning meets tiles whose id ranges overlap
+    without sharing ids."""
+    for seed in range(3):
+        rng = np.random.default_rng(7000 + 100 * li + seed)
+        lens = LENGTH_SETS[li]
+        seg, role, turn = W.random_metadata(rng, kind, lens, id_alphabet=4)
+        w = W.Workload(f"rand_ids_{kind}", kind, W._cu(lens), 1, 128, torch.bfloat16,
+                       seg=seg, role=role, turn=turn)
+        assert_matches_oracle(w, build_on_gpu(w))
