@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing issued, nothing to drain
   } else if (warp == kWarpKLoad) {
     // ------------------------------------------------------------ Q, K, key codes
-    int nk = 0, nq = 0, ue = 0;
+    int nk = 0, nq = 0, up = 0;  // K loads, Q loads, PARTIAL entries given key codes
     bool ok = true;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
@@ -373,21 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = it.e0; e < it.e1; ++e) {
         const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, it.L - j0);
         const int lab = __ldg(p.klabel + e);
-        // Keys' mask codes for the softmax of a PARTIAL tile, in buffer ue % NCODE
-        // once the softmax is done with the buffer's previous entry.
-        const int cb = ue % C::NCODE;
-        if (ue >= C::NCODE &&
-            !warp_wait(bar(C::B_CODEFREE + cb), uint32_t(ue / C::NCODE - 1) & 1u, abort_flag, err, 10)) {
-          ok = false;
-          break;
-        }
         if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL) {
+          // Keys' mask codes for the softmax of a PARTIAL tile, in buffer up % NCODE
+          // once the softmax is done with the buffer's previous PARTIAL entry.
+          const int cb = up % C::NCODE;
+          if (up >= C::NCODE &&
+              !warp_wait(bar(C::B_CODEFREE + cb), uint32_t(up / C::NCODE - 1) & 1u, abort_flag, err, 10)) {
+            ok = false;
+            break;
+          }
           for (int c = lane; c < kTile; c += 32)
             key_codes[cb * kTile + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
           __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(C::B_CODE + cb));
+          ++up;
         }
-        if (lane == 0) ptx::mbar_arrive(bar(C::B_CODE + cb));
-        ++ue;
         // K(j)
         const int slot = nk % C::NK;
         if (nk >= C::NK &&
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xmax = reinterpret_cast<float*>(sbase + C::OFF_XMAX);  // [entry parity][half][row]
     float* xsum = reinterpret_cast<float*>(sbase + C::OFF_XSUM);  // [item parity][half][row]
     int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % 3
-    int ue = 0;      // the same count for the code buffers
+    int up = 0;      // PARTIAL entries with key codes (all items): code buffer up % NCODE
     int nodone = 0;  // items whose final O this warp has waited for
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -613,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(v[c >> 5][c & 31]);
         }
-        const int cb = ue % C::NCODE;
         if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
           // bit c of vis[c / 32]: key column 64 * hf + c is visible to this row.
           // Causal part and bounds: columns below upto; PARTIAL tiles of the
@@ -622,7 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t vis[2] = {prefix_bits(upto), prefix_bits(upto - 32)};
           if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
             // the K producer staged this entry's key codes
-            if (!warp_wait(bar(C::B_CODE + cb), uint32_t(ue / C::NCODE) & 1u, abort_flag, err, 9)) {
+            const int cb = up % C::NCODE;
+            if (!warp_wait(bar(C::B_CODE + cb), uint32_t(up / C::NCODE) & 1u, abort_flag, err, 9)) {
               ok = false;
               break;
             }
@@ -652,6 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
             }
+            // done with the buffer
+            ptx::mbar_arrive(bar(C::B_CODEFREE + cb));
+            ++up;
           }
           // A word the whole warp sees needs no select.
 #pragma unroll
@@ -661,9 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 32; ++c) s[32 * q + c] = (vis[q] >> c) & 1u ? s[32 * q + c] : -INFINITY;
           }
         }
-        // done with this entry's code buffer (used or not)
-        ptx::mbar_arrive(bar(C::B_CODEFREE + cb));
-        ++ue;
         float mx4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
