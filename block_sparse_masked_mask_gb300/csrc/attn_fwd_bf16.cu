@@ -759,34 +759,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nodone;
       }
       ptx::tc_fence_after();
-      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      __nv_bfloat16* orow = p.o + (size_t(s0 + il) * p.H + it.h) * D + DH * hf;
-#pragma unroll 1
-      for (int q = 0; q < DH / 16; ++q) {
-        uint32_t v[16];
-        if (cnt_item > 0) {
-          ptx::tmem_ld16(lane_base + col_oh + q * 16, v);
-          ptx::tmem_wait_ld();
+      // All of this half's O columns into registers at once (one wait), and O
+      // is released for the next item's P.V before the stores to global memory.
+      uint32_t ov[DH];
+      if (cnt_item > 0) {
+        if constexpr (DH >= 32) {
+#pragma unroll
+          for (int q = 0; q < DH / 32; ++q)
+            ptx::tmem_ld32(lane_base + col_oh + q * 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32 * q));
         } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) v[c] = 0u;
+          ptx::tmem_ld16(lane_base + col_oh, *reinterpret_cast<uint32_t(*)[16]>(ov));
         }
-        uint32_t w[8];
+        ptx::tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          w[c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * inv_l, __uint_as_float(v[2 * c + 1]) * inv_l);
-        if (row_in) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + q * 16);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        for (int c = 0; c < DH; ++c) ov[c] = 0u;
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_OFREE));
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+      if (row_in) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (size_t(s0 + il) * p.H + it.h) * D + DH * hf);
+#pragma unroll
+        for (int c = 0; c < DH / 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            w[x] = ptx::pack_bf16(__uint_as_float(ov[8 * c + 2 * x]) * inv_l, __uint_as_float(ov[8 * c + 2 * x + 1]) * inv_l);
+          dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       if (row_in && hf == 0)
         p.lse[size_t(it.h) * p.T + s0 + il] =
             lt > 0.f ? (m_ref + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
-      // O may now take the next item's P.V.
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE));
     }
   }
 
