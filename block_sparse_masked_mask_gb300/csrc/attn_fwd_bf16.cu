@@ -74,7 +74,9 @@ struct Cfg {
   static constexpr int OFF_CODES = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;  // per buffer: 128 key codes
   static constexpr int OFF_XMAX = OFF_CODES + NCODE * kTile * 4;  // [entry parity][half][row] floats
   static constexpr int OFF_XSUM = OFF_XMAX + 2 * 2 * kTile * 4;    // [item parity][half][row] floats
-  static constexpr int SMEM_USED = OFF_XSUM + 2 * 2 * kTile * 4;
+  static constexpr int OFF_OSTAGE = (OFF_XSUM + 2 * 2 * kTile * 4 + 127) & ~127;  // per softmax warp: 16 O rows
+  static constexpr int OSTAGE_WARP = 16 * 128;                                    // bytes per warp
+  static constexpr int SMEM_USED = OFF_OSTAGE + 8 * OSTAGE_WARP;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
@@ -778,15 +780,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE));
       const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      if (row_in) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (size_t(s0 + il) * p.H + it.h) * D + DH * hf);
+      // Stores of whole 128-byte row segments: the warp's rows pass through
+      // shared memory 16 at a time (chunk c of row q at slot c ^ (q & 7), so
+      // neither side conflicts on banks), then 8 lanes write each row's DH
+      // columns as consecutive 16-byte pieces.
+      {
+        constexpr int CPR = DH / 8;              // 16-byte chunks per row half (8, 4 or 2)
+        constexpr int RPI = 32 / CPR;            // rows per store instruction
+        uint8_t* stage = sbase + C::OFF_OSTAGE + warp * C::OSTAGE_WARP;
+        __nv_bfloat16* obase = p.o + (size_t(s0 + it.qi0 + quarter * 32) * p.H + it.h) * D + DH * hf;
+        const size_t rstride = size_t(p.H) * D;  // elements between consecutive tokens
 #pragma unroll
-        for (int c = 0; c < DH / 8; ++c) {
-          uint32_t w[4];
+        for (int half16 = 0; half16 < 2; ++half16) {
+          if ((lane >> 4) == half16) {
+            const int q = lane & 15;
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
-            w[x] = ptx::pack_bf16(__uint_as_float(ov[8 * c + 2 * x]) * inv_l, __uint_as_float(ov[8 * c + 2 * x + 1]) * inv_l);
-          dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < CPR; ++c) {
+              uint32_t w[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                w[x] = ptx::pack_bf16(__uint_as_float(ov[8 * c + 2 * x]) * inv_l,
+                                      __uint_as_float(ov[8 * c + 2 * x + 1]) * inv_l);
+              *reinterpret_cast<uint4*>(stage + q * 128 + ((c ^ (q & 7)) & (CPR - 1)) * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 16 / RPI; ++i) {
+            const int q = i * RPI + lane / CPR, c = lane % CPR;  // row within these 16, chunk
+            const int rr = half16 * 16 + q;                       // row within the warp's 32
+            const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 128 + ((c ^ (q & 7)) & (CPR - 1)) * 16);
+            if (quarter * 32 + rr < qn)
+              *reinterpret_cast<uint4*>(obase + size_t(rr) * rstride + 8 * c) = val;
+          }
+          __syncwarp();
         }
       }
       if (row_in && hf == 0)
