@@ -174,6 +174,94 @@ def attention(q, k, v, kind: str, cu_seqlens, meta=None, scale=None, heads=None,
     return O, LSE
 
 
+def masked_attention_backward(q, k, v, do, mask, scale):
+    """dQ, dK, dV of O = softmax(q k^T * scale, masked) v for one sequence and
+    one head, in fp64, given the upstream gradient dO.
+
+    The plain definition: the chain rule through the three-pass forward above
+    (the forward of "Triton from first principles" Ch. 21, Section 21.1), with
+    masked entries carrying zero weight and no gradient:
+      P = softmax(S), S = q k^T * scale (masked), O = P v
+      dV = P^T dO,  dP = dO v^T,  D_i = sum_j P_ij dP_ij = sum_d dO_id O_id,
+      dS = P * (dP - D),  dQ = dS k * scale,  dK = dS^T q * scale.
+    Rows with no visible key have P = 0 and contribute nothing.  The xorl
+    issue (Verified FA4 gaps, items 1 and 3) asks for this backward over the
+    same block-sparse masks.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    mask = np.asarray(mask, bool)
+    s = (q @ k.T) * float(scale)
+    s = np.where(mask, s, -np.inf)
+    m = s.max(axis=1) if s.shape[1] else np.full(s.shape[0], -np.inf)
+    has_key = np.isfinite(m)
+    m_safe = np.where(has_key, m, 0.0)
+    e = np.where(mask, np.exp(s - m_safe[:, None]), 0.0)
+    l = e.sum(axis=1)
+    p = np.zeros_like(e)
+    p[has_key] = e[has_key] / l[has_key, None]
+    o = p @ v
+    dv = p.T @ do
+    dp = do @ v.T
+    dlt = (do * o).sum(axis=1)
+    ds = p * (dp - dlt[:, None])
+    dq = (ds @ k) * float(scale)
+    dk = (ds.T @ q) * float(scale)
+    return dq, dk, dv
+
+
+def attention_backward(q, k, v, do, kind: str, cu_seqlens, meta=None, scale=None, heads=None):
+    """dQ, dK, dV [T, H, D] of the masked attention (fp64), for upstream
+    gradient dO [T, H, D]; sequences of cu_seqlens are independent.  Heads not
+    selected by ``heads`` stay NaN."""
+    T, H, D = q.shape
+    cu = np.asarray(cu_seqlens, np.int64)
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(D)
+    heads = range(H) if heads is None else heads
+    dQ = np.full((T, H, D), np.nan)
+    dK = np.full((T, H, D), np.nan)
+    dV = np.full((T, H, D), np.nan)
+    for b in range(len(cu) - 1):
+        start, end = int(cu[b]), int(cu[b + 1])
+        if end == start:
+            continue
+        mask = sequence_mask(kind, cu, b, meta)
+        for h in heads:
+            dq, dk, dv = masked_attention_backward(_as_f64(q[start:end, h]), _as_f64(k[start:end, h]),
+                                                   _as_f64(v[start:end, h]), _as_f64(do[start:end, h]),
+                                                   mask, scale)
+            dQ[start:end, h] = dq
+            dK[start:end, h] = dk
+            dV[start:end, h] = dv
+    return dQ, dK, dV
+
+
+def block_lists_transposed(labels):
+    """Per-k-tile compacted lists (the backward's orientation) from per-sequence
+    label matrices: the transpose of block_lists.  For every k-tile (sequences
+    in order, k-tiles ascending) the ascending q-tiles whose label is not EMPTY,
+    with their labels.  Returns qcount, qoff (CSR), qidx (q-tile index within
+    the sequence), qlabel.  The xorl issue (Verified FA4 gaps, item 1) names
+    this transposed view as the backward's missing metadata.
+    """
+    qcount, qidx, qlabel = [], [], []
+    for lab in labels:
+        for kt in range(lab.shape[1]):
+            col = lab[:, kt]
+            nz = np.nonzero(col)[0]
+            qcount.append(len(nz))
+            qidx.extend(nz.tolist())
+            qlabel.extend(col[nz].tolist())
+    qcount = np.asarray(qcount, np.int32)
+    qoff = np.zeros(len(qcount) + 1, np.int32)
+    qoff[1:] = np.cumsum(qcount)
+    return {"qcount": qcount, "qoff": qoff, "qidx": np.asarray(qidx, np.int32),
+            "qlabel": np.asarray(qlabel, np.uint8)}
+
+
 def unmasked_pairs(kind: str, cu_seqlens, meta=None, row_block: int = 1024) -> int:
     """Number of visible (query, key) pairs per head: the nnz that the
     effective-FLOP count 4*D*H*nnz is built on."""

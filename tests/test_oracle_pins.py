@@ -426,3 +426,161 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     monkeypatch.setattr(oa, "masked_attention", attn)
     monkeypatch.setattr(oracle, "masked_attention", attn)
     assert not _pins_pass()
+
+
+# ----------------------------------------------------------------------------
+# Backward (dQ, dK, dV).  The oracle is the chain rule through the forward;
+# pinned against torch autograd in fp64, finite differences, and invariants.
+# ----------------------------------------------------------------------------
+
+def _bwd_case(kind, seed=21, lens=(70, 1, 33, 150), H=2, D=16):
+    rng = np.random.default_rng(seed)
+    lens = list(lens)
+    seg, role, turn = W.random_metadata(rng, kind, lens)
+    cu = W._cu(lens)
+    meta = {"seg": seg, "role": role, "turn": turn, "role_think": 1}
+    T = sum(lens)
+    g = torch.Generator().manual_seed(seed)
+    q, k, v, do = (torch.randn(T, H, D, dtype=torch.float64, generator=g) for _ in range(4))
+    return cu, meta, q, k, v, do
+
+
+def _autograd_grads(kind, cu, meta, q, k, v, do, scale):
+    T, H, D = q.shape
+    dq, dk, dv = (np.zeros((T, H, D)) for _ in range(3))
+    for b in range(len(cu) - 1):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        mask = torch.from_numpy(oracle.sequence_mask(kind, cu, b, meta))
+        for h in range(H):
+            qh, kh, vh = (t[s0:s1, h].clone().requires_grad_(True) for t in (q, k, v))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qh[None], kh[None], vh[None], attn_mask=mask[None], scale=scale)[0]
+            o.backward(do[s0:s1, h])
+            dq[s0:s1, h], dk[s0:s1, h], dv[s0:s1, h] = qh.grad.numpy(), kh.grad.numpy(), vh.grad.numpy()
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("kind", oracle.KINDS)
+def test_backward_matches_torch_autograd_fp64(kind):
+    """The backward reduces to a library routine: torch autograd through fp64
+    SDPA with a boolean mask."""
+    cu, meta, q, k, v, do = _bwd_case(kind)
+    scale = 1 / math.sqrt(q.shape[2])
+    got = oracle.attention_backward(q, k, v, do, kind, cu, meta)
+    want = _autograd_grads(kind, cu, meta, q, k, v, do, scale)
+    for g_, w_ in zip(got, want):
+        assert np.abs(g_ - w_).max() < 1e-11
+
+
+def test_backward_matches_finite_differences():
+    """Central differences of sum(O * dO) on a tiny causal case."""
+    rng = np.random.default_rng(3)
+    L, D, scale = 5, 3, 0.7
+    q, k, v, do = (rng.standard_normal((L, D)) for _ in range(4))
+    mask = oracle.sequence_mask("causal", np.array([0, L]), 0, {})
+    dq, dk, dv = oracle.masked_attention_backward(q, k, v, do, mask, scale)
+
+    def loss(q_, k_, v_):
+        return float((oracle.masked_attention(q_, k_, v_, mask, scale)[0] * do).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{k2 + "_": a for k2, a in args_p.items()}) -
+                        loss(**{k2 + "_": a for k2, a in args_m.items()})) / (2 * eps)
+        assert np.abs(num - g).max() < 1e-7, name
+
+
+@pytest.mark.parametrize("kind", oracle.KINDS)
+def test_backward_invariants(kind):
+    """Per sequence and head: the rows of dS sum to zero, so the keys' dK sum to
+    zero; the keys' dV sum to the dO of rows that see any key."""
+    cu, meta, q, k, v, do = _bwd_case(kind, seed=5)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, kind, cu, meta)
+    for b in range(len(cu) - 1):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        for h in range(q.shape[1]):
+            assert np.abs(dk[s0:s1, h].sum(axis=0)).max() < 1e-10
+            assert np.abs(dv[s0:s1, h].sum(axis=0) - do[s0:s1, h].numpy().sum(axis=0)).max() < 1e-10
+
+
+def test_transposed_lists_are_the_transpose():
+    lens = np.array([0, 300, 300, 301, 700])
+    for kind, meta in (("causal", {}),):
+        lab = oracle.tile_labels(kind, lens, meta)
+        fwd = oracle.block_lists(lab)
+        bwd = oracle.block_lists_transposed(lab)
+        pairs_f = set()
+        for g in range(len(fwd["kcount"])):
+            for e in range(fwd["koff"][g], fwd["koff"][g + 1]):
+                pairs_f.add((int(fwd["qt_seq"][g]), int(fwd["qt_idx"][g]), int(fwd["kidx"][e]), int(fwd["klabel"][e])))
+        pairs_b = set()
+        col = 0
+        for b, l_ in enumerate(lab):
+            for kt in range(l_.shape[1]):
+                for e in range(bwd["qoff"][col], bwd["qoff"][col + 1]):
+                    pairs_b.add((b, int(bwd["qidx"][e]), kt, int(bwd["qlabel"][e])))
+                col += 1
+        assert pairs_f == pairs_b
+    # a causal 300-token sequence: k-tile 0 is seen by q-tiles 0 (PARTIAL), 1, 2 (FULL)
+    bwd = oracle.block_lists_transposed(oracle.tile_labels("causal", np.array([0, 300])))
+    assert bwd["qcount"].tolist() == [3, 2, 1]
+    assert bwd["qidx"].tolist() == [0, 1, 2, 1, 2, 2]
+    assert bwd["qlabel"].tolist() == [1, 2, 2, 1, 2, 1]
+
+
+def _bwd_pins_pass(bwd):
+    try:
+        for kind in ("causal", "shared_prefix"):
+            cu, meta, q, k, v, do = _bwd_case(kind, lens=(40, 17))
+            mask_fn = lambda b: oracle.sequence_mask(kind, cu, b, meta)
+            scale = 1 / math.sqrt(q.shape[2])
+            want = _autograd_grads(kind, cu, meta, q, k, v, do, scale)
+            for b in range(len(cu) - 1):
+                s0, s1 = int(cu[b]), int(cu[b + 1])
+                for h in range(q.shape[1]):
+                    got = bwd(q[s0:s1, h].numpy(), k[s0:s1, h].numpy(), v[s0:s1, h].numpy(),
+                              do[s0:s1, h].numpy(), mask_fn(b), scale)
+                    for g_, w_ in zip(got, want):
+                        assert np.abs(g_ - w_[s0:s1, h]).max() < 1e-11
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("mutant", ["drop_delta", "dq_no_scale", "dk_untransposed", "dv_from_dp"])
+def test_backward_pins_catch_planted_mistakes(mutant):
+    real = oracle.masked_attention_backward
+    assert _bwd_pins_pass(real)
+
+    def bad(q, k, v, do, mask, scale):
+        dq, dk, dv = real(q, k, v, do, mask, scale)
+        s = np.where(mask, (q @ k.T) * scale, -np.inf)
+        m = np.where(np.isfinite(s.max(1)), s.max(1), 0)
+        p = np.where(mask, np.exp(s - m[:, None]), 0)
+        p = p / np.maximum(p.sum(1, keepdims=True), 1e-300)
+        dp = do @ v.T
+        if mutant == "drop_delta":
+            ds = p * dp
+            return (ds @ k) * scale, (ds.T @ q) * scale, dv
+        if mutant == "dq_no_scale":
+            return dq / scale, dk, dv
+        if mutant == "dk_untransposed":
+            ds = p * (dp - (do * (p @ v)).sum(1)[:, None])
+            return dq, (ds @ q) * scale if ds.shape[0] == ds.shape[1] else dk * 0, dv
+        if mutant == "dv_from_dp":
+            return dq, dk, dp.T @ do
+        return dq, dk, dv
+
+    assert not _bwd_pins_pass(bad)
