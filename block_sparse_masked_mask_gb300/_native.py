@@ -49,6 +49,11 @@ class AttnBlockMask(ctypes.Structure):
         ("off_pair_off", ctypes.c_uint64),
         ("off_pair_q0", ctypes.c_uint64),
         ("off_pair_order", ctypes.c_uint64),
+        ("off_qcount", ctypes.c_uint64),
+        ("off_qoff", ctypes.c_uint64),
+        ("off_qidx", ctypes.c_uint64),
+        ("off_qlabel", ctypes.c_uint64),
+        ("off_korder", ctypes.c_uint64),
     ]
 
 

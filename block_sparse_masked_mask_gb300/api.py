@@ -117,6 +117,11 @@ class BlockMask:
             "pair_off": self._array(s.off_pair_off, s.batch + 1, torch.int32),
             "pair_q0": self._array(s.off_pair_q0, int(hdr[3]), torch.int32),
             "pair_order": self._array(s.off_pair_order, int(hdr[3]), torch.int32),
+            "qcount": self._array(s.off_qcount, n, torch.int32),
+            "qoff": self._array(s.off_qoff, n + 1, torch.int32),
+            "qidx": self._array(s.off_qidx, nent, torch.int32),
+            "qlabel": self._array(s.off_qlabel, nent, torch.uint8),
+            "korder": self._array(s.off_korder, n, torch.int32),
         }
 
 

@@ -41,6 +41,11 @@ bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out) {
   l.pair_off = take(4 * (uint64_t(batch) + 1));
   l.pair_q0 = take(4 * nq);
   l.pair_order = take(4 * nq);
+  l.qcount = take(4 * nq);
+  l.qoff = take(4 * (nq + 1));
+  l.qidx = take(4 * nq * nk);
+  l.qlabel = take(nq * nk);
+  l.korder = take(4 * nq);
   l.total = p;
   *out = l;
   return true;
@@ -63,6 +68,11 @@ static BmView make_view(const attn_block_mask* bm) {
   v.pair_off = reinterpret_cast<int32_t*>(base + bm->off_pair_off);
   v.pair_q0 = reinterpret_cast<int32_t*>(base + bm->off_pair_q0);
   v.pair_order = reinterpret_cast<int32_t*>(base + bm->off_pair_order);
+  v.qcount = reinterpret_cast<int32_t*>(base + bm->off_qcount);
+  v.qoff = reinterpret_cast<int32_t*>(base + bm->off_qoff);
+  v.qidx = reinterpret_cast<int32_t*>(base + bm->off_qidx);
+  v.qlabel = reinterpret_cast<uint8_t*>(base + bm->off_qlabel);
+  v.korder = reinterpret_cast<int32_t*>(base + bm->off_korder);
   v.cu = bm->cu_seqlens;
   v.max_qt = bm->max_qtiles;
   v.max_nt = bm->max_ktiles;
@@ -163,6 +173,11 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   bm.off_pair_off = l.pair_off;
   bm.off_pair_q0 = l.pair_q0;
   bm.off_pair_order = l.pair_order;
+  bm.off_qcount = l.qcount;
+  bm.off_qoff = l.qoff;
+  bm.off_qidx = l.qidx;
+  bm.off_qlabel = l.qlabel;
+  bm.off_korder = l.korder;
 
   MaskArgs m{kind, bm.role_think, seg_id, role, turn};
   cudaError_t e = launch_block_mask_build(make_view(&bm), m, reinterpret_cast<cudaStream_t>(stream));

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
     }
     v.qt_seq[g] = lo;
     v.qt_idx[g] = g - v.qt_off[lo];
+    v.qcount[g] = 0;  // counted by the classifier
   }
   for (int p = tid; p < n_pairs; p += blockDim.x) {
     int lo = 0, hi = B;
@@ -287,7 +288,10 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
       }
       __syncthreads();
     }
-    if (bt < nt) row[bt] = s_lab[r];
+    if (bt < nt) {
+      row[bt] = s_lab[r];
+      if (s_lab[r] != ATTN_TILE_EMPTY) atomicAdd(v.qcount + gbase + bt, 1);  // k-tile bt's column
+    }
     const int fl = bt < nt ? s_lab[r] : -1;
     const int e = warp_sum(fl == ATTN_TILE_EMPTY), pa = warp_sum(fl == ATTN_TILE_PARTIAL),
               fu = warp_sum(fl == ATTN_TILE_FULL);
@@ -311,17 +315,14 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
   }
 }
 
-// 1 CTA: CSR offsets koff = exclusive prefix sum of kcount.
-__global__ void __launch_bounds__(1024) bm_scan_kernel(BmView v) {
-  __shared__ int s_warp[32];
-  __shared__ int s_carry;
+// Exclusive prefix sum of n counts into off[0..n] (1 CTA of 1024 threads).
+__device__ void csr_offsets(const int32_t* count, int32_t* off, int n, int* s_warp, int* s_carry) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int n = v.header[kHdrQtiles];
-  if (tid == 0) s_carry = 0;
+  if (tid == 0) *s_carry = 0;
   __syncthreads();
   for (int base = 0; base < n; base += blockDim.x) {
     const int g = base + tid;
-    const int x = g < n ? v.kcount[g] : 0;
+    const int x = g < n ? count[g] : 0;
     int incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -340,15 +341,23 @@ __global__ void __launch_bounds__(1024) bm_scan_kernel(BmView v) {
       if (lane < nw) s_warp[lane] = w;
     }
     __syncthreads();
-    if (g < n) v.koff[g] = s_carry + (warp ? s_warp[warp - 1] : 0) + incl - x;
+    if (g < n) off[g] = *s_carry + (warp ? s_warp[warp - 1] : 0) + incl - x;
     __syncthreads();
-    if (tid == 0) s_carry += s_warp[nw - 1];
+    if (tid == 0) *s_carry += s_warp[nw - 1];
     __syncthreads();
   }
-  if (tid == 0) {
-    v.koff[n] = s_carry;
-    v.header[kHdrEntries] = s_carry;
-  }
+  if (tid == 0) off[n] = *s_carry;
+  __syncthreads();
+}
+
+// 1 CTA: CSR offsets koff (q-major lists) and qoff (k-major lists).
+__global__ void __launch_bounds__(1024) bm_scan_kernel(BmView v) {
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int n = v.header[kHdrQtiles];
+  csr_offsets(v.kcount, v.koff, n, s_warp, &s_carry);
+  if (threadIdx.x == 0) v.header[kHdrEntries] = v.koff[n];
+  csr_offsets(v.qcount, v.qoff, n, s_warp, &s_carry);
 }
 
 // One CTA per q-tile: compact its row into ascending (kidx, klabel) entries,
@@ -391,6 +400,41 @@ __global__ void __launch_bounds__(128) bm_fill_kernel(BmView v) {
   if (lane == 0) s_warp[warp] = ahead;
   __syncthreads();
   if (r == 0) v.order[s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3]] = g;
+  __syncthreads();
+  // The same CTA compacts k-tile g's column (the backward's lists) and places
+  // it in the k-tiles' longest-first order.
+  {
+    const int gbase = v.qt_off[b], bt = v.qt_idx[g];
+    int qpos = v.qoff[g];
+    for (int a0 = 0; a0 < nt; a0 += kTile) {
+      const int a = a0 + r;
+      const int lab = a < nt ? v.labels[size_t(gbase + a) * v.max_nt + bt] : ATTN_TILE_EMPTY;
+      const bool keep = lab != ATTN_TILE_EMPTY;
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) s_warp[warp] = __popc(bal);
+      __syncthreads();
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += s_warp[w];
+      before += __popc(bal & ((1u << lane) - 1u));
+      if (keep) {
+        v.qidx[qpos + before] = a;
+        v.qlabel[qpos + before] = uint8_t(lab);
+      }
+      qpos += s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3];
+      __syncthreads();
+    }
+    const int qmine = v.qcount[g];
+    int qahead = 0;
+    for (int g2 = r; g2 < n_qt; g2 += blockDim.x) {
+      const int c2 = v.qcount[g2];
+      qahead += (c2 > qmine) || (c2 == qmine && g2 < g);
+    }
+    qahead = warp_sum(qahead);
+    if (lane == 0) s_warp[warp] = qahead;
+    __syncthreads();
+    if (r == 0) v.korder[s_warp[0] + s_warp[1] + s_warp[2] + s_warp[3]] = g;
+    __syncthreads();
+  }
   // The CTA of a pair's first q-tile places the pair in the longest-first
   // pair order (work = kcount of both q-tiles, ties by pair number).
   const int qa = v.qt_idx[g];

@@ -129,6 +129,11 @@ extern "C" attn_status attn_block_mask_build_noalloc(
   bm.off_pair_off = l.pair_off;
   bm.off_pair_q0 = l.pair_q0;
   bm.off_pair_order = l.pair_order;
+  bm.off_qcount = l.qcount;
+  bm.off_qoff = l.qoff;
+  bm.off_qidx = l.qidx;
+  bm.off_qlabel = l.qlabel;
+  bm.off_korder = l.korder;
 
   char* base = static_cast<char*>(workspace);
   char* sbase = static_cast<char*>(scratch);
@@ -147,6 +152,11 @@ extern "C" attn_status attn_block_mask_build_noalloc(
   v.pair_off = reinterpret_cast<int32_t*>(sbase + s_pair_off);
   v.pair_q0 = reinterpret_cast<int32_t*>(base + l.pair_q0);
   v.pair_order = reinterpret_cast<int32_t*>(base + l.pair_order);
+  v.qcount = reinterpret_cast<int32_t*>(base + l.qcount);
+  v.qoff = reinterpret_cast<int32_t*>(base + l.qoff);
+  v.qidx = reinterpret_cast<int32_t*>(base + l.qidx);
+  v.qlabel = reinterpret_cast<uint8_t*>(base + l.qlabel);
+  v.korder = reinterpret_cast<int32_t*>(base + l.korder);
   v.cu = cu_seqlens;
   v.max_qt = l.max_qt;
   v.max_nt = l.max_nt;

@@ -38,7 +38,7 @@ struct BmLayout {
   int max_qt = 0, max_nt = 0;
   uint64_t header = 0, qt_seq = 0, qt_idx = 0, labels = 0, kcount = 0, koff = 0, kidx = 0,
            klabel = 0, order = 0, qt_off = 0, summary = 0, pair_off = 0, pair_q0 = 0,
-           pair_order = 0, total = 0;
+           pair_order = 0, qcount = 0, qoff = 0, qidx = 0, qlabel = 0, korder = 0, total = 0;
 };
 
 // Returns false on overflow / invalid sizes.
@@ -60,6 +60,11 @@ struct BmView {
   int32_t* pair_off;
   int32_t* pair_q0;
   int32_t* pair_order;
+  int32_t* qcount;   // transposed (k-major) lists
+  int32_t* qoff;
+  int32_t* qidx;
+  uint8_t* qlabel;
+  int32_t* korder;
   const int32_t* cu;
   int max_qt, max_nt, batch, total_tokens, max_seqlen;
 };

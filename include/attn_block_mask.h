@@ -129,7 +129,14 @@ typedef struct attn_mask_params {
  *                                  q-tiles (2j, 2j+1) of one sequence, the second
  *                                  absent when the sequence has an odd count
  *   off_pair_order int32[NQ]       q-tile pairs by descending summed kcount,
- *                                  ties by pair number (the forward's schedule)
+ *                                  ties by pair number
+ * The transposed (k-major) lists the backward walks: k-tiles are numbered like
+ * q-tiles (tile g of its sequence is k-tile g, for the same g), and
+ *   off_qcount  int32[NQ]       number of non-EMPTY q-tiles of each k-tile
+ *   off_qoff    int32[NQ + 1]   CSR offsets into qidx / qlabel
+ *   off_qidx    int32[NQ * NK]  ascending q-tile indices (inside the sequence)
+ *   off_qlabel  uint8[NQ * NK]  ATTN_TILE_PARTIAL or ATTN_TILE_FULL per entry
+ *   off_korder  int32[NQ]       k-tiles by descending qcount, ties by index
  */
 typedef struct attn_block_mask {
   uint32_t magic;          /* set by the builder; checked by attn_fwd */
@@ -147,7 +154,7 @@ typedef struct attn_block_mask {
   size_t workspace_bytes;
   uint64_t off_header, off_qt_seq, off_qt_idx, off_labels, off_kcount, off_koff,
       off_kidx, off_klabel, off_order, off_qt_off, off_summary, off_pair_off, off_pair_q0,
-      off_pair_order;
+      off_pair_order, off_qcount, off_qoff, off_qidx, off_qlabel, off_korder;
 } attn_block_mask;
 
 /*

@@ -1,7 +1,8 @@
 """GPU block-mask builder vs the oracle's brute-force labels: bit-exact.
 
-Labels, per-q-tile compacted lists, q-tile descriptors, pair totals and the
-longest-first order must equal what counting the materialised mask gives.
+Labels, per-q-tile compacted lists, q-tile descriptors, pair totals, the
+longest-first orders and the transposed (k-major) lists must equal what
+counting the materialised mask gives.
 """
 import numpy as np
 import pytest
@@ -49,6 +50,13 @@ def assert_matches_oracle(w, bm):
     work = [int(want["kcount"][g]) + (int(want["kcount"][g + 1])
             if g + 1 < n and want["qt_seq"][g + 1] == want["qt_seq"][g] else 0) for g in q0]
     assert got["pair_order"].tolist() == oracle.lpt_order(work).tolist()
+    # transposed (k-major) lists for the backward, and the k-tiles' order
+    wt = oracle.block_lists_transposed(labels)
+    assert np.array_equal(got["qcount"].numpy(), wt["qcount"])
+    assert np.array_equal(got["qoff"].numpy(), wt["qoff"])
+    assert np.array_equal(got["qidx"].numpy(), wt["qidx"])
+    assert np.array_equal(got["qlabel"].numpy(), wt["qlabel"])
+    assert np.array_equal(got["korder"].numpy(), oracle.lpt_order(wt["qcount"]))
 
 
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5])

@@ -23,7 +23,7 @@ from block_sparse_masked_mask_gb300 import _native, api
 from block_sparse_masked_mask_gb300 import workloads as W
 
 OUTPUT_ARRAYS = ["header", "qt_seq", "qt_idx", "kcount", "koff", "kidx", "klabel", "order",
-                 "pair_q0", "pair_order"]
+                 "pair_q0", "pair_order", "qcount", "qoff", "qidx", "qlabel", "korder"]
 
 
 def _both_masks(w):
