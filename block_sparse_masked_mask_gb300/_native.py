@@ -87,6 +87,11 @@ def lib() -> ctypes.CDLL:
         c_int32, ctypes.c_float, c_void_p, c_int32, c_int32, ctypes.c_int, P(AttnMaskParams),
         c_void_p, c_void_p, c_void_p, P(AttnBlockMask), c_void_p]
     L.attn_fwd.restype = ctypes.c_int
+    L.attn_bwd.argtypes = [
+        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+        c_void_p, ctypes.c_int, c_int32, c_int32, c_int32, ctypes.c_float, c_void_p, c_int32, c_int32,
+        ctypes.c_int, P(AttnMaskParams), c_void_p, c_void_p, c_void_p, P(AttnBlockMask), c_void_p]
+    L.attn_bwd.restype = ctypes.c_int
     L.attn_get_status.argtypes = [P(AttnBlockMask), c_void_p]
     L.attn_get_status.restype = ctypes.c_int
     L.attn_status_string.argtypes = [ctypes.c_int]

@@ -191,6 +191,31 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, k
     return out, lse
 
 
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, bm: BlockMask, kind, cu_seqlens: torch.Tensor,
+             max_seqlen: int, seg_id=None, role=None, turn=None, role_think: int = 1,
+             scale: float = 0.0, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             delta: Optional[torch.Tensor] = None, stream=None):
+    """Masked attention backward (bf16); returns (dQ, dK, dV), each [T, H, D]."""
+    T, H, D = q.shape
+    if q.dtype != torch.bfloat16:
+        raise AttnError(2, "attn_bwd: dtype must be bfloat16")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if delta is None:
+        delta = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    params = _native.AttnMaskParams(role_think)
+    _check(_native.lib().attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dq), _ptr(dk),
+        _ptr(dv), DTYPES[q.dtype], T, H, D, float(scale), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+        max_seqlen, _kind(kind), ctypes.byref(params), _ptr(seg_id), _ptr(role), _ptr(turn),
+        ctypes.byref(bm.struct), _stream(stream)),
+        "attn_bwd")
+    return dq, dk, dv
+
+
 def attn_get_status(bm: BlockMask, stream=None) -> int:
     """Synchronise and return the device status code of the mask's error word."""
     return int(_native.lib().attn_get_status(ctypes.byref(bm.struct), _stream(stream)))

@@ -19,8 +19,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libattnmask.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["api.cu", "blockmask.cu", "blockmask_noalloc.cu", "attn_fwd_bf16.cu", "attn_fwd_f32.cu"]
-HEADERS = ["common.cuh", "ptx.cuh"]
+SOURCES = ["api.cu", "blockmask.cu", "blockmask_noalloc.cu", "attn_fwd_bf16.cu", "attn_fwd_f32.cu",
+           "attn_bwd_bf16.cu"]
+HEADERS = ["common.cuh", "ptx.cuh", "tile_pipeline.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

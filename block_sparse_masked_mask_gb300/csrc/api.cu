@@ -227,6 +227,55 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return dtype == ATTN_DTYPE_BF16 ? launch_attn_fwd_bf16(a, s) : launch_attn_fwd_f32(a, s);
 }
 
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, float* delta, void* dq, void* dk, void* dv, attn_dtype dtype,
+                     int32_t total_tokens, int32_t num_heads, int32_t head_dim, float scale,
+                     const int32_t* cu_seqlens, int32_t batch, int32_t max_seqlen,
+                     attn_mask_kind kind, const attn_mask_params* params, const int32_t* seg_id,
+                     const int8_t* role, const int32_t* turn, const attn_block_mask* bm,
+                     attn_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !delta || !dq || !dk || !dv || !cu_seqlens || !bm)
+    return ATTN_ERR_INVALID_ARG;
+  if (!valid_kind(kind) || total_tokens < 0 || num_heads < 1 || batch < 1) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale)) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP32) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!metadata_present(kind, seg_id, role, turn)) return ATTN_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(delta) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  const int role_think = params ? params->role_think : 1;
+  if (bm->magic != kMaskMagic || bm->kind != kind || bm->cu_seqlens != cu_seqlens ||
+      bm->batch != batch || bm->total_tokens != total_tokens || bm->max_seqlen != max_seqlen ||
+      bm->role_think != role_think || bm->block_m != kTile || bm->block_n != kTile)
+    return ATTN_ERR_MASK_MISMATCH;
+  if (uint64_t(total_tokens) * uint64_t(num_heads) * uint64_t(head_dim) > (uint64_t(1) << 40))
+    return ATTN_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return ATTN_OK;
+
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.total_tokens = total_tokens;
+  a.num_heads = num_heads;
+  a.head_dim = head_dim;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(float(head_dim));
+  a.bm = make_view(bm);
+  a.mask = MaskArgs{kind, role_think, seg_id, role, turn};
+  return launch_attn_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 attn_status attn_get_status(const attn_block_mask* bm, attn_stream_t stream) {
   if (bm == nullptr || bm->magic != kMaskMagic) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -1,0 +1,956 @@
+// bf16 attention backward on the sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// Gradients of O = softmax(scale Q K^T, masked) V for an upstream dO, with the
+// forward's LSE: P = exp(scale S - LSE) is recomputed tile by tile, and
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_d dO_id O_id,  dS = P * (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+// The xorl issue (Verified FA4 gaps, items 1-3) asks for this backward over
+// the block-sparse masks, walking the transposed (k-major) lists for dK and
+// dV, and with a deterministic dQ.  Three kernels:
+//   * delta: D = rowsum(dO * O) per (token, head), fp32;
+//   * dK/dV: one work item per (k-tile, head) walks its k-major list of
+//     q-tiles, accumulating dK and dV in TMEM (K, V stay in shared memory);
+//   * dQ: one work item per (q-tile, head) walks its q-major list of k-tiles,
+//     accumulating dQ in TMEM.  dQ is a sum over k-tiles in a fixed order
+//     inside one CTA, so it is bit-reproducible, with no atomics.
+// Both list-walking kernels recompute S and dP (seven GEMMs where a dQ with
+// atomics would need five); the masks are applied on PARTIAL tiles only and
+// EMPTY tiles are never loaded.  Warp roles (256 threads): warps 0-3 one
+// thread per TMEM lane (a query row for dQ, a key row for dK/dV), warp 4 the
+// TMA producer, warp 5 the tcgen05 issuer (one thread, TMEM owner), warps 6-7
+// idle.  Every mbarrier wait is bounded as in the forward.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tile_pipeline.cuh"
+
+namespace attnmask {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kWarpLoad = 4, kWarpMma = 5;
+
+// ---------------------------------------------------------------------------
+// D = rowsum(dO * O): one warp per (token, head) row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, int T, int H) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + warp;  // t * H + h
+  if (row >= (long long)T * H) return;
+  const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(o + row * D);
+  const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(dout + row * D);
+  float acc = 0.f;
+#pragma unroll
+  for (int c = lane; c < D / 2; c += 32) {
+    const float2 a = __bfloat1622float2(po[c]), b = __bfloat1622float2(pd[c]);
+    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    const int t = int(row / H), h = int(row % H);
+    delta[size_t(h) * T + t] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared layout of the two list-walking kernels.
+template <int D>
+struct BwdCfg : TileLayout<D> {
+  using TileLayout<D>::TILE;
+  using TileLayout<D>::CHUNK;
+  using TileLayout<D>::CE;
+  using TileLayout<D>::NCH;
+  using TileLayout<D>::ROWB;
+  static constexpr int NSLOT = 4;  // ring of streamed tiles (two per list entry)
+  // fixed tiles (Q and dO for dQ; K and V for dK/dV), then the ring
+  static constexpr int OFF_A = 0, OFF_B = TILE, OFF_RING = 2 * TILE;
+  static constexpr int B_FIX = 0, B_FIXFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
+                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 1, B_ODONE = B_PFULL + 1,
+                       B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
+                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_RINGI = OFF_MISC + 16;                 // two decoded work items, 8 ints each
+  // per ring slot: 128 ints of side data (key codes, or the q-tile's LSE, D and
+  // query codes: 3 x 128 words for the dK/dV kernel's Q slots)
+  static constexpr int OFF_SIDE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
+  static constexpr int SIDE_WORDS = 3 * kTile;
+  static constexpr int OFF_STAGE = OFF_SIDE + NSLOT * SIDE_WORDS * 4;  // per warp: 16 output rows
+  static constexpr int STAGE_WARP = 16 * 2 * D;
+  static constexpr int SMEM_USED = OFF_STAGE + 4 * STAGE_WARP;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
+struct BwdParams {
+  int32_t* header;
+  const int32_t* order;   // items' tile order (q-major for dQ, k-major for dK/dV)
+  const int32_t* qt_seq;
+  const int32_t* qt_idx;
+  const int32_t* off;     // CSR offsets of the walked lists
+  const int32_t* idx;     // tile index inside the sequence
+  const uint8_t* label;
+  const int32_t* cu;
+  MaskArgs mask;
+  const float* lse;       // [H, T]
+  const float* delta;     // [H, T]
+  __nv_bfloat16* out0;    // dQ, or dK
+  __nv_bfloat16* out1;    // unused, or dV
+  int H, T;
+  float scale;
+  float scale_log2;
+};
+
+// One work item: a tile of one sequence and one head, and its list.
+struct BwdItem {
+  int h, s0, L, i0, e0, e1;  // i0: first row of the item's tile, local to the sequence
+};
+
+__device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
+  BwdItem it;
+  it.h = item / n_t;
+  const int g = p.order[item % n_t];
+  const int b = p.qt_seq[g];
+  it.s0 = p.cu[b];
+  it.L = p.cu[b + 1] - it.s0;
+  it.i0 = p.qt_idx[g] * kTile;
+  it.e0 = p.off[g];
+  it.e1 = p.off[g + 1];
+  return it;
+}
+
+__device__ __forceinline__ void bwd_store(volatile int* d, const BwdItem& it, bool valid) {
+  d[0] = valid ? 1 : 0;
+  d[1] = it.h;
+  d[2] = it.s0;
+  d[3] = it.L;
+  d[4] = it.i0;
+  d[5] = it.e0;
+  d[6] = it.e1;
+}
+__device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
+  if (!d[0]) return false;
+  it.h = d[1];
+  it.s0 = d[2];
+  it.L = d[3];
+  it.i0 = d[4];
+  it.e0 = d[5];
+  it.e1 = d[6];
+  return true;
+}
+
+// The producer takes a ticket and publishes the item in ring slot k & 1.
+__device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, int n_items, int n_t, BwdItem& it,
+                                           volatile int* ring, uint32_t iempty0, uint32_t ifull0,
+                                           volatile uint32_t* abort_flag, int32_t* err) {
+  int ticket = 0;
+  if (lane == 0) ticket = atomicAdd(p.header + kHdrTicket, 1);
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  const bool valid = ticket < n_items;
+  if (valid) it = bwd_decode(p, ticket, n_t);
+  const int slot_i = k & 1;
+  if (k >= 2 && !warp_wait(iempty0 + 8u * slot_i, uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 15)) return -1;
+  if (lane == 0) {
+    bwd_store(ring + 8 * slot_i, it, valid);
+    ptx::mbar_arrive(ifull0 + 8u * slot_i);
+  }
+  return valid ? 1 : 0;
+}
+
+// Write this warp's 32 rows of COLS bf16 values (`w`, packed pairs) to rows
+// 0 .. nrows-1 of `base` (row stride `rstride` elements) as whole 16-byte
+// pieces, 16 rows at a time through the warp's shared-memory stage (chunks
+// XOR-swizzled by row so that neither side has bank conflicts).
+template <int COLS>
+__device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint32_t (&w)[COLS / 2],
+                                           __nv_bfloat16* base, size_t rstride, int nrows) {
+  constexpr int RB = COLS * 2;   // bytes per row
+  constexpr int CPR = RB / 16;   // 16-byte chunks per row
+  constexpr int RPI = 32 / CPR;  // rows per warp-wide store
+#pragma unroll
+  for (int half16 = 0; half16 < 2; ++half16) {
+    if ((lane >> 4) == half16) {
+      const int q = lane & 15;
+#pragma unroll
+      for (int c = 0; c < CPR; ++c)
+        *reinterpret_cast<uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 16 / RPI; ++i) {
+      const int q = i * RPI + lane / CPR, c = lane % CPR;
+      const int rr = half16 * 16 + q;
+      const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
+      if (rr < nrows) *reinterpret_cast<uint4*>(base + size_t(rr) * rstride + 8 * c) = val;
+    }
+    __syncwarp();
+  }
+}
+
+// TMEM -> registers: D fp32 columns of this thread's lane from `taddr`, times
+// `mul`, rounded to bf16 pairs (zeros when `have` is false).
+template <int D>
+__device__ __forceinline__ void tmem_row_bf16(uint32_t taddr, float mul, bool have, uint32_t (&w)[D / 2]) {
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    uint32_t v[32];
+    if (have) {
+      ptx::tmem_ld32(taddr + 32 * q, v);
+      ptx::tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[c] = 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      w[16 * q + c] = ptx::pack_bf16(__uint_as_float(v[2 * c]) * mul, __uint_as_float(v[2 * c + 1]) * mul);
+  }
+}
+
+// Producer: rows [row0, row0 + 128) of head h from maps ma and mb into ring
+// slots sa and sb, completing FULL + slot.  When only `valid` < 128 rows
+// belong to the sequence, both copies complete the tail barrier instead and
+// the other rows are zeroed before FULL opens: they hold the next sequence's
+// values (or the zero fill past the tensor), and an inf there would turn the
+// zero weights these rows get in the products into NaN.
+template <int D>
+__device__ __forceinline__ bool load_pair(const CUtensorMap* ma, const CUtensorMap* mb, int h, int row0, int valid,
+                                          uint32_t ring, uint8_t* ring_gen, int sa, int sb, uint32_t full0,
+                                          uint32_t tail_bar, int& ntail, bool& tail_pending, int lane,
+                                          volatile uint32_t* abort_flag, int32_t* err) {
+  using C = BwdCfg<D>;
+  const uint32_t da = ring + uint32_t(sa) * C::TILE, db = ring + uint32_t(sb) * C::TILE;
+  const bool tail = valid < kTile;
+  const uint32_t ba = tail ? tail_bar : full0 + 8u * uint32_t(sa);
+  const uint32_t bb = tail ? tail_bar : full0 + 8u * uint32_t(sb);
+  if (lane == 0) {
+    if (tail) {
+      ptx::mbar_arrive_expect_tx(tail_bar, 2 * C::TILE);
+    } else {
+      ptx::mbar_arrive_expect_tx(ba, C::TILE);
+      ptx::mbar_arrive_expect_tx(bb, C::TILE);
+    }
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c) {
+      ptx::tma_load_3d(da + c * C::CHUNK, ma, ba, c * C::CE, h, row0);
+      ptx::tma_load_3d(db + c * C::CHUNK, mb, bb, c * C::CE, h, row0);
+    }
+  }
+  if (!tail) return true;
+  tail_pending = true;
+  if (!warp_wait(tail_bar, uint32_t(ntail) & 1u, abort_flag, err, 2)) return false;
+  tail_pending = false;
+  ++ntail;
+  for (int rr = valid + lane; rr < kTile; rr += 32) {
+#pragma unroll
+    for (int c = 0; c < C::NCH; ++c) {
+      uint4* ra = reinterpret_cast<uint4*>(ring_gen + sa * C::TILE + c * C::CHUNK + rr * C::ROWB);
+      uint4* rb = reinterpret_cast<uint4*>(ring_gen + sb * C::TILE + c * C::CHUNK + rr * C::ROWB);
+#pragma unroll
+      for (int x = 0; x < C::ROWB / 16; ++x) {
+        ra[x] = make_uint4(0u, 0u, 0u, 0u);
+        rb[x] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::mbar_arrive(full0 + 8u * uint32_t(sa));
+    ptx::mbar_arrive(full0 + 8u * uint32_t(sb));
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one item per (q-tile, head); per listed k-tile j:
+//   S = Q K_j^T, dP = dO V_j^T (TMEM), dS = P (dP - D) over S, dQ += dS K_j.
+// TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_t = p.header[kHdrQtiles];
+  const int n_items = n_t * p.H;
+  int32_t* err = p.header + kHdrError;
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_A, sDO = base + C::OFF_B, sRing = base + C::OFF_RING;
+  const uint32_t bars = base + C::OFF_BAR;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+  volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
+  int* side = reinterpret_cast<int*>(sbase + C::OFF_SIDE);
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_FIX), 1);
+    ptx::mbar_init(bar(C::B_FIXFREE), 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(bar(C::B_FULL + s), 1);
+      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+    }
+    ptx::mbar_init(bar(C::B_VTMA), 1);
+    ptx::mbar_init(bar(C::B_SFULL), 1);
+    ptx::mbar_init(bar(C::B_PFULL), 128);
+    ptx::mbar_init(bar(C::B_ODONE), 1);
+    ptx::mbar_init(bar(C::B_OFREE), 128);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(C::B_IFULL + i), 1);
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);  // row threads, MMA thread
+    }
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const bool skip = *abort_flag != 0u;
+
+  if (skip) {
+  } else if (warp == kWarpLoad) {
+    // ---------------------------------------------------------- producer
+    int nload = 0, ntail = 0, nfix = 0;
+    bool tail_pending = false, ok = true;
+    BwdItem it_next;
+    int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+                              abort_flag, err);
+    for (int k = 0; ok && st_next == 1; ++k) {
+      const BwdItem it = it_next;
+      st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+                            abort_flag, err);
+      if (st_next < 0) break;
+      // Q and dO of this q-tile, once the previous item's MMAs no longer read them
+      if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE);
+        for (int c = 0; c < C::NCH; ++c) {
+          ptx::tma_load_3d(sQ + c * C::CHUNK, &tmQ, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+          ptx::tma_load_3d(sDO + c * C::CHUNK, &tmDO, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+        }
+      }
+      ++nfix;
+      for (int e = it.e0; e < it.e1; ++e) {
+        const int j0 = __ldg(p.idx + e) * kTile, kn = min(kTile, it.L - j0);
+        const int lab = __ldg(p.label + e);
+        // K(j) and V(j) into two free slots; the keys' mask codes of a PARTIAL
+        // tile go to K's side words
+        const int ks = nload % C::NSLOT, vs = (nload + 1) % C::NSLOT;
+        if (nload >= C::NSLOT &&
+            (!warp_wait(bar(C::B_EMPTY + ks), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
+             !warp_wait(bar(C::B_EMPTY + vs), uint32_t((nload + 1) / C::NSLOT - 1) & 1u, abort_flag, err, 1))) {
+          ok = false;
+          break;
+        }
+        if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL) {
+          for (int c = lane; c < kTile; c += 32)
+            side[ks * C::SIDE_WORDS + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
+          __syncwarp();
+        }
+        if (!load_pair<D>(&tmK, &tmV, it.h, it.s0 + j0, kn, sRing, sbase + C::OFF_RING, ks, vs, bar(C::B_FULL),
+                          bar(C::B_VTMA), ntail, tail_pending, lane, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        nload += 2;
+      }
+    }
+    if (lane == 0) {
+      for (int s = 0; s < C::NSLOT; ++s) {
+        if (nload <= s) continue;
+        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
+        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
+      }
+      if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
+      if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int nload = 0, nent = 0;
+      bool ok = true;
+      const uint64_t qdesc = kmajor_base<D>(sQ), dodesc = kmajor_base<D>(sDO);
+      const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
+      for (int k = 0; ok; ++k) {
+        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+        BwdItem it;
+        const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
+        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        if (!valid) break;
+        if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
+        const int n = it.e1 - it.e0;
+        for (int j = 0; j < n; ++j) {
+          const int ks = nload % C::NSLOT, vs = (nload + 1) % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + ks), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4) ||
+              !wait_bar(bar(C::B_FULL + vs), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // S = Q K^T and dP = dO V^T (V read K-major like K here)
+          issue_s<D>(tmem + COL_S, qdesc, kdesc0 + uint64_t(ks) * (C::TILE >> 4));
+          issue_s<D>(tmem + COL_DP, dodesc, kmajor_base<D>(sRing) + uint64_t(vs) * (C::TILE >> 4));
+          ptx::mma_commit(bar(C::B_SFULL));
+          if (!wait_bar(bar(C::B_PFULL), uint32_t(nent) & 1u, abort_flag, err, 5)) { ok = false; break; }
+          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // dQ += dS K (dS written over S; K read MN-major)
+          issue_pv<D>(tmem + COL_DQ, tmem + COL_S, vdesc0 + uint64_t(ks) * (C::TILE >> 4), j > 0);
+          ptx::mma_commit(bar(C::B_EMPTY + ks));
+          ptx::mma_commit(bar(C::B_EMPTY + vs));
+          nload += 2;
+          ++nent;
+        }
+        if (!ok) break;
+        // every MMA of this item reading Q and dO has been issued
+        ptx::mma_commit(bar(C::B_FIXFREE));
+        if (n > 0) ptx::mma_commit(bar(C::B_ODONE));
+      }
+      ptx::mma_commit(bar(C::B_DRAIN));
+      drain_bar(bar(C::B_DRAIN), 0, err);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------------------------------------------------- dS (query rows)
+    const int r = warp * 32 + lane;
+    const int kind = p.mask.kind;
+    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const float c2 = p.scale_log2;
+    int nent = 0, nodone = 0, nload = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      BwdItem it;
+      const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
+      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      const int qn = min(kTile, it.L - it.i0);
+      const bool row_in = r < qn;
+      const int il = it.i0 + r;
+      const int tok = it.s0 + il;
+      const float lse = row_in ? p.lse[size_t(it.h) * p.T + tok] : -INFINITY;
+      // a row that sees no key has P = 0 (its LSE is -inf)
+      const float lse2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
+      const float dlt = row_in ? p.delta[size_t(it.h) * p.T + tok] : 0.f;
+      const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, tok) : 0;
+      const int n = it.e1 - it.e0;
+      for (int jj = 0; jj < n; ++jj) {
+        const int e = it.e0 + jj;
+        const int j0 = __ldg(p.idx + e) * kTile, kn = min(kTile, it.L - j0);
+        const int lab = __ldg(p.label + e);
+        const int ks = nload % C::NSLOT;
+        nload += 2;
+        if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t vis[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
+          const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
+          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+            // the key codes came with K(j): its load has landed (S(j) is done)
+            if (!warp_wait(bar(C::B_FULL + ks), uint32_t((nload - 2) / C::NSLOT) & 1u, abort_flag, err, 9)) {
+              ok = false;
+              break;
+            }
+            const int* codes = side + ks * C::SIDE_WORDS;
+            if (kind == ATTN_MASK_STRIP_THINKING) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(codes, q, qcode);
+            } else if (kind == ATTN_MASK_SHARED_PREFIX) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(codes, q, qcode);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
+            }
+          }
+        }
+        // dS = P (dP - D), P = 2^(S c2 - LSE log2 e), two 64-column halves; each
+        // half's bf16 dS goes over the first 32 of its own S columns.
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sv[2][32], dv[2][32];
+          ptx::tmem_ld32(lane_base + COL_S + 64 * hf, sv[0]);
+          ptx::tmem_ld32(lane_base + COL_S + 64 * hf + 32, sv[1]);
+          ptx::tmem_ld32(lane_base + COL_DP + 64 * hf, dv[0]);
+          ptx::tmem_ld32(lane_base + COL_DP + 64 * hf + 32, dv[1]);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t vw = vis[2 * hf + q];
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[q][c]), __uint_as_float(sv[q][c + 1])),
+                                          make_float2(c2, c2), make_float2(-lse2, -lse2));
+              float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
+              p0 = (vw >> c) & 1u ? p0 : 0.f;
+              p1 = (vw >> (c + 1)) & 1u ? p1 : 0.f;
+              const float d0 = p0 * (__uint_as_float(dv[q][c]) - dlt);
+              const float d1 = p1 * (__uint_as_float(dv[q][c + 1]) - dlt);
+              pk[c >> 1] = ptx::pack_bf16(d0, d1);
+            }
+            ptx::tmem_st16(lane_base + COL_S + 64 * hf + 16 * q, pk);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL));
+        ++nent;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (n > 0) {
+        if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
+        ++nodone;
+      }
+      ptx::tc_fence_after();
+      uint32_t w[D / 2];
+      tmem_row_bf16<D>(lane_base + COL_DQ, p.scale, n > 0, w);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_OFREE));
+      store_rows<D>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
+                       p.out0 + (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D, size_t(p.H) * D,
+                       qn - warp * 32);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
+      atomicExch(p.header + kHdrTicket, 0);
+      atomicExch(p.header + kHdrFinished, 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one item per (k-tile, head); per listed q-tile i:
+//   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, TMEM lane = key),
+//   P^T = 2^(S^T c2 - LSE_i log2 e), dS^T = P^T (dP^T - D_i),
+//   dV += P^T dO_i, dK += dS^T Q_i.
+// TMEM: dV [0, D), dK [128, 128+D), S^T [256,384), dP^T [384,512).
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                         const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_t = p.header[kHdrQtiles];
+  const int n_items = n_t * p.H;
+  int32_t* err = p.header + kHdrError;
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t sK = base + C::OFF_A, sV = base + C::OFF_B, sRing = base + C::OFF_RING;
+  const uint32_t bars = base + C::OFF_BAR;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+  volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
+  int* side = reinterpret_cast<int*>(sbase + C::OFF_SIDE);
+  constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_ST = 256, COL_DPT = 384;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_FIX), 1);
+    ptx::mbar_init(bar(C::B_FIXFREE), 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(bar(C::B_FULL + s), 1);
+      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
+    }
+    ptx::mbar_init(bar(C::B_VTMA), 1);
+    ptx::mbar_init(bar(C::B_SFULL), 1);
+    ptx::mbar_init(bar(C::B_PFULL), 128);
+    ptx::mbar_init(bar(C::B_ODONE), 1);
+    ptx::mbar_init(bar(C::B_OFREE), 128);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(C::B_IFULL + i), 1);
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);
+    }
+    ptx::mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const bool skip = *abort_flag != 0u;
+
+  if (skip) {
+  } else if (warp == kWarpLoad) {
+    // ---------------------------------------------------------- producer
+    int nload = 0, ntail = 0, nfix = 0;
+    bool tail_pending = false, ok = true;
+    BwdItem it_next;
+    int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+                              abort_flag, err);
+    for (int k = 0; ok && st_next == 1; ++k) {
+      const BwdItem it = it_next;
+      st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+                            abort_flag, err);
+      if (st_next < 0) break;
+      // K and V of this k-tile, once the previous item's MMAs no longer read
+      // them (rows past the sequence end only reach their own dK, dV rows,
+      // which are not stored)
+      if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE);
+        for (int c = 0; c < C::NCH; ++c) {
+          ptx::tma_load_3d(sK + c * C::CHUNK, &tmK, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+          ptx::tma_load_3d(sV + c * C::CHUNK, &tmV, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+        }
+      }
+      ++nfix;
+      for (int e = it.e0; e < it.e1; ++e) {
+        const int a0 = __ldg(p.idx + e) * kTile, an = min(kTile, it.L - a0);
+        const int lab = __ldg(p.label + e);
+        // Q(i) and dO(i) into two free slots; Q's side words get the q-tile's
+        // LSE (times log2 e; +inf for rows that see no key or lie past the
+        // end), D and, on PARTIAL tiles, the query codes
+        const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
+        if (nload >= C::NSLOT &&
+            (!warp_wait(bar(C::B_EMPTY + qs), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
+             !warp_wait(bar(C::B_EMPTY + ds), uint32_t((nload + 1) / C::NSLOT - 1) & 1u, abort_flag, err, 1))) {
+          ok = false;
+          break;
+        }
+        {
+          float* sl = reinterpret_cast<float*>(side + qs * C::SIDE_WORDS);
+          for (int c = lane; c < kTile; c += 32) {
+            const bool in = c < an;
+            const size_t at = size_t(it.h) * p.T + it.s0 + a0 + c;
+            const float l = in ? p.lse[at] : -INFINITY;
+            sl[c] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+            sl[kTile + c] = in ? p.delta[at] : 0.f;
+            if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL)
+              side[qs * C::SIDE_WORDS + 2 * kTile + c] = query_code(p.mask, it.s0 + a0 + min(c, an - 1));
+          }
+          __syncwarp();
+        }
+        if (!load_pair<D>(&tmQ, &tmDO, it.h, it.s0 + a0, an, sRing, sbase + C::OFF_RING, qs, ds, bar(C::B_FULL),
+                          bar(C::B_VTMA), ntail, tail_pending, lane, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        nload += 2;
+      }
+    }
+    if (lane == 0) {
+      for (int s = 0; s < C::NSLOT; ++s) {
+        if (nload <= s) continue;
+        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
+        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
+      }
+      if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
+      if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int nload = 0, nent = 0;
+      bool ok = true;
+      const uint64_t kdesc = kmajor_base<D>(sK), vdesc = kmajor_base<D>(sV);
+      const uint64_t rk0 = kmajor_base<D>(sRing), rv0 = v_base<D>(sRing);
+      for (int k = 0; ok; ++k) {
+        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+        BwdItem it;
+        const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
+        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        if (!valid) break;
+        if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
+        const int n = it.e1 - it.e0;
+        for (int j = 0; j < n; ++j) {
+          const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + qs), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4) ||
+              !wait_bar(bar(C::B_FULL + ds), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // S^T = K Q^T and dP^T = V dO^T
+          issue_s<D>(tmem + COL_ST, kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4));
+          issue_s<D>(tmem + COL_DPT, vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4));
+          ptx::mma_commit(bar(C::B_SFULL));
+          if (!wait_bar(bar(C::B_PFULL), uint32_t(nent) & 1u, abort_flag, err, 5)) { ok = false; break; }
+          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q (P^T over S^T, dS^T over dP^T; dO, Q read MN-major)
+          issue_pv<D>(tmem + COL_DV, tmem + COL_ST, rv0 + uint64_t(ds) * (C::TILE >> 4), j > 0);
+          issue_pv<D>(tmem + COL_DK, tmem + COL_DPT, rv0 + uint64_t(qs) * (C::TILE >> 4), j > 0);
+          ptx::mma_commit(bar(C::B_EMPTY + qs));
+          ptx::mma_commit(bar(C::B_EMPTY + ds));
+          nload += 2;
+          ++nent;
+        }
+        if (!ok) break;
+        ptx::mma_commit(bar(C::B_FIXFREE));
+        if (n > 0) ptx::mma_commit(bar(C::B_ODONE));
+      }
+      ptx::mma_commit(bar(C::B_DRAIN));
+      drain_bar(bar(C::B_DRAIN), 0, err);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------------------------------------------------- P^T, dS^T (key rows)
+    const int r = warp * 32 + lane;
+    const int kind = p.mask.kind;
+    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const float c2 = p.scale_log2;
+    int nent = 0, nodone = 0, nload = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      BwdItem it;
+      const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
+      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      const int kn = min(kTile, it.L - it.i0);
+      const bool row_in = r < kn;
+      const int kl = it.i0 + r;  // local key index
+      const int kcode = (row_in && kind != ATTN_MASK_CAUSAL) ? key_code(p.mask, it.s0 + kl) : 0;
+      // keys of a warp usually share one code: then a query's visibility is the
+      // same for all of them, and one ballot over the queries' codes gives a word
+      const int kcode_w = __shfl_sync(0xffffffffu, kcode, 0);
+      const bool uniform_k = __all_sync(0xffffffffu, !row_in || kcode == kcode_w);
+      const int n = it.e1 - it.e0;
+      for (int jj = 0; jj < n; ++jj) {
+        const int e = it.e0 + jj;
+        const int a0 = __ldg(p.idx + e) * kTile, an = min(kTile, it.L - a0);
+        const int lab = __ldg(p.label + e);
+        const int qs = nload % C::NSLOT;
+        nload += 2;
+        if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
+        ptx::tc_fence_after();
+        // the q-tile's LSE, D and codes came with Q(i): its load has landed
+        if (!warp_wait(bar(C::B_FULL + qs), uint32_t((nload - 2) / C::NSLOT) & 1u, abort_flag, err, 9)) {
+          ok = false;
+          break;
+        }
+        const float* sl = reinterpret_cast<const float*>(side + qs * C::SIDE_WORDS);
+        // bit c of vis[c / 32]: query column c sees this key.  Causal part and
+        // bounds: a0 + c >= kl and c < an, a suffix of a prefix.
+        uint32_t vis[4];
+        {
+          const int lo = kl - a0;  // first visible column
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vis[q] = ~prefix_bits(lo - 32 * q) & prefix_bits(an - 32 * q);
+        }
+        if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+          const int* qc = side + qs * C::SIDE_WORDS + 2 * kTile;
+          if (uniform_k) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int qcv = qc[32 * q + lane];
+              bool ok_v;
+              if (kind == ATTN_MASK_STRIP_THINKING) ok_v = code_visible(ATTN_MASK_STRIP_THINKING, qcv, kcode_w);
+              else if (kind == ATTN_MASK_SHARED_PREFIX) ok_v = code_visible(ATTN_MASK_SHARED_PREFIX, qcv, kcode_w);
+              else ok_v = code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcv, kcode_w);
+              vis[q] &= __ballot_sync(0xffffffffu, ok_v);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w = 0;
+              for (int c = 0; c < 32; ++c) w |= uint32_t(code_visible(kind, qc[32 * q + c], kcode)) << c;
+              vis[q] &= w;
+            }
+          }
+        }
+        if (lab != ATTN_TILE_PARTIAL) {
+          // FULL: only the bounds
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(an - 32 * q);
+        }
+        // one 32-column quarter at a time: quarter qq reads S^T and dP^T columns
+        // [32qq, 32qq+32) and writes bf16 pairs to columns 64(qq/2) + 16(qq%2)
+        // + [0,16), which the quarters before it have already read
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const int cq = 32 * qq;
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(lane_base + COL_ST + cq, sv);
+          ptx::tmem_ld32(lane_base + COL_DPT + cq, dv);
+          ptx::tmem_wait_ld();
+          const uint32_t vw = vis[qq];
+          uint32_t pp[16], pd[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float l0 = sl[cq + c], l1 = sl[cq + c + 1];
+            const float g0 = sl[kTile + cq + c], g1 = sl[kTile + cq + c + 1];
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                        make_float2(c2, c2), make_float2(-l0, -l1));
+            float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
+            p0 = (vw >> c) & 1u ? p0 : 0.f;
+            p1 = (vw >> (c + 1)) & 1u ? p1 : 0.f;
+            pp[c >> 1] = ptx::pack_bf16(p0, p1);
+            pd[c >> 1] = ptx::pack_bf16(p0 * (__uint_as_float(dv[c]) - g0), p1 * (__uint_as_float(dv[c + 1]) - g1));
+          }
+          const uint32_t at = 64u * uint32_t(qq >> 1) + 16u * uint32_t(qq & 1);
+          ptx::tmem_st16(lane_base + COL_ST + at, pp);
+          ptx::tmem_st16(lane_base + COL_DPT + at, pd);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL));
+        ++nent;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (n > 0) {
+        if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
+        ++nodone;
+      }
+      ptx::tc_fence_after();
+      const size_t row0 = (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D;
+      uint8_t* stage = sbase + C::OFF_STAGE + warp * C::STAGE_WARP;
+      {
+        uint32_t w[D / 2];
+        tmem_row_bf16<D>(lane_base + COL_DV, 1.f, n > 0, w);
+        store_rows<D>(stage, lane, w, p.out1 + row0, size_t(p.H) * D, kn - warp * 32);
+      }
+      uint32_t w[D / 2];
+      tmem_row_bf16<D>(lane_base + COL_DK, p.scale, n > 0, w);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_OFREE));
+      store_rows<D>(stage, lane, w, p.out0 + row0, size_t(p.H) * D, kn - warp * 32);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
+      atomicExch(p.header + kHdrTicket, 0);
+      atomicExch(p.header + kHdrFinished, 0);
+    }
+  }
+}
+
+template <int D>
+attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map<D>(&mq, a.q, a.total_tokens, a.num_heads) || !make_map<D>(&mk, a.k, a.total_tokens, a.num_heads) ||
+      !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads) ||
+      !make_map<D>(&mdo, a.dout, a.total_tokens, a.num_heads))
+    return record_cuda_error(cudaErrorInvalidValue, "attn_bwd tensor map encoding");
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd configure");
+    configured = true;
+  }
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd device query");
+  }
+  const long long rows = (long long)a.total_tokens * a.num_heads;
+  bwd_delta_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.total_tokens,
+      a.num_heads);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd delta launch");
+  const long long items = (long long)a.bm.max_qt * a.num_heads;
+  if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const unsigned grid = unsigned(items < num_sms ? items : num_sms);
+  BwdParams p;
+  p.header = a.bm.header;
+  p.qt_seq = a.bm.qt_seq;
+  p.qt_idx = a.bm.qt_idx;
+  p.cu = a.bm.cu;
+  p.mask = a.mask;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.H = a.num_heads;
+  p.T = a.total_tokens;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  // dK, dV over the k-major lists
+  p.order = a.bm.korder;
+  p.off = a.bm.qoff;
+  p.idx = a.bm.qidx;
+  p.label = a.bm.qlabel;
+  p.out0 = static_cast<__nv_bfloat16*>(a.dk);
+  p.out1 = static_cast<__nv_bfloat16*>(a.dv);
+  attn_bwd_dkdv_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
+  // dQ over the q-major lists
+  p.order = a.bm.order;
+  p.off = a.bm.koff;
+  p.idx = a.bm.kidx;
+  p.label = a.bm.klabel;
+  p.out0 = static_cast<__nv_bfloat16*>(a.dq);
+  p.out1 = nullptr;
+  attn_bwd_dq_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_bwd dq launch");
+}
+
+}  // namespace
+
+attn_status launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t s) {
+  switch (a.head_dim) {
+    case 32: return launch_bwd<32>(a, s);
+    case 64: return launch_bwd<64>(a, s);
+    case 128: return launch_bwd<128>(a, s);
+  }
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attnmask

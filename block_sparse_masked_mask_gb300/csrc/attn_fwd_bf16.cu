@@ -37,28 +37,25 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tile_pipeline.cuh"
 
 namespace attnmask {
 namespace {
 
-constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: far above any legitimate wait
-constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // bound on waiting for in-flight work
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 256
 constexpr int kThreads = 384;
 constexpr int kWarpKLoad = 8, kWarpPV = 9, kWarpVLoad = 10, kWarpS = 11;
 
 template <int D>
-struct Cfg {
+struct Cfg : TileLayout<D> {
+  using TileLayout<D>::TILE;
+  using TileLayout<D>::CHUNK;
+  using TileLayout<D>::CE;
+  using TileLayout<D>::NCH;
+  using TileLayout<D>::ROWB;
   static constexpr int NK = 3;                        // K ring slots
   static constexpr int NV = 2;                        // V ring slots
   static constexpr int NCODE = 6;                     // key-code buffers (entries in flight)
-  static constexpr int CE = D >= 64 ? 64 : 32;        // bf16 elements per swizzled row chunk
-  static constexpr int ROWB = CE * 2;                 // bytes per row chunk (128 or 64)
-  static constexpr int NCH = D / CE;                  // row chunks per tile
-  static constexpr int CHUNK = kTile * ROWB;          // bytes of one chunk of a 128-row tile
-  static constexpr int TILE = NCH * CHUNK;            // 128 x D bf16
-  static constexpr uint32_t SW = D >= 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
-  static constexpr int SBO = 8 * ROWB;                // 8-row core-matrix group stride
   static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = OFF_K + NK * TILE;
   static constexpr int NS = 3;                        // S buffers in TMEM
   // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; XSUM: per item parity
@@ -81,8 +78,6 @@ struct Cfg {
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(128, 128, false, false);
-  static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, D, false, true);
   static constexpr uint32_t COL_O = 384;
   __host__ __device__ static constexpr uint32_t col_s(int i) { return uint32_t(i) * 128u; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -103,110 +98,6 @@ struct FwdParams {
   int H, T;
   float scale_log2;  // scale * log2(e)
 };
-
-// Bounded wait on an mbarrier phase.  Returns false when this CTA is aborting.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         int32_t* err, int site) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (ptx::globaltimer() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1u;
-        atomicOr(err, kErrTimeout | (site << 9));
-        return false;
-      }
-    }
-  }
-}
-
-// The same, agreed by the whole warp: every lane waits, and the warp goes on only
-// if all lanes saw the phase (keeps later .sync.aligned instructions convergent).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          int32_t* err, int site) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err, site));
-}
-
-// Bounded wait that ignores the abort flag: used to let copies and MMAs this
-// CTA issued finish before it frees shared and tensor memory.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int32_t* err) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer() - t0 > kDrainTimeoutNs) {
-      atomicOr(err, kErrTimeout);
-      return;
-    }
-  }
-}
-
-__device__ __forceinline__ uint32_t prefix_bits(int n) {
-  return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
-}
-
-// Visibility bits of keys [32q, 32q+32) of a k-tile for one query code, from
-// the keys' codes the producer staged in shared memory.
-template <int KIND>
-__device__ __forceinline__ uint32_t code_word(const int* codes, int q, int qcode) {
-  uint32_t w = 0;
-  const int4* c4 = reinterpret_cast<const int4*>(codes + 32 * q);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int4 k = c4[c];
-    w |= (uint32_t(code_visible(KIND, qcode, k.x)) << (4 * c)) |
-         (uint32_t(code_visible(KIND, qcode, k.y)) << (4 * c + 1)) |
-         (uint32_t(code_visible(KIND, qcode, k.z)) << (4 * c + 2)) |
-         (uint32_t(code_visible(KIND, qcode, k.w)) << (4 * c + 3));
-  }
-  return w;
-}
-
-// Shared-memory descriptors: one base per tile; each k-step adds a constant to
-// the start-address field (addresses stay below 2^18, so no carry leaves it).
-// K-major operand (Q or K): k-step kk covers elements [16kk, 16kk+16) of D.
-template <int D>
-__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile_addr) {
-  using C = Cfg<D>;
-  return ptx::smem_desc(tile_addr, 16u, C::SBO, C::SW);
-}
-template <int D>
-__host__ __device__ constexpr uint64_t kmajor_step(int kk) {
-  using C = Cfg<D>;
-  return uint64_t(((16 * kk) / C::CE) * C::CHUNK + ((16 * kk) % C::CE) * 2) >> 4;
-}
-// MN-major operand V (N = D across chunks, K = keys): k-step kk covers keys [16kk, 16kk+16).
-template <int D>
-__device__ __forceinline__ uint64_t v_base(uint32_t tile_addr) {
-  using C = Cfg<D>;
-  return ptx::smem_desc(tile_addr, C::CHUNK, C::SBO, C::SW);
-}
-template <int D>
-__host__ __device__ constexpr uint64_t v_step(int kk) {
-  using C = Cfg<D>;
-  return uint64_t(kk * 16 * C::ROWB) >> 4;
-}
-
-
-template <int D>
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
-  using C = Cfg<D>;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    ptx::mma_ss(d_tmem, q_desc + kmajor_step<D>(kk), k_desc + kmajor_step<D>(kk), C::IDESC_S, kk > 0);
-}
-
-// O += P V over the 128 keys of a k-tile: P (bf16) of keys 0-63 sits over the
-// first 32 columns of the S buffer, P of keys 64-127 over columns 64-95 (each
-// half writes P over its own score columns); eight k-steps of 16 keys.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t s_tmem, uint64_t v_desc, bool acc) {
-  using C = Cfg<D>;
-#pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    ptx::mma_ts(d_tmem, s_tmem + uint32_t(kk >> 2) * 64u + uint32_t(kk & 3) * 8u, v_desc + v_step<D>(kk),
-                C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-}
 
 // One work item: a q-tile of one sequence and one head; its k-tile list is
 // entries e0 .. e1 of the CSR arrays.
@@ -838,35 +729,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(p.header + kHdrFinished, 0);
     }
   }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// [T, H, D] bf16 viewed as a 3-D tensor (d, h, t); box = one swizzled row chunk x 128 tokens.
-template <int D>
-bool make_map(CUtensorMap* m, const void* ptr, int T, int H) {
-  using C = Cfg<D>;
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(T)};
-  cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(H) * D * 2};
-  cuuint32_t box[3] = {cuuint32_t(C::CE), 1, cuuint32_t(kTile)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 

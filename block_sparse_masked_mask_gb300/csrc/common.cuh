@@ -135,4 +135,23 @@ struct FwdArgs {
 attn_status launch_attn_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 attn_status launch_attn_fwd_f32(const FwdArgs& a, cudaStream_t s);
 
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* delta;
+  void* dq;
+  void* dk;
+  void* dv;
+  int total_tokens, num_heads, head_dim;
+  float scale;
+  BmView bm;
+  MaskArgs mask;
+};
+
+attn_status launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t s);
+
 }  // namespace attnmask

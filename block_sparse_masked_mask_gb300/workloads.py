@@ -117,6 +117,13 @@ def _fill_tensors(w: Workload, g: torch.Generator) -> None:
     w.v = _randn(g, T, H, D, w.sigma, w.dtype)
 
 
+def grad_output(w: Workload, seed: int = 1000) -> torch.Tensor:
+    """A seeded upstream gradient dO [T, H, D] for the backward: N(0, 1) in fp32
+    from ``torch.Generator`` seeded with ``seed``, cast to the workload dtype."""
+    g = torch.Generator().manual_seed(seed)
+    return _randn(g, w.total_tokens, w.num_heads, w.head_dim, 1.0, w.dtype)
+
+
 def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> Workload:
     """Workload number ``c`` (1..5).
 

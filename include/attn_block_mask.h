@@ -108,10 +108,11 @@ typedef struct attn_mask_params {
  * comments, with NQ = max_qtiles and NK = max_ktiles.
  *   off_header  int32[16]: [0] n_qtiles, [1] n_entries (sum of kcount),
  *               [2] error bits, [3] n_qpairs, [4] EMPTY, [5] PARTIAL,
- *               [6] FULL tile-pair totals, [8] [9] the forward's work
- *               counters (zero between launches), others reserved.
- *               Because of [8] and [9], attn_fwd calls that share one block
- *               mask must not run concurrently (same stream, or ordered).
+ *               [6] FULL tile-pair totals, [8] [9] the work counters of
+ *               the forward and backward kernels (zero between launches),
+ *               others reserved.  Because of [8] and [9], attn_fwd and
+ *               attn_bwd calls that share one block mask must not run
+ *               concurrently (same stream, or ordered).
  *   off_qt_seq  int32[NQ]       sequence of each q-tile (q-tiles are numbered
  *                               sequence-major, ascending inside a sequence)
  *   off_qt_idx  int32[NQ]       index of the q-tile inside its sequence
@@ -218,6 +219,39 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      const attn_mask_params* params, const int32_t* seg_id,
                      const int8_t* role, const int32_t* turn, const attn_block_mask* bm,
                      attn_stream_t stream);
+
+/*
+ * Attention backward with the structured mask: the gradients of attn_fwd()'s
+ * O with respect to q, k and v for an upstream gradient dout ("the xorl issue",
+ * Verified FA4 gaps, items 1-3: a backward over the same block-sparse masks,
+ * walking the transposed lists for dK and dV, with a deterministic dQ).
+ *   q, k, v, o, dout  device bf16 [total_tokens, num_heads, head_dim]: the
+ *             forward's inputs, its output O and dL/dO
+ *   lse       device fp32 [num_heads, total_tokens]: the forward's LSE
+ *   delta     device fp32 [num_heads, total_tokens] scratch, written with
+ *             D = rowsum(dout * o) (caller-owned, read back by the kernels)
+ *   dq, dk, dv  device bf16 outputs, layout of q (rows of every sequence are
+ *             written; nothing else is touched)
+ *   head_dim, scale, cu_seqlens, batch, max_seqlen, kind, params, seg_id,
+ *             role, turn, bm: as for attn_fwd(), with the same checks; the
+ *             block mask's transposed (k-major) lists drive dk and dv
+ * Math: P = exp(scale q k^T - LSE) over the visible pairs, dV = P^T dO,
+ * dP = dO V^T, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q; P and dS
+ * are rounded to bf16 for the tensor-core products, accumulation is fp32 in
+ * tensor memory, outputs are rounded to nearest even.  Deterministic: each
+ * output row is summed by one CTA in a fixed tile order, no atomics.
+ * Inputs must be finite inside each sequence.  Only ATTN_DTYPE_BF16 exists
+ * (ATTN_ERR_UNSUPPORTED otherwise).  Launches that share one block mask must
+ * not run concurrently with each other or with attn_fwd() (header [8], [9]).
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, float* delta, void* dq, void* dk,
+                              void* dv, attn_dtype dtype, int32_t total_tokens, int32_t num_heads,
+                              int32_t head_dim, float scale, const int32_t* cu_seqlens,
+                              int32_t batch, int32_t max_seqlen, attn_mask_kind kind,
+                              const attn_mask_params* params, const int32_t* seg_id,
+                              const int8_t* role, const int32_t* turn,
+                              const attn_block_mask* bm, attn_stream_t stream);
 
 /*
  * Same as attn_block_mask_build(), for callers that cannot allocate device

@@ -239,6 +239,69 @@ def attention_backward(q, k, v, do, kind: str, cu_seqlens, meta=None, scale=None
     return dQ, dK, dV
 
 
+def attention_backward_sampled(q, k, v, do, kind: str, cu_seqlens, meta=None, scale=None,
+                               heads=None, q_rows=(), k_rows=(), row_block: int = 512):
+    """dQ at sampled query rows and dK, dV at sampled key rows (global token
+    indices), fp64, for sequences too long for the whole L x L backward.
+
+    The same definition as masked_attention_backward, evaluated row by row for
+    dQ and column by column for dK and dV, with P written as
+    P_ij = exp(s_ij - LSE_i) over the visible pairs (the softmax normalised by
+    its log-sum-exp; LSE and O of every query row come from ``attention``, the
+    three-pass forward, and give D_i = sum_d dO_id O_id):
+      dQ_i = scale * sum_j P_ij (dP_ij - D_i) k_j,  dP_ij = dO_i . v_j
+      dV_j = sum_i P_ij dO_i,  dK_j = scale * sum_i P_ij (dP_ij - D_i) q_i
+    Returns dQ, dK, dV [T, H, D] with NaN outside the sampled rows and heads.
+    """
+    T, H, D = q.shape
+    cu = np.asarray(cu_seqlens, np.int64)
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(D)
+    scale = float(scale)
+    heads = list(range(H)) if heads is None else list(heads)
+    qr = np.unique(np.asarray(q_rows, np.int64))
+    kr = np.unique(np.asarray(k_rows, np.int64))
+    meta = meta or {}
+    dQ = np.full((T, H, D), np.nan)
+    dK = np.full((T, H, D), np.nan)
+    dV = np.full((T, H, D), np.nan)
+    for b in range(len(cu) - 1):
+        start, end = int(cu[b]), int(cu[b + 1])
+        sq = qr[(qr >= start) & (qr < end)]
+        sk = kr[(kr >= start) & (kr < end)]
+        if len(sq) == 0 and len(sk) == 0:
+            continue
+        # LSE and O of every query row of this sequence (the forward oracle)
+        need = np.arange(start, end) if len(sk) else sq
+        O, LSE = attention(q, k, v, kind, cu, meta, scale, heads=heads, rows=need,
+                           row_block=row_block)
+        tok = np.arange(start, end)
+        for h in heads:
+            qh, kh, vh, doh = (_as_f64(x[start:end, h]) for x in (q, k, v, do))
+            lse_h = LSE[h, start:end]
+            lse_safe = np.where(np.isfinite(lse_h), lse_h, 0.0)  # rows with no key have P = 0
+            dlt = (doh * O[start:end, h]).sum(axis=1) if len(sk) else None
+            if len(sq):
+                li = sq - start
+                vis = predicate(kind, sq[:, None], tok[None, :], meta.get("seg"), meta.get("role"),
+                                meta.get("turn"), meta.get("role_think", 1))
+                s = (qh[li] @ kh.T) * scale
+                p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[li, None]), 0.0)
+                d_i = (doh[li] * O[sq, h]).sum(axis=1)
+                ds = p * ((doh[li] @ vh.T) - d_i[:, None])
+                dQ[sq, h] = (ds @ kh) * scale
+            if len(sk):
+                lj = sk - start
+                vis = predicate(kind, tok[:, None], sk[None, :], meta.get("seg"), meta.get("role"),
+                                meta.get("turn"), meta.get("role_think", 1))
+                s = (qh @ kh[lj].T) * scale
+                p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[:, None]), 0.0)
+                ds = p * ((doh @ vh[lj].T) - dlt[:, None])
+                dV[sk, h] = p.T @ doh
+                dK[sk, h] = (ds.T @ qh) * scale
+    return dQ, dK, dV
+
+
 def block_lists_transposed(labels):
     """Per-k-tile compacted lists (the backward's orientation) from per-sequence
     label matrices: the transpose of block_lists.  For every k-tile (sequences

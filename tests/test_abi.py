@@ -18,7 +18,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = set(declared_functions())
-    assert {"attn_block_mask_workspace_size", "attn_block_mask_build", "attn_fwd",
+    assert {"attn_block_mask_workspace_size", "attn_block_mask_build", "attn_fwd", "attn_bwd",
             "attn_get_status", "attn_status_string", "attn_version",
             "attn_last_error_message"} <= names
 
@@ -115,6 +115,41 @@ def test_fwd_rejects_bad_arguments_before_any_launch(native_lib):
     assert call(bmref=bm2, kind=1, seg=_fake()) == 4
     assert call(bmref=bm2, cu=_fake(0x40000)) == 4
     assert call(bmref=bm2, T=512) == 4
+
+
+def test_bwd_rejects_bad_arguments_before_any_launch(native_lib):
+    from block_sparse_masked_mask_gb300 import _native
+    lib = native_lib
+    bm = _native.AttnBlockMask()   # magic 0: never built
+    prm = _native.AttnMaskParams(1)
+    base = dict(q=_fake(), k=_fake(), v=_fake(), o=_fake(), do=_fake(), lse=_fake(),
+                delta=_fake(0x50000), dq=_fake(0x60000), dk=_fake(0x70000), dv=_fake(0x80000),
+                dtype=0, T=256, H=2, D=128, scale=0.0, cu=_fake(0x30000), batch=1, maxL=256,
+                kind=0, seg=None, role=None, turn=None)
+
+    def call(bmref=bm, **kw):
+        a = dict(base, **kw)
+        return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["delta"], a["dq"],
+                            a["dk"], a["dv"], a["dtype"], a["T"], a["H"], a["D"], a["scale"],
+                            a["cu"], a["batch"], a["maxL"], a["kind"], ctypes.byref(prm), a["seg"],
+                            a["role"], a["turn"], ctypes.byref(bmref), None)
+
+    for name in ("q", "do", "lse", "delta", "dq", "dk", "dv"):
+        assert call(**{name: None}) == 1, name
+    assert call(dtype=1) == 2                   # fp32 backward is not provided
+    assert call(dtype=5) == 1
+    assert call(D=96) == 2
+    assert call(scale=float("nan")) == 1
+    assert call(dk=_fake(0x70008)) == 1         # dk not 16-byte aligned
+    assert call(delta=_fake(0x50002)) == 1      # delta not 4-byte aligned
+    assert call(kind=3, role=_fake()) == 1      # strip_thinking without turn
+    assert call() == 4                          # block mask never built
+    bm2 = _native.AttnBlockMask()
+    bm2.magic = 0x4B53414D
+    bm2.kind, bm2.role_think, bm2.batch, bm2.total_tokens, bm2.max_seqlen = 0, 1, 1, 256, 256
+    bm2.block_m = bm2.block_n = 128
+    bm2.cu_seqlens = 0x30000
+    assert call(bmref=bm2, maxL=128) == 4
 
 
 def test_get_status_rejects_unbuilt_mask(native_lib):

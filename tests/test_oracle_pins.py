@@ -474,6 +474,23 @@ def test_backward_matches_torch_autograd_fp64(kind):
         assert np.abs(g_ - w_).max() < 1e-11
 
 
+@pytest.mark.parametrize("kind", oracle.KINDS)
+def test_sampled_backward_matches_torch_autograd_fp64(kind):
+    """The row/column-sampled backward (used on sequences too long for the whole
+    L x L backward) equals torch autograd through fp64 SDPA on the sampled rows,
+    including rows of empty and single-token sequences and tile edges."""
+    cu, meta, q, k, v, do = _bwd_case(kind, seed=33, lens=(150, 0, 1, 300))
+    scale = 1 / math.sqrt(q.shape[2])
+    want = _autograd_grads(kind, cu, meta, q, k, v, do, scale)
+    rows = [0, 5, 127, 128, 149, 150, 151, 280, 450]
+    dq, dk, dv = oracle.attention_backward_sampled(q, k, v, do, kind, cu, meta, q_rows=rows,
+                                                   k_rows=rows[::-1], row_block=64)
+    for got, ref in ((dq, want[0]), (dk, want[1]), (dv, want[2])):
+        assert np.abs(got[rows] - ref[rows]).max() < 1e-11
+        others = np.setdiff1d(np.arange(q.shape[0]), rows)
+        assert np.isnan(got[others]).all()
+
+
 def test_backward_matches_finite_differences():
     """Central differences of sum(O * dO) on a tiny causal case."""
     rng = np.random.default_rng(3)
