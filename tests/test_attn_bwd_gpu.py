@@ -8,6 +8,8 @@ rounding errors, so its error is a few u relative to the size of the terms,
 not of the (often cancelling) sum.  The bar for every output tensor X:
   * max |X - X_ref| <= 2^-6 * max |X_ref|      (two bf16 ULPs of the largest)
   * sum |X - X_ref| <= 2^-8 * sum |X_ref|      (mean error within one u)
+Where X_ref is exactly zero (dQ of a one-token sequence), the bar is an
+absolute 1e-5: the fp32 rounding left over when dP - D cancels.
 The forward that produces O and LSE for the backward is the library's own, as
 a caller would run it; the oracle computes everything from Q, K, V, dO alone.
 """
@@ -59,7 +61,10 @@ def check(name, got, ref, rows=None, heads=None):
     assert np.isfinite(err).all(), f"{name}: non-finite output"
     scale = np.abs(ref).max()
     if scale == 0:
-        assert err.max() == 0, f"{name}: expected zeros"
+        # an exact zero, e.g. dQ of a one-token sequence, where dP - D cancels:
+        # the kernel forms dP on the tensor cores and D in its own fp32 sum, so
+        # what is left is their fp32 rounding difference, times scale and K
+        assert err.max() <= 1e-5, f"{name}: expected zeros, max abs {err.max()}"
         return 0.0, 0.0
     mx = err.max() / scale
     mean = err.sum() / np.abs(ref).sum()
