@@ -8,6 +8,11 @@ Metric: effective TFLOP/s counting only unmasked score FLOPs, 4*D*H*nnz per
 step (2*D for q.k and 2*D for p.v per visible pair), and its fraction of the
 measured dense bf16 tensor peak.
 
+After the forward's timed steps, the backward (dQ, dK, dV for a seeded
+upstream gradient, on the forward's own O and LSE) is timed over its own K
+steps and reported under "backward", in effective TFLOP/s (10*D*H*nnz, the
+usual 2.5x the forward's count); ``--no-backward`` skips it.
+
 Default workload: the 32768-token causal+document mask (12 documents, H=32,
 D=128, bf16), the largest configuration.  ``--impl reference`` times the fp64
 CPU oracle on the host cores on a bounded sample of the same workload.
@@ -329,6 +334,45 @@ def run_ours(args):
         roofline["traffic"] = traffic
         roofline["traffic_source"] = traffic_src
 
+    # ---- the backward on the same workload: dQ, dK, dV of the forward just
+    # timed, for a seeded upstream gradient, inputs resident (its own K steps)
+    bwd = None
+    if not args.no_backward:
+        do = W.grad_output(w, seed=1).to(dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        delta = torch.empty_like(lse)
+        kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think)
+
+        def bwd_step():
+            api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                         dq=gq, dk=gk, dv=gv, delta=delta, **kw)
+
+        for _ in range(args.warmup):
+            bwd_step()
+        b0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        b1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            b0[i].record(stream)
+            bwd_step()
+            b1[i].record(stream)
+        torch.cuda.synchronize(dev)
+        status = api.attn_get_status(bm)
+        if status != 0:
+            raise RuntimeError(f"device status {api.attn_status_string(status)}")
+        bwd_ms = [b0[i].elapsed_time(b1[i]) for i in range(args.steps)]
+        bwd_s = sum(bwd_ms) / len(bwd_ms) / 1e3
+        eff = 2.5 * flops / bwd_s / 1e12
+        bwd = {"ms_mean": bwd_s * 1e3, "ms_min": min(bwd_ms),
+               "tflops_effective": eff, "frac_effective": eff / peak,
+               "flops_effective_per_step": 2.5 * flops,
+               "tflops_executed": 3.5 * flops / bwd_s / 1e12,
+               "flop_counting": "effective = 10*D*H*nnz (five GEMMs: the usual 2.5x the "
+                                "forward); executed = 14*D*H*nnz (S and dP are formed in both "
+                                "the dK/dV and the dQ kernel)",
+               "kernels": ["bwd_delta_kernel", "attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel"],
+               "gpu_launches": 3 * args.steps}
+
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs (Q, K, V and the mask metadata) from pinned host memory and reads
     # O and LSE back.  Two streams and two device buffer sets: the host->device
@@ -418,6 +462,7 @@ def run_ours(args):
             "clocks": clk.summary(),
             "e2e": e2e,
             "gpu_launches": 6 * args.steps,
+            "backward": bwd,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -437,6 +482,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward measurement that follows the forward's")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (a smaller case of the same mask for profiling)")
     args = ap.parse_args()

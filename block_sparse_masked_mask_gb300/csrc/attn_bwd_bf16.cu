@@ -70,7 +70,7 @@ struct BwdCfg : TileLayout<D> {
   // fixed tiles (Q and dO for dQ; K and V for dK/dV), then the ring
   static constexpr int OFF_A = 0, OFF_B = TILE, OFF_RING = 2 * TILE;
   static constexpr int B_FIX = 0, B_FIXFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
-                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 1, B_ODONE = B_PFULL + 1,
+                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 1, B_ODONE = B_PFULL + 2,
                        B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
                        B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
@@ -269,6 +269,20 @@ __device__ __forceinline__ bool load_pair(const CUtensorMap* ma, const CUtensorM
   return true;
 }
 
+// Half `hf` of a product over the 128 rows of a streamed tile: k-steps
+// 4hf .. 4hf+3 of issue_pv (rows 64hf .. 64hf+63), so that the first half can
+// run while the row threads still produce the second.
+template <int D>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, int hf, bool acc) {
+  using C = BwdCfg<D>;
+#pragma unroll
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = 4 * hf + k4;
+    ptx::mma_ts(d_tmem, a_tmem + uint32_t(hf) * 64u + uint32_t(k4) * 8u, b_desc + v_step<D>(kk), C::IDESC_PV,
+                (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dQ: one item per (q-tile, head); per listed k-tile j:
 //   S = Q K_j^T, dP = dO V_j^T (TMEM), dS = P (dP - D) over S, dQ += dS K_j.
@@ -306,6 +320,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_VTMA), 1);
     ptx::mbar_init(bar(C::B_SFULL), 1);
     ptx::mbar_init(bar(C::B_PFULL), 128);
+    ptx::mbar_init(bar(C::B_PFULL + 1), 128);
     ptx::mbar_init(bar(C::B_ODONE), 1);
     ptx::mbar_init(bar(C::B_OFREE), 128);
     for (int i = 0; i < 2; ++i) {
@@ -411,14 +426,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_s<D>(tmem + COL_S, qdesc, kdesc0 + uint64_t(ks) * (C::TILE >> 4));
           issue_s<D>(tmem + COL_DP, dodesc, kmajor_base<D>(sRing) + uint64_t(vs) * (C::TILE >> 4));
           ptx::mma_commit(bar(C::B_SFULL));
-          if (!wait_bar(bar(C::B_PFULL), uint32_t(nent) & 1u, abort_flag, err, 5)) { ok = false; break; }
           if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          // dQ += dS K (dS written over S; K read MN-major)
-          issue_pv<D>(tmem + COL_DQ, tmem + COL_S, vdesc0 + uint64_t(ks) * (C::TILE >> 4), j > 0);
+          // dQ += dS K (dS written over S; K read MN-major), one half of the
+          // keys as soon as the row threads have written it
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            if (!wait_bar(bar(C::B_PFULL + hf), uint32_t(nent) & 1u, abort_flag, err, 5)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv_half<D>(tmem + COL_DQ, tmem + COL_S, vdesc0 + uint64_t(ks) * (C::TILE >> 4), hf, j > 0);
+          }
+          if (!ok) break;
           ptx::mma_commit(bar(C::B_EMPTY + ks));
           ptx::mma_commit(bar(C::B_EMPTY + vs));
           nload += 2;
@@ -519,10 +541,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             ptx::tmem_st16(lane_base + COL_S + 64 * hf + 16 * q, pk);
           }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(C::B_PFULL + hf));
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_PFULL));
         ++nent;
       }
       if (!ok) break;
@@ -596,6 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_VTMA), 1);
     ptx::mbar_init(bar(C::B_SFULL), 1);
     ptx::mbar_init(bar(C::B_PFULL), 128);
+    ptx::mbar_init(bar(C::B_PFULL + 1), 128);
     ptx::mbar_init(bar(C::B_ODONE), 1);
     ptx::mbar_init(bar(C::B_OFREE), 128);
     for (int i = 0; i < 2; ++i) {
@@ -712,15 +735,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_s<D>(tmem + COL_ST, kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4));
           issue_s<D>(tmem + COL_DPT, vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4));
           ptx::mma_commit(bar(C::B_SFULL));
-          if (!wait_bar(bar(C::B_PFULL), uint32_t(nent) & 1u, abort_flag, err, 5)) { ok = false; break; }
           if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q (P^T over S^T, dS^T over dP^T; dO, Q read MN-major)
-          issue_pv<D>(tmem + COL_DV, tmem + COL_ST, rv0 + uint64_t(ds) * (C::TILE >> 4), j > 0);
-          issue_pv<D>(tmem + COL_DK, tmem + COL_DPT, rv0 + uint64_t(qs) * (C::TILE >> 4), j > 0);
+          // dV += P^T dO and dK += dS^T Q (P^T over S^T, dS^T over dP^T; dO, Q
+          // read MN-major), one half of the queries at a time
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            if (!wait_bar(bar(C::B_PFULL + hf), uint32_t(nent) & 1u, abort_flag, err, 5)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, rv0 + uint64_t(ds) * (C::TILE >> 4), hf, j > 0);
+            issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, rv0 + uint64_t(qs) * (C::TILE >> 4), hf, j > 0);
+          }
+          if (!ok) break;
           ptx::mma_commit(bar(C::B_EMPTY + qs));
           ptx::mma_commit(bar(C::B_EMPTY + ds));
           nload += 2;
@@ -832,10 +862,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t at = 64u * uint32_t(qq >> 1) + 16u * uint32_t(qq & 1);
           ptx::tmem_st16(lane_base + COL_ST + at, pp);
           ptx::tmem_st16(lane_base + COL_DPT + at, pd);
+          if (qq & 1) {  // queries 64(qq/2) .. +63 are ready for the products
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::B_PFULL + (qq >> 1)));
+          }
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_PFULL));
         ++nent;
       }
       if (!ok) break;
