@@ -340,12 +340,12 @@ def run_ours(args):
     if not args.no_backward:
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        delta = torch.empty_like(lse)
+        bws = torch.empty(api.attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=dev)
         kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think)
 
         def bwd_step():
             api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
-                         dq=gq, dk=gk, dv=gv, delta=delta, **kw)
+                         dq=gq, dk=gk, dv=gv, workspace=bws, **kw)
 
         for _ in range(args.warmup):
             bwd_step()
@@ -366,12 +366,13 @@ def run_ours(args):
         bwd = {"ms_mean": bwd_s * 1e3, "ms_min": min(bwd_ms),
                "tflops_effective": eff, "frac_effective": eff / peak,
                "flops_effective_per_step": 2.5 * flops,
-               "tflops_executed": 3.5 * flops / bwd_s / 1e12,
                "flop_counting": "effective = 10*D*H*nnz (five GEMMs: the usual 2.5x the "
-                                "forward); executed = 14*D*H*nnz (S and dP are formed in both "
-                                "the dK/dV and the dQ kernel)",
-               "kernels": ["bwd_delta_kernel", "attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel"],
-               "gpu_launches": 3 * args.steps}
+                                "forward), which is also what the kernels execute (dS is "
+                                "stored once and read back for dQ)",
+               "kernels": ["bwd_delta_kernel", "bwd_kpos_kernel", "attn_bwd_dkdv_kernel",
+                           "attn_bwd_dq_kernel"],
+               "workspace_bytes": bws.numel(),
+               "gpu_launches": 4 * args.steps}
 
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs (Q, K, V and the mask metadata) from pinned host memory and reads

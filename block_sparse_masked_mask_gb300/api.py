@@ -191,27 +191,40 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, k
     return out, lse
 
 
+def attn_bwd_workspace_size(bm: BlockMask, num_heads: int) -> int:
+    """Bytes of backward workspace that run all heads in one pass."""
+    out = ctypes.c_size_t()
+    _check(_native.lib().attn_bwd_workspace_size(ctypes.byref(bm.struct), num_heads,
+                                                 ctypes.byref(out)), "attn_bwd_workspace_size")
+    return int(out.value)
+
+
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, dout: torch.Tensor, bm: BlockMask, kind, cu_seqlens: torch.Tensor,
              max_seqlen: int, seg_id=None, role=None, turn=None, role_think: int = 1,
              scale: float = 0.0, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-             delta: Optional[torch.Tensor] = None, stream=None):
-    """Masked attention backward (bf16); returns (dQ, dK, dV), each [T, H, D]."""
+             workspace: Optional[torch.Tensor] = None, stream=None):
+    """Masked attention backward (bf16); returns (dQ, dK, dV), each [T, H, D].
+
+    ``workspace`` (uint8, device) defaults to a fresh buffer of
+    attn_bwd_workspace_size(bm, H) bytes; a smaller one runs the heads in groups.
+    """
     T, H, D = q.shape
     if q.dtype != torch.bfloat16:
         raise AttnError(2, "attn_bwd: dtype must be bfloat16")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    if delta is None:
-        delta = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=q.device)
     params = _native.AttnMaskParams(role_think)
     _check(_native.lib().attn_bwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dq), _ptr(dk),
-        _ptr(dv), DTYPES[q.dtype], T, H, D, float(scale), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        DTYPES[q.dtype], T, H, D, float(scale), _ptr(cu_seqlens), cu_seqlens.numel() - 1,
         max_seqlen, _kind(kind), ctypes.byref(params), _ptr(seg_id), _ptr(role), _ptr(turn),
-        ctypes.byref(bm.struct), _stream(stream)),
+        ctypes.byref(bm.struct), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)),
         "attn_bwd")
     return dq, dk, dv
 

@@ -1,6 +1,7 @@
 // C ABI of libattnmask: argument checks, workspace layout and dispatch.
 #include <cmath>
 #include <cstdio>
+#include <cstdint>
 #include <cstring>
 
 #include "common.cuh"
@@ -47,6 +48,24 @@ bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out) {
   l.qlabel = take(nq * nk);
   l.korder = take(4 * nq);
   l.total = p;
+  *out = l;
+  return true;
+}
+
+bool bwd_layout(int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out) {
+  BmLayout bl;
+  if (num_heads < 1 || !bm_layout(batch, total_tokens, max_seqlen, &bl)) return false;
+  const uint64_t nq = uint64_t(bl.max_qt), nk = uint64_t(bl.max_nt);
+  uint64_t e = (nq * (nk + 1) + 1) / 2;
+  if (e > nq * nk) e = nq * nk;
+  if (e > uint64_t(INT_MAX)) return false;
+  BwdLayout l;
+  l.e_bound = int(e);
+  l.delta = 0;
+  l.kpos = align256(uint64_t(num_heads) * uint64_t(total_tokens) * 4u);
+  l.ds = align256(l.kpos + 4u * (e ? e : 1));
+  l.ds_per_head = e * uint64_t(kTile) * kTile * 2u;
+  l.total = l.ds + uint64_t(num_heads) * l.ds_per_head;
   *out = l;
   return true;
 }
@@ -227,14 +246,23 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return dtype == ATTN_DTYPE_BF16 ? launch_attn_fwd_bf16(a, s) : launch_attn_fwd_f32(a, s);
 }
 
+attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads, size_t* bytes) {
+  if (bm == nullptr || bytes == nullptr || num_heads < 1) return ATTN_ERR_INVALID_ARG;
+  BwdLayout l;
+  if (!bwd_layout(bm->batch, bm->total_tokens, bm->max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
+  if (l.total > uint64_t(SIZE_MAX)) return ATTN_ERR_INVALID_ARG;
+  *bytes = size_t(l.total);
+  return ATTN_OK;
+}
+
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                     const float* lse, float* delta, void* dq, void* dk, void* dv, attn_dtype dtype,
+                     const float* lse, void* dq, void* dk, void* dv, attn_dtype dtype,
                      int32_t total_tokens, int32_t num_heads, int32_t head_dim, float scale,
                      const int32_t* cu_seqlens, int32_t batch, int32_t max_seqlen,
                      attn_mask_kind kind, const attn_mask_params* params, const int32_t* seg_id,
                      const int8_t* role, const int32_t* turn, const attn_block_mask* bm,
-                     attn_stream_t stream) {
-  if (!q || !k || !v || !o || !dout || !lse || !delta || !dq || !dk || !dv || !cu_seqlens || !bm)
+                     void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !cu_seqlens || !bm || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!valid_kind(kind) || total_tokens < 0 || num_heads < 1 || batch < 1) return ATTN_ERR_INVALID_ARG;
   if (!(std::isfinite(scale)) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
@@ -245,7 +273,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv)})
     if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return ATTN_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(delta) & 3u) != 0)
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return ATTN_ERR_INVALID_ARG;
   const int role_think = params ? params->role_think : 1;
   if (bm->magic != kMaskMagic || bm->kind != kind || bm->cu_seqlens != cu_seqlens ||
@@ -254,6 +282,9 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     return ATTN_ERR_MASK_MISMATCH;
   if (uint64_t(total_tokens) * uint64_t(num_heads) * uint64_t(head_dim) > (uint64_t(1) << 40))
     return ATTN_ERR_UNSUPPORTED;
+  BwdLayout l;
+  if (!bwd_layout(batch, total_tokens, max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
+  if (uint64_t(workspace_bytes) < l.ds + l.ds_per_head) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   if (total_tokens == 0) return ATTN_OK;
 
   BwdArgs a;
@@ -263,10 +294,13 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.delta = delta;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.workspace = workspace;
+  a.ws = l;
+  const uint64_t fit = (uint64_t(workspace_bytes) - l.ds) / (l.ds_per_head ? l.ds_per_head : 1);
+  a.heads_per_pass = int(fit < uint64_t(num_heads) ? fit : uint64_t(num_heads));
   a.total_tokens = total_tokens;
   a.num_heads = num_heads;
   a.head_dim = head_dim;

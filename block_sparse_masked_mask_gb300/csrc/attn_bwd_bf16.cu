@@ -81,7 +81,7 @@ struct BwdCfg : TileLayout<D> {
   static constexpr int OFF_SIDE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
   static constexpr int SIDE_WORDS = 3 * kTile;
   static constexpr int OFF_STAGE = OFF_SIDE + NSLOT * SIDE_WORDS * 4;  // per warp: 16 output rows
-  static constexpr int STAGE_WARP = 16 * 2 * D;
+  static constexpr int STAGE_WARP = 16 * 2 * (D > kTile ? D : kTile);  // 16 rows of 128 bf16 (dS) or D
   static constexpr int SMEM_USED = OFF_STAGE + 4 * STAGE_WARP;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -102,10 +102,17 @@ struct BwdParams {
   const float* delta;     // [H, T]
   __nv_bfloat16* out0;    // dQ, or dK
   __nv_bfloat16* out1;    // unused, or dV
+  uint8_t* ds;            // dS blocks of heads h0 .. h0+G-1: [G][entries][128 x 128 bf16]
+  const int32_t* kpos;    // k-major position of every q-major entry
   int H, T;
+  int h0, G;              // heads of this launch
+  int e_bound;            // entries the dS blocks were sized for
   float scale;
   float scale_log2;
 };
+
+// Bytes of one stored dS block: 128 keys x 128 queries, bf16.
+constexpr int kDsBlock = kTile * kTile * 2;
 
 // One work item: a tile of one sequence and one head, and its list.
 struct BwdItem {
@@ -114,7 +121,7 @@ struct BwdItem {
 
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
   BwdItem it;
-  it.h = item / n_t;
+  it.h = p.h0 + item / n_t;
   const int g = p.order[item % n_t];
   const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
@@ -189,6 +196,34 @@ __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint3
       const int rr = half16 * 16 + q;
       const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
       if (rr < nrows) *reinterpret_cast<uint4*>(base + size_t(rr) * rstride + 8 * c) = val;
+    }
+    __syncwarp();
+  }
+}
+
+// Write this warp's 32 rows (rows row0 .. row0+31 of a 128 x 128 bf16 block,
+// 64 packed words per lane) into global memory as the image of the block in
+// shared memory for an MN-major SW128 operand: two 16 KB chunks of 64 columns,
+// row r of a chunk at r * 128 bytes with its 16-byte pieces XOR-swizzled by
+// r & 7.  A bulk copy of the 32 KB image then gives the operand directly.
+__device__ __forceinline__ void store_ds_block(uint8_t* stage, int lane, const uint32_t (&w)[64], uint8_t* blk,
+                                               int row0) {
+#pragma unroll
+  for (int half16 = 0; half16 < 2; ++half16) {
+    if ((lane >> 4) == half16) {
+      const int q = lane & 15;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(stage + q * 256 + ((c ^ q) & 15) * 16) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = 2 * i + (lane >> 4), c = lane & 15;  // row q of the 16, piece c of its 256 bytes
+      const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 256 + ((c ^ q) & 15) * 16);
+      const int r = row0 + half16 * 16 + q;
+      *reinterpret_cast<uint4*>(blk + (c >> 3) * (kDsBlock / 2) + r * 128 + (((c & 7) ^ (r & 7)) * 16)) = val;
     }
     __syncwarp();
   }
@@ -284,51 +319,77 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 // ---------------------------------------------------------------------------
-// dQ: one item per (q-tile, head); per listed k-tile j:
-//   S = Q K_j^T, dP = dO V_j^T (TMEM), dS = P (dP - D) over S, dQ += dS K_j.
-// TMEM: S [0,128), dP [128,256), dQ [256, 256+D).
+// dQ from the stored dS blocks: one item per (q-tile, head); per listed k-tile
+// j, dQ += dS(i, j) K_j, with dS(i, j) the block the dK/dV kernel wrote for the
+// pair (bulk-copied as the MN-major A operand) and K_j the MN-major B operand.
+// Warps 0-3 are the epilogue (one thread per query row), warp 4 the producer,
+// warp 5 the MMA issuer; dQ is double-buffered in TMEM so one item's epilogue
+// runs under the next item's products.  Each dQ row is a sum over its k-tiles
+// in ascending order inside one CTA: deterministic.
+template <int D>
+struct DqCfg : TileLayout<D> {
+  using TileLayout<D>::TILE;
+  using TileLayout<D>::CHUNK;
+  using TileLayout<D>::CE;
+  using TileLayout<D>::NCH;
+  using TileLayout<D>::ROWB;
+  static constexpr int SLOT = kDsBlock + TILE;  // dS block, then the K tile
+  static constexpr int NSLOT = D == 128 ? 3 : 4;
+  static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_TAIL = 2 * NSLOT, B_ODONE = B_TAIL + 1,
+                       B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
+                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_BAR = NSLOT * SLOT;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_RINGI = OFF_MISC + 16;
+  static constexpr int OFF_STAGE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
+  static constexpr int STAGE_WARP = 16 * 2 * D;
+  static constexpr int SMEM_USED = OFF_STAGE + 4 * STAGE_WARP;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
+  static constexpr uint32_t DQ_COLS = D;                          // one dQ buffer
+  static constexpr uint32_t TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;  // two buffers
+  // dS as the A operand: M = 128 queries (two 64-column chunks), K = keys
+  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16_f32(128, D, true, true);
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const BwdParams p) {
-  using C = BwdCfg<D>;
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const BwdParams p) {
+  using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = p.header[kHdrQtiles];
-  const int n_items = n_t * p.H;
+  const int n_entries = p.header[kHdrEntries];
+  const int n_items = n_t * p.G;
   int32_t* err = p.header + kHdrError;
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::OFF_A, sDO = base + C::OFF_B, sRing = base + C::OFF_RING;
+  const uint32_t sRing = base;
   const uint32_t bars = base + C::OFF_BAR;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
   volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
-  int* side = reinterpret_cast<int*>(sbase + C::OFF_SIDE);
-  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(C::B_FIX), 1);
-    ptx::mbar_init(bar(C::B_FIXFREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    ptx::mbar_init(bar(C::B_VTMA), 1);
-    ptx::mbar_init(bar(C::B_SFULL), 1);
-    ptx::mbar_init(bar(C::B_PFULL), 128);
-    ptx::mbar_init(bar(C::B_PFULL + 1), 128);
-    ptx::mbar_init(bar(C::B_ODONE), 1);
-    ptx::mbar_init(bar(C::B_OFREE), 128);
+    ptx::mbar_init(bar(C::B_TAIL), 1);
     for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(C::B_ODONE + i), 1);
+      ptx::mbar_init(bar(C::B_OFREE + i), 128);
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);  // row threads, MMA thread
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);  // epilogue threads, MMA thread
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
-    *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & (kErrTimeout | kErrCapacity)) ? 1u : 0u;
+    if (n_entries > p.e_bound) {
+      atomicOr(err, kErrCapacity);
+      *abort_flag = 1u;
+    }
     ptx::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -344,7 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (skip) {
   } else if (warp == kWarpLoad) {
     // ---------------------------------------------------------- producer
-    int nload = 0, ntail = 0, nfix = 0;
+    int nload = 0, ntail = 0;
     bool tail_pending = false, ok = true;
     BwdItem it_next;
     int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
@@ -354,39 +415,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
                             abort_flag, err);
       if (st_next < 0) break;
-      // Q and dO of this q-tile, once the previous item's MMAs no longer read them
-      if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE);
-        for (int c = 0; c < C::NCH; ++c) {
-          ptx::tma_load_3d(sQ + c * C::CHUNK, &tmQ, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
-          ptx::tma_load_3d(sDO + c * C::CHUNK, &tmDO, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
-        }
-      }
-      ++nfix;
+      const uint8_t* ds_head = p.ds + size_t(it.h - p.h0) * size_t(n_entries) * kDsBlock;
       for (int e = it.e0; e < it.e1; ++e) {
         const int j0 = __ldg(p.idx + e) * kTile, kn = min(kTile, it.L - j0);
-        const int lab = __ldg(p.label + e);
-        // K(j) and V(j) into two free slots; the keys' mask codes of a PARTIAL
-        // tile go to K's side words
-        const int ks = nload % C::NSLOT, vs = (nload + 1) % C::NSLOT;
+        const uint8_t* blk = ds_head + size_t(__ldg(p.kpos + e)) * kDsBlock;
+        const int slot = nload % C::NSLOT;
         if (nload >= C::NSLOT &&
-            (!warp_wait(bar(C::B_EMPTY + ks), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
-             !warp_wait(bar(C::B_EMPTY + vs), uint32_t((nload + 1) / C::NSLOT - 1) & 1u, abort_flag, err, 1))) {
+            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
           ok = false;
           break;
         }
-        if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL) {
-          for (int c = lane; c < kTile; c += 32)
-            side[ks * C::SIDE_WORDS + c] = key_code(p.mask, it.s0 + j0 + min(c, kn - 1));
+        const uint32_t dst = sRing + uint32_t(slot) * C::SLOT, kdst = dst + kDsBlock;
+        const uint32_t full = bar(C::B_FULL + slot);
+        if (kn == kTile) {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full, kDsBlock + C::TILE);
+            ptx::bulk_load(dst, blk, kDsBlock, full);
+            for (int c = 0; c < C::NCH; ++c)
+              ptx::tma_load_3d(kdst + c * C::CHUNK, &tmK, full, c * C::CE, it.h, it.s0 + j0);
+          }
+        } else {
+          // K rows past the sequence end are zeroed before FULL opens: their dS
+          // is zero, but an inf there would make the product NaN
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::B_TAIL), C::TILE);
+            for (int c = 0; c < C::NCH; ++c)
+              ptx::tma_load_3d(kdst + c * C::CHUNK, &tmK, bar(C::B_TAIL), c * C::CE, it.h, it.s0 + j0);
+          }
+          tail_pending = true;
+          if (!warp_wait(bar(C::B_TAIL), uint32_t(ntail) & 1u, abort_flag, err, 2)) {
+            ok = false;
+            break;
+          }
+          tail_pending = false;
+          ++ntail;
+          uint8_t* kgen = sbase + size_t(slot) * C::SLOT + kDsBlock;
+          for (int rr = kn + lane; rr < kTile; rr += 32) {
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              uint4* row = reinterpret_cast<uint4*>(kgen + c * C::CHUNK + rr * C::ROWB);
+#pragma unroll
+              for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full, kDsBlock);
+            ptx::bulk_load(dst, blk, kDsBlock, full);
+          }
         }
-        if (!load_pair<D>(&tmK, &tmV, it.h, it.s0 + j0, kn, sRing, sbase + C::OFF_RING, ks, vs, bar(C::B_FULL),
-                          bar(C::B_VTMA), ntail, tail_pending, lane, abort_flag, err)) {
-          ok = false;
-          break;
-        }
-        nload += 2;
+        ++nload;
       }
     }
     if (lane == 0) {
@@ -395,172 +474,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
         drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
       }
-      if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
-      if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
+      if (tail_pending) drain_bar(bar(C::B_TAIL), uint32_t(ntail) & 1u, err);
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int nload = 0, nent = 0;
+      int nload = 0;
       bool ok = true;
-      const uint64_t qdesc = kmajor_base<D>(sQ), dodesc = kmajor_base<D>(sDO);
-      const uint64_t kdesc0 = kmajor_base<D>(sRing), vdesc0 = v_base<D>(sRing);
+      const uint64_t ds0 = ptx::smem_desc(sRing, kDsBlock / 2, 1024u, ptx::kSwizzle128B);
+      const uint64_t k0 = v_base<D>(sRing + kDsBlock);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
         BwdItem it;
         const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
-        if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
+        const int b = k & 1;
+        if (k >= 2 && !wait_bar(bar(C::B_OFREE + b), uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 14)) break;
+        const uint32_t dq_t = tmem + uint32_t(b) * C::DQ_COLS;
         const int n = it.e1 - it.e0;
         for (int j = 0; j < n; ++j) {
-          const int ks = nload % C::NSLOT, vs = (nload + 1) % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + ks), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4) ||
-              !wait_bar(bar(C::B_FULL + vs), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+          const int slot = nload % C::NSLOT;
+          if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          // S = Q K^T and dP = dO V^T (V read K-major like K here)
-          issue_s<D>(tmem + COL_S, qdesc, kdesc0 + uint64_t(ks) * (C::TILE >> 4));
-          issue_s<D>(tmem + COL_DP, dodesc, kmajor_base<D>(sRing) + uint64_t(vs) * (C::TILE >> 4));
-          ptx::mma_commit(bar(C::B_SFULL));
-          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
-            ok = false;
-            break;
-          }
-          // dQ += dS K (dS written over S; K read MN-major), one half of the
-          // keys as soon as the row threads have written it
-          for (int hf = 0; hf < 2 && ok; ++hf) {
-            if (!wait_bar(bar(C::B_PFULL + hf), uint32_t(nent) & 1u, abort_flag, err, 5)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_pv_half<D>(tmem + COL_DQ, tmem + COL_S, vdesc0 + uint64_t(ks) * (C::TILE >> 4), hf, j > 0);
-          }
-          if (!ok) break;
-          ptx::mma_commit(bar(C::B_EMPTY + ks));
-          ptx::mma_commit(bar(C::B_EMPTY + vs));
-          nload += 2;
-          ++nent;
+          const uint64_t so = uint64_t(slot) * (C::SLOT >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            ptx::mma_ss(dq_t, ds0 + so + uint64_t(kk * 16 * 128 >> 4), k0 + so + v_step<D>(kk), C::IDESC_DQ,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_commit(bar(C::B_EMPTY + slot));
+          ++nload;
         }
         if (!ok) break;
-        // every MMA of this item reading Q and dO has been issued
-        ptx::mma_commit(bar(C::B_FIXFREE));
-        if (n > 0) ptx::mma_commit(bar(C::B_ODONE));
+        ptx::mma_commit(bar(C::B_ODONE + b));
       }
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
   } else if (warp < 4) {
-    // ---------------------------------------------------------- dS (query rows)
-    const int r = warp * 32 + lane;
-    const int kind = p.mask.kind;
+    // ---------------------------------------------------------- epilogue
     const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    const float c2 = p.scale_log2;
-    int nent = 0, nodone = 0, nload = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
+    for (int k = 0;; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
       BwdItem it;
       const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
       ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
       if (!valid) break;
-      const int qn = min(kTile, it.L - it.i0);
-      const bool row_in = r < qn;
-      const int il = it.i0 + r;
-      const int tok = it.s0 + il;
-      const float lse = row_in ? p.lse[size_t(it.h) * p.T + tok] : -INFINITY;
-      // a row that sees no key has P = 0 (its LSE is -inf)
-      const float lse2 = lse == -INFINITY ? INFINITY : lse * 1.4426950408889634f;
-      const float dlt = row_in ? p.delta[size_t(it.h) * p.T + tok] : 0.f;
-      const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, tok) : 0;
-      const int n = it.e1 - it.e0;
-      for (int jj = 0; jj < n; ++jj) {
-        const int e = it.e0 + jj;
-        const int j0 = __ldg(p.idx + e) * kTile, kn = min(kTile, it.L - j0);
-        const int lab = __ldg(p.label + e);
-        const int ks = nload % C::NSLOT;
-        nload += 2;
-        if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
-        ptx::tc_fence_after();
-        uint32_t vis[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
-          const int upto = lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(upto - 32 * q);
-          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-            // the key codes came with K(j): its load has landed (S(j) is done)
-            if (!warp_wait(bar(C::B_FULL + ks), uint32_t((nload - 2) / C::NSLOT) & 1u, abort_flag, err, 9)) {
-              ok = false;
-              break;
-            }
-            const int* codes = side + ks * C::SIDE_WORDS;
-            if (kind == ATTN_MASK_STRIP_THINKING) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_STRIP_THINKING>(codes, q, qcode);
-            } else if (kind == ATTN_MASK_SHARED_PREFIX) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(codes, q, qcode);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
-            }
-          }
-        }
-        // dS = P (dP - D), P = 2^(S c2 - LSE log2 e), two 64-column halves; each
-        // half's bf16 dS goes over the first 32 of its own S columns.
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sv[2][32], dv[2][32];
-          ptx::tmem_ld32(lane_base + COL_S + 64 * hf, sv[0]);
-          ptx::tmem_ld32(lane_base + COL_S + 64 * hf + 32, sv[1]);
-          ptx::tmem_ld32(lane_base + COL_DP + 64 * hf, dv[0]);
-          ptx::tmem_ld32(lane_base + COL_DP + 64 * hf + 32, dv[1]);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t vw = vis[2 * hf + q];
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[q][c]), __uint_as_float(sv[q][c + 1])),
-                                          make_float2(c2, c2), make_float2(-lse2, -lse2));
-              float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
-              p0 = (vw >> c) & 1u ? p0 : 0.f;
-              p1 = (vw >> (c + 1)) & 1u ? p1 : 0.f;
-              const float d0 = p0 * (__uint_as_float(dv[q][c]) - dlt);
-              const float d1 = p1 * (__uint_as_float(dv[q][c + 1]) - dlt);
-              pk[c >> 1] = ptx::pack_bf16(d0, d1);
-            }
-            ptx::tmem_st16(lane_base + COL_S + 64 * hf + 16 * q, pk);
-          }
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(C::B_PFULL + hf));
-        }
-        ++nent;
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      if (n > 0) {
-        if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
-        ++nodone;
-      }
+      const int b = k & 1;
+      if (!warp_wait(bar(C::B_ODONE + b), uint32_t(k >> 1) & 1u, abort_flag, err, 11)) break;
       ptx::tc_fence_after();
       uint32_t w[D / 2];
-      tmem_row_bf16<D>(lane_base + COL_DQ, p.scale, n > 0, w);
+      tmem_row_bf16<D>(lane_base + uint32_t(b) * C::DQ_COLS, p.scale, it.e1 > it.e0, w);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE));
+      ptx::mbar_arrive(bar(C::B_OFREE + b));
+      const int qn = min(kTile, it.L - it.i0);
       store_rows<D>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
-                       p.out0 + (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D, size_t(p.H) * D,
-                       qn - warp * 32);
+                    p.out0 + (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D, size_t(p.H) * D,
+                    qn - warp * 32);
     }
   }
 
@@ -579,6 +554,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// k-major position of every q-major entry: for the pair (q-tile i, k-tile j),
+// the rank of i in k-tile j's ascending list (one block per q-tile).
+__global__ void __launch_bounds__(128) bwd_kpos_kernel(const int32_t* __restrict__ header,
+                                                       const int32_t* __restrict__ qt_idx,
+                                                       const int32_t* __restrict__ koff,
+                                                       const int32_t* __restrict__ kidx,
+                                                       const int32_t* __restrict__ qoff,
+                                                       const int32_t* __restrict__ qidx, int32_t* kpos) {
+  const int g = blockIdx.x;
+  if (g >= header[kHdrQtiles]) return;
+  const int i = qt_idx[g], g0 = g - i;  // tiles of one sequence are numbered contiguously
+  for (int e = koff[g] + threadIdx.x; e < koff[g + 1]; e += blockDim.x) {
+    const int gj = g0 + kidx[e];
+    int lo = qoff[gj], hi = qoff[gj + 1];
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (qidx[mid] < i) lo = mid + 1;
+      else hi = mid;
+    }
+    kpos[e] = lo;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dK, dV: one item per (k-tile, head); per listed q-tile i:
 //   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, TMEM lane = key),
@@ -594,7 +592,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = p.header[kHdrQtiles];
-  const int n_items = n_t * p.H;
+  const int n_entries = p.header[kHdrEntries];
+  const int n_items = n_t * p.G;
   int32_t* err = p.header + kHdrError;
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -627,6 +626,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
+    if (n_entries > p.e_bound) {  // the dS blocks cannot hold this mask's entries
+      atomicOr(err, kErrCapacity);
+      *abort_flag = 1u;
+    }
     ptx::fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -835,6 +838,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(an - 32 * q);
         }
+        if (!row_in) {
+          // a key past the sequence end: its P and dS are exactly zero, so the
+          // stored dS block holds no value from another sequence
+#pragma unroll
+          for (int q = 0; q < 4; ++q) vis[q] = 0u;
+        }
         // one 32-column quarter at a time: quarter qq reads S^T and dP^T columns
         // [32qq, 32qq+32) and writes bf16 pairs to columns 64(qq/2) + 16(qq%2)
         // + [0,16), which the quarters before it have already read
@@ -857,7 +866,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             p0 = (vw >> c) & 1u ? p0 : 0.f;
             p1 = (vw >> (c + 1)) & 1u ? p1 : 0.f;
             pp[c >> 1] = ptx::pack_bf16(p0, p1);
-            pd[c >> 1] = ptx::pack_bf16(p0 * (__uint_as_float(dv[c]) - g0), p1 * (__uint_as_float(dv[c + 1]) - g1));
+            const float d0 = (vw >> c) & 1u ? p0 * (__uint_as_float(dv[c]) - g0) : 0.f;
+            const float d1 = (vw >> (c + 1)) & 1u ? p1 * (__uint_as_float(dv[c + 1]) - g1) : 0.f;
+            pd[c >> 1] = ptx::pack_bf16(d0, d1);
           }
           const uint32_t at = 64u * uint32_t(qq >> 1) + 16u * uint32_t(qq & 1);
           ptx::tmem_st16(lane_base + COL_ST + at, pp);
@@ -867,6 +878,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::B_PFULL + (qq >> 1)));
           }
+        }
+        {
+          // dS of this entry, read back from its two 32-column runs, to the
+          // block the dQ kernel multiplies by K
+          uint32_t w[64];
+          ptx::tmem_ld32(lane_base + COL_DPT, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+          ptx::tmem_ld32(lane_base + COL_DPT + 64, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+          ptx::tmem_wait_ld();
+          uint8_t* blk = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock;
+          store_ds_block(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w, blk, warp * 32);
         }
         ++nent;
       }
@@ -910,6 +931,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D>
 attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
+  using Q = DqCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map<D>(&mq, a.q, a.total_tokens, a.num_heads) || !make_map<D>(&mk, a.k, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads) ||
@@ -918,7 +940,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
+                                         Q::SMEM_ALLOC);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd configure");
@@ -931,15 +953,19 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd device query");
   }
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  float* delta = reinterpret_cast<float*>(ws + a.ws.delta);
+  int32_t* kpos = reinterpret_cast<int32_t*>(ws + a.ws.kpos);
   const long long rows = (long long)a.total_tokens * a.num_heads;
   bwd_delta_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.total_tokens,
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), delta, a.total_tokens,
       a.num_heads);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd delta launch");
-  const long long items = (long long)a.bm.max_qt * a.num_heads;
-  if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-  const unsigned grid = unsigned(items < num_sms ? items : num_sms);
+  bwd_kpos_kernel<<<unsigned(a.bm.max_qt), 128, 0, s>>>(a.bm.header, a.bm.qt_idx, a.bm.koff, a.bm.kidx,
+                                                          a.bm.qoff, a.bm.qidx, kpos);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd entry map launch");
   BwdParams p;
   p.header = a.bm.header;
   p.qt_seq = a.bm.qt_seq;
@@ -947,31 +973,42 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   p.cu = a.bm.cu;
   p.mask = a.mask;
   p.lse = a.lse;
-  p.delta = a.delta;
+  p.delta = delta;
+  p.ds = ws + a.ws.ds;
+  p.kpos = kpos;
+  p.e_bound = a.ws.e_bound;
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  // dK, dV over the k-major lists
-  p.order = a.bm.korder;
-  p.off = a.bm.qoff;
-  p.idx = a.bm.qidx;
-  p.label = a.bm.qlabel;
-  p.out0 = static_cast<__nv_bfloat16*>(a.dk);
-  p.out1 = static_cast<__nv_bfloat16*>(a.dv);
-  attn_bwd_dkdv_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
-  // dQ over the q-major lists
-  p.order = a.bm.order;
-  p.off = a.bm.koff;
-  p.idx = a.bm.kidx;
-  p.label = a.bm.klabel;
-  p.out0 = static_cast<__nv_bfloat16*>(a.dq);
-  p.out1 = nullptr;
-  attn_bwd_dq_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
-  e = cudaGetLastError();
-  return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_bwd dq launch");
+  // head groups whose dS blocks fit the workspace: dK, dV over the k-major
+  // lists (writing dS), then dQ over the q-major lists (reading it)
+  for (int h0 = 0; h0 < a.num_heads; h0 += a.heads_per_pass) {
+    p.h0 = h0;
+    p.G = a.num_heads - h0 < a.heads_per_pass ? a.num_heads - h0 : a.heads_per_pass;
+    const long long items = (long long)a.bm.max_qt * p.G;
+    if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+    const unsigned grid = unsigned(items < num_sms ? items : num_sms);
+    p.order = a.bm.korder;
+    p.off = a.bm.qoff;
+    p.idx = a.bm.qidx;
+    p.label = a.bm.qlabel;
+    p.out0 = static_cast<__nv_bfloat16*>(a.dk);
+    p.out1 = static_cast<__nv_bfloat16*>(a.dv);
+    attn_bwd_dkdv_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
+    p.order = a.bm.order;
+    p.off = a.bm.koff;
+    p.idx = a.bm.kidx;
+    p.label = a.bm.klabel;
+    p.out0 = static_cast<__nv_bfloat16*>(a.dq);
+    p.out1 = nullptr;
+    attn_bwd_dq_kernel<D><<<grid, kBwdThreads, Q::SMEM_ALLOC, s>>>(mk, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dq launch");
+  }
+  return ATTN_OK;
 }
 
 }  // namespace

@@ -21,8 +21,9 @@ enum : int32_t {
   kErrCuOrder = 1 << 1,      // cu_seqlens decreases somewhere
   kErrCuLast = 1 << 2,       // cu_seqlens[batch] != total_tokens
   kErrSeqTooLong = 1 << 3,   // a sequence is longer than max_seqlen
+  kErrCapacity = 1 << 4,     // more tile entries than the backward's dS blocks were sized for
   kErrTimeout = 1 << 8,      // a pipeline wait gave up (bits 9.. hold the wait site)
-  kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong,
+  kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong | kErrCapacity,
 };
 
 // kHdrTicket / kHdrFinished: the forward's work-item counter and finished-CTA
@@ -135,6 +136,17 @@ struct FwdArgs {
 attn_status launch_attn_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 attn_status launch_attn_fwd_f32(const FwdArgs& a, cudaStream_t s);
 
+// Byte layout of the backward's workspace: D = rowsum(dO * O) as fp32 [H, T],
+// the k-major position of every q-major tile entry, then the dS blocks
+// (128 x 128 bf16 per entry and head) of as many heads as fit.  e_bound bounds
+// the entries of any mask of these sizes: every kind keeps only keys at or
+// before the query, so a sequence of n tiles has at most n (n + 1) / 2 pairs.
+struct BwdLayout {
+  uint64_t delta = 0, kpos = 0, ds = 0, ds_per_head = 0, total = 0;
+  int e_bound = 0;
+};
+bool bwd_layout(int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out);
+
 struct BwdArgs {
   const void* q;
   const void* k;
@@ -142,10 +154,12 @@ struct BwdArgs {
   const void* o;
   const void* dout;
   const float* lse;
-  float* delta;
   void* dq;
   void* dk;
   void* dv;
+  void* workspace;
+  BwdLayout ws;
+  int heads_per_pass;
   int total_tokens, num_heads, head_dim;
   float scale;
   BmView bm;

@@ -73,7 +73,8 @@ typedef enum attn_status {
   ATTN_ERR_MASK_MISMATCH = 4,        /* block mask built for another kind / cu_seqlens / sizes */
   ATTN_ERR_CUDA = 5,                 /* a CUDA runtime or driver call failed */
   ATTN_ERR_DEVICE_TIMEOUT = 6,       /* a kernel gave up on a pipeline wait (reported later) */
-  ATTN_ERR_DEVICE_INVALID_INPUT = 7  /* the device found cu_seqlens malformed (reported later) */
+  ATTN_ERR_DEVICE_INVALID_INPUT = 7  /* the device found cu_seqlens malformed, or more tile entries
+                                        than the backward workspace was sized for (reported later) */
 } attn_status;
 
 typedef enum attn_mask_kind {
@@ -221,6 +222,21 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_stream_t stream);
 
 /*
+ * Bytes of device workspace attn_bwd() needs to run all `num_heads` heads in
+ * one pass over the mask `bm` (built by attn_block_mask_build()).  Pure host
+ * function.  The workspace holds, 256-byte aligned:
+ *   D = rowsum(dout * o)        fp32 [num_heads, total_tokens]
+ *   entry map                   int32 per tile entry: the position of each
+ *                               q-major entry in the k-major lists
+ *   dS blocks                   128 x 128 bf16 per tile entry and head
+ * The entry count is bounded on the host from the mask's sizes (a sequence of
+ * n tiles has at most n (n + 1) / 2 tile pairs with keys at or before the
+ * query); only the entries the mask keeps are written and read.
+ */
+ATTN_API attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads,
+                                             size_t* bytes);
+
+/*
  * Attention backward with the structured mask: the gradients of attn_fwd()'s
  * O with respect to q, k and v for an upstream gradient dout ("the xorl issue",
  * Verified FA4 gaps, items 1-3: a backward over the same block-sparse masks,
@@ -228,30 +244,36 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  *   q, k, v, o, dout  device bf16 [total_tokens, num_heads, head_dim]: the
  *             forward's inputs, its output O and dL/dO
  *   lse       device fp32 [num_heads, total_tokens]: the forward's LSE
- *   delta     device fp32 [num_heads, total_tokens] scratch, written with
- *             D = rowsum(dout * o) (caller-owned, read back by the kernels)
  *   dq, dk, dv  device bf16 outputs, layout of q (rows of every sequence are
  *             written; nothing else is touched)
  *   head_dim, scale, cu_seqlens, batch, max_seqlen, kind, params, seg_id,
  *             role, turn, bm: as for attn_fwd(), with the same checks; the
  *             block mask's transposed (k-major) lists drive dk and dv
+ *   workspace device, 256-byte aligned, caller-owned scratch (layout above);
+ *             workspace_bytes below attn_bwd_workspace_size() for one head
+ *             gives ATTN_ERR_WORKSPACE_TOO_SMALL, and a size between the
+ *             one-head and all-head figures runs the heads in groups
  * Math: P = exp(scale q k^T - LSE) over the visible pairs, dV = P^T dO,
- * dP = dO V^T, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q; P and dS
- * are rounded to bf16 for the tensor-core products, accumulation is fp32 in
- * tensor memory, outputs are rounded to nearest even.  Deterministic: each
- * output row is summed by one CTA in a fixed tile order, no atomics.
- * Inputs must be finite inside each sequence.  Only ATTN_DTYPE_BF16 exists
- * (ATTN_ERR_UNSUPPORTED otherwise).  Launches that share one block mask must
- * not run concurrently with each other or with attn_fwd() (header [8], [9]).
+ * dP = dO V^T, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q.  One
+ * kernel walks every k-tile's list (dK, dV, and dS stored as bf16 blocks), a
+ * second walks every q-tile's list (dQ from the stored dS blocks): five
+ * products per visible tile pair.  P and dS are rounded to bf16 for the
+ * tensor-core products, accumulation is fp32 in tensor memory, outputs are
+ * rounded to nearest even.  Deterministic: each output row is summed by one
+ * CTA in a fixed tile order, with no atomics.  Inputs must be finite inside
+ * each sequence.  Only ATTN_DTYPE_BF16 exists (ATTN_ERR_UNSUPPORTED
+ * otherwise).  Launches that share one block mask must not run concurrently
+ * with each other or with attn_fwd() (header [8], [9]).
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                              const void* dout, const float* lse, float* delta, void* dq, void* dk,
-                              void* dv, attn_dtype dtype, int32_t total_tokens, int32_t num_heads,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              attn_dtype dtype, int32_t total_tokens, int32_t num_heads,
                               int32_t head_dim, float scale, const int32_t* cu_seqlens,
                               int32_t batch, int32_t max_seqlen, attn_mask_kind kind,
                               const attn_mask_params* params, const int32_t* seg_id,
                               const int8_t* role, const int32_t* turn,
-                              const attn_block_mask* bm, attn_stream_t stream);
+                              const attn_block_mask* bm, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
 
 /*
  * Same as attn_block_mask_build(), for callers that cannot allocate device

@@ -123,25 +123,25 @@ def test_bwd_rejects_bad_arguments_before_any_launch(native_lib):
     bm = _native.AttnBlockMask()   # magic 0: never built
     prm = _native.AttnMaskParams(1)
     base = dict(q=_fake(), k=_fake(), v=_fake(), o=_fake(), do=_fake(), lse=_fake(),
-                delta=_fake(0x50000), dq=_fake(0x60000), dk=_fake(0x70000), dv=_fake(0x80000),
-                dtype=0, T=256, H=2, D=128, scale=0.0, cu=_fake(0x30000), batch=1, maxL=256,
-                kind=0, seg=None, role=None, turn=None)
+                dq=_fake(0x60000), dk=_fake(0x70000), dv=_fake(0x80000), dtype=0, T=256, H=2,
+                D=128, scale=0.0, cu=_fake(0x30000), batch=1, maxL=256, kind=0, seg=None,
+                role=None, turn=None, ws=_fake(0x90000), wsb=1 << 30)
 
     def call(bmref=bm, **kw):
         a = dict(base, **kw)
-        return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["delta"], a["dq"],
-                            a["dk"], a["dv"], a["dtype"], a["T"], a["H"], a["D"], a["scale"],
-                            a["cu"], a["batch"], a["maxL"], a["kind"], ctypes.byref(prm), a["seg"],
-                            a["role"], a["turn"], ctypes.byref(bmref), None)
+        return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                            a["dv"], a["dtype"], a["T"], a["H"], a["D"], a["scale"], a["cu"],
+                            a["batch"], a["maxL"], a["kind"], ctypes.byref(prm), a["seg"],
+                            a["role"], a["turn"], ctypes.byref(bmref), a["ws"], a["wsb"], None)
 
-    for name in ("q", "do", "lse", "delta", "dq", "dk", "dv"):
+    for name in ("q", "do", "lse", "dq", "dk", "dv", "ws"):
         assert call(**{name: None}) == 1, name
     assert call(dtype=1) == 2                   # fp32 backward is not provided
     assert call(dtype=5) == 1
     assert call(D=96) == 2
     assert call(scale=float("nan")) == 1
     assert call(dk=_fake(0x70008)) == 1         # dk not 16-byte aligned
-    assert call(delta=_fake(0x50002)) == 1      # delta not 4-byte aligned
+    assert call(ws=_fake(0x90010)) == 1         # workspace not 256-byte aligned
     assert call(kind=3, role=_fake()) == 1      # strip_thinking without turn
     assert call() == 4                          # block mask never built
     bm2 = _native.AttnBlockMask()
@@ -150,6 +150,19 @@ def test_bwd_rejects_bad_arguments_before_any_launch(native_lib):
     bm2.block_m = bm2.block_n = 128
     bm2.cu_seqlens = 0x30000
     assert call(bmref=bm2, maxL=128) == 4
+    # workspace sizes: all heads, and below one head's dS blocks
+    out = ctypes.c_size_t()
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, ctypes.byref(out)) == 0
+    full = out.value
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 1, ctypes.byref(out)) == 0
+    one = out.value
+    # 256 tokens in one sequence: 2 tiles and 3 tile pairs, but the host bound
+    # is nq (nk + 1) / 2 with nq = ceil(T / 128) + batch = 3 and nk = 2, i.e. 5
+    # pairs of 32 KB per head, plus D's [H, T] fp32 (256-byte aligned)
+    assert full - one == 5 * 128 * 128 * 2 + 1024
+    assert call(bmref=bm2, wsb=one - 1) == 3
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 0, ctypes.byref(out)) == 1
+    assert lib.attn_bwd_workspace_size(None, 2, ctypes.byref(out)) == 1
 
 
 def test_get_status_rejects_unbuilt_mask(native_lib):

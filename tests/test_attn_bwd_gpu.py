@@ -235,3 +235,39 @@ def test_invalid_dtype_and_mask_mismatch():
     with pytest.raises(api.AttnError) as e:
         api.attn_bwd(q, q, q, q, lse, q, bm, "causal", dm["cu_seqlens"], w.max_seqlen)
     assert e.value.status == 4
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_head_groups_match_one_pass_bit_exact():
+    """A workspace that holds the dS blocks of fewer heads runs the heads in
+    groups; every gradient is bit-identical to the one-pass run."""
+    w = W.random_workload(72, "shared_prefix", [700, 255, 1000], num_heads=3, head_dim=64)
+    do = W.grad_output(w, seed=72)
+    dm = w.device_meta()
+    bm = build_mask(w, dm)
+    q, k, v, dod = w.q.cuda(), w.k.cuda(), w.v.cuda(), do.cuda()
+    kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think)
+    o, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+    ref = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+    # the documented layout: D [H, T] fp32, the entry map, then e_bound blocks per head
+    H, T = w.num_heads, w.total_tokens
+    nq = -(-T // 128) + w.batch
+    nk = -(-w.max_seqlen // 128)
+    e_bound = min(nq * nk, (nq * (nk + 1) + 1) // 2)
+    head = e_bound * 128 * 128 * 2
+    base = _align256(_align256(H * T * 4) + 4 * e_bound)
+    assert api.attn_bwd_workspace_size(bm, H) == base + H * head
+    for heads_per_pass in (1, 2):
+        ws = torch.empty(base + heads_per_pass * head, dtype=torch.uint8, device="cuda")
+        got = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                           workspace=ws, **kw)
+        assert api.attn_get_status(bm) == api.ATTN_OK
+        for x, y in zip(ref, got):
+            assert torch.equal(x, y)
+    with pytest.raises(api.AttnError) as e:
+        api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                     workspace=torch.empty(base + head - 256, dtype=torch.uint8, device="cuda"), **kw)
+    assert e.value.status == 3
