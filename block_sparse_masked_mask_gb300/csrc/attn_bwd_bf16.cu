@@ -29,7 +29,12 @@
 namespace attnmask {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 256;                        // dQ kernel: 4 epilogue warps, producer, MMA
+constexpr int kDkdvThreads = 320;                       // dK/dV kernel: 8 row warps, producer, MMA
+constexpr int kDkdvLoad = 8, kDkdvMma = 9;
+// The producers copy an item's list to shared memory this many entries at a
+// time, so that no list read sits between a free slot and the next copy.
+constexpr int kPlist = 256;
 constexpr int kWarpLoad = 4, kWarpMma = 5;
 
 // ---------------------------------------------------------------------------
@@ -81,8 +86,9 @@ struct BwdCfg : TileLayout<D> {
   static constexpr int OFF_SIDE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
   static constexpr int SIDE_WORDS = 3 * kTile;
   static constexpr int OFF_STAGE = OFF_SIDE + NSLOT * SIDE_WORDS * 4;  // per warp: 16 output rows
-  static constexpr int STAGE_WARP = 16 * 2 * (D > kTile ? D : kTile);  // 16 rows of 128 bf16 (dS) or D
-  static constexpr int SMEM_USED = OFF_STAGE + 4 * STAGE_WARP;
+  static constexpr int STAGE_WARP = 2048;                       // per row warp: output rows in rounds
+  static constexpr int OFF_PLIST = OFF_STAGE + 8 * STAGE_WARP;  // the producer's staged list
+  static constexpr int SMEM_USED = OFF_PLIST + 2 * kPlist * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -172,18 +178,20 @@ __device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, 
 
 // Write this warp's 32 rows of COLS bf16 values (`w`, packed pairs) to rows
 // 0 .. nrows-1 of `base` (row stride `rstride` elements) as whole 16-byte
-// pieces, 16 rows at a time through the warp's shared-memory stage (chunks
-// XOR-swizzled by row so that neither side has bank conflicts).
-template <int COLS>
+// pieces, a few rows at a time through the warp's STAGE-byte shared-memory
+// stage (pieces XOR-swizzled by row so that neither side has bank conflicts).
+template <int COLS, int STAGE>
 __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint32_t (&w)[COLS / 2],
                                            __nv_bfloat16* base, size_t rstride, int nrows) {
-  constexpr int RB = COLS * 2;   // bytes per row
-  constexpr int CPR = RB / 16;   // 16-byte chunks per row
-  constexpr int RPI = 32 / CPR;  // rows per warp-wide store
+  constexpr int RB = COLS * 2;                              // bytes per row
+  constexpr int CPR = RB / 16;                              // 16-byte pieces per row
+  constexpr int RPI = 32 / CPR;                             // rows per warp-wide store
+  constexpr int RR = STAGE / RB < 32 ? STAGE / RB : 32;     // rows per round
+  static_assert(RR >= RPI && RR % RPI == 0 && 32 % RR == 0, "stage too small");
 #pragma unroll
-  for (int half16 = 0; half16 < 2; ++half16) {
-    if ((lane >> 4) == half16) {
-      const int q = lane & 15;
+  for (int round = 0; round < 32 / RR; ++round) {
+    if (lane / RR == round) {
+      const int q = lane % RR;
 #pragma unroll
       for (int c = 0; c < CPR; ++c)
         *reinterpret_cast<uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16) =
@@ -191,9 +199,9 @@ __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint3
     }
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 16 / RPI; ++i) {
+    for (int i = 0; i < RR / RPI; ++i) {
       const int q = i * RPI + lane / CPR, c = lane % CPR;
-      const int rr = half16 * 16 + q;
+      const int rr = round * RR + q;
       const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
       if (rr < nrows) *reinterpret_cast<uint4*>(base + size_t(rr) * rstride + 8 * c) = val;
     }
@@ -201,29 +209,30 @@ __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint3
   }
 }
 
-// Write this warp's 32 rows (rows row0 .. row0+31 of a 128 x 128 bf16 block,
-// 64 packed words per lane) into global memory as the image of the block in
-// shared memory for an MN-major SW128 operand: two 16 KB chunks of 64 columns,
-// row r of a chunk at r * 128 bytes with its 16-byte pieces XOR-swizzled by
-// r & 7.  A bulk copy of the 32 KB image then gives the operand directly.
-__device__ __forceinline__ void store_ds_block(uint8_t* stage, int lane, const uint32_t (&w)[64], uint8_t* blk,
-                                               int row0) {
+// A stored dS block is the image, in shared memory, of a 128-key x 128-query
+// bf16 MN-major SW128 operand: two 16 KB chunks of 64 queries, key row r of a
+// chunk at r * 128 bytes with its eight 16-byte pieces XOR-swizzled by r & 7,
+// so one bulk copy of the 32 KB gives the dQ kernel its A operand.  This
+// writes this warp's 32 key rows (row0 ..) of one chunk (32 packed words per
+// lane), 16 rows at a time through a 2 KB stage, as whole 128-byte lines.
+__device__ __forceinline__ void store_ds_half(uint8_t* stage, int lane, const uint32_t (&w)[32], uint8_t* chunk,
+                                              int row0) {
 #pragma unroll
   for (int half16 = 0; half16 < 2; ++half16) {
     if ((lane >> 4) == half16) {
       const int q = lane & 15;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(stage + q * 256 + ((c ^ q) & 15) * 16) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(stage + q * 128 + ((u ^ q) & 7) * 16) =
+            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
     }
     __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int q = 2 * i + (lane >> 4), c = lane & 15;  // row q of the 16, piece c of its 256 bytes
-      const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 256 + ((c ^ q) & 15) * 16);
+    for (int i = 0; i < 4; ++i) {
+      const int q = 4 * i + (lane >> 3), u = lane & 7;  // row q of the 16, piece u of its 128 bytes
+      const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 128 + ((u ^ q) & 7) * 16);
       const int r = row0 + half16 * 16 + q;
-      *reinterpret_cast<uint4*>(blk + (c >> 3) * (kDsBlock / 2) + r * 128 + (((c & 7) ^ (r & 7)) * 16)) = val;
+      *reinterpret_cast<uint4*>(chunk + r * 128 + ((u ^ (r & 7)) * 16)) = val;
     }
     __syncwarp();
   }
@@ -343,7 +352,8 @@ struct DqCfg : TileLayout<D> {
   static constexpr int OFF_RINGI = OFF_MISC + 16;
   static constexpr int OFF_STAGE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
   static constexpr int STAGE_WARP = 16 * 2 * D;
-  static constexpr int SMEM_USED = OFF_STAGE + 4 * STAGE_WARP;
+  static constexpr int OFF_PLIST = OFF_STAGE + 4 * STAGE_WARP;  // the producer's staged list
+  static constexpr int SMEM_USED = OFF_PLIST + 2 * kPlist * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t DQ_COLS = D;                          // one dQ buffer
   static constexpr uint32_t TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;  // two buffers
@@ -416,9 +426,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             abort_flag, err);
       if (st_next < 0) break;
       const uint8_t* ds_head = p.ds + size_t(it.h - p.h0) * size_t(n_entries) * kDsBlock;
+      int* s_idx = reinterpret_cast<int*>(sbase + C::OFF_PLIST);
+      int* s_pos = s_idx + kPlist;
       for (int e = it.e0; e < it.e1; ++e) {
-        const int j0 = __ldg(p.idx + e) * kTile, kn = min(kTile, it.L - j0);
-        const uint8_t* blk = ds_head + size_t(__ldg(p.kpos + e)) * kDsBlock;
+        const int r = (e - it.e0) & (kPlist - 1);
+        if (r == 0) {  // the next kPlist entries of the list and their dS block positions
+          __syncwarp();
+          for (int x = lane; x < kPlist && e + x < it.e1; x += 32) {
+            s_idx[x] = __ldg(p.idx + e + x);
+            s_pos[x] = __ldg(p.kpos + e + x);
+          }
+          __syncwarp();
+        }
+        const int j0 = s_idx[r] * kTile, kn = min(kTile, it.L - j0);
+        const uint8_t* blk = ds_head + size_t(s_pos[r]) * kDsBlock;
         const int slot = nload % C::NSLOT;
         if (nload >= C::NSLOT &&
             !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
@@ -533,7 +554,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE + b));
       const int qn = min(kTile, it.L - it.i0);
-      store_rows<D>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
+      store_rows<D, C::STAGE_WARP>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
                     p.out0 + (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D, size_t(p.H) * D,
                     qn - warp * 32);
     }
@@ -583,8 +604,13 @@ __global__ void __launch_bounds__(128) bwd_kpos_kernel(const int32_t* __restrict
 //   P^T = 2^(S^T c2 - LSE_i log2 e), dS^T = P^T (dP^T - D_i),
 //   dV += P^T dO_i, dK += dS^T Q_i.
 // TMEM: dV [0, D), dK [128, 128+D), S^T [256,384), dP^T [384,512).
+// Warps 0-7 are the row warps: warp w owns TMEM lanes (keys) 32 (w % 4) ..
+// +31 and query columns 64 (w / 4) .. +63, so each half of the queries has its
+// own four warps (two warps per SM sub-partition hide each other's latency);
+// at the end of an item the first four store dV and the other four dK.  Warp 8
+// is the TMA producer, warp 9 the tcgen05 issuer.
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const BwdParams p) {
@@ -611,7 +637,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_FIX), 1);
     ptx::mbar_init(bar(C::B_FIXFREE), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
-      ptx::mbar_init(bar(C::B_FULL + s), 1);
+      ptx::mbar_init(bar(C::B_FULL + s), (s & 1) ? 1 : 2);  // Q slots: copy + side words
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
     ptx::mbar_init(bar(C::B_VTMA), 1);
@@ -619,10 +645,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_PFULL), 128);
     ptx::mbar_init(bar(C::B_PFULL + 1), 128);
     ptx::mbar_init(bar(C::B_ODONE), 1);
-    ptx::mbar_init(bar(C::B_OFREE), 128);
+    ptx::mbar_init(bar(C::B_OFREE), 256);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 1);  // row threads, MMA thread
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
@@ -632,7 +658,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ptx::fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kDkdvMma) {
     ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -643,7 +669,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const bool skip = *abort_flag != 0u;
 
   if (skip) {
-  } else if (warp == kWarpLoad) {
+  } else if (warp == kDkdvLoad) {
     // ---------------------------------------------------------- producer
     int nload = 0, ntail = 0, nfix = 0;
     bool tail_pending = false, ok = true;
@@ -667,12 +693,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       ++nfix;
+      // Q(i) and dO(i) of every listed q-tile into two free slots.  Q's side
+      // words get the q-tile's LSE (times log2 e; +inf for rows that see no
+      // key or lie past the end), D and, on PARTIAL tiles, the query codes;
+      // those come from global memory one entry ahead of their use, and the
+      // list itself from the staged copy, so a free slot is refilled at once.
+      int* s_idx = reinterpret_cast<int*>(sbase + C::OFF_PLIST);
+      int* s_lab = s_idx + kPlist;
+      float nl[4], ng[4];
+      int nc[4];
+      int a0 = 0, an = 0, lab = 0;
+      auto fetch = [&](int e, int r) {  // list entry e (staged at r, if r >= 0) and its side values
+        const int ix = r >= 0 ? s_idx[r] : __ldg(p.idx + e);
+        lab = r >= 0 ? s_lab[r] : __ldg(p.label + e);
+        a0 = ix * kTile;
+        an = min(kTile, it.L - a0);
+        const bool codes = p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int c = lane + 32 * m;
+          const size_t at = size_t(it.h) * p.T + it.s0 + a0 + c;
+          nl[m] = c < an ? __ldg(p.lse + at) : -INFINITY;
+          ng[m] = c < an ? __ldg(p.delta + at) : 0.f;
+          nc[m] = codes ? query_code(p.mask, it.s0 + a0 + min(c, an - 1)) : 0;
+        }
+      };
       for (int e = it.e0; e < it.e1; ++e) {
-        const int a0 = __ldg(p.idx + e) * kTile, an = min(kTile, it.L - a0);
-        const int lab = __ldg(p.label + e);
-        // Q(i) and dO(i) into two free slots; Q's side words get the q-tile's
-        // LSE (times log2 e; +inf for rows that see no key or lie past the
-        // end), D and, on PARTIAL tiles, the query codes
+        const int r = (e - it.e0) & (kPlist - 1);
+        if (r == 0) {
+          __syncwarp();
+          for (int x = lane; x < kPlist && e + x < it.e1; x += 32) {
+            s_idx[x] = __ldg(p.idx + e + x);
+            s_lab[x] = __ldg(p.label + e + x);
+          }
+          __syncwarp();
+          if (e == it.e0) fetch(e, 0);
+        }
+        const int ca0 = a0, can = an, clab = lab;
+        float cl[4], cg[4];
+        int cc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          cl[m] = nl[m];
+          cg[m] = ng[m];
+          cc[m] = nc[m];
+        }
         const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
         if (nload >= C::NSLOT &&
             (!warp_wait(bar(C::B_EMPTY + qs), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
@@ -680,25 +745,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
-        {
-          float* sl = reinterpret_cast<float*>(side + qs * C::SIDE_WORDS);
-          for (int c = lane; c < kTile; c += 32) {
-            const bool in = c < an;
-            const size_t at = size_t(it.h) * p.T + it.s0 + a0 + c;
-            const float l = in ? p.lse[at] : -INFINITY;
-            sl[c] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-            sl[kTile + c] = in ? p.delta[at] : 0.f;
-            if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL)
-              side[qs * C::SIDE_WORDS + 2 * kTile + c] = query_code(p.mask, it.s0 + a0 + min(c, an - 1));
-          }
-          __syncwarp();
-        }
-        if (!load_pair<D>(&tmQ, &tmDO, it.h, it.s0 + a0, an, sRing, sbase + C::OFF_RING, qs, ds, bar(C::B_FULL),
+        if (!load_pair<D>(&tmQ, &tmDO, it.h, it.s0 + ca0, can, sRing, sbase + C::OFF_RING, qs, ds, bar(C::B_FULL),
                           bar(C::B_VTMA), ntail, tail_pending, lane, abort_flag, err)) {
           ok = false;
           break;
         }
+        {
+          float* sl = reinterpret_cast<float*>(side + qs * C::SIDE_WORDS);
+          const bool codes = p.mask.kind != ATTN_MASK_CAUSAL && clab == ATTN_TILE_PARTIAL;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int c = lane + 32 * m;
+            sl[c] = cl[m] == -INFINITY ? INFINITY : cl[m] * 1.4426950408889634f;
+            sl[kTile + c] = cg[m];
+            if (codes) side[qs * C::SIDE_WORDS + 2 * kTile + c] = cc[m];
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(C::B_FULL + qs));
+        }
         nload += 2;
+        if (e + 1 < it.e1) fetch(e + 1, r + 1 < kPlist ? r + 1 : -1);
       }
     }
     if (lane == 0) {
@@ -711,7 +777,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == kDkdvMma) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int nload = 0, nent = 0;
@@ -767,11 +833,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ---------------------------------------------------------- P^T, dS^T (key rows)
-    const int r = warp * 32 + lane;
+    const int qd = warp & 3, hf = warp >> 2;  // lane quarter, query half
+    const int r = qd * 32 + lane;
     const int kind = p.mask.kind;
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
     const float c2 = p.scale_log2;
     int nent = 0, nodone = 0, nload = 0;
     bool ok = true;
@@ -789,11 +856,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // same for all of them, and one ballot over the queries' codes gives a word
       const int kcode_w = __shfl_sync(0xffffffffu, kcode, 0);
       const bool uniform_k = __all_sync(0xffffffffu, !row_in || kcode == kcode_w);
+      const bool all_in = __all_sync(0xffffffffu, row_in);
       const int n = it.e1 - it.e0;
+      int nx_idx = n > 0 ? __ldg(p.idx + it.e0) : 0, nx_lab = n > 0 ? __ldg(p.label + it.e0) : 0;
       for (int jj = 0; jj < n; ++jj) {
         const int e = it.e0 + jj;
-        const int a0 = __ldg(p.idx + e) * kTile, an = min(kTile, it.L - a0);
-        const int lab = __ldg(p.label + e);
+        const int a0 = nx_idx * kTile, an = min(kTile, it.L - a0);
+        const int lab = nx_lab;
+        if (jj + 1 < n) {  // the next entry's list values, one entry ahead
+          nx_idx = __ldg(p.idx + e + 1);
+          nx_lab = __ldg(p.label + e + 1);
+        }
         const int qs = nload % C::NSLOT;
         nload += 2;
         if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
@@ -804,90 +877,100 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         const float* sl = reinterpret_cast<const float*>(side + qs * C::SIDE_WORDS);
-        // bit c of vis[c / 32]: query column c sees this key.  Causal part and
-        // bounds: a0 + c >= kl and c < an, a suffix of a prefix.
-        uint32_t vis[4];
-        {
+        // every pair of the warp's rows and columns visible: no masking at all
+        const bool fast = lab == ATTN_TILE_FULL && an == kTile && all_in;
+        // bit c of vis[m]: query column 64 hf + 32 m + c sees this key.  Causal
+        // part and bounds: a0 + column >= kl and column < an.
+        uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+        if (!fast) {
           const int lo = kl - a0;  // first visible column
 #pragma unroll
-          for (int q = 0; q < 4; ++q) vis[q] = ~prefix_bits(lo - 32 * q) & prefix_bits(an - 32 * q);
-        }
-        if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
-          const int* qc = side + qs * C::SIDE_WORDS + 2 * kTile;
-          if (uniform_k) {
+          for (int m = 0; m < 2; ++m) {
+            const int c0 = 64 * hf + 32 * m;
+            vis[m] = lab == ATTN_TILE_PARTIAL ? ~prefix_bits(lo - c0) & prefix_bits(an - c0) : prefix_bits(an - c0);
+          }
+          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+            const int* qc = side + qs * C::SIDE_WORDS + 2 * kTile + 64 * hf;
+            if (uniform_k) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int qcv = qc[32 * q + lane];
-              bool ok_v;
-              if (kind == ATTN_MASK_STRIP_THINKING) ok_v = code_visible(ATTN_MASK_STRIP_THINKING, qcv, kcode_w);
-              else if (kind == ATTN_MASK_SHARED_PREFIX) ok_v = code_visible(ATTN_MASK_SHARED_PREFIX, qcv, kcode_w);
-              else ok_v = code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcv, kcode_w);
-              vis[q] &= __ballot_sync(0xffffffffu, ok_v);
-            }
-          } else {
+              for (int m = 0; m < 2; ++m) {
+                const int qcv = qc[32 * m + lane];
+                bool ok_v;
+                if (kind == ATTN_MASK_STRIP_THINKING) ok_v = code_visible(ATTN_MASK_STRIP_THINKING, qcv, kcode_w);
+                else if (kind == ATTN_MASK_SHARED_PREFIX) ok_v = code_visible(ATTN_MASK_SHARED_PREFIX, qcv, kcode_w);
+                else ok_v = code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcv, kcode_w);
+                vis[m] &= __ballot_sync(0xffffffffu, ok_v);
+              }
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t w = 0;
-              for (int c = 0; c < 32; ++c) w |= uint32_t(code_visible(kind, qc[32 * q + c], kcode)) << c;
-              vis[q] &= w;
+              for (int m = 0; m < 2; ++m) {
+                uint32_t w = 0;
+                for (int c = 0; c < 32; ++c) w |= uint32_t(code_visible(kind, qc[32 * m + c], kcode)) << c;
+                vis[m] &= w;
+              }
             }
           }
+          if (!row_in) {
+            // a key past the sequence end: its P and dS are exactly zero, so the
+            // stored dS block holds no value from another sequence
+            vis[0] = vis[1] = 0u;
+          }
         }
-        if (lab != ATTN_TILE_PARTIAL) {
-          // FULL: only the bounds
+        // the warp's two 32-column quarters: quarter m reads S^T and dP^T
+        // columns 64 hf + 32 m + [0,32) and writes bf16 pairs to columns
+        // 64 hf + 16 m + [0,16), which this warp has already read
 #pragma unroll
-          for (int q = 0; q < 4; ++q) vis[q] = prefix_bits(an - 32 * q);
-        }
-        if (!row_in) {
-          // a key past the sequence end: its P and dS are exactly zero, so the
-          // stored dS block holds no value from another sequence
-#pragma unroll
-          for (int q = 0; q < 4; ++q) vis[q] = 0u;
-        }
-        // one 32-column quarter at a time: quarter qq reads S^T and dP^T columns
-        // [32qq, 32qq+32) and writes bf16 pairs to columns 64(qq/2) + 16(qq%2)
-        // + [0,16), which the quarters before it have already read
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const int cq = 32 * qq;
+        for (int m = 0; m < 2; ++m) {
+          const int cq = 64 * hf + 32 * m;
           uint32_t sv[32], dv[32];
           ptx::tmem_ld32(lane_base + COL_ST + cq, sv);
           ptx::tmem_ld32(lane_base + COL_DPT + cq, dv);
           ptx::tmem_wait_ld();
-          const uint32_t vw = vis[qq];
           uint32_t pp[16], pd[16];
+          if (fast) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float l0 = sl[cq + c], l1 = sl[cq + c + 1];
-            const float g0 = sl[kTile + cq + c], g1 = sl[kTile + cq + c + 1];
-            const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                        make_float2(c2, c2), make_float2(-l0, -l1));
-            float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
-            p0 = (vw >> c) & 1u ? p0 : 0.f;
-            p1 = (vw >> (c + 1)) & 1u ? p1 : 0.f;
-            pp[c >> 1] = ptx::pack_bf16(p0, p1);
-            const float d0 = (vw >> c) & 1u ? p0 * (__uint_as_float(dv[c]) - g0) : 0.f;
-            const float d1 = (vw >> (c + 1)) & 1u ? p1 * (__uint_as_float(dv[c + 1]) - g1) : 0.f;
-            pd[c >> 1] = ptx::pack_bf16(d0, d1);
+            for (int c = 0; c < 32; c += 2) {
+              const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
+              const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                          make_float2(c2, c2), make_float2(-l.x, -l.y));
+              const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+              pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
+              const float2 dd = ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                                          make_float2(-g.x, -g.y)));
+              pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
+            }
+          } else {
+            const uint32_t vw = vis[m];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
+              const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                          make_float2(c2, c2), make_float2(-l.x, -l.y));
+              const bool v0 = (vw >> c) & 1u, v1 = (vw >> (c + 1)) & 1u;
+              const float p0 = v0 ? ptx::ex2(x.x) : 0.f, p1 = v1 ? ptx::ex2(x.y) : 0.f;
+              pp[c >> 1] = ptx::pack_bf16(p0, p1);
+              const float d0 = v0 ? p0 * (__uint_as_float(dv[c]) - g.x) : 0.f;
+              const float d1 = v1 ? p1 * (__uint_as_float(dv[c + 1]) - g.y) : 0.f;
+              pd[c >> 1] = ptx::pack_bf16(d0, d1);
+            }
           }
-          const uint32_t at = 64u * uint32_t(qq >> 1) + 16u * uint32_t(qq & 1);
+          const uint32_t at = 64u * uint32_t(hf) + 16u * uint32_t(m);
           ptx::tmem_st16(lane_base + COL_ST + at, pp);
           ptx::tmem_st16(lane_base + COL_DPT + at, pd);
-          if (qq & 1) {  // queries 64(qq/2) .. +63 are ready for the products
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::B_PFULL + (qq >> 1)));
-          }
         }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C::B_PFULL + hf));  // queries 64 hf .. +63 are ready for the products
         {
-          // dS of this entry, read back from its two 32-column runs, to the
+          // this half's dS, read back from its 32 columns, to its chunk of the
           // block the dQ kernel multiplies by K
-          uint32_t w[64];
-          ptx::tmem_ld32(lane_base + COL_DPT, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
-          ptx::tmem_ld32(lane_base + COL_DPT + 64, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+          uint32_t w[32];
+          ptx::tmem_ld32(lane_base + COL_DPT + 64 * hf, w);
           ptx::tmem_wait_ld();
           uint8_t* blk = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock;
-          store_ds_block(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w, blk, warp * 32);
+          store_ds_half(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w, blk + hf * (kDsBlock / 2), qd * 32);
         }
         ++nent;
       }
@@ -898,24 +981,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nodone;
       }
       ptx::tc_fence_after();
-      const size_t row0 = (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D;
-      uint8_t* stage = sbase + C::OFF_STAGE + warp * C::STAGE_WARP;
-      {
-        uint32_t w[D / 2];
-        tmem_row_bf16<D>(lane_base + COL_DV, 1.f, n > 0, w);
-        store_rows<D>(stage, lane, w, p.out1 + row0, size_t(p.H) * D, kn - warp * 32);
-      }
+      // the first four warps store dV, the other four dK (times the scale)
       uint32_t w[D / 2];
-      tmem_row_bf16<D>(lane_base + COL_DK, p.scale, n > 0, w);
+      tmem_row_bf16<D>(lane_base + (hf ? COL_DK : COL_DV), hf ? p.scale : 1.f, n > 0, w);
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE));
-      store_rows<D>(stage, lane, w, p.out0 + row0, size_t(p.H) * D, kn - warp * 32);
+      const size_t row0 = (size_t(it.s0 + it.i0 + qd * 32) * p.H + it.h) * D;
+      store_rows<D, C::STAGE_WARP>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
+                                   (hf ? p.out0 : p.out1) + row0, size_t(p.H) * D, kn - qd * 32);
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kDkdvMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -995,7 +1074,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
     p.label = a.bm.qlabel;
     p.out0 = static_cast<__nv_bfloat16*>(a.dk);
     p.out1 = static_cast<__nv_bfloat16*>(a.dv);
-    attn_bwd_dkdv_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
+    attn_bwd_dkdv_kernel<D><<<grid, kDkdvThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
     p.order = a.bm.order;
