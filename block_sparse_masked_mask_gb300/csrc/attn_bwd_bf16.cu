@@ -30,7 +30,7 @@ namespace attnmask {
 namespace {
 
 constexpr int kBwdThreads = 256;                        // dQ kernel: 4 epilogue warps, producer, MMA
-constexpr int kDkdvThreads = 320;                       // dK/dV kernel: 8 row warps, producer, MMA
+constexpr int kDkdvThreads = 384;                       // dK/dV kernel: 8 row warps, producer, MMA, 2 idle
 constexpr int kDkdvLoad = 8, kDkdvMma = 9;
 // The producers copy an item's list to shared memory this many entries at a
 // time, so that no list read sits between a free slot and the next copy.
@@ -77,7 +77,7 @@ struct BwdCfg : TileLayout<D> {
   static constexpr int B_FIX = 0, B_FIXFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
                        B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 1, B_ODONE = B_PFULL + 2,
                        B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_IEMPTY + 2, B_YFREE = B_DRAIN + 1, NBAR = B_YFREE + 1;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;                 // two decoded work items, 8 ints each
@@ -603,12 +603,19 @@ __global__ void __launch_bounds__(128) bwd_kpos_kernel(const int32_t* __restrict
 //   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, TMEM lane = key),
 //   P^T = 2^(S^T c2 - LSE_i log2 e), dS^T = P^T (dP^T - D_i),
 //   dV += P^T dO_i, dK += dS^T Q_i.
-// TMEM: dV [0, D), dK [128, 128+D), S^T [256,384), dP^T [384,512).
+// TMEM: dV [0, D), dK [128, 128+D), and two 128-column regions [256,384),
+// [384,512) that alternate by entry: S^T of entry j goes to region j % 2 and
+// dP^T to the other; the row warps write bf16 P^T and dS^T over S^T's region
+// (P^T over the first 32 columns of each 64-column half, dS^T over the other
+// 32), so dP^T's region is free once they have read it, and S^T of entry j+1
+// goes there while they are still working on entry j.
 // Warps 0-7 are the row warps: warp w owns TMEM lanes (keys) 32 (w % 4) ..
 // +31 and query columns 64 (w / 4) .. +63, so each half of the queries has its
 // own four warps (two warps per SM sub-partition hide each other's latency);
 // at the end of an item the first four store dV and the other four dK.  Warp 8
-// is the TMA producer, warp 9 the tcgen05 issuer.
+// is the TMA producer, warp 9 the tcgen05 issuer, warps 10-11 idle; the row
+// warpgroups run with 192 registers a thread and the third with 112 (within
+// the 168 x 384 the block is launched with).
 template <int D>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -631,7 +638,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   volatile uint32_t* abort_flag = misc + 1;
   volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
   int* side = reinterpret_cast<int*>(sbase + C::OFF_SIDE);
-  constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_ST = 256, COL_DPT = 384;
+  constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_R0 = 256;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(C::B_FIX), 1);
@@ -651,6 +658,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 1);  // row threads, MMA thread
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
+    ptx::mbar_init(bar(C::B_YFREE), 256);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     if (n_entries > p.e_bound) {  // the dS blocks cannot hold this mask's entries
       atomicOr(err, kErrCapacity);
@@ -669,7 +677,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   const bool skip = *abort_flag != 0u;
 
   if (skip) {
-  } else if (warp == kDkdvLoad) {
+  } else if (warp >= 8) {
+    ptx::regs_dec<112>();
+    if (warp == kDkdvLoad) {
     // ---------------------------------------------------------- producer
     int nload = 0, ntail = 0, nfix = 0;
     bool tail_pending = false, ok = true;
@@ -792,32 +802,52 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (!valid) break;
         if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
         const int n = it.e1 - it.e0;
+        bool s_early = false;  // S^T of the current entry was issued during the previous one
         for (int j = 0; j < n; ++j) {
           const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + qs), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4) ||
-              !wait_bar(bar(C::B_FULL + ds), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+          const uint32_t rs = tmem + COL_R0 + 128u * uint32_t(nent & 1);        // S^T, then P^T and dS^T
+          const uint32_t rp = tmem + COL_R0 + 128u * uint32_t((nent & 1) ^ 1);  // dP^T
+          if (!s_early) {
+            if (!wait_bar(bar(C::B_FULL + qs), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_s<D>(rs, kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4));  // S^T = K Q^T
+          }
+          if (!wait_bar(bar(C::B_FULL + ds), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T
-          issue_s<D>(tmem + COL_ST, kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4));
-          issue_s<D>(tmem + COL_DPT, vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4));
+          issue_s<D>(rp, vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4));  // dP^T = V dO^T
           ptx::mma_commit(bar(C::B_SFULL));
           if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
             ok = false;
             break;
           }
-          // dV += P^T dO and dK += dS^T Q (P^T over S^T, dS^T over dP^T; dO, Q
-          // read MN-major), one half of the queries at a time
+          // dV += P^T dO and dK += dS^T Q (dO, Q read MN-major), one half of the
+          // queries at a time; between the halves, S^T of the next entry
+          s_early = false;
           for (int hf = 0; hf < 2 && ok; ++hf) {
             if (!wait_bar(bar(C::B_PFULL + hf), uint32_t(nent) & 1u, abort_flag, err, 5)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, rv0 + uint64_t(ds) * (C::TILE >> 4), hf, j > 0);
-            issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, rv0 + uint64_t(qs) * (C::TILE >> 4), hf, j > 0);
+            issue_pv_half<D>(tmem + COL_DV, rs, rv0 + uint64_t(ds) * (C::TILE >> 4), hf, j > 0);
+            issue_pv_half<D>(tmem + COL_DK, rs + 32u, rv0 + uint64_t(qs) * (C::TILE >> 4), hf, j > 0);
+            if (hf == 0 && j + 1 < n) {
+              const int nq = (nload + 2) % C::NSLOT;
+              if (!wait_bar(bar(C::B_YFREE), uint32_t(nent) & 1u, abort_flag, err, 6) ||
+                  !wait_bar(bar(C::B_FULL + nq), uint32_t((nload + 2) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              issue_s<D>(rp, kdesc, rk0 + uint64_t(nq) * (C::TILE >> 4));
+              s_early = true;
+            }
           }
           if (!ok) break;
           ptx::mma_commit(bar(C::B_EMPTY + qs));
@@ -833,7 +863,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-  } else if (warp < 8) {
+    }
+  } else {
+    ptx::regs_inc<192>();
     // ---------------------------------------------------------- P^T, dS^T (key rows)
     const int qd = warp & 3, hf = warp >> 2;  // lane quarter, query half
     const int r = qd * 32 + lane;
@@ -916,23 +948,34 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             vis[0] = vis[1] = 0u;
           }
         }
-        // the warp's two 32-column quarters: quarter m reads S^T and dP^T
-        // columns 64 hf + 32 m + [0,32) and writes bf16 pairs to columns
-        // 64 hf + 16 m + [0,16), which this warp has already read
+        // this warp's 64 columns: S^T (both quarters) and dP^T (first quarter)
+        // first; dP^T's second quarter loads while the first is computed, after
+        // which dP^T's region is released for the next entry's S^T.  Quarter m
+        // writes P^T to columns 64 hf + 16 m + [0,16) and dS^T to 64 hf + 32 +
+        // 16 m + [0,16) of the S^T region, all of which this warp has read.
+        const uint32_t rs = COL_R0 + 128u * uint32_t(nent & 1), rp = COL_R0 + 128u * uint32_t((nent & 1) ^ 1);
+        uint32_t sv[2][32], dv0[32], dv1[32];
+        ptx::tmem_ld32(lane_base + rs + 64 * hf, sv[0]);
+        ptx::tmem_ld32(lane_base + rs + 64 * hf + 32, sv[1]);
+        ptx::tmem_ld32(lane_base + rp + 64 * hf, dv0);
+        ptx::tmem_wait_ld();
+        ptx::tmem_ld32(lane_base + rp + 64 * hf + 32, dv1);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           const int cq = 64 * hf + 32 * m;
-          uint32_t sv[32], dv[32];
-          ptx::tmem_ld32(lane_base + COL_ST + cq, sv);
-          ptx::tmem_ld32(lane_base + COL_DPT + cq, dv);
-          ptx::tmem_wait_ld();
+          if (m == 1) {
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::B_YFREE));
+          }
+          const uint32_t(&dv)[32] = m ? dv1 : dv0;
           uint32_t pp[16], pd[16];
           if (fast) {
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
               const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
               const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
-              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[m][c]), __uint_as_float(sv[m][c + 1])),
                                           make_float2(c2, c2), make_float2(-l.x, -l.y));
               const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
               pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
@@ -946,7 +989,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             for (int c = 0; c < 32; c += 2) {
               const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
               const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
-              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[m][c]), __uint_as_float(sv[m][c + 1])),
                                           make_float2(c2, c2), make_float2(-l.x, -l.y));
               const bool v0 = (vw >> c) & 1u, v1 = (vw >> (c + 1)) & 1u;
               const float p0 = v0 ? ptx::ex2(x.x) : 0.f, p1 = v1 ? ptx::ex2(x.y) : 0.f;
@@ -956,9 +999,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
               pd[c >> 1] = ptx::pack_bf16(d0, d1);
             }
           }
-          const uint32_t at = 64u * uint32_t(hf) + 16u * uint32_t(m);
-          ptx::tmem_st16(lane_base + COL_ST + at, pp);
-          ptx::tmem_st16(lane_base + COL_DPT + at, pd);
+          ptx::tmem_st16(lane_base + rs + 64 * hf + 16 * m, pp);
+          ptx::tmem_st16(lane_base + rs + 64 * hf + 32 + 16 * m, pd);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -967,7 +1009,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           // this half's dS, read back from its 32 columns, to its chunk of the
           // block the dQ kernel multiplies by K
           uint32_t w[32];
-          ptx::tmem_ld32(lane_base + COL_DPT + 64 * hf, w);
+          ptx::tmem_ld32(lane_base + rs + 64 * hf + 32, w);
           ptx::tmem_wait_ld();
           uint8_t* blk = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock;
           store_ds_half(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w, blk + hf * (kDsBlock / 2), qd * 32);
