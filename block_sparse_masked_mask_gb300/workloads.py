@@ -5,7 +5,7 @@ turn metadata and random Q, K, V.  It holds none of the method's arithmetic
 (no predicate, no softmax, no tiling), so both the CUDA path and the fp64
 oracle can be fed from it without sharing any code that computes a result.
 
-The five workloads follow the shapes the block-mask pages describe:
+The six workloads follow the shapes the block-mask pages describe:
 
 * ``causal_s64_d32_fp32`` - one causal sequence, S=64, H=1, D=32, fp32
   ("Triton from first principles" Ch. 21, Section 21.2, which checks causal
@@ -23,8 +23,12 @@ The five workloads follow the shapes the block-mask pages describe:
 * ``causal_document_32k`` - 32768 tokens cut into twelve documents of seeded
   lengths (each at least 512), causal inside a document and block-diagonal
   across (the issue's "Move document boundaries into the mask" decision).
+* ``strip_thinking_dup_8turns`` - the strip-thinking conversation with each
+  answer span followed by its history copy (ANSWER_HISTORY=3): user 128 /
+  think 768 / answer 256 / history 256 per turn, 11264 tokens (same issue,
+  "The exactness question", option (b), token duplication).
 
-Generation recipe (per workload number ``c`` = 1..5): a CPU
+Generation recipe (per workload number ``c`` = 1..6): a CPU
 ``torch.Generator`` seeded with ``c``; metadata lengths are drawn first, then
 Q, K and V, each ``torch.randn((T, H, D)) * sigma`` in fp32, then cast to the
 workload dtype.  The inputs are synthetic stand-ins: the pages measure on
@@ -41,6 +45,7 @@ import torch
 ROLE_USER = 0
 ROLE_THINK = 1
 ROLE_ANSWER = 2
+ROLE_ANSWER_HISTORY = 3  # the duplicated answer copy later turns attend
 
 
 @dataclasses.dataclass
@@ -96,6 +101,7 @@ WORKLOAD_NAMES = {
     3: "shared_prefix_2048_16x512",
     4: "strip_thinking_8turns",
     5: "causal_document_32k",
+    6: "strip_thinking_dup_8turns",
 }
 
 
@@ -125,7 +131,10 @@ def grad_output(w: Workload, seed: int = 1000) -> torch.Tensor:
 
 
 def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> Workload:
-    """Workload number ``c`` (1..5).
+    """Workload number ``c`` (1..6).  Workload 6 is workload 4's conversation
+    with every answer span duplicated (user 128 / think 768 / answer 256 /
+    answer history copy 256 per turn, 11264 tokens): the exact variant of
+    strip-thinking.
 
     ``document_form`` only matters for workload 5: ``"mask"`` is one packed
     sequence with the document index in ``seg`` and kind causal_document;
@@ -147,6 +156,10 @@ def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> 
         role, turn = strip_thinking_layout([(128, 768, 256)] * 8)
         w = Workload(WORKLOAD_NAMES[4], "strip_thinking", _cu([len(role)]), 32, 128,
                      torch.bfloat16, sigma=0.5, role=role, turn=turn, seed=c)
+    elif c == 6:
+        role, turn = strip_thinking_dup_layout([(128, 768, 256)] * 8)
+        w = Workload(WORKLOAD_NAMES[6], "strip_thinking_dup", _cu([len(role)]), 32, 128,
+                     torch.bfloat16, sigma=0.5, role=role, turn=turn, seed=c)
     elif c == 5:
         cuts = torch.randint(0, 26625, (11,), generator=g).sort().values.tolist()
         bounds = [0] + cuts + [26624]
@@ -161,7 +174,7 @@ def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> 
         else:
             raise ValueError(document_form)
     else:
-        raise ValueError(f"workload number must be 1..5, got {c}")
+        raise ValueError(f"workload number must be 1..6, got {c}")
     if tensors:
         _fill_tensors(w, g)
     return w
@@ -173,6 +186,16 @@ def strip_thinking_layout(turns):
     for t, (nu, nt, na) in enumerate(turns, start=1):
         role += [ROLE_USER] * nu + [ROLE_THINK] * nt + [ROLE_ANSWER] * na
         turn += [t] * (nu + nt + na)
+    return np.asarray(role, np.int8), np.asarray(turn, np.int32)
+
+
+def strip_thinking_dup_layout(turns):
+    """Role and turn arrays for turns given as (user, think, answer) lengths,
+    each answer span followed by its history copy of the same length."""
+    role, turn = [], []
+    for t, (nu, nt, na) in enumerate(turns, start=1):
+        role += [ROLE_USER] * nu + [ROLE_THINK] * nt + [ROLE_ANSWER] * na + [ROLE_ANSWER_HISTORY] * na
+        turn += [t] * (nu + nt + 2 * na)
     return np.asarray(role, np.int8), np.asarray(turn, np.int32)
 
 
@@ -199,15 +222,17 @@ def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: in
                 s += n
                 cur += 1
             pos += L
-    if kind == "strip_thinking":
+    if kind in ("strip_thinking", "strip_thinking_dup"):
         role = np.empty(T, np.int8)
         turn = np.empty(T, np.int32)
+        spans = (ROLE_USER, role_think, ROLE_ANSWER) if kind == "strip_thinking" else \
+            (ROLE_USER, role_think, ROLE_ANSWER, ROLE_ANSWER_HISTORY)
         pos = 0
         for L in lengths:
             s, t = 0, 1
             while s < L:
                 tt = t if id_alphabet <= 0 else int(rng.integers(1, id_alphabet + 1))
-                for r in (ROLE_USER, role_think, ROLE_ANSWER):
+                for r in spans:
                     n = int(rng.integers(1, 200))
                     role[pos + s: pos + min(L, s + n)] = r
                     turn[pos + s: pos + min(L, s + n)] = tt

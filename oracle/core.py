@@ -35,7 +35,11 @@ from __future__ import annotations
 
 import numpy as np
 
-KINDS = ("causal", "causal_document", "shared_prefix", "strip_thinking")
+KINDS = ("causal", "causal_document", "shared_prefix", "strip_thinking", "strip_thinking_dup")
+
+# Roles of the duplicated-answer layout: the answer copy that attends its own
+# turn's thinking (and carries the loss), and the history copy later turns see.
+ROLE_ANSWER, ROLE_ANSWER_HISTORY = 2, 3
 
 EMPTY, PARTIAL, FULL = 0, 1, 2
 
@@ -58,6 +62,19 @@ def predicate(kind: str, qi, ki, seg=None, role=None, turn=None, role_think: int
                         (the xorl issue, Mask specifications, "Shared prefix").
     * strip_thinking  : ``(qi >= ki) & ~((role[ki] == THINK) & (turn[ki] < turn[qi]))``
                         (the xorl issue, Mask specifications, "Strip-thinking").
+    * strip_thinking_dup : the same conversation with every answer span
+                        duplicated (the xorl issue, "The exactness question",
+                        option (b)): the ANSWER copy attends its own turn's
+                        thinking, the ANSWER_HISTORY copy attends the stripped
+                        context and is what later turns see.  With the key at
+                        or before the query, a key is visible when it is
+                        - neither THINK nor an answer copy (user / context);
+                        - THINK of the query's own turn, and the query is THINK
+                          or ANSWER of that turn;
+                        - ANSWER of the query's own turn, and the query is
+                          ANSWER (the copy itself, causally);
+                        - ANSWER_HISTORY of an earlier turn, or of the query's
+                          own turn with the query ANSWER_HISTORY too.
     """
     qi = np.asarray(qi)
     ki = np.asarray(ki)
@@ -70,6 +87,15 @@ def predicate(kind: str, qi, ki, seg=None, role=None, turn=None, role_think: int
         return causal & ((seg[ki] == 0) | (seg[ki] == seg[qi]))
     if kind == "strip_thinking":
         return causal & ~((role[ki] == role_think) & (turn[ki] < turn[qi]))
+    if kind == "strip_thinking_dup":
+        rk, rq, tk, tq = role[ki], role[qi], turn[ki], turn[qi]
+        same = tk == tq
+        think_k, ans_k, hist_k = rk == role_think, rk == ROLE_ANSWER, rk == ROLE_ANSWER_HISTORY
+        context_k = ~(think_k | ans_k | hist_k)
+        think_seen = think_k & same & ((rq == role_think) | (rq == ROLE_ANSWER))
+        ans_seen = ans_k & same & (rq == ROLE_ANSWER)
+        hist_seen = hist_k & ((tk < tq) | (same & (rq == ROLE_ANSWER_HISTORY)))
+        return causal & (context_k | think_seen | ans_seen | hist_seen)
     raise ValueError(f"unknown mask kind {kind!r}")
 
 

@@ -222,6 +222,85 @@ def test_strip_thinking_equals_per_turn_recomputation():
         assert np.abs(LSE[:, keep[rows]] - Lt[:, rows]).max() < 1e-12
 
 
+def _dup_inference_context(role, turn, i):
+    """Tokens an inference engine holds when it produces token i of the
+    duplicated layout, built from spans, not from the predicate: for turn t,
+    every earlier turn contributes its user tokens and its answer-history copy;
+    the own turn contributes its user tokens, then its thinking (for THINK and
+    ANSWER tokens), then the span of token i itself up to i."""
+    t, r = turn[i], role[i]
+    idx = np.arange(len(role))
+    ctx = [idx[(turn == u) & ((role == W.ROLE_USER) | (role == W.ROLE_ANSWER_HISTORY))] for u in range(1, t)]
+    ctx.append(idx[(turn == t) & (role == W.ROLE_USER) & (idx <= i)])
+    if r in (W.ROLE_THINK, W.ROLE_ANSWER):
+        ctx.append(idx[(turn == t) & (role == W.ROLE_THINK) & (idx <= i)])
+    if r in (W.ROLE_ANSWER, W.ROLE_ANSWER_HISTORY):
+        ctx.append(idx[(turn == t) & (role == r) & (idx <= i)])
+    return np.concatenate(ctx)
+
+
+def test_strip_thinking_dup_equals_inference_contexts():
+    """xorl issue, "The exactness question", option (b): with every answer
+    duplicated, each token's output is exactly what inference computes from the
+    context it would hold then: earlier turns stripped of thinking (user and
+    answer-history tokens), its own turn's user tokens, its own thinking for
+    THINK and ANSWER tokens, and its own span causally.  One softmax per token
+    over exactly those keys."""
+    rng = np.random.default_rng(24)
+    turns = [(5, 9, 4), (3, 11, 6), (7, 2, 5), (4, 6, 3)]
+    role, turn = W.strip_thinking_dup_layout(turns)
+    T, H, D = len(role), 2, 8
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    meta = {"role": role, "turn": turn, "role_think": W.ROLE_THINK}
+    O, LSE = oracle.attention(q, k, v, "strip_thinking_dup", np.array([0, T]), meta)
+    scale = 1 / np.sqrt(D)
+    for i in range(T):
+        ctx = _dup_inference_context(role, turn, i)
+        for h in range(H):
+            s = k[ctx, h] @ q[i, h] * scale
+            p = np.exp(s - s.max())
+            assert abs(LSE[h, i] - (s.max() + np.log(p.sum()))) < 1e-12
+            assert np.abs(O[i, h] - p @ v[ctx, h] / p.sum()).max() < 1e-12
+    # the answer copy and its history copy differ (the history copy does not
+    # see the thinking), and later turns see the history copy, not the answer
+    a_rows = np.nonzero(role == W.ROLE_ANSWER)[0]
+    h_rows = np.nonzero(role == W.ROLE_ANSWER_HISTORY)[0]
+    assert np.abs(O[a_rows] - O[h_rows]).max() > 1e-2
+    m = oracle.sequence_mask("strip_thinking_dup", np.array([0, T]), 0, meta)
+    later = turn[:, None] > turn[None, :]
+    assert not (m & later & (role[None, :] == W.ROLE_ANSWER)).any()
+    assert not (m & later & (role[None, :] == W.ROLE_THINK)).any()
+    assert (m | ~(later & (role[None, :] == W.ROLE_ANSWER_HISTORY))).all()
+
+
+def test_strip_thinking_dup_workload_counts_closed_form():
+    """Workload 6: per turn, tiles of user 128 (1) / think 768 (6) / answer
+    256 (2) / history 256 (2), all spans tile-aligned."""
+    w = W.make_workload(6, tensors=False)
+    assert w.total_tokens == 11264
+    nturn, u, th, a = 8, 128, 768, 256
+    lab = oracle.tile_labels(w.kind, w.cu_seqlens, w.meta())[0]
+    # closed forms for the pairs: own turn (user, think, answer copy causal over
+    # user+think+itself, history copy over user+itself) and earlier turns
+    # (user + history copy of each earlier turn, for every token of the turn)
+    own = (u * (u + 1) // 2 + th * u + th * (th + 1) // 2 + a * (u + th) + a * (a + 1) // 2
+           + a * u + a * (a + 1) // 2)
+    per_turn_tokens = u + th + 2 * a
+    hist = per_turn_tokens * (u + a)
+    nnz = nturn * own + hist * sum(range(nturn))
+    assert oracle.unmasked_pairs(w.kind, w.cu_seqlens, w.meta()) == nnz
+    # tile labels: within a turn (11 tiles: U, T x6, A x2, H x2) the visible
+    # key tiles of each query tile are whole spans, so only diagonal tiles are
+    # PARTIAL; earlier turns contribute their U and H tiles FULL
+    per = 11
+    own_full = sum(len(r) for r in [[], [0], [0, 1], [0, 1, 2], [0, 1, 2, 3], [0, 1, 2, 3, 4],
+                                    [0, 1, 2, 3, 4, 5], [0, 1, 2, 3, 4, 5, 6], [0, 1, 2, 3, 4, 5, 6, 7],
+                                    [0], [0, 9]])
+    full = nturn * own_full + per * 3 * sum(range(nturn))
+    partial = nturn * per
+    assert oracle.label_totals([lab]) == (full, partial, (nturn * per) ** 2 - full - partial)
+
+
 def test_varlen_equals_independent_sequences():
     """cu_seqlens packing (xorl issue, Summary): a causal square per sequence and
     nothing across, i.e. each sequence alone."""
@@ -386,6 +465,7 @@ def _pins_pass():
         test_predicate_truth_tables()
         test_shared_prefix_equals_separate_runs()
         test_strip_thinking_equals_per_turn_recomputation()
+        test_strip_thinking_dup_equals_inference_contexts()
         test_wrong_task_max_diff_matches_page()
     except AssertionError:
         return False
@@ -397,7 +477,8 @@ def test_pins_pass_on_the_real_oracle():
 
 
 @pytest.mark.parametrize("mutant", ["strict_diagonal", "prefix_drops_seg0", "think_le_turn",
-                                    "no_scale", "transposed_scores"])
+                                    "no_scale", "transposed_scores", "dup_history_sees_think",
+                                    "dup_later_sees_answer"])
 def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     real_pred, real_attn = oa.predicate, oa.masked_attention
 
@@ -410,6 +491,12 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
             return (qi >= ki) & (seg[ki] == seg[qi])
         if mutant == "think_le_turn" and kind == "strip_thinking":
             return (qi >= ki) & ~((role[ki] == role_think) & (turn[ki] <= turn[qi]))
+        if kind == "strip_thinking_dup" and mutant.startswith("dup_"):
+            base = real_pred(kind, qi, ki, seg, role, turn, role_think)
+            same, causal = turn[ki] == turn[qi], qi >= ki
+            if mutant == "dup_history_sees_think":
+                return base | (causal & same & (role[ki] == role_think) & (role[qi] == W.ROLE_ANSWER_HISTORY))
+            return base | (causal & (turn[ki] < turn[qi]) & (role[ki] == W.ROLE_ANSWER))
         return real_pred(kind, qi, ki, seg, role, turn, role_think)
 
     def attn(q, k, v, mask, scale):
