@@ -149,7 +149,8 @@ def workload_config(w, nnz, extra=None):
 # (seeded) sequence / document lengths; workload 3 is P(P+1)/2 + n(sP + s(s+1)/2)
 # with P=2048, n=16, s=512; workload 4 is 8 L(L+1)/2 + L*384*(0+1+...+7) with
 # L=1152.  tests/test_bench_host.py checks each against the oracle's count.
-UNMASKED_PAIRS = {1: 2080, 2: 8_172_171, 3: 20_976_640, 4: 17_699_328, 5: 67_979_834}
+UNMASKED_PAIRS = {1: 2080, 2: 8_172_171, 3: 20_976_640, 4: 17_699_328, 5: 67_979_834,
+                  6: 20_977_152}
 
 
 def count_pairs(w, c):
@@ -478,8 +479,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5],
-                    help="workload number (2-5 are the bf16 block-mask workloads)")
+    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5, 6],
+                    help="workload number (2-5: the bf16 block-mask workloads; 6: strip-thinking with duplicated answers)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

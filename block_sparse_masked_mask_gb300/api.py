@@ -19,7 +19,8 @@ STATUS = {
     3: "ATTN_ERR_WORKSPACE_TOO_SMALL", 4: "ATTN_ERR_MASK_MISMATCH", 5: "ATTN_ERR_CUDA",
     6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_DEVICE_INVALID_INPUT",
 }
-MASK_KINDS = {"causal": 0, "causal_document": 1, "shared_prefix": 2, "strip_thinking": 3}
+MASK_KINDS = {"causal": 0, "causal_document": 1, "shared_prefix": 2, "strip_thinking": 3,
+              "strip_thinking_dup": 4}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 BLOCK_M = BLOCK_N = 128

@@ -101,13 +101,21 @@ static BmView make_view(const attn_block_mask* bm) {
   return v;
 }
 
-static bool valid_kind(int kind) { return kind >= ATTN_MASK_CAUSAL && kind <= ATTN_MASK_STRIP_THINKING; }
+// The duplicated-answer kind reserves role codes 2 (ANSWER) and 3
+// (ANSWER_HISTORY); THINK must be another code.
+bool role_think_valid(int kind, const attn_mask_params* params) {
+  const int rt = params ? params->role_think : 1;
+  return kind != ATTN_MASK_STRIP_THINKING_DUP || (rt != 2 && rt != 3);
+}
+
+static bool valid_kind(int kind) { return kind >= ATTN_MASK_CAUSAL && kind <= ATTN_MASK_STRIP_THINKING_DUP; }
 
 static bool metadata_present(int kind, const int32_t* seg, const int8_t* role, const int32_t* turn) {
   switch (kind) {
     case ATTN_MASK_CAUSAL_DOCUMENT:
     case ATTN_MASK_SHARED_PREFIX: return seg != nullptr;
-    case ATTN_MASK_STRIP_THINKING: return role != nullptr && turn != nullptr;
+    case ATTN_MASK_STRIP_THINKING:
+    case ATTN_MASK_STRIP_THINKING_DUP: return role != nullptr && turn != nullptr;
     default: return true;
   }
 }
@@ -158,6 +166,7 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   if (!valid_kind(kind) || batch < 1 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
   if (block_m != kTile || block_n != kTile) return ATTN_ERR_UNSUPPORTED;
   if (!metadata_present(kind, seg_id, role, turn)) return ATTN_ERR_INVALID_ARG;
+  if (!role_think_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   BmLayout l;
   if (!bm_layout(batch, total_tokens, max_seqlen, &l)) return ATTN_ERR_INVALID_ARG;

@@ -926,12 +926,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             if (uniform_k) {
 #pragma unroll
               for (int m = 0; m < 2; ++m) {
-                const int qcv = qc[32 * m + lane];
-                bool ok_v;
-                if (kind == ATTN_MASK_STRIP_THINKING) ok_v = code_visible(ATTN_MASK_STRIP_THINKING, qcv, kcode_w);
-                else if (kind == ATTN_MASK_SHARED_PREFIX) ok_v = code_visible(ATTN_MASK_SHARED_PREFIX, qcv, kcode_w);
-                else ok_v = code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcv, kcode_w);
-                vis[m] &= __ballot_sync(0xffffffffu, ok_v);
+                vis[m] &= __ballot_sync(0xffffffffu, code_visible(kind, qc[32 * m + lane], kcode_w));
               }
             } else {
 #pragma unroll

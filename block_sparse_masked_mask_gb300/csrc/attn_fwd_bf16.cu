@@ -528,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (kind == ATTN_MASK_SHARED_PREFIX) {
                 vis[0] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc0));
                 vis[1] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_SHARED_PREFIX, qcode_w, kc1));
+              } else if (kind == ATTN_MASK_STRIP_THINKING_DUP) {
+                vis[0] &= __ballot_sync(0xffffffffu, dup_visible(qcode_w, kc0));
+                vis[1] &= __ballot_sync(0xffffffffu, dup_visible(qcode_w, kc1));
               } else {
                 vis[0] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc0));
                 vis[1] &= __ballot_sync(0xffffffffu, code_visible(ATTN_MASK_CAUSAL_DOCUMENT, qcode_w, kc1));
@@ -540,10 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_SHARED_PREFIX>(codes, q, qcode);
-            } else {
+            } else if (kind == ATTN_MASK_CAUSAL_DOCUMENT) {
 #pragma unroll
               for (int q = 0; q < 2; ++q)
                 if (vis[q]) vis[q] &= code_word<ATTN_MASK_CAUSAL_DOCUMENT>(codes, q, qcode);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 2; ++q)
+                if (vis[q]) vis[q] &= code_word_rt(kind, codes, q, qcode);
             }
             // done with the buffer
             ptx::mbar_arrive(bar(C::B_CODEFREE + cb));

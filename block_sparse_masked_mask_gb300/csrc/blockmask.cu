@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
   __shared__ int s_warp[32];
   __shared__ int s_carry;
   __shared__ int s_pcarry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) { s_err = 0; s_carry = 0; s_pcarry = 0; }
   __syncthreads();
   const int B = v.batch;
@@ -143,39 +143,49 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
 //   causal_document / shared_prefix: [0] min seg, [1] max seg, [2] any seg == 0
 //   strip_thinking: [0] min turn, [1] max turn, [2] #THINK tokens,
 //                   [3] min THINK turn, [4] max THINK turn, [5] #tokens
+//   strip_thinking_dup: as strip_thinking with [2]-[4] over the private
+//                   tokens (THINK and ANSWER copies), [6] the max turn of
+//                   ANSWER_HISTORY tokens and [7] the set of classes present
+//                   (bit c for class c of dup_class)
 __global__ void __launch_bounds__(128) bm_summary_kernel(BmView v, MaskArgs m) {
   const int g = blockIdx.x;
   if (g >= v.header[kHdrQtiles] || m.kind == ATTN_MASK_CAUSAL) return;
-  __shared__ int s_red[4][6];
+  __shared__ int s_red[4][8];
   const int b = v.qt_seq[g], a = v.qt_idx[g];
   const int s0 = v.cu[b], L = v.cu[b + 1] - s0;
   const int n = min(kTile, L - a * kTile);
   const int r = threadIdx.x, lane = r & 31, warp = r >> 5;
   const bool in = r < n;
   const int tok = s0 + a * kTile + r;
-  int x[6];
-  if (m.kind == ATTN_MASK_STRIP_THINKING) {
+  int x[8];
+  if (m.kind == ATTN_MASK_STRIP_THINKING || m.kind == ATTN_MASK_STRIP_THINKING_DUP) {
     const int t = in ? m.turn[tok] : 0;
-    const bool th = in && (int)m.role[tok] == m.role_think;
+    const int cls = in ? (m.kind == ATTN_MASK_STRIP_THINKING ? ((int)m.role[tok] == m.role_think ? 1 : 0)
+                                                             : dup_class(m.role[tok], m.role_think))
+                       : 0;
+    const bool priv = cls == 1 || cls == 2;  // THINK (and, duplicated, the ANSWER copy)
     x[0] = warp_min(in ? t : INT_MAX);
     x[1] = warp_max(in ? t : INT_MIN);
-    x[2] = warp_sum(th ? 1 : 0);
-    x[3] = warp_min(th ? t : INT_MAX);
-    x[4] = warp_max(th ? t : INT_MIN);
+    x[2] = warp_sum(priv ? 1 : 0);
+    x[3] = warp_min(priv ? t : INT_MAX);
+    x[4] = warp_max(priv ? t : INT_MIN);
     x[5] = warp_sum(in ? 1 : 0);
+    x[6] = warp_max(cls == 3 ? t : INT_MIN);
+    x[7] = int(__reduce_or_sync(0xffffffffu, in ? (1u << cls) : 0u));
   } else {
     const int sg = in ? m.seg[tok] : 0;
     x[0] = warp_min(in ? sg : INT_MAX);
     x[1] = warp_max(in ? sg : INT_MIN);
     x[2] = warp_sum(in && sg == 0 ? 1 : 0);
-    x[3] = x[4] = x[5] = 0;
+    x[3] = x[4] = x[5] = x[7] = 0;
+    x[6] = INT_MIN;
   }
   if (lane == 0)
-    for (int i = 0; i < 6; ++i) s_red[warp][i] = x[i];
+    for (int i = 0; i < 8; ++i) s_red[warp][i] = x[i];
   __syncthreads();
   if (r == 0) {
     int* out = v.summary + size_t(g) * kSumInts;
-    int mn0 = INT_MAX, mx1 = INT_MIN, c2 = 0, mn3 = INT_MAX, mx4 = INT_MIN, c5 = 0;
+    int mn0 = INT_MAX, mx1 = INT_MIN, c2 = 0, mn3 = INT_MAX, mx4 = INT_MIN, c5 = 0, mx6 = INT_MIN, or7 = 0;
     for (int w = 0; w < 4; ++w) {
       mn0 = min(mn0, s_red[w][0]);
       mx1 = max(mx1, s_red[w][1]);
@@ -183,9 +193,11 @@ __global__ void __launch_bounds__(128) bm_summary_kernel(BmView v, MaskArgs m) {
       mn3 = min(mn3, s_red[w][3]);
       mx4 = max(mx4, s_red[w][4]);
       c5 += s_red[w][5];
+      mx6 = max(mx6, s_red[w][6]);
+      or7 |= s_red[w][7];
     }
     out[0] = mn0; out[1] = mx1; out[2] = c2; out[3] = mn3; out[4] = mx4; out[5] = c5;
-    out[6] = 0; out[7] = 0;
+    out[6] = mx6; out[7] = or7;
   }
 }
 
@@ -223,6 +235,25 @@ __device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
       // hidden iff key is THINK with an earlier turn than the query
       if (all_causal && (sk[2] == 0 || sk[3] >= sq[1])) return ATTN_TILE_FULL;
       if (sk[2] == sk[5] && sk[4] < sq[0]) return ATTN_TILE_EMPTY;
+      return kUnknown;
+    case ATTN_MASK_STRIP_THINKING_DUP:
+      // only context keys and history copies of turns before every query's
+      if (all_causal && sk[2] == 0 && sk[6] < sq[0]) return ATTN_TILE_FULL;
+      // only THINK / ANSWER-copy keys of turns before every query's
+      if (sk[2] == sk[5] && sk[4] < sq[0]) return ATTN_TILE_EMPTY;
+      // Both tiles inside one turn each, every key before every query: a pair
+      // is visible by its two classes alone, and every combination of a key
+      // class and a query class present in the tiles occurs as a pair.
+      if (all_causal && sq[0] == sq[1] && sk[0] == sk[1]) {
+        bool seen = false, hidden = false;
+        for (int kc = 0; kc < 4; ++kc)
+          for (int qc = 0; qc < 4; ++qc)
+            if (((sk[7] >> kc) & 1) && ((sq[7] >> qc) & 1)) {
+              if (dup_visible(4 * sq[0] + qc, 4 * sk[0] + kc)) seen = true;
+              else hidden = true;
+            }
+        return seen ? (hidden ? ATTN_TILE_PARTIAL : ATTN_TILE_FULL) : ATTN_TILE_EMPTY;
+      }
       return kUnknown;
   }
   return kUnknown;

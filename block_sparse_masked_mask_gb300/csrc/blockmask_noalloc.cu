@@ -73,13 +73,16 @@ extern "C" attn_status attn_block_mask_build_noalloc(
     const int32_t* turn, int32_t block_m, int32_t block_n, void* workspace, size_t workspace_bytes,
     attn_block_mask* out, attn_stream_t stream) {
   if (out == nullptr || cu_seqlens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (kind < ATTN_MASK_CAUSAL || kind > ATTN_MASK_STRIP_THINKING || batch < 1 || total_tokens < 0 ||
+  if (kind < ATTN_MASK_CAUSAL || kind > ATTN_MASK_STRIP_THINKING_DUP || batch < 1 || total_tokens < 0 ||
       max_seqlen < 0)
     return ATTN_ERR_INVALID_ARG;
   if (block_m != kTile || block_n != kTile) return ATTN_ERR_UNSUPPORTED;
   if ((kind == ATTN_MASK_CAUSAL_DOCUMENT || kind == ATTN_MASK_SHARED_PREFIX) && seg_id == nullptr)
     return ATTN_ERR_INVALID_ARG;
-  if (kind == ATTN_MASK_STRIP_THINKING && (role == nullptr || turn == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if ((kind == ATTN_MASK_STRIP_THINKING || kind == ATTN_MASK_STRIP_THINKING_DUP) &&
+      (role == nullptr || turn == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (!role_think_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   BmLayout l;
   if (!bm_layout(batch, total_tokens, max_seqlen, &l)) return ATTN_ERR_INVALID_ARG;

@@ -42,6 +42,9 @@ struct BmLayout {
            pair_order = 0, qcount = 0, qoff = 0, qidx = 0, qlabel = 0, korder = 0, total = 0;
 };
 
+// False when a STRIP_THINKING_DUP mask names role 2 or 3 as THINK.
+bool role_think_valid(int kind, const attn_mask_params* params);
+
 // Returns false on overflow / invalid sizes.
 bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out);
 
@@ -86,11 +89,31 @@ struct MaskArgs {
 //   strip_thinking  : !(role[k] == THINK && turn[k] < turn[q]); the key code is
 //                     turn[k] for THINK keys and INT_MAX otherwise, so the test
 //                     becomes kcode >= turn[q].
+//   strip_thinking_dup: both codes are 4 turn + class, class 1 THINK, 2 ANSWER
+//                     (the copy that sees its own thinking), 3 ANSWER_HISTORY,
+//                     0 anything else; see dup_visible.
+__device__ __forceinline__ int dup_class(int role, int role_think) {
+  return role == role_think ? 1 : (role == 2 ? 2 : (role == 3 ? 3 : 0));
+}
+
+// Duplicated answers: context keys are seen by every later query; THINK keys
+// by their own turn's THINK and ANSWER queries; ANSWER keys only by their own
+// turn's ANSWER queries; ANSWER_HISTORY keys by every later turn and by their
+// own turn's ANSWER_HISTORY queries.
+__device__ __forceinline__ bool dup_visible(int qcode, int kcode) {
+  const int kc = kcode & 3, qc = qcode & 3, kt = kcode >> 2, qt = qcode >> 2;
+  if (kc == 0) return true;
+  if (kc == 1) return kt == qt && (qc == 1 || qc == 2);
+  if (kc == 2) return kt == qt && qc == 2;
+  return kt < qt || (kt == qt && qc == 3);
+}
+
 __device__ __forceinline__ int query_code(const MaskArgs& m, int qi) {
   switch (m.kind) {
     case ATTN_MASK_CAUSAL_DOCUMENT:
     case ATTN_MASK_SHARED_PREFIX: return m.seg[qi];
     case ATTN_MASK_STRIP_THINKING: return m.turn[qi];
+    case ATTN_MASK_STRIP_THINKING_DUP: return 4 * m.turn[qi] + dup_class(m.role[qi], m.role_think);
     default: return 0;
   }
 }
@@ -101,6 +124,7 @@ __device__ __forceinline__ int key_code(const MaskArgs& m, int ki) {
     case ATTN_MASK_SHARED_PREFIX: return m.seg[ki];
     case ATTN_MASK_STRIP_THINKING:
       return (int)m.role[ki] == m.role_think ? m.turn[ki] : INT_MAX;
+    case ATTN_MASK_STRIP_THINKING_DUP: return 4 * m.turn[ki] + dup_class(m.role[ki], m.role_think);
     default: return 0;
   }
 }
@@ -110,6 +134,7 @@ __device__ __forceinline__ bool code_visible(int kind, int qcode, int kcode) {
     case ATTN_MASK_CAUSAL_DOCUMENT: return kcode == qcode;
     case ATTN_MASK_SHARED_PREFIX: return kcode == 0 || kcode == qcode;
     case ATTN_MASK_STRIP_THINKING: return kcode >= qcode;
+    case ATTN_MASK_STRIP_THINKING_DUP: return dup_visible(qcode, kcode);
     default: return true;
   }
 }

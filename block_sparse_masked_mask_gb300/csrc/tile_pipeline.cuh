@@ -91,6 +91,23 @@ __device__ __forceinline__ uint32_t code_word(const int* codes, int q, int qcode
   return w;
 }
 
+// The same for a kind known only at run time, as a compact loop, for kinds
+// whose rows rarely hold different codes: it keeps the hot loop around it
+// small enough for the instruction cache.
+__device__ __forceinline__ uint32_t code_word_rt(int kind, const int* codes, int q, int qcode) {
+  uint32_t w = 0;
+  const int4* c4 = reinterpret_cast<const int4*>(codes + 32 * q);
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    const int4 k = c4[c];
+    w |= (uint32_t(code_visible(kind, qcode, k.x)) << (4 * c)) |
+         (uint32_t(code_visible(kind, qcode, k.y)) << (4 * c + 1)) |
+         (uint32_t(code_visible(kind, qcode, k.z)) << (4 * c + 2)) |
+         (uint32_t(code_visible(kind, qcode, k.w)) << (4 * c + 3));
+  }
+  return w;
+}
+
 // Shared-memory descriptors: one base per tile; each k-step adds a constant to
 // the start-address field (addresses stay below 2^18, so no carry leaves it).
 // K-major operand (Q or K): k-step kk covers elements [16kk, 16kk+16) of D.

@@ -23,6 +23,18 @@
  *                              (xorl issue, Mask specifications, "Shared prefix")
  *   ATTN_MASK_STRIP_THINKING   (qi >= ki) & ~((role[ki] == THINK) & (turn[ki] < turn[qi]))
  *                              (xorl issue, Mask specifications, "Strip-thinking")
+ *   ATTN_MASK_STRIP_THINKING_DUP  the exact variant with every answer span
+ *                              duplicated (xorl issue, "The exactness
+ *                              question", option (b)).  Roles: THINK =
+ *                              role_think, ANSWER = 2 (the copy that sees its
+ *                              own turn's thinking), ANSWER_HISTORY = 3 (the
+ *                              copy later turns see), anything else context.
+ *                              With ki <= qi, a key is visible when it is
+ *                              context; THINK of the query's turn and the query
+ *                              THINK or ANSWER; ANSWER of the query's turn and
+ *                              the query ANSWER; ANSWER_HISTORY of an earlier
+ *                              turn, or of the query's turn with the query
+ *                              ANSWER_HISTORY.  role_think must not be 2 or 3.
  *
  * Tiles
  *   Each sequence is cut into 128-token tiles starting at its first token.
@@ -81,7 +93,8 @@ typedef enum attn_mask_kind {
   ATTN_MASK_CAUSAL = 0,
   ATTN_MASK_CAUSAL_DOCUMENT = 1,
   ATTN_MASK_SHARED_PREFIX = 2,
-  ATTN_MASK_STRIP_THINKING = 3
+  ATTN_MASK_STRIP_THINKING = 3,
+  ATTN_MASK_STRIP_THINKING_DUP = 4
 } attn_mask_kind;
 
 typedef enum attn_dtype {
@@ -99,7 +112,7 @@ typedef enum attn_dtype {
 #define ATTN_BLOCK_N 128
 
 typedef struct attn_mask_params {
-  int32_t role_think; /* role code of THINK tokens for ATTN_MASK_STRIP_THINKING (default 1) */
+  int32_t role_think; /* role code of THINK tokens for the STRIP_THINKING kinds (default 1) */
 } attn_mask_params;
 
 /*
@@ -175,7 +188,8 @@ ATTN_API attn_status attn_block_mask_workspace_size(int32_t batch, int32_t total
  * cu_seqlens[batch] = total_tokens, every length <= max_seqlen) and the
  * per-token metadata the kind needs (device arrays of total_tokens entries):
  *   CAUSAL: none; CAUSAL_DOCUMENT and SHARED_PREFIX: seg_id;
- *   STRIP_THINKING: role and turn.  Unused pointers may be NULL.
+ *   STRIP_THINKING and STRIP_THINKING_DUP: role and turn.  Unused pointers
+ *   may be NULL.
  * The mask is built once and can be reused by any number of attn_fwd calls
  * while the metadata does not change (xorl issue, Proposed work, item 3:
  * masks compiled and cached across steps).  It follows the forward (q-major)

@@ -78,8 +78,22 @@ def test_build_rejects_bad_arguments_before_any_launch(native_lib):
     assert call(kind=1) == 1            # causal_document needs seg_id
     assert call(kind=2) == 1            # shared_prefix needs seg_id
     assert call(kind=3, role=_fake()) == 1  # strip_thinking needs role and turn
+    assert call(kind=4, turn=_fake()) == 1  # so does its duplicated-answer variant
+    assert call(kind=5) == 1
     assert call(ws=_fake(0x20010)) == 1   # workspace not 256-byte aligned
     assert call(wsb=16) == 3             # workspace too small
+
+
+def test_dup_kind_reserves_answer_role_codes(native_lib):
+    """The duplicated-answer kind takes roles 2 and 3 for the two answer
+    copies, so THINK may not be either."""
+    from block_sparse_masked_mask_gb300 import _native
+    out = _native.AttnBlockMask()
+    for rt, want in ((2, 1), (3, 1)):
+        prm = _native.AttnMaskParams(rt)
+        for fn in (native_lib.attn_block_mask_build, native_lib.attn_block_mask_build_noalloc):
+            assert fn(4, ctypes.byref(prm), _fake(), 1, 256, 256, None, _fake(), _fake(), 128, 128,
+                      _fake(0x20000), 1 << 20, ctypes.byref(out), None) == want
 
 
 def test_fwd_rejects_bad_arguments_before_any_launch(native_lib):

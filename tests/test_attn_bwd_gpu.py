@@ -90,7 +90,8 @@ def test_small_all_elements(kind, D):
     compare_all(w, do, run_bwd(w, do))
 
 
-@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking"])
+@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking",
+                                  "strip_thinking_dup"])
 def test_small_repeating_ids_all_elements(kind):
     """Ids and turns from a small alphabet: keys of one warp often hold different
     codes, so the dK/dV side takes the per-key predicate path."""
@@ -132,7 +133,8 @@ def sample_rows(w, n=48, seed=0):
 
 @pytest.mark.parametrize("c,form,heads", [(2, "mask", (0, 15)),
                                           (3, "mask", (0, 31)), (4, "mask", (0, 31)),
-                                          (5, "cu_seqlens", (0, 31)), (5, "mask", (31,))])
+                                          (5, "cu_seqlens", (0, 31)), (5, "mask", (31,)),
+                                          (6, "mask", (0, 31))])
 def test_full_size_workloads_sampled(c, form, heads):
     """The bf16 workloads at full size, on sampled query rows (dQ) and key rows
     (dK, dV) that the oracle computes one by one."""

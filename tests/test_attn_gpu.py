@@ -68,7 +68,8 @@ def test_small_all_elements(kind, D, dtype):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking"])
+@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking",
+                                  "strip_thinking_dup"])
 def test_small_repeating_ids_all_elements(kind, D):
     """Ids and turns drawn from a small alphabet: the rows of a warp often hold
     different query codes, so PARTIAL tiles take the per-row predicate path
@@ -112,7 +113,7 @@ def sample_rows(w, n=96, seed=0):
 
 
 @pytest.mark.parametrize("c,form", [(1, "mask"), (2, "mask"), (3, "mask"), (4, "mask"),
-                                    (5, "mask"), (5, "cu_seqlens")])
+                                    (5, "mask"), (5, "cu_seqlens"), (6, "mask")])
 def test_full_size_workloads_sampled(c, form):
     w = full_workload(c, form)
     o, lse = run_gpu(w)

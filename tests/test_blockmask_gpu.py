@@ -59,7 +59,7 @@ def assert_matches_oracle(w, bm):
     assert np.array_equal(got["korder"].numpy(), oracle.lpt_order(wt["qcount"]))
 
 
-@pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 6])
 def test_workload_masks_bit_exact(c):
     w = W.make_workload(c, tensors=False)
     assert_matches_oracle(w, build_on_gpu(w))
@@ -123,7 +123,8 @@ def test_last_entry_must_equal_total_tokens():
     assert api.attn_get_status(bm) == 7
 
 
-@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking"])
+@pytest.mark.parametrize("kind", ["causal_document", "shared_prefix", "strip_thinking",
+                                  "strip_thinking_dup"])
 @pytest.mark.parametrize("li", [4, 5, 7])
 def test_random_metadata_repeating_ids_bit_exact(kind, li):
     """Ids drawn from a small alphabet (they repeat, fall and skip), so the
