@@ -60,6 +60,8 @@ class Workload:
     seg: Optional[np.ndarray] = None    # int32 [T]
     role: Optional[np.ndarray] = None   # int8  [T]
     turn: Optional[np.ndarray] = None   # int32 [T]
+    dense_bits: Optional[np.ndarray] = None     # uint32, the "dense" kind's bit rows
+    dense_offsets: Optional[np.ndarray] = None  # int64 [B+1], first word of each sequence
     role_think: int = ROLE_THINK
     seed: int = 0
     q: Optional[torch.Tensor] = None    # [T, H, D] on CPU, workload dtype
@@ -85,14 +87,18 @@ class Workload:
 
     def meta(self) -> dict:
         return {"seg": self.seg, "role": self.role, "turn": self.turn,
-                "role_think": self.role_think}
+                "role_think": self.role_think, "dense_bits": self.dense_bits,
+                "dense_offsets": self.dense_offsets}
 
     def device_meta(self, device="cuda") -> dict:
-        """cu_seqlens and the per-token metadata as device tensors."""
+        """cu_seqlens and the per-token metadata as device tensors (the dense
+        mask's uint32 words as int32, the same bytes)."""
         def dev(a):
             return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        bits = None if self.dense_bits is None else self.dense_bits.view(np.int32)
         return {"cu_seqlens": dev(self.cu_seqlens), "seg_id": dev(self.seg),
-                "role": dev(self.role), "turn": dev(self.turn)}
+                "role": dev(self.role), "turn": dev(self.turn), "dense_bits": dev(bits),
+                "dense_offsets": dev(self.dense_offsets)}
 
 
 WORKLOAD_NAMES = {
@@ -244,14 +250,76 @@ def random_metadata(rng: np.random.Generator, kind: str, lengths, role_think: in
     return seg, role, turn
 
 
+def dense_offsets(lengths) -> np.ndarray:
+    """First uint32 word of each sequence's bit rows (L rows of ceil(L / 32)
+    words each), and the total, as int64 [B+1]."""
+    words = [L * ((L + 31) // 32) for L in lengths]
+    return np.concatenate([[0], np.cumsum(words)]).astype(np.int64)
+
+
+def pack_rows(rows: np.ndarray, pad_rng: Optional[np.random.Generator] = None) -> np.ndarray:
+    """Bool rows [R, L] packed as uint32 words, bit j % 32 of word j // 32.  The
+    bits past L in the last word are random when ``pad_rng`` is given (they
+    must be ignored), else zero."""
+    R, L = rows.shape
+    W = (L + 31) // 32
+    full = np.zeros((R, W * 32), bool)
+    full[:, :L] = rows
+    if pad_rng is not None and W * 32 > L:
+        full[:, L:] = pad_rng.random((R, W * 32 - L)) < 0.5
+    return np.packbits(full, axis=1, bitorder="little").view(np.uint32).reshape(R, W)
+
+
+def random_dense_mask(rng: np.random.Generator, lengths, tile: int = 128):
+    """A random caller-supplied mask per sequence for the "dense" kind: every
+    tile x tile block is drawn as all hidden, all visible, random bits, or a
+    random lower-left staircase; a few rows see nothing at all; the bits past
+    a row's end are random.  Returns (bits uint32, offsets int64 [B+1])."""
+    out = []
+    for L in lengths:
+        nt = -(-L // tile)
+        m = np.zeros((L, L), bool)
+        for a in range(nt):
+            for c in range(nt):
+                r0, r1, c0, c1 = a * tile, min(L, (a + 1) * tile), c * tile, min(L, (c + 1) * tile)
+                mode = rng.choice(4, p=[0.3, 0.3, 0.25, 0.15])
+                if mode == 1:
+                    m[r0:r1, c0:c1] = True
+                elif mode == 2:
+                    m[r0:r1, c0:c1] = rng.random((r1 - r0, c1 - c0)) < rng.uniform(0.05, 0.95)
+                elif mode == 3:
+                    shift = int(rng.integers(-tile, tile))
+                    ii = np.arange(r0, r1)[:, None]
+                    jj = np.arange(c0, c1)[None, :]
+                    m[r0:r1, c0:c1] = jj - c0 <= ii - r0 + shift
+        empty = rng.random(L) < 0.02
+        m[empty] = False
+        out.append(pack_rows(m, rng).ravel())
+    bits = np.concatenate(out) if out else np.zeros(0, np.uint32)
+    return bits.astype(np.uint32), dense_offsets(lengths)
+
+
+def random_meta(rng: np.random.Generator, kind: str, lengths, role_think: int = ROLE_THINK,
+                id_alphabet: int = 0) -> dict:
+    """random_metadata as the dict the oracle takes, with a random dense mask
+    for the "dense" kind."""
+    seg, role, turn = random_metadata(rng, kind, lengths, role_think, id_alphabet)
+    bits = offs = None
+    if kind == "dense":
+        bits, offs = random_dense_mask(rng, lengths)
+    return {"seg": seg, "role": role, "turn": turn, "role_think": role_think,
+            "dense_bits": bits, "dense_offsets": offs}
+
+
 def random_workload(seed: int, kind: str, lengths, num_heads: int, head_dim: int,
                     dtype: torch.dtype = torch.bfloat16, sigma: float = 1.0,
                     id_alphabet: int = 0) -> Workload:
     """A small seeded case for parity tests (ragged lengths, any kind); see
     random_metadata for ``id_alphabet``."""
     rng = np.random.default_rng(seed)
-    seg, role, turn = random_metadata(rng, kind, lengths, id_alphabet=id_alphabet)
+    m = random_meta(rng, kind, lengths, id_alphabet=id_alphabet)
     w = Workload(f"random_{kind}_{seed}", kind, _cu(lengths), num_heads, head_dim, dtype,
-                 sigma=sigma, seg=seg, role=role, turn=turn, seed=seed)
+                 sigma=sigma, seg=m["seg"], role=m["role"], turn=m["turn"],
+                 dense_bits=m["dense_bits"], dense_offsets=m["dense_offsets"], seed=seed)
     _fill_tensors(w, torch.Generator().manual_seed(10_000 + seed))
     return w

@@ -35,7 +35,8 @@ from __future__ import annotations
 
 import numpy as np
 
-KINDS = ("causal", "causal_document", "shared_prefix", "strip_thinking", "strip_thinking_dup")
+KINDS = ("causal", "causal_document", "shared_prefix", "strip_thinking", "strip_thinking_dup",
+         "none", "dense")
 
 # Roles of the duplicated-answer layout: the answer copy that attends its own
 # turn's thinking (and carries the loss), and the history copy later turns see.
@@ -99,6 +100,37 @@ def predicate(kind: str, qi, ki, seg=None, role=None, turn=None, role_think: int
     raise ValueError(f"unknown mask kind {kind!r}")
 
 
+def dense_bits(meta: dict, cu_seqlens, b: int, rows, cols):
+    """The caller-supplied mask of sequence ``b`` at local rows x cols, for the
+    ``dense`` kind: bit (i, j) of the sequence, row-major with rows of
+    ceil(L / 32) uint32 words from word ``dense_offsets[b]``, bit j % 32 of
+    word j // 32, 1 = visible."""
+    L = int(cu_seqlens[b + 1] - cu_seqlens[b])
+    W = (L + 31) // 32
+    rows = np.asarray(rows, np.int64)[:, None]
+    cols = np.asarray(cols, np.int64)[None, :]
+    words = np.asarray(meta["dense_bits"], np.uint32)[int(meta["dense_offsets"][b]) + rows * W + cols // 32]
+    return ((words >> (cols % 32).astype(np.uint32)) & 1).astype(bool)
+
+
+def visible(kind: str, cu_seqlens, b: int, meta: dict, rows, cols):
+    """Mask of sequence ``b`` at local query rows x key columns, [rows, cols]:
+    the predicate for the metadata kinds, all True for ``none`` (attention
+    without a mask inside each sequence: "Triton from first principles"
+    Ch. 21, Section 21.1, the plain flash_attn_kernel), and the caller's bits
+    for ``dense``."""
+    meta = meta or {}
+    rows = np.asarray(rows, np.int64)
+    cols = np.asarray(cols, np.int64)
+    if kind == "none":
+        return np.ones((len(rows), len(cols)), bool)
+    if kind == "dense":
+        return dense_bits(meta, cu_seqlens, b, rows, cols)
+    start = int(cu_seqlens[b])
+    return predicate(kind, start + rows[:, None], start + cols[None, :], meta.get("seg"),
+                     meta.get("role"), meta.get("turn"), meta.get("role_think", 1))
+
+
 def sequence_mask(kind: str, cu_seqlens, b: int, meta: dict, row_lo: int = 0, row_hi=None,
                   rows=None):
     """Rows of sequence ``b``'s full boolean mask, shape [rows, L].
@@ -113,11 +145,7 @@ def sequence_mask(kind: str, cu_seqlens, b: int, meta: dict, row_lo: int = 0, ro
         if row_hi is None:
             row_hi = L
         rows = np.arange(row_lo, row_hi)
-    qi = (start + np.asarray(rows, np.int64))[:, None]
-    ki = np.arange(start, end)[None, :]
-    meta = meta or {}
-    return predicate(kind, qi, ki, meta.get("seg"), meta.get("role"), meta.get("turn"),
-                     meta.get("role_think", 1))
+    return visible(kind, cu_seqlens, b, meta, rows, np.arange(L))
 
 
 # ----------------------------------------------------------------------------
@@ -309,8 +337,7 @@ def attention_backward_sampled(q, k, v, do, kind: str, cu_seqlens, meta=None, sc
             dlt = (doh * O[start:end, h]).sum(axis=1) if len(sk) else None
             if len(sq):
                 li = sq - start
-                vis = predicate(kind, sq[:, None], tok[None, :], meta.get("seg"), meta.get("role"),
-                                meta.get("turn"), meta.get("role_think", 1))
+                vis = visible(kind, cu, b, meta, sq - start, tok - start)
                 s = (qh[li] @ kh.T) * scale
                 p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[li, None]), 0.0)
                 d_i = (doh[li] * O[sq, h]).sum(axis=1)
@@ -318,8 +345,7 @@ def attention_backward_sampled(q, k, v, do, kind: str, cu_seqlens, meta=None, sc
                 dQ[sq, h] = (ds @ kh) * scale
             if len(sk):
                 lj = sk - start
-                vis = predicate(kind, tok[:, None], sk[None, :], meta.get("seg"), meta.get("role"),
-                                meta.get("turn"), meta.get("role_think", 1))
+                vis = visible(kind, cu, b, meta, tok - start, sk - start)
                 s = (qh @ kh[lj].T) * scale
                 p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[:, None]), 0.0)
                 ds = p * ((doh @ vh[lj].T) - dlt[:, None])

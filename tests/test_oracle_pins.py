@@ -89,6 +89,91 @@ def test_wrong_task_max_diff_matches_page():
     assert abs(diff - want) < 1e-6, diff
 
 
+def test_none_kind_reproduces_the_pages_wrong_task_numbers():
+    """The "none" kind through the full attention() path is the non-causal
+    attention of Worked Example 21.2.2: against the causal kind on the same
+    inputs its largest difference is the page's printed figure."""
+    vals = {}
+    with open(os.path.join(GOLDEN, "wrong_task.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            a, b = line.split()
+            vals[a] = b
+    q, k, v = (x[:, None, :] for x in _wrong_task_inputs())
+    cu = np.array([0, 20])
+    on, _ = oracle.attention(q, k, v, "none", cu, scale=1 / math.sqrt(8))
+    oc, _ = oracle.attention(q, k, v, "causal", cu, scale=1 / math.sqrt(8))
+    assert abs(np.abs(oc - on).max() - float(vals["max_abs_diff_causal_vs_noncausal"])) < 1e-6
+
+
+def test_none_kind_is_plain_softmax_per_sequence():
+    """Ch. 21, Worked Example 21.1.1: flash attention verified against
+    softmax(Q K^T / sqrt(d)) V computed the naive way on shapes aligned to no
+    block; here per packed sequence, through the oracle's none kind."""
+    rng = np.random.default_rng(17)
+    lens = [17, 23, 1]
+    cu = W._cu(lens)
+    T, H, D = sum(lens), 2, 8
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, "none", cu)
+    for b in range(len(lens)):
+        s = slice(cu[b], cu[b + 1])
+        for h in range(H):
+            sc = q[s, h] @ k[s, h].T / np.sqrt(D)
+            p = np.exp(sc - sc.max(axis=1, keepdims=True))
+            assert np.abs(O[s, h] - (p / p.sum(axis=1, keepdims=True)) @ v[s, h]).max() < 1e-12
+
+
+def _dense_from(kind, cu, meta):
+    """The bits of another kind's mask, packed as the dense kind reads them."""
+    rows = [W.pack_rows(oracle.sequence_mask(kind, cu, b, meta)).ravel() for b in range(len(cu) - 1)]
+    return np.concatenate(rows).astype(np.uint32), W.dense_offsets(np.diff(cu))
+
+
+@pytest.mark.parametrize("kind", ["causal", "causal_document", "strip_thinking_dup"])
+def test_dense_kind_carrying_a_predicate_equals_that_kind(kind):
+    """A dense mask holding another kind's pairs gives that kind's outputs
+    exactly, and the same tile labels."""
+    rng = np.random.default_rng(31)
+    lens = [150, 1, 290]
+    meta = W.random_meta(rng, kind, lens)
+    cu = W._cu(lens)
+    bits, offs = _dense_from(kind, cu, meta)
+    dmeta = {"dense_bits": bits, "dense_offsets": offs}
+    T, H, D = sum(lens), 2, 16
+    q, k, v = (rng.standard_normal((T, H, D)) for _ in range(3))
+    O1, L1 = oracle.attention(q, k, v, kind, cu, meta)
+    O2, L2 = oracle.attention(q, k, v, "dense", cu, dmeta)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    for a, b in zip(oracle.tile_labels(kind, cu, meta), oracle.tile_labels("dense", cu, dmeta)):
+        assert np.array_equal(a, b)
+
+
+def test_dense_causal_document_padding_equals_the_tokens_without_padding():
+    """The causal + document + padding composition (xorl issue, "Current state
+    in this tree": make_causal_block_mask) as a dense mask: padding tokens
+    neither attend nor are attended, so every other token's output is the
+    causal+document output of the sequence with the padding taken out; a
+    padding token's row sees nothing (O = 0, LSE = -inf)."""
+    rng = np.random.default_rng(32)
+    docs = [40, 1, 75]
+    pad = 30
+    L = sum(docs) + pad
+    seg = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(docs)] + [np.full(pad, -1, np.int32)])
+    keep = seg >= 0
+    qi, ki = np.arange(L)[:, None], np.arange(L)[None, :]
+    m = (ki <= qi) & (seg[ki] == seg[qi]) & keep[ki] & keep[qi]
+    dmeta = {"dense_bits": W.pack_rows(m, rng).ravel(), "dense_offsets": W.dense_offsets([L])}
+    H, D = 2, 8
+    q, k, v = (rng.standard_normal((L, H, D)) for _ in range(3))
+    O, LSE = oracle.attention(q, k, v, "dense", np.array([0, L]), dmeta)
+    Ok, Lk = oracle.attention(q[keep], k[keep], v[keep], "causal_document", np.array([0, keep.sum()]),
+                              {"seg": seg[keep]})
+    assert np.abs(O[keep] - Ok).max() < 1e-12 and np.abs(LSE[:, keep] - Lk).max() < 1e-12
+    assert (O[~keep] == 0).all() and (LSE[:, ~keep] == -np.inf).all()
+
+
 # ----------------------------------------------------------------------------
 # Closed forms and special cases.
 # ----------------------------------------------------------------------------
@@ -129,9 +214,8 @@ def test_matches_torch_sdpa_fp64(kind):
     boolean mask, and logsumexp for LSE."""
     rng = np.random.default_rng(11)
     lens = [70, 1, 33, 150]
-    seg, role, turn = W.random_metadata(rng, kind, lens)
+    meta = W.random_meta(rng, kind, lens)
     cu = W._cu(lens)
-    meta = {"seg": seg, "role": role, "turn": turn, "role_think": 1}
     T, H, D = sum(lens), 3, 24
     q, k, v = (torch.randn(T, H, D, dtype=torch.float64) for _ in range(3))
     O, LSE = oracle.attention(q, k, v, kind, cu, meta)
@@ -143,9 +227,13 @@ def test_matches_torch_sdpa_fp64(kind):
             qh, kh, vh = q[s0:s1, h], k[s0:s1, h], v[s0:s1, h]
             ref = torch.nn.functional.scaled_dot_product_attention(
                 qh[None], kh[None], vh[None], attn_mask=mask[None], scale=scale)[0]
-            assert np.abs(O[s0:s1, h] - ref.numpy()).max() < 1e-12
             sc = (qh @ kh.T * scale).masked_fill(~mask, -math.inf)
-            assert np.abs(LSE[h, s0:s1] - torch.logsumexp(sc, -1).numpy()).max() < 1e-12
+            lse = torch.logsumexp(sc, -1).numpy()
+            # a row that sees no key: O = 0 and LSE = -inf (SDPA gives NaN there)
+            seen = mask.any(-1).numpy()
+            assert (O[s0:s1, h][~seen] == 0).all() and (LSE[h, s0:s1][~seen] == -np.inf).all()
+            assert np.abs(O[s0:s1, h][seen] - ref.numpy()[seen]).max(initial=0) < 1e-12
+            assert np.abs(LSE[h, s0:s1][seen] - lse[seen]).max(initial=0) < 1e-12
 
 
 def test_online_softmax_equals_three_pass():
@@ -332,6 +420,9 @@ def test_predicate_truth_tables():
                 meta["role"] = np.array(toks[1:], np.int8)
             elif toks[0] == "len":
                 pass
+            elif toks[0] == "words":
+                meta["dense_bits"] = np.array([int(x, 16) for x in toks[1:]], np.uint32)
+                meta["dense_offsets"] = np.array([0, len(toks) - 1], np.int64)
             else:
                 rows.append([int(x) for x in toks])
         want = np.array(rows, bool)
@@ -467,6 +558,8 @@ def _pins_pass():
         test_strip_thinking_equals_per_turn_recomputation()
         test_strip_thinking_dup_equals_inference_contexts()
         test_wrong_task_max_diff_matches_page()
+        test_none_kind_reproduces_the_pages_wrong_task_numbers()
+        test_dense_causal_document_padding_equals_the_tokens_without_padding()
     except AssertionError:
         return False
     return True
@@ -478,7 +571,7 @@ def test_pins_pass_on_the_real_oracle():
 
 @pytest.mark.parametrize("mutant", ["strict_diagonal", "prefix_drops_seg0", "think_le_turn",
                                     "no_scale", "transposed_scores", "dup_history_sees_think",
-                                    "dup_later_sees_answer"])
+                                    "dup_later_sees_answer", "dense_msb_first", "none_is_causal"])
 def test_pins_catch_planted_mistakes(monkeypatch, mutant):
     real_pred, real_attn = oa.predicate, oa.masked_attention
 
@@ -509,6 +602,21 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
                 return real_attn(k, q, v, mask, scale)
         return real_attn(q, k, v, mask, scale)
 
+    real_bits, real_visible = oa.dense_bits, oa.visible
+
+    def bits(meta, cu_seqlens, b, rows, cols):
+        if mutant == "dense_msb_first":
+            cols = np.asarray(cols, np.int64)
+            return real_bits(meta, cu_seqlens, b, rows, (cols // 32) * 32 + 31 - cols % 32)
+        return real_bits(meta, cu_seqlens, b, rows, cols)
+
+    def vis(kind, cu_seqlens, b, meta, rows, cols):
+        if mutant == "none_is_causal" and kind == "none":
+            return np.asarray(cols)[None, :] <= np.asarray(rows)[:, None]
+        return real_visible(kind, cu_seqlens, b, meta, rows, cols)
+
+    monkeypatch.setattr(oa, "dense_bits", bits)
+    monkeypatch.setattr(oa, "visible", vis)
     monkeypatch.setattr(oa, "predicate", pred)
     monkeypatch.setattr(oa, "masked_attention", attn)
     monkeypatch.setattr(oracle, "masked_attention", attn)
@@ -523,9 +631,8 @@ def test_pins_catch_planted_mistakes(monkeypatch, mutant):
 def _bwd_case(kind, seed=21, lens=(70, 1, 33, 150), H=2, D=16):
     rng = np.random.default_rng(seed)
     lens = list(lens)
-    seg, role, turn = W.random_metadata(rng, kind, lens)
+    meta = W.random_meta(rng, kind, lens)
     cu = W._cu(lens)
-    meta = {"seg": seg, "role": role, "turn": turn, "role_think": 1}
     T = sum(lens)
     g = torch.Generator().manual_seed(seed)
     q, k, v, do = (torch.randn(T, H, D, dtype=torch.float64, generator=g) for _ in range(4))
@@ -614,9 +721,11 @@ def test_backward_invariants(kind):
         s0, s1 = int(cu[b]), int(cu[b + 1])
         if s1 == s0:
             continue
+        seen = oracle.sequence_mask(kind, cu, b, meta).any(axis=1)
         for h in range(q.shape[1]):
             assert np.abs(dk[s0:s1, h].sum(axis=0)).max() < 1e-10
-            assert np.abs(dv[s0:s1, h].sum(axis=0) - do[s0:s1, h].numpy().sum(axis=0)).max() < 1e-10
+            want = do[s0:s1, h].numpy()[seen].sum(axis=0)
+            assert np.abs(dv[s0:s1, h].sum(axis=0) - want).max() < 1e-10
 
 
 def test_transposed_lists_are_the_transpose():
