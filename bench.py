@@ -150,7 +150,7 @@ def workload_config(w, nnz, extra=None):
 # with P=2048, n=16, s=512; workload 4 is 8 L(L+1)/2 + L*384*(0+1+...+7) with
 # L=1152.  tests/test_bench_host.py checks each against the oracle's count.
 UNMASKED_PAIRS = {1: 2080, 2: 8_172_171, 3: 20_976_640, 4: 17_699_328, 5: 67_979_834,
-                  6: 20_977_152}
+                  6: 20_977_152, 7: 16_334_146, 8: 53_960_250}
 
 
 def count_pairs(w, c):
@@ -280,15 +280,14 @@ def run_ours(args):
     ws_bytes = api.attn_block_mask_workspace_size(w.batch, T, w.max_seqlen)
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    mkw = w.api_kwargs(dm)
 
     def step(ev=None):
         bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], T, w.max_seqlen,
-                                       seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"],
-                                       role_think=w.role_think, workspace=workspace)
+                                       workspace=workspace, **mkw)
         if ev is not None:
             ev.record(stream)
-        api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, seg_id=dm["seg_id"],
-                     role=dm["role"], turn=dm["turn"], role_think=w.role_think, out=out, lse=lse)
+        api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, out=out, lse=lse, **mkw)
         return bm
 
     for _ in range(args.warmup):
@@ -342,7 +341,7 @@ def run_ours(args):
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         bws = torch.empty(api.attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=dev)
-        kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think)
+        kw = mkw
 
         def bwd_step():
             api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
@@ -413,12 +412,11 @@ def run_ours(args):
         with torch.cuda.stream(comp_s):
             comp_s.wait_event(h2d_done[b])
             m = dmeta[b]
-            bm2 = api.attn_block_mask_build(w.kind, m["cu_seqlens"], T, w.max_seqlen, seg_id=m["seg_id"],
-                                            role=m["role"], turn=m["turn"], role_think=w.role_think,
-                                            workspace=dws[b])
+            mk = w.api_kwargs(m)
+            bm2 = api.attn_block_mask_build(w.kind, m["cu_seqlens"], T, w.max_seqlen,
+                                            workspace=dws[b], **mk)
             api.attn_fwd(dq[b], dk[b], dv[b], bm2, w.kind, m["cu_seqlens"], w.max_seqlen,
-                         seg_id=m["seg_id"], role=m["role"], turn=m["turn"], role_think=w.role_think,
-                         out=dout[b], lse=dlse[b])
+                         out=dout[b], lse=dlse[b], **mk)
             ho[b].copy_(dout[b], non_blocking=True)
             hl[b].copy_(dlse[b], non_blocking=True)
             comp_done[b].record(comp_s)
@@ -479,8 +477,9 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5, 6],
-                    help="workload number (2-5: the bf16 block-mask workloads; 6: strip-thinking with duplicated answers)")
+    ap.add_argument("--workload", type=int, default=5, choices=[2, 3, 4, 5, 6, 7, 8],
+                    help="workload number (2-5: the bf16 block-mask workloads; 6: strip-thinking with "
+                         "duplicated answers; 7: non-causal varlen; 8: dense causal+document+padding)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="time budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -16,7 +16,8 @@ c_void_p = ctypes.c_void_p
 
 
 class AttnMaskParams(ctypes.Structure):
-    _fields_ = [("role_think", c_int32)]
+    """Mirror of ``attn_mask_params``."""
+    _fields_ = [("role_think", c_int32), ("dense_bits", c_void_p), ("dense_offsets", c_void_p)]
 
 
 class AttnBlockMask(ctypes.Structure):
@@ -33,6 +34,8 @@ class AttnBlockMask(ctypes.Structure):
         ("max_qtiles", c_int32),
         ("max_ktiles", c_int32),
         ("cu_seqlens", c_void_p),
+        ("dense_bits", c_void_p),
+        ("dense_offsets", c_void_p),
         ("workspace", c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("off_header", ctypes.c_uint64),

@@ -20,7 +20,7 @@ STATUS = {
     6: "ATTN_ERR_DEVICE_TIMEOUT", 7: "ATTN_ERR_DEVICE_INVALID_INPUT",
 }
 MASK_KINDS = {"causal": 0, "causal_document": 1, "shared_prefix": 2, "strip_thinking": 3,
-              "strip_thinking_dup": 4}
+              "strip_thinking_dup": 4, "none": 5, "dense": 6}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 TILE_EMPTY, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 BLOCK_M = BLOCK_N = 128
@@ -126,23 +126,29 @@ class BlockMask:
         }
 
 
+def _params(role_think: int, dense_bits, dense_offsets) -> "_native.AttnMaskParams":
+    return _native.AttnMaskParams(role_think, _ptr(dense_bits), _ptr(dense_offsets))
+
+
 def attn_block_mask_build(kind, cu_seqlens: torch.Tensor, total_tokens: int, max_seqlen: int,
                           seg_id: Optional[torch.Tensor] = None, role: Optional[torch.Tensor] = None,
                           turn: Optional[torch.Tensor] = None, role_think: int = 1,
-                          workspace: Optional[torch.Tensor] = None, stream=None) -> BlockMask:
+                          workspace: Optional[torch.Tensor] = None, stream=None,
+                          dense_bits: Optional[torch.Tensor] = None,
+                          dense_offsets: Optional[torch.Tensor] = None) -> BlockMask:
     """Build the block mask on the device (asynchronous on ``stream``)."""
     batch = cu_seqlens.numel() - 1
     need = attn_block_mask_workspace_size(batch, total_tokens, max_seqlen)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=cu_seqlens.device)
-    params = _native.AttnMaskParams(role_think)
+    params = _params(role_think, dense_bits, dense_offsets)
     out = _native.AttnBlockMask()
     _check(_native.lib().attn_block_mask_build(
         _kind(kind), ctypes.byref(params), _ptr(cu_seqlens), batch, total_tokens, max_seqlen,
         _ptr(seg_id), _ptr(role), _ptr(turn), BLOCK_M, BLOCK_N, _ptr(workspace),
         workspace.numel() * workspace.element_size(), ctypes.byref(out), _stream(stream)),
         "attn_block_mask_build")
-    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn))
+    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets))
 
 
 def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: int,
@@ -150,7 +156,8 @@ def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: 
                                   seg_id: Optional[torch.Tensor] = None,
                                   role: Optional[torch.Tensor] = None,
                                   turn: Optional[torch.Tensor] = None, role_think: int = 1,
-                                  stream=None) -> BlockMask:
+                                  stream=None, dense_bits: Optional[torch.Tensor] = None,
+                                  dense_offsets: Optional[torch.Tensor] = None) -> BlockMask:
     """Block-mask build that allocates nothing, for callers that cannot.
 
     The caller passes the output buffer ``workspace`` (at least
@@ -161,20 +168,21 @@ def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: 
     the arrays the forward reads are stored (``labels`` is not).
     """
     batch = cu_seqlens.numel() - 1
-    params = _native.AttnMaskParams(role_think)
+    params = _params(role_think, dense_bits, dense_offsets)
     out = _native.AttnBlockMask()
     _check(_native.lib().attn_block_mask_build_noalloc(
         _kind(kind), ctypes.byref(params), _ptr(cu_seqlens), batch, total_tokens, max_seqlen,
         _ptr(seg_id), _ptr(role), _ptr(turn), BLOCK_M, BLOCK_N, _ptr(workspace),
         workspace.numel() * workspace.element_size(), ctypes.byref(out), _stream(stream)),
         "attn_block_mask_build_noalloc")
-    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn))
+    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets))
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, kind,
              cu_seqlens: torch.Tensor, max_seqlen: int, seg_id=None, role=None, turn=None,
              role_think: int = 1, scale: float = 0.0, out: Optional[torch.Tensor] = None,
-             lse: Optional[torch.Tensor] = None, stream=None):
+             lse: Optional[torch.Tensor] = None, stream=None,
+             dense_bits: Optional[torch.Tensor] = None, dense_offsets: Optional[torch.Tensor] = None):
     """Masked attention forward; returns (O [T, H, D], LSE [H, T] fp32)."""
     T, H, D = q.shape
     if out is None:
@@ -183,7 +191,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, k
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
     if q.dtype not in DTYPES:
         raise AttnError(1, "attn_fwd: dtype must be bfloat16 or float32")
-    params = _native.AttnMaskParams(role_think)
+    params = _params(role_think, dense_bits, dense_offsets)
     _check(_native.lib().attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), DTYPES[q.dtype], T, H, D, float(scale),
         _ptr(cu_seqlens), cu_seqlens.numel() - 1, max_seqlen, _kind(kind), ctypes.byref(params),
@@ -205,7 +213,8 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              max_seqlen: int, seg_id=None, role=None, turn=None, role_think: int = 1,
              scale: float = 0.0, dq: Optional[torch.Tensor] = None,
              dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None, stream=None):
+             workspace: Optional[torch.Tensor] = None, stream=None,
+             dense_bits: Optional[torch.Tensor] = None, dense_offsets: Optional[torch.Tensor] = None):
     """Masked attention backward (bf16); returns (dQ, dK, dV), each [T, H, D].
 
     ``workspace`` (uint8, device) defaults to a fresh buffer of
@@ -219,7 +228,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
         workspace = torch.empty(attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=q.device)
-    params = _native.AttnMaskParams(role_think)
+    params = _params(role_think, dense_bits, dense_offsets)
     _check(_native.lib().attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         DTYPES[q.dtype], T, H, D, float(scale), _ptr(cu_seqlens), cu_seqlens.numel() - 1,

@@ -52,11 +52,11 @@ bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out) {
   return true;
 }
 
-bool bwd_layout(int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out) {
+bool bwd_layout(int kind, int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out) {
   BmLayout bl;
   if (num_heads < 1 || !bm_layout(batch, total_tokens, max_seqlen, &bl)) return false;
   const uint64_t nq = uint64_t(bl.max_qt), nk = uint64_t(bl.max_nt);
-  uint64_t e = (nq * (nk + 1) + 1) / 2;
+  uint64_t e = kind_causal(kind) ? (nq * (nk + 1) + 1) / 2 : nq * nk;
   if (e > nq * nk) e = nq * nk;
   if (e > uint64_t(INT_MAX)) return false;
   BwdLayout l;
@@ -108,7 +108,21 @@ bool role_think_valid(int kind, const attn_mask_params* params) {
   return kind != ATTN_MASK_STRIP_THINKING_DUP || (rt != 2 && rt != 3);
 }
 
-static bool valid_kind(int kind) { return kind >= ATTN_MASK_CAUSAL && kind <= ATTN_MASK_STRIP_THINKING_DUP; }
+// ATTN_MASK_DENSE needs its bit rows and offsets (8-byte aligned offsets).
+bool dense_valid(int kind, const attn_mask_params* params) {
+  if (kind != ATTN_MASK_DENSE) return true;
+  return params && params->dense_bits && params->dense_offsets &&
+         (reinterpret_cast<uintptr_t>(params->dense_bits) & 3u) == 0 &&
+         (reinterpret_cast<uintptr_t>(params->dense_offsets) & 7u) == 0;
+}
+
+// A DENSE mask is used with the bits it was built from.
+static bool dense_matches(int kind, const attn_mask_params* params, const attn_block_mask* bm) {
+  if (kind != ATTN_MASK_DENSE) return true;
+  return params && params->dense_bits == bm->dense_bits && params->dense_offsets == bm->dense_offsets;
+}
+
+static bool valid_kind(int kind) { return kind >= ATTN_MASK_CAUSAL && kind <= ATTN_MASK_DENSE; }
 
 static bool metadata_present(int kind, const int32_t* seg, const int8_t* role, const int32_t* turn) {
   switch (kind) {
@@ -166,7 +180,7 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   if (!valid_kind(kind) || batch < 1 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
   if (block_m != kTile || block_n != kTile) return ATTN_ERR_UNSUPPORTED;
   if (!metadata_present(kind, seg_id, role, turn)) return ATTN_ERR_INVALID_ARG;
-  if (!role_think_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
+  if (!role_think_valid(kind, params) || !dense_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   BmLayout l;
   if (!bm_layout(batch, total_tokens, max_seqlen, &l)) return ATTN_ERR_INVALID_ARG;
@@ -177,6 +191,10 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   bm.magic = kMaskMagic;
   bm.kind = kind;
   bm.role_think = params ? params->role_think : 1;
+  if (kind == ATTN_MASK_DENSE) {
+    bm.dense_bits = params->dense_bits;
+    bm.dense_offsets = params->dense_offsets;
+  }
   bm.batch = batch;
   bm.total_tokens = total_tokens;
   bm.max_seqlen = max_seqlen;
@@ -207,7 +225,7 @@ attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_params* p
   bm.off_qlabel = l.qlabel;
   bm.off_korder = l.korder;
 
-  MaskArgs m{kind, bm.role_think, seg_id, role, turn};
+  MaskArgs m{kind, bm.role_think, seg_id, role, turn, bm.dense_bits, bm.dense_offsets};
   cudaError_t e = launch_block_mask_build(make_view(&bm), m, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_cuda_error(e, "attn_block_mask_build launch");
   *out = bm;
@@ -233,7 +251,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const int role_think = params ? params->role_think : 1;
   if (bm->magic != kMaskMagic || bm->kind != kind || bm->cu_seqlens != cu_seqlens ||
       bm->batch != batch || bm->total_tokens != total_tokens || bm->max_seqlen != max_seqlen ||
-      bm->role_think != role_think || bm->block_m != kTile || bm->block_n != kTile)
+      bm->role_think != role_think || bm->block_m != kTile || bm->block_n != kTile ||
+      !dense_matches(kind, params, bm))
     return ATTN_ERR_MASK_MISMATCH;
   if (uint64_t(total_tokens) * uint64_t(num_heads) * uint64_t(head_dim) > (uint64_t(1) << 40))
     return ATTN_ERR_UNSUPPORTED;
@@ -250,7 +269,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   a.head_dim = head_dim;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(float(head_dim));
   a.bm = make_view(bm);
-  a.mask = MaskArgs{kind, role_think, seg_id, role, turn};
+  a.mask = MaskArgs{kind, role_think, seg_id, role, turn, bm->dense_bits, bm->dense_offsets};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return dtype == ATTN_DTYPE_BF16 ? launch_attn_fwd_bf16(a, s) : launch_attn_fwd_f32(a, s);
 }
@@ -258,7 +277,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads, size_t* bytes) {
   if (bm == nullptr || bytes == nullptr || num_heads < 1) return ATTN_ERR_INVALID_ARG;
   BwdLayout l;
-  if (!bwd_layout(bm->batch, bm->total_tokens, bm->max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
+  if (!bwd_layout(bm->kind, bm->batch, bm->total_tokens, bm->max_seqlen, num_heads, &l))
+    return ATTN_ERR_INVALID_ARG;
   if (l.total > uint64_t(SIZE_MAX)) return ATTN_ERR_INVALID_ARG;
   *bytes = size_t(l.total);
   return ATTN_OK;
@@ -287,12 +307,13 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   const int role_think = params ? params->role_think : 1;
   if (bm->magic != kMaskMagic || bm->kind != kind || bm->cu_seqlens != cu_seqlens ||
       bm->batch != batch || bm->total_tokens != total_tokens || bm->max_seqlen != max_seqlen ||
-      bm->role_think != role_think || bm->block_m != kTile || bm->block_n != kTile)
+      bm->role_think != role_think || bm->block_m != kTile || bm->block_n != kTile ||
+      !dense_matches(kind, params, bm))
     return ATTN_ERR_MASK_MISMATCH;
   if (uint64_t(total_tokens) * uint64_t(num_heads) * uint64_t(head_dim) > (uint64_t(1) << 40))
     return ATTN_ERR_UNSUPPORTED;
   BwdLayout l;
-  if (!bwd_layout(batch, total_tokens, max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
+  if (!bwd_layout(kind, batch, total_tokens, max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
   if (uint64_t(workspace_bytes) < l.ds + l.ds_per_head) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   if (total_tokens == 0) return ATTN_OK;
 
@@ -315,7 +336,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.head_dim = head_dim;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(float(head_dim));
   a.bm = make_view(bm);
-  a.mask = MaskArgs{kind, role_think, seg_id, role, turn};
+  a.mask = MaskArgs{kind, role_think, seg_id, role, turn, bm->dense_bits, bm->dense_offsets};
   return launch_attn_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

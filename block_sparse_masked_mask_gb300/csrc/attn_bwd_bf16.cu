@@ -122,7 +122,7 @@ constexpr int kDsBlock = kTile * kTile * 2;
 
 // One work item: a tile of one sequence and one head, and its list.
 struct BwdItem {
-  int h, s0, L, i0, e0, e1;  // i0: first row of the item's tile, local to the sequence
+  int h, s0, L, i0, e0, e1, b;  // i0: first row of the item's tile, local to the sequence
 };
 
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
@@ -135,6 +135,7 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int 
   it.i0 = p.qt_idx[g] * kTile;
   it.e0 = p.off[g];
   it.e1 = p.off[g + 1];
+  it.b = b;
   return it;
 }
 
@@ -146,6 +147,7 @@ __device__ __forceinline__ void bwd_store(volatile int* d, const BwdItem& it, bo
   d[4] = it.i0;
   d[5] = it.e0;
   d[6] = it.e1;
+  d[7] = it.b;
 }
 __device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
   if (!d[0]) return false;
@@ -155,6 +157,7 @@ __device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
   it.i0 = d[4];
   it.e0 = d[5];
   it.e1 = d[6];
+  it.b = d[7];
   return true;
 }
 
@@ -718,7 +721,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         lab = r >= 0 ? s_lab[r] : __ldg(p.label + e);
         a0 = ix * kTile;
         an = min(kTile, it.L - a0);
-        const bool codes = p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL;
+        const bool codes = kind_codes(p.mask.kind) && lab == ATTN_TILE_PARTIAL;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int c = lane + 32 * m;
@@ -762,7 +765,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         {
           float* sl = reinterpret_cast<float*>(side + qs * C::SIDE_WORDS);
-          const bool codes = p.mask.kind != ATTN_MASK_CAUSAL && clab == ATTN_TILE_PARTIAL;
+          const bool codes = kind_codes(p.mask.kind) && clab == ATTN_TILE_PARTIAL;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const int c = lane + 32 * m;
@@ -883,7 +886,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int kn = min(kTile, it.L - it.i0);
       const bool row_in = r < kn;
       const int kl = it.i0 + r;  // local key index
-      const int kcode = (row_in && kind != ATTN_MASK_CAUSAL) ? key_code(p.mask, it.s0 + kl) : 0;
+      const int kcode = (row_in && kind_codes(kind)) ? key_code(p.mask, it.s0 + kl) : 0;
+      const int kbase = it.i0 + qd * 32;  // the warp's first key (local), a multiple of 32
       // keys of a warp usually share one code: then a query's visibility is the
       // same for all of them, and one ballot over the queries' codes gives a word
       const int kcode_w = __shfl_sync(0xffffffffu, kcode, 0);
@@ -901,6 +905,16 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         const int qs = nload % C::NSLOT;
         nload += 2;
+        // the dense kind: each lane loads the caller's word of query row
+        // a0 + 64 hf + 32 m + lane over the warp's 32 keys, before the wait
+        uint32_t dw[2] = {0u, 0u};
+        if (kind == ATTN_MASK_DENSE && lab == ATTN_TILE_PARTIAL && kbase < it.L) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int qrow = a0 + 64 * hf + 32 * m + lane;
+            if (qrow < it.L) dw[m] = dense_word(p.mask, it.b, it.L, qrow, kbase >> 5);
+          }
+        }
         if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
         ptx::tc_fence_after();
         // the q-tile's LSE, D and codes came with Q(i): its load has landed
@@ -919,9 +933,23 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             const int c0 = 64 * hf + 32 * m;
-            vis[m] = lab == ATTN_TILE_PARTIAL ? ~prefix_bits(lo - c0) & prefix_bits(an - c0) : prefix_bits(an - c0);
+            vis[m] = lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? ~prefix_bits(lo - c0) & prefix_bits(an - c0)
+                                                                   : prefix_bits(an - c0);
           }
-          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+          if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
+            // transpose the 32 x 32 bit block: ballot j gathers bit j (key
+            // lane j) of every lane's (query's) word, and lane j keeps it
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              uint32_t mine = 0u;
+#pragma unroll 4
+              for (int j = 0; j < 32; ++j) {
+                const uint32_t t = __ballot_sync(0xffffffffu, (dw[m] >> j) & 1u);
+                mine = lane == j ? t : mine;
+              }
+              vis[m] &= mine;
+            }
+          } else if (lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
             const int* qc = side + qs * C::SIDE_WORDS + 2 * kTile + 64 * hf;
             if (uniform_k) {
 #pragma unroll

@@ -102,7 +102,7 @@ struct FwdParams {
 // One work item: a q-tile of one sequence and one head; its k-tile list is
 // entries e0 .. e1 of the CSR arrays.
 struct Item {
-  int h, s0, L, qi0, e0, e1;
+  int h, s0, L, qi0, e0, e1, b;
 };
 
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_qt) {
@@ -115,6 +115,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_
   it.qi0 = p.qt_idx[g] * kTile;  // first query row of the q-tile, local to the sequence
   it.e0 = p.koff[g];
   it.e1 = p.koff[g + 1];
+  it.b = b;
   return it;
 }
 
@@ -127,6 +128,7 @@ __device__ __forceinline__ void store_item(volatile int* d, const Item& it, bool
   d[4] = it.qi0;
   d[5] = it.e0;
   d[6] = it.e1;
+  d[7] = it.b;
 }
 __device__ __forceinline__ bool load_item(const volatile int* d, Item& it) {
   if (!d[0]) return false;
@@ -136,6 +138,7 @@ __device__ __forceinline__ bool load_item(const volatile int* d, Item& it) {
   it.qi0 = d[4];
   it.e0 = d[5];
   it.e1 = d[6];
+  it.b = d[7];
   return true;
 }
 
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = it.e0; e < it.e1; ++e) {
         const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, it.L - j0);
         const int lab = __ldg(p.klabel + e);
-        if (p.mask.kind != ATTN_MASK_CAUSAL && lab == ATTN_TILE_PARTIAL) {
+        if (kind_codes(p.mask.kind) && lab == ATTN_TILE_PARTIAL) {
           // Keys' mask codes for the softmax of a PARTIAL tile, in buffer up % NCODE
           // once the softmax is done with the buffer's previous PARTIAL entry.
           const int cb = up % C::NCODE;
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_in = r < qn;
       const int il = it.qi0 + r;               // local query index
       const int s0 = it.s0, L = it.L;
-      const int qcode = (row_in && kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
+      const int qcode = (row_in && kind_codes(kind)) ? query_code(p.mask, s0 + il) : 0;
       // The rows of a warp usually share one query code (one document, one
       // turn).  A key's visibility is then the same for all of them, and one
       // ballot over the keys' codes replaces 32 tests per row.
@@ -492,6 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = it.e0; e < it.e1; ++e) {
         const int j0 = __ldg(p.kidx + e) * kTile, kn = min(kTile, L - j0);
         const int lab = __ldg(p.klabel + e);
+        // the dense kind's bits of this row for a PARTIAL tile, loaded before
+        // the wait for the scores so that their latency hides behind it
+        uint32_t dwords[2] = {0u, 0u};
+        if (kind == ATTN_MASK_DENSE && lab == ATTN_TILE_PARTIAL && row_in) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (64 * hf + 32 * q < kn) dwords[q] = dense_word(p.mask, it.b, L, il, ((j0 + 64 * hf) >> 5) + q);
+        }
         const int sb = nsf % 3, xb = nsf & 1;
         const uint32_t col_s = C::col_s(sb) + 64u * hf;  // this half's 64 score columns; its P goes
                                                          // over the first 32 of them
@@ -509,10 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lab == ATTN_TILE_PARTIAL || kn < kTile) {
           // bit c of vis[c / 32]: key column 64 * hf + c is visible to this row.
           // Causal part and bounds: columns below upto; PARTIAL tiles of the
-          // metadata kinds also AND in the per-key predicate.
-          const int upto = (lab == ATTN_TILE_PARTIAL ? min(kn, il - j0 + 1) : kn) - 64 * hf;
+          // metadata kinds also AND in the per-key predicate, those of the
+          // dense kind the caller's bits.
+          const int upto = (lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? min(kn, il - j0 + 1) : kn) - 64 * hf;
           uint32_t vis[2] = {prefix_bits(upto), prefix_bits(upto - 32)};
-          if (lab == ATTN_TILE_PARTIAL && kind != ATTN_MASK_CAUSAL) {
+          if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
+            vis[0] &= dwords[0];  // zero for rows past the end
+            vis[1] &= dwords[1];
+          } else if (lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
             // the K producer staged this entry's key codes
             const int cb = up % C::NCODE;
             if (!warp_wait(bar(C::B_CODE + cb), uint32_t(up / C::NCODE) & 1u, abort_flag, err, 9)) {

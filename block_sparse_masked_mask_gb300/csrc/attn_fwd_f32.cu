@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const F32Params p) {
     const int rr = x / D, d = x % D;
     sQ[rr * DP + d] = rr < qn ? p.q[(size_t(s0 + i0 + rr) * p.H + h) * D + d] : 0.f;
   }
-  const int qcode = (row_in && p.mask.kind != ATTN_MASK_CAUSAL) ? query_code(p.mask, s0 + il) : 0;
+  const int qcode = (row_in && kind_codes(p.mask.kind)) ? query_code(p.mask, s0 + il) : 0;
+  const bool causal = kind_causal(p.mask.kind), dense = p.mask.kind == ATTN_MASK_DENSE;
   const float c2 = p.scale_log2;
   float m = -INFINITY, l = 0.f;
   float acc[D];
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const F32Params p) {
         sV[x] = c < cn ? p.v[src] : 0.f;
       }
       if (threadIdx.x < kChunk)
-        sCode[threadIdx.x] = (partial && threadIdx.x < cn && p.mask.kind != ATTN_MASK_CAUSAL)
+        sCode[threadIdx.x] = (partial && threadIdx.x < cn && kind_codes(p.mask.kind))
                                  ? key_code(p.mask, s0 + j0 + c0 + threadIdx.x) : 0;
       __syncthreads();
       float* srow = sS + r * (kChunk + 1);
@@ -91,7 +92,11 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const F32Params p) {
 #pragma unroll
         for (int d = 0; d < D; ++d) dot = fmaf(sQ[r * DP + d], sK[c * D + d], dot);
         bool vis = c < cn;
-        if (partial) vis = vis && (j0 + c0 + c <= il) && code_visible(p.mask.kind, qcode, sCode[c]);
+        if (partial && dense) {
+          vis = vis && row_in && ((dense_word(p.mask, b, L, il, (j0 + c0 + c) >> 5) >> ((j0 + c0 + c) & 31)) & 1u);
+        } else if (partial) {
+          vis = vis && (!causal || j0 + c0 + c <= il) && code_visible(p.mask.kind, qcode, sCode[c]);
+        }
         const float sc = vis ? dot * c2 : -INFINITY;
         srow[c] = sc;
         mx = fmaxf(mx, sc);

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(1024) bm_prepare_kernel(BmView v) {
 //                   (bit c for class c of dup_class)
 __global__ void __launch_bounds__(128) bm_summary_kernel(BmView v, MaskArgs m) {
   const int g = blockIdx.x;
-  if (g >= v.header[kHdrQtiles] || m.kind == ATTN_MASK_CAUSAL) return;
+  if (g >= v.header[kHdrQtiles] || !kind_codes(m.kind)) return;
   __shared__ int s_red[4][8];
   const int b = v.qt_seq[g], a = v.qt_idx[g];
   const int s0 = v.cu[b], L = v.cu[b + 1] - s0;
@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(128) bm_summary_kernel(BmView v, MaskArgs m) {
 // summaries prove it, else kUnknown.  Every rule is a sufficient condition.
 __device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
                                       const int* sq, const int* sk) {
+  if (kind == ATTN_MASK_NONE) return ATTN_TILE_FULL;
   if (j0 > i1) return ATTN_TILE_EMPTY;           // every key after every query
   const bool all_causal = j1 <= i0;              // every key at or before every query
   switch (kind) {
@@ -259,6 +260,26 @@ __device__ __forceinline__ int decide(int kind, int i0, int i1, int j0, int j1,
   return kUnknown;
 }
 
+// ATTN_MASK_DENSE: the label of q-tile rows i0 .. i0+qn-1 against k-tile bt,
+// by counting the caller's bits (one thread per k-tile, so a warp's loads of
+// one row are contiguous); bits past the sequence end do not count.
+__device__ __forceinline__ int dense_label(const MaskArgs& m, int b, int L, int i0, int qn, int bt) {
+  const int j0 = bt * kTile, kn = min(kTile, L - j0);
+  uint32_t keep[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int n = kn - 32 * w;
+    keep[w] = n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
+  }
+  const int nw = (kn + 31) >> 5;
+  int cnt = 0;
+  for (int i = i0; i < i0 + qn; ++i)
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (w < nw) cnt += __popc(dense_word(m, b, L, i, (j0 >> 5) + w) & keep[w]);
+  return cnt == 0 ? ATTN_TILE_EMPTY : (cnt == qn * kn ? ATTN_TILE_FULL : ATTN_TILE_PARTIAL);
+}
+
 // One CTA per q-tile: labels of its whole row, and its non-EMPTY count.
 // Each thread decides one k-tile from the summaries; only the pairs the
 // summaries leave undecided are counted pair by pair, one at a time.
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
   const int qcode = row_in ? query_code(m, s0 + i0 + r) : 0;
   int sq[kSumInts];
   const int* qsum = v.summary + size_t(g) * kSumInts;
-  for (int i = 0; i < kSumInts; ++i) sq[i] = m.kind == ATTN_MASK_CAUSAL ? 0 : qsum[i];
+  for (int i = 0; i < kSumInts; ++i) sq[i] = kind_codes(m.kind) ? qsum[i] : 0;
   const int gbase = v.qt_off[b];
   uint8_t* row = v.labels + size_t(g) * v.max_nt;
   int n_empty = 0, n_partial = 0, n_full = 0;  // meaningful in thread 0
@@ -288,10 +309,12 @@ __global__ void __launch_bounds__(128) bm_classify_kernel(BmView v, MaskArgs m) 
     int lab = ATTN_TILE_EMPTY;
     if (r == 0) s_nunk = 0;
     __syncthreads();
-    if (bt < nt) {
+    if (bt < nt && m.kind == ATTN_MASK_DENSE) {
+      lab = dense_label(m, b, L, i0, qn, bt);
+    } else if (bt < nt) {
       int sk[kSumInts];
       const int* ks = v.summary + size_t(gbase + bt) * kSumInts;
-      for (int i = 0; i < kSumInts; ++i) sk[i] = m.kind == ATTN_MASK_CAUSAL ? 0 : ks[i];
+      for (int i = 0; i < kSumInts; ++i) sk[i] = kind_codes(m.kind) ? ks[i] : 0;
       const int j0 = bt * kTile, j1 = min(L, j0 + kTile) - 1;
       lab = decide(m.kind, i0, i1, j0, j1, sq, sk);
       if (lab == kUnknown) s_unknown[atomicAdd(&s_nunk, 1)] = r;

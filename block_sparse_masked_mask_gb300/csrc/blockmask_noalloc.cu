@@ -73,7 +73,7 @@ extern "C" attn_status attn_block_mask_build_noalloc(
     const int32_t* turn, int32_t block_m, int32_t block_n, void* workspace, size_t workspace_bytes,
     attn_block_mask* out, attn_stream_t stream) {
   if (out == nullptr || cu_seqlens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (kind < ATTN_MASK_CAUSAL || kind > ATTN_MASK_STRIP_THINKING_DUP || batch < 1 || total_tokens < 0 ||
+  if (kind < ATTN_MASK_CAUSAL || kind > ATTN_MASK_DENSE || batch < 1 || total_tokens < 0 ||
       max_seqlen < 0)
     return ATTN_ERR_INVALID_ARG;
   if (block_m != kTile || block_n != kTile) return ATTN_ERR_UNSUPPORTED;
@@ -82,7 +82,7 @@ extern "C" attn_status attn_block_mask_build_noalloc(
   if ((kind == ATTN_MASK_STRIP_THINKING || kind == ATTN_MASK_STRIP_THINKING_DUP) &&
       (role == nullptr || turn == nullptr))
     return ATTN_ERR_INVALID_ARG;
-  if (!role_think_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
+  if (!role_think_valid(kind, params) || !dense_valid(kind, params)) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
   BmLayout l;
   if (!bm_layout(batch, total_tokens, max_seqlen, &l)) return ATTN_ERR_INVALID_ARG;
@@ -106,6 +106,10 @@ extern "C" attn_status attn_block_mask_build_noalloc(
   bm.magic = kMaskMagic;
   bm.kind = kind;
   bm.role_think = params ? params->role_think : 1;
+  if (kind == ATTN_MASK_DENSE) {
+    bm.dense_bits = params->dense_bits;
+    bm.dense_offsets = params->dense_offsets;
+  }
   bm.batch = batch;
   bm.total_tokens = total_tokens;
   bm.max_seqlen = max_seqlen;
@@ -167,7 +171,7 @@ extern "C" attn_status attn_block_mask_build_noalloc(
   v.total_tokens = total_tokens;
   v.max_seqlen = max_seqlen;
 
-  MaskArgs m{kind, bm.role_think, seg_id, role, turn};
+  MaskArgs m{kind, bm.role_think, seg_id, role, turn, bm.dense_bits, bm.dense_offsets};
   e = launch_block_mask_build(v, m, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return record_cuda_error(e, "attn_block_mask_build_noalloc launch");
   *out = bm;

@@ -44,6 +44,8 @@ struct BmLayout {
 
 // False when a STRIP_THINKING_DUP mask names role 2 or 3 as THINK.
 bool role_think_valid(int kind, const attn_mask_params* params);
+// False when a DENSE mask lacks its bits or offsets (or they are misaligned).
+bool dense_valid(int kind, const attn_mask_params* params);
 
 // Returns false on overflow / invalid sizes.
 bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out);
@@ -80,7 +82,22 @@ struct MaskArgs {
   const int32_t* seg;
   const int8_t* role;
   const int32_t* turn;
+  const uint32_t* bits;    // ATTN_MASK_DENSE: the caller's bit rows
+  const int64_t* bit_off;  // ATTN_MASK_DENSE: first word of each sequence
 };
+
+// Kinds that only keep keys at or before the query.
+__host__ __device__ constexpr bool kind_causal(int kind) { return kind <= ATTN_MASK_STRIP_THINKING_DUP; }
+// Kinds whose PARTIAL tiles are decided by per-token codes (below).
+__host__ __device__ constexpr bool kind_codes(int kind) {
+  return kind >= ATTN_MASK_CAUSAL_DOCUMENT && kind <= ATTN_MASK_STRIP_THINKING_DUP;
+}
+
+// ATTN_MASK_DENSE: word jw (keys 32 jw .. 32 jw + 31) of local row i of
+// sequence b, whose length is L.
+__device__ __forceinline__ uint32_t dense_word(const MaskArgs& m, int b, int L, int i, int jw) {
+  return __ldg(m.bits + m.bit_off[b] + int64_t(i) * ((L + 31) >> 5) + jw);
+}
 
 // The four predicates factor as  (ki <= qi) && code_visible(qcode(qi), kcode(ki)):
 //   causal          : always true
@@ -164,13 +181,14 @@ attn_status launch_attn_fwd_f32(const FwdArgs& a, cudaStream_t s);
 // Byte layout of the backward's workspace: D = rowsum(dO * O) as fp32 [H, T],
 // the k-major position of every q-major tile entry, then the dS blocks
 // (128 x 128 bf16 per entry and head) of as many heads as fit.  e_bound bounds
-// the entries of any mask of these sizes: every kind keeps only keys at or
-// before the query, so a sequence of n tiles has at most n (n + 1) / 2 pairs.
+// the entries of any mask of these sizes and kind: a causal kind keeps only
+// keys at or before the query, so a sequence of n tiles has at most
+// n (n + 1) / 2 pairs; the others up to n^2.
 struct BwdLayout {
   uint64_t delta = 0, kpos = 0, ds = 0, ds_per_head = 0, total = 0;
   int e_bound = 0;
 };
-bool bwd_layout(int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out);
+bool bwd_layout(int kind, int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out);
 
 struct BwdArgs {
   const void* q;

@@ -100,6 +100,12 @@ class Workload:
                 "role": dev(self.role), "turn": dev(self.turn), "dense_bits": dev(bits),
                 "dense_offsets": dev(self.dense_offsets)}
 
+    def api_kwargs(self, dm: dict) -> dict:
+        """The mask keyword arguments of the library calls, from device_meta()."""
+        return {"seg_id": dm["seg_id"], "role": dm["role"], "turn": dm["turn"],
+                "role_think": self.role_think, "dense_bits": dm["dense_bits"],
+                "dense_offsets": dm["dense_offsets"]}
+
 
 WORKLOAD_NAMES = {
     1: "causal_s64_d32_fp32",
@@ -108,6 +114,8 @@ WORKLOAD_NAMES = {
     4: "strip_thinking_8turns",
     5: "causal_document_32k",
     6: "strip_thinking_dup_8turns",
+    7: "varlen_noncausal_8seq",
+    8: "dense_causal_document_padding_32k",
 }
 
 
@@ -137,10 +145,13 @@ def grad_output(w: Workload, seed: int = 1000) -> torch.Tensor:
 
 
 def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> Workload:
-    """Workload number ``c`` (1..6).  Workload 6 is workload 4's conversation
+    """Workload number ``c`` (1..8).  Workload 6 is workload 4's conversation
     with every answer span duplicated (user 128 / think 768 / answer 256 /
     answer history copy 256 per turn, 11264 tokens): the exact variant of
-    strip-thinking.
+    strip-thinking.  Workload 7 is workload 2's sequences without a mask
+    inside a sequence (the "none" kind).  Workload 8 is workload 5's 32768
+    tokens as a caller-supplied dense mask: causal, inside a document, and
+    with the last 2048 tokens padding (they neither attend nor are attended).
 
     ``document_form`` only matters for workload 5: ``"mask"`` is one packed
     sequence with the document index in ``seg`` and kind causal_document;
@@ -162,6 +173,19 @@ def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> 
         role, turn = strip_thinking_layout([(128, 768, 256)] * 8)
         w = Workload(WORKLOAD_NAMES[4], "strip_thinking", _cu([len(role)]), 32, 128,
                      torch.bfloat16, sigma=0.5, role=role, turn=turn, seed=c)
+    elif c == 7:
+        lens = torch.randint(128, 2049, (8,), generator=torch.Generator().manual_seed(2)).tolist()
+        w = Workload(WORKLOAD_NAMES[7], "none", _cu(lens), 16, 128, torch.bfloat16, seed=c)
+    elif c == 8:
+        g5 = torch.Generator().manual_seed(5)
+        cuts = torch.randint(0, 26625, (11,), generator=g5).sort().values.tolist()
+        bounds = [0] + cuts + [26624]
+        lens = [bounds[i + 1] - bounds[i] + 512 for i in range(12)]
+        seg = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lens)])
+        seg[-2048:] = -1  # padding
+        bits, offs = causal_document_padding_bits(seg)
+        w = Workload(WORKLOAD_NAMES[8], "dense", _cu([len(seg)]), 32, 128, torch.bfloat16,
+                     seg=None, dense_bits=bits, dense_offsets=offs, seed=c)
     elif c == 6:
         role, turn = strip_thinking_dup_layout([(128, 768, 256)] * 8)
         w = Workload(WORKLOAD_NAMES[6], "strip_thinking_dup", _cu([len(role)]), 32, 128,
@@ -180,7 +204,7 @@ def make_workload(c: int, tensors: bool = True, document_form: str = "mask") -> 
         else:
             raise ValueError(document_form)
     else:
-        raise ValueError(f"workload number must be 1..6, got {c}")
+        raise ValueError(f"workload number must be 1..8, got {c}")
     if tensors:
         _fill_tensors(w, g)
     return w
@@ -268,6 +292,20 @@ def pack_rows(rows: np.ndarray, pad_rng: Optional[np.random.Generator] = None) -
     if pad_rng is not None and W * 32 > L:
         full[:, L:] = pad_rng.random((R, W * 32 - L)) < 0.5
     return np.packbits(full, axis=1, bitorder="little").view(np.uint32).reshape(R, W)
+
+
+def causal_document_padding_bits(seg: np.ndarray, block: int = 128):
+    """A caller's dense mask for one sequence composed as the pages' causal +
+    document + padding: key at or before the query, same document id, and
+    neither token padding (id < 0).  Returns (bits uint32, offsets int64 [2])."""
+    L = len(seg)
+    rows = []
+    for r0 in range(0, L, block):
+        qi = np.arange(r0, min(L, r0 + block))[:, None]
+        ki = np.arange(L)[None, :]
+        m = (ki <= qi) & (seg[ki] == seg[qi]) & (seg[ki] >= 0) & (seg[qi] >= 0)
+        rows.append(pack_rows(m).ravel())
+    return np.concatenate(rows).astype(np.uint32), dense_offsets([L])
 
 
 def random_dense_mask(rng: np.random.Generator, lengths, tile: int = 128):

@@ -35,6 +35,19 @@
  *                              the query ANSWER; ANSWER_HISTORY of an earlier
  *                              turn, or of the query's turn with the query
  *                              ANSWER_HISTORY.  role_think must not be 2 or 3.
+ *   ATTN_MASK_NONE             every key of the sequence (no mask inside a
+ *                              sequence; "Triton from first principles"
+ *                              Ch. 21, Section 21.1, the plain kernel)
+ *   ATTN_MASK_DENSE            the caller's bits (attn_mask_params.dense_bits):
+ *                              any pattern, e.g. causal + document + padding
+ *                              composed by the caller (xorl issue, "Current
+ *                              state in this tree", make_causal_block_mask).
+ *                              Sequence b's rows are L = cu[b+1] - cu[b] rows
+ *                              of ceil(L / 32) uint32 words starting at word
+ *                              dense_offsets[b]; key j of row i is bit j % 32
+ *                              of word j / 32 of row i, 1 = visible; bits past
+ *                              a row's end are ignored.
+ * Rows that see no key get O = 0 and LSE = -inf (possible only for DENSE).
  *
  * Tiles
  *   Each sequence is cut into 128-token tiles starting at its first token.
@@ -94,7 +107,9 @@ typedef enum attn_mask_kind {
   ATTN_MASK_CAUSAL_DOCUMENT = 1,
   ATTN_MASK_SHARED_PREFIX = 2,
   ATTN_MASK_STRIP_THINKING = 3,
-  ATTN_MASK_STRIP_THINKING_DUP = 4
+  ATTN_MASK_STRIP_THINKING_DUP = 4,
+  ATTN_MASK_NONE = 5,
+  ATTN_MASK_DENSE = 6
 } attn_mask_kind;
 
 typedef enum attn_dtype {
@@ -113,6 +128,9 @@ typedef enum attn_dtype {
 
 typedef struct attn_mask_params {
   int32_t role_think; /* role code of THINK tokens for the STRIP_THINKING kinds (default 1) */
+  const uint32_t* dense_bits;    /* device, ATTN_MASK_DENSE only: the bit rows */
+  const int64_t* dense_offsets;  /* device int64[batch + 1], ATTN_MASK_DENSE only: first
+                                    word of each sequence's rows */
 } attn_mask_params;
 
 /*
@@ -165,6 +183,8 @@ typedef struct attn_block_mask {
   int32_t max_qtiles;      /* NQ = ceil(total_tokens / block_m) + batch */
   int32_t max_ktiles;      /* NK = ceil(max_seqlen / block_n) */
   const int32_t* cu_seqlens; /* device pointer the mask was built from */
+  const uint32_t* dense_bits;    /* ATTN_MASK_DENSE: the params it was built from */
+  const int64_t* dense_offsets;
   void* workspace;
   size_t workspace_bytes;
   uint64_t off_header, off_qt_seq, off_qt_idx, off_labels, off_kcount, off_koff,
@@ -188,8 +208,9 @@ ATTN_API attn_status attn_block_mask_workspace_size(int32_t batch, int32_t total
  * cu_seqlens[batch] = total_tokens, every length <= max_seqlen) and the
  * per-token metadata the kind needs (device arrays of total_tokens entries):
  *   CAUSAL: none; CAUSAL_DOCUMENT and SHARED_PREFIX: seg_id;
- *   STRIP_THINKING and STRIP_THINKING_DUP: role and turn.  Unused pointers
- *   may be NULL.
+ *   STRIP_THINKING and STRIP_THINKING_DUP: role and turn; NONE: none; DENSE:
+ *   params->dense_bits and params->dense_offsets.  Unused pointers may be
+ *   NULL.
  * The mask is built once and can be reused by any number of attn_fwd calls
  * while the metadata does not change (xorl issue, Proposed work, item 3:
  * masks compiled and cached across steps).  It follows the forward (q-major)
@@ -220,7 +241,8 @@ ATTN_API attn_status attn_block_mask_build(attn_mask_kind kind, const attn_mask_
  *   scale     score scale; 0 means 1/sqrt(head_dim)
  *   cu_seqlens, batch, max_seqlen, kind, params, seg_id, role, turn: the same
  *             values the block mask was built from (checked: kind, the
- *             cu_seqlens pointer, batch, total_tokens, max_seqlen, role_think)
+ *             cu_seqlens pointer, batch, total_tokens, max_seqlen, role_think,
+ *             and for DENSE the two dense pointers)
  *   bm        the block mask from attn_block_mask_build()
  * bf16 runs on the tensor cores (tcgen05, fp32 accumulation in tensor
  * memory, P rounded to bf16 for the P.V product, O rounded to nearest even);
@@ -243,9 +265,10 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  *   entry map                   int32 per tile entry: the position of each
  *                               q-major entry in the k-major lists
  *   dS blocks                   128 x 128 bf16 per tile entry and head
- * The entry count is bounded on the host from the mask's sizes (a sequence of
- * n tiles has at most n (n + 1) / 2 tile pairs with keys at or before the
- * query); only the entries the mask keeps are written and read.
+ * The entry count is bounded on the host from the mask's sizes and kind (a
+ * sequence of n tiles has at most n (n + 1) / 2 tile pairs with keys at or
+ * before the query under the causal kinds, n^2 under NONE and DENSE); only
+ * the entries the mask keeps are written and read.
  */
 ATTN_API attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads,
                                              size_t* bytes);

@@ -79,7 +79,7 @@ def test_build_rejects_bad_arguments_before_any_launch(native_lib):
     assert call(kind=2) == 1            # shared_prefix needs seg_id
     assert call(kind=3, role=_fake()) == 1  # strip_thinking needs role and turn
     assert call(kind=4, turn=_fake()) == 1  # so does its duplicated-answer variant
-    assert call(kind=5) == 1
+    assert call(kind=6) == 1                # dense needs its bits and offsets
     assert call(ws=_fake(0x20010)) == 1   # workspace not 256-byte aligned
     assert call(wsb=16) == 3             # workspace too small
 
@@ -175,6 +175,13 @@ def test_bwd_rejects_bad_arguments_before_any_launch(native_lib):
     # pairs of 32 KB per head, plus D's [H, T] fp32 (256-byte aligned)
     assert full - one == 5 * 128 * 128 * 2 + 1024
     assert call(bmref=bm2, wsb=one - 1) == 3
+    # without a causal restriction (the none and dense kinds) the bound is nq x nk
+    bm2.kind = 5
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, ctypes.byref(out)) == 0
+    full5 = out.value
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 1, ctypes.byref(out)) == 0
+    assert full5 - out.value == 6 * 128 * 128 * 2 + 1024
+    bm2.kind = 0
     assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 0, ctypes.byref(out)) == 1
     assert lib.attn_bwd_workspace_size(None, 2, ctypes.byref(out)) == 1
 

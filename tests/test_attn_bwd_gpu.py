@@ -31,8 +31,7 @@ MEAN_REL = 2.0 ** -8
 
 def build_mask(w, dm):
     return api.attn_block_mask_build(w.kind, dm["cu_seqlens"], w.total_tokens, w.max_seqlen,
-                                     seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"],
-                                     role_think=w.role_think)
+                                     **w.api_kwargs(dm))
 
 
 def run_bwd(w, do, q=None, k=None, v=None, bm=None, scale=0.0):
@@ -41,8 +40,7 @@ def run_bwd(w, do, q=None, k=None, v=None, bm=None, scale=0.0):
     q = (w.q if q is None else q).cuda()
     k = (w.k if k is None else k).cuda()
     v = (w.v if v is None else v).cuda()
-    kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think,
-              scale=scale)
+    kw = dict(w.api_kwargs(dm), scale=scale)
     o, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
     dq, dk, dv = api.attn_bwd(q, k, v, o, lse, do.cuda(), bm, w.kind, dm["cu_seqlens"],
                               w.max_seqlen, **kw)
@@ -134,7 +132,8 @@ def sample_rows(w, n=48, seed=0):
 @pytest.mark.parametrize("c,form,heads", [(2, "mask", (0, 15)),
                                           (3, "mask", (0, 31)), (4, "mask", (0, 31)),
                                           (5, "cu_seqlens", (0, 31)), (5, "mask", (31,)),
-                                          (6, "mask", (0, 31))])
+                                          (6, "mask", (0, 31)), (7, "mask", (0, 15)),
+                                          (8, "mask", (31,))])
 def test_full_size_workloads_sampled(c, form, heads):
     """The bf16 workloads at full size, on sampled query rows (dQ) and key rows
     (dK, dV) that the oracle computes one by one."""

@@ -17,7 +17,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 
-@pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_unmasked_pair_table_matches_oracle(c):
     w = W.make_workload(c, tensors=False)
     assert bench.UNMASKED_PAIRS[c] == oracle.unmasked_pairs(w.kind, w.cu_seqlens, w.meta())

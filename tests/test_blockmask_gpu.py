@@ -18,8 +18,7 @@ pytestmark = pytest.mark.gpu
 def build_on_gpu(w):
     dm = w.device_meta()
     bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], w.total_tokens, w.max_seqlen,
-                                   seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"],
-                                   role_think=w.role_think)
+                                   **w.api_kwargs(dm))
     assert api.attn_get_status(bm) == api.ATTN_OK
     return bm
 
@@ -59,7 +58,7 @@ def assert_matches_oracle(w, bm):
     assert np.array_equal(got["korder"].numpy(), oracle.lpt_order(wt["qcount"]))
 
 
-@pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("c", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_workload_masks_bit_exact(c):
     w = W.make_workload(c, tensors=False)
     assert_matches_oracle(w, build_on_gpu(w))
@@ -82,9 +81,10 @@ def test_random_metadata_bit_exact(kind, li):
     for seed in range(3):
         rng = np.random.default_rng(1000 * li + seed)
         lens = LENGTH_SETS[li]
-        seg, role, turn = W.random_metadata(rng, kind, lens)
+        m = W.random_meta(rng, kind, lens)
         w = W.Workload(f"rand_{kind}", kind, W._cu(lens), 1, 128, torch.bfloat16,
-                       seg=seg, role=role, turn=turn)
+                       seg=m["seg"], role=m["role"], turn=m["turn"], dense_bits=m["dense_bits"],
+                       dense_offsets=m["dense_offsets"])
         assert_matches_oracle(w, build_on_gpu(w))
 
 

@@ -484,6 +484,26 @@ def test_strip_thinking_workload_counts_closed_form():
     assert oracle.unmasked_pairs(w.kind, w.cu_seqlens, w.meta()) == nnz == 17_699_328
 
 
+def test_generic_workload_counts_closed_form():
+    """Workload 7 (no mask inside a sequence) sees L^2 pairs per sequence;
+    workload 8 (causal + document + padding, dense) sees m (m + 1) / 2 per
+    document of m non-padding tokens, and its padding rows see nothing."""
+    w7 = W.make_workload(7, tensors=False)
+    assert w7.seqlens == W.make_workload(2, tensors=False).seqlens
+    assert oracle.unmasked_pairs(w7.kind, w7.cu_seqlens) == sum(L * L for L in w7.seqlens) == 16_334_146
+    lab7 = oracle.tile_labels("none", w7.cu_seqlens)
+    assert all((l == oracle.FULL).all() for l in lab7)
+    w5 = W.make_workload(5, tensors=False)
+    seg = w5.seg.copy()
+    seg[-2048:] = -1
+    m = np.bincount(seg[seg >= 0])
+    want = int((m * (m + 1) // 2).sum())
+    assert want == 53_960_250
+    w8 = W.make_workload(8, tensors=False)
+    rows = oracle.sequence_mask("dense", w8.cu_seqlens, 0, w8.meta(), rows=np.arange(30000, 32768, 7))
+    assert not rows[np.arange(30000, 32768, 7) >= 32768 - 2048].any()
+
+
 def test_varlen_and_document_workload_counts_closed_form():
     w2 = W.make_workload(2, tensors=False)
     assert w2.seqlens == [860, 289, 1664, 1816, 272, 1814, 1638, 1843]
