@@ -170,7 +170,9 @@ __device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane,
 // memory.  Barrier phases run on across items: the next item's Q load and
 // first S MMAs overlap the current item's last P.V and O epilogue.  The last
 // CTA to finish returns the counters to zero for the next launch.
-template <int D>
+// kDense: the instantiation for ATTN_MASK_DENSE; the others leave its code out
+// (the softmax loop is sensitive to its own size).
+template <int D, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -498,10 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the dense kind's bits of this row for a PARTIAL tile, loaded before
         // the wait for the scores so that their latency hides behind it
         uint32_t dwords[2] = {0u, 0u};
-        if (kind == ATTN_MASK_DENSE && lab == ATTN_TILE_PARTIAL && row_in) {
+        if constexpr (kDense) {
+          if (lab == ATTN_TILE_PARTIAL && row_in) {
 #pragma unroll
-          for (int q = 0; q < 2; ++q)
-            if (64 * hf + 32 * q < kn) dwords[q] = dense_word(p.mask, it.b, L, il, ((j0 + 64 * hf) >> 5) + q);
+            for (int q = 0; q < 2; ++q)
+              if (64 * hf + 32 * q < kn) dwords[q] = dense_word(p.mask, it.b, L, il, ((j0 + 64 * hf) >> 5) + q);
+          }
         }
         const int sb = nsf % 3, xb = nsf & 1;
         const uint32_t col_s = C::col_s(sb) + 64u * hf;  // this half's 64 score columns; its P goes
@@ -522,12 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Causal part and bounds: columns below upto; PARTIAL tiles of the
           // metadata kinds also AND in the per-key predicate, those of the
           // dense kind the caller's bits.
-          const int upto = (lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? min(kn, il - j0 + 1) : kn) - 64 * hf;
+          const int upto = (lab == ATTN_TILE_PARTIAL && (!kDense && kind_causal(kind)) ? min(kn, il - j0 + 1) : kn) -
+                           64 * hf;
           uint32_t vis[2] = {prefix_bits(upto), prefix_bits(upto - 32)};
-          if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
+          if (kDense && lab == ATTN_TILE_PARTIAL) {
             vis[0] &= dwords[0];  // zero for rows past the end
             vis[1] &= dwords[1];
-          } else if (lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
+          } else if (!kDense && lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
             // the K producer staged this entry's key codes
             const int cb = up % C::NCODE;
             if (!warp_wait(bar(C::B_CODE + cb), uint32_t(up / C::NCODE) & 1u, abort_flag, err, 9)) {
@@ -754,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 
-template <int D>
+template <int D, bool kDense>
 attn_status launch(const FwdArgs& a, cudaStream_t s) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv;
@@ -765,7 +770,8 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_ALLOC);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
     configured = true;
   }
@@ -796,7 +802,7 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   const long long items = (long long)a.bm.max_qt * a.num_heads;
   if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const long long grid = items < num_sms ? items : num_sms;
-  attn_fwd_bf16_kernel<D><<<unsigned(grid), kThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
+  attn_fwd_bf16_kernel<D, kDense><<<unsigned(grid), kThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");
 }
@@ -804,10 +810,11 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 attn_status launch_attn_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  const bool dense = a.mask.kind == ATTN_MASK_DENSE;
   switch (a.head_dim) {
-    case 32: return launch<32>(a, s);
-    case 64: return launch<64>(a, s);
-    case 128: return launch<128>(a, s);
+    case 32: return dense ? launch<32, true>(a, s) : launch<32, false>(a, s);
+    case 64: return dense ? launch<64, true>(a, s) : launch<64, false>(a, s);
+    case 128: return dense ? launch<128, true>(a, s) : launch<128, false>(a, s);
   }
   return ATTN_ERR_UNSUPPORTED;
 }
