@@ -324,7 +324,7 @@ def run_ours(args):
     fwd_avg_s = sum(fwd_ms) / len(fwd_ms) / 1e3
     achieved = flops / fwd_avg_s / 1e12
     peak = float(peaks["bf16_tflops"])
-    roofline = {"bound": "tensor", "kernel": "attn_fwd_bf16_kernel<128>", "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": "attn_fwd_bf16_kernel<128, false>", "achieved": achieved,
                 "peak": peak, "unit": UNIT, "frac": achieved / peak,
                 "peak_source": f"{peak_kind} bf16_tflops (burst)",
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
