@@ -978,6 +978,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         // 16 m + [0,16) of the S^T region, all of which this warp has read.
         const uint32_t rs = COL_R0 + 128u * uint32_t(nent & 1), rp = COL_R0 + 128u * uint32_t((nent & 1) ^ 1);
         uint32_t sv[2][32], dv0[32], dv1[32];
+        uint32_t dsw[32];  // this half's dS (bf16 pairs), kept for the block store
         ptx::tmem_ld32(lane_base + rs + 64 * hf, sv[0]);
         ptx::tmem_ld32(lane_base + rs + 64 * hf + 32, sv[1]);
         ptx::tmem_ld32(lane_base + rp + 64 * hf, dv0);
@@ -1024,18 +1025,18 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           }
           ptx::tmem_st16(lane_base + rs + 64 * hf + 16 * m, pp);
           ptx::tmem_st16(lane_base + rs + 64 * hf + 32 + 16 * m, pd);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dsw[16 * m + i] = pd[i];
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(C::B_PFULL + hf));  // queries 64 hf .. +63 are ready for the products
         {
-          // this half's dS, read back from its 32 columns, to its chunk of the
-          // block the dQ kernel multiplies by K
-          uint32_t w[32];
-          ptx::tmem_ld32(lane_base + rs + 64 * hf + 32, w);
-          ptx::tmem_wait_ld();
+          // this half's dS, from registers (its TMEM columns may already be
+          // the next entry's dP by now), to its chunk of the block the dQ
+          // kernel multiplies by K
           uint8_t* blk = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock;
-          store_ds_half(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w, blk + hf * (kDsBlock / 2), qd * 32);
+          store_ds_half(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, dsw, blk + hf * (kDsBlock / 2), qd * 32);
         }
         ++nent;
       }
