@@ -9,7 +9,7 @@
 //
 // A work item is one 128-row q-tile of one sequence and one head; persistent
 // CTAs (one per SM) take the items longest first and walk each q-tile's k-tile
-// list in ascending order.  Warp roles (384 threads):
+// list in ascending order.  Warp roles (512 threads):
 //   warps 0-7  softmax, two threads per query row: warps 0-3 take score
 //              columns 0-63 of every k-tile, warps 4-7 columns 64-127
 //   warp 8     TMA producer of Q and of the K ring (three slots); stages the
@@ -19,13 +19,20 @@
 //   warp 10    TMA producer of the V ring (two slots); zeroes V rows past a
 //              sequence end
 //   warp 11    tcgen05 issuer of the S = Q K^T products (one thread)
+//   warps 12-15 epilogue: one thread per query row reads the item's final O
+//              from TMEM, divides by l and writes O (bf16) and LSE, while the
+//              softmax warps already work on the next item
+// The softmax warpgroups run with 160 registers a thread, the other two with
+// 96 (setmaxnreg, within the 128 x 512 the block is launched with).
 // The two issuers work independently: an MMA issue blocks while the tensor
 // pipe's short queue is full, and with two threads one waits on its barriers
 // while the other keeps the queue fed.
-// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384) hold S of three
-// consecutive k-tiles, O [384, 384+D).  Each half of a row writes its bf16 P
-// over the first 32 of its own 64 S columns.  With three S buffers the tensor
-// cores compute S(j+1), S(j+2) and P(j-1).V while the softmax works on S(j).
+// TMEM columns: S0 [0,128), S1 [128,256) hold S of two consecutive k-tiles,
+// O0 [256, 256+D) and O1 [384, 384+D) the accumulators of alternate items, so
+// an item's epilogue overlaps the next item's products.  Each half of a row
+// writes its bf16 P over the first 32 of its own 64 S columns.  With two S
+// buffers the tensor cores compute S(j+1) and P(j-1).V while the softmax
+// works on S(j).
 //
 // The row maximum used as the exponent reference only moves when a new tile
 // raises it by more than 2^8 (factor 256 in p); O and l are then rescaled
@@ -43,8 +50,9 @@ namespace attnmask {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 256
-constexpr int kThreads = 384;
-constexpr int kWarpKLoad = 8, kWarpPV = 9, kWarpVLoad = 10, kWarpS = 11;
+constexpr int kThreads = 512;
+constexpr int kWarpKLoad = 8, kWarpPV = 9, kWarpVLoad = 10, kWarpS = 11, kWarpEpi = 12;
+constexpr int kRegsSoftmax = 160, kRegsOther = 96;  // 2 x 128 x 160 + 2 x 128 x 96 = 512 x 128
 
 template <int D>
 struct Cfg : TileLayout<D> {
@@ -57,28 +65,29 @@ struct Cfg : TileLayout<D> {
   static constexpr int NV = 2;                        // V ring slots
   static constexpr int NCODE = 6;                     // key-code buffers (entries in flight)
   static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = OFF_K + NK * TILE;
-  static constexpr int NS = 3;                        // S buffers in TMEM
-  // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; XSUM: per item parity
+  static constexpr int NS = 2;                        // S buffers in TMEM
+  // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; ODONE, OFREE,
+  // STATS: per O buffer (item parity)
   static constexpr int B_Q = 0, B_QFREE = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
                        B_VEMPTY = B_VFULL + NV, B_VTMA = B_VEMPTY + NV, B_SFULL = B_VTMA + 1,
                        B_PFULL = B_SFULL + NS, B_PDONE = B_PFULL + NS, B_ODONE = B_PDONE + NS,
-                       B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
+                       B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
                        B_CODE = B_IEMPTY + 2, B_CODEFREE = B_CODE + NCODE, B_XMAX = B_CODEFREE + NCODE,
-                       B_XSUM = B_XMAX + 2, B_DRAIN = B_XSUM + 2, NBAR = B_DRAIN + 1;
+                       B_STATS = B_XMAX + 2, B_DRAIN = B_STATS + 2, NBAR = B_DRAIN + 1;
   static constexpr int OFF_BAR = OFF_V + NV * TILE;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int OFF_RINGI = OFF_MISC + 16;            // two decoded work items, 8 ints each
   static constexpr int OFF_CODES = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;  // per buffer: 128 key codes
   static constexpr int OFF_XMAX = OFF_CODES + NCODE * kTile * 4;  // [entry parity][half][row] floats
-  static constexpr int OFF_XSUM = OFF_XMAX + 2 * 2 * kTile * 4;    // [item parity][half][row] floats
-  static constexpr int OFF_OSTAGE = (OFF_XSUM + 2 * 2 * kTile * 4 + 127) & ~127;  // per softmax warp: 16 O rows
-  static constexpr int OSTAGE_WARP = 16 * 128;                                    // bytes per warp
-  static constexpr int SMEM_USED = OFF_OSTAGE + 8 * OSTAGE_WARP;
+  static constexpr int OFF_STATS = OFF_XMAX + 2 * 2 * kTile * 4;  // [item parity][l0, l1, m][row] floats
+  static constexpr int OFF_OSTAGE = (OFF_STATS + 2 * 3 * kTile * 4 + 127) & ~127;  // per epilogue warp
+  static constexpr int OSTAGE_WARP = 4096;                                        // 16 rows of 256 bytes
+  static constexpr int SMEM_USED = OFF_OSTAGE + 4 * OSTAGE_WARP;
   // + slack to align the base to 1024 B; at least 116 KB so that one CTA holds an SM
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_O = 384;
+  __host__ __device__ static constexpr uint32_t col_o(int b) { return 256u + uint32_t(b) * 128u; }
   __host__ __device__ static constexpr uint32_t col_s(int i) { return uint32_t(i) * 128u; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -210,17 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(C::B_VTMA), 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 3);  // softmax threads, both MMA threads, V producer
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 3 + 128);  // softmax, MMA threads, V producer, epilogue
       ptx::mbar_init(bar(C::B_XMAX + i), 256);
-      ptx::mbar_init(bar(C::B_XSUM + i), 256);
+      ptx::mbar_init(bar(C::B_STATS + i), 256);
+      ptx::mbar_init(bar(C::B_ODONE + i), 1);
+      ptx::mbar_init(bar(C::B_OFREE + i), 128);
     }
     for (int i = 0; i < C::NS; ++i) {
       ptx::mbar_init(bar(C::B_SFULL + i), 1);
       ptx::mbar_init(bar(C::B_PFULL + i), 256);
       ptx::mbar_init(bar(C::B_PDONE + i), 1);
     }
-    ptx::mbar_init(bar(C::B_ODONE), 1);
-    ptx::mbar_init(bar(C::B_OFREE), 256);
     for (int c = 0; c < C::NCODE; ++c) {
       ptx::mbar_init(bar(C::B_CODE + c), 1);
       ptx::mbar_init(bar(C::B_CODEFREE + c), 256);
@@ -242,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (skip) {
     // nothing issued, nothing to drain
-  } else if (warp == kWarpKLoad) {
+  } else if (warp >= 8) {
+   ptx::regs_dec<kRegsOther>();
+   if (warp == kWarpKLoad) {
     // ------------------------------------------------------------ Q, K, key codes
     int nk = 0, nq = 0, up = 0;  // K loads, Q loads, PARTIAL entries given key codes
     bool ok = true;
@@ -429,30 +440,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
         const int n = it.e1 - it.e0;
+        const int ob = k & 1;  // this item's O buffer, free once the epilogue of item k - 2 has read it
+        if (n > 0 && k >= 2 &&
+            !wait_bar(bar(C::B_OFREE + ob), uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 14)) {
+          ok = false;
+          break;
+        }
         for (int j = 0; j < n; ++j) {
           const int pb = np % C::NS, vs = nvc % C::NV;
-          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
-            ok = false;
-            break;
-          }
           if (!wait_bar(bar(C::B_VFULL + vs), uint32_t(nvc / C::NV) & 1u, abort_flag, err, 6)) { ok = false; break; }
           if (!wait_bar(bar(C::B_PFULL + pb), uint32_t(np / C::NS) & 1u, abort_flag, err, 5)) { ok = false; break; }
           ptx::tc_fence_after();
-          issue_pv<D>(tmem + C::COL_O, tmem + C::col_s(pb), vdesc0 + uint64_t(vs) * (C::TILE >> 4), j > 0);
+          issue_pv<D>(tmem + C::col_o(ob), tmem + C::col_s(pb), vdesc0 + uint64_t(vs) * (C::TILE >> 4), j > 0);
           // P(j) and V(j) are read by no later MMA
           ptx::mma_commit(bar(C::B_PDONE + pb));
           ptx::mma_commit(bar(C::B_VEMPTY + vs));
           ++np;
           ++nvc;
         }
-        // The item's last P.V: O is final once this arrives.
-        if (ok && n > 0) ptx::mma_commit(bar(C::B_ODONE));
+        // The item's last P.V: O is final once this arrives (at once for an
+        // item without entries).
+        if (ok) ptx::mma_commit(bar(C::B_ODONE + ob));
       }
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-  } else if (warp < 8) {
+   } else {
+    // ------------------------------------------------------------ epilogue
+    // One thread per query row (TMEM lane): once the softmax has posted the
+    // row's statistics and the item's last P.V is done, O / l is read from
+    // the item's O buffer and written as whole rows through a 4 KB stage, 16
+    // rows at a time (the O columns are read twice, once per 16 rows, so that
+    // no thread holds a whole row); the buffer is released after the reads.
+    const int quarter = warp - kWarpEpi;       // TMEM lanes 32 quarter ..
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const float* stats = reinterpret_cast<const float*>(sbase + C::OFF_STATS);
+    uint8_t* stage = sbase + C::OFF_OSTAGE + quarter * C::OSTAGE_WARP;
+    constexpr int RB = D * 2;                  // bytes per output row
+    constexpr int CPR = RB / 16;               // 16-byte pieces per row
+    constexpr int RPI = 32 / CPR;              // rows per warp-wide store
+    for (int k = 0;; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      Item it;
+      const bool valid = load_item(item_ring + 8 * (k & 1), it);
+      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      const int ob = k & 1;
+      if (!warp_wait(bar(C::B_STATS + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 18)) break;
+      const float* st = stats + ob * 3 * kTile;
+      const float lt = st[r] + st[kTile + r];  // the halves' row sums, in a fixed order
+      const float m = st[2 * kTile + r];
+      const int qn = min(kTile, it.L - it.qi0);
+      const bool has = it.e1 > it.e0;
+      if (!warp_wait(bar(C::B_ODONE + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 11)) break;
+      ptx::tc_fence_after();
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* obase = p.o + (size_t(it.s0 + it.qi0 + quarter * 32) * p.H + it.h) * D;
+      const size_t rstride = size_t(p.H) * D;
+#pragma unroll 1
+      for (int half16 = 0; half16 < 2; ++half16) {
+#pragma unroll
+        for (int q32 = 0; q32 < (D + 31) / 32; ++q32) {
+          constexpr int W = D < 32 ? D : 32;   // columns per TMEM read
+          uint32_t v[32];
+          if (has) {
+            if constexpr (W == 32) ptx::tmem_ld32(lane_base + C::col_o(ob) + q32 * 32, v);
+            else ptx::tmem_ld16(lane_base + C::col_o(ob), *reinterpret_cast<uint32_t(*)[16]>(v));
+            ptx::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = 0u;
+          }
+          if ((lane >> 4) == half16) {
+            const int q = lane & 15;
+#pragma unroll
+            for (int c4 = 0; c4 < W / 8; ++c4) {
+              const int c = q32 * (W / 8) + c4;  // 16-byte piece of the row
+              uint32_t w[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                w[x] = ptx::pack_bf16(__uint_as_float(v[8 * c4 + 2 * x]) * inv_l,
+                                      __uint_as_float(v[8 * c4 + 2 * x + 1]) * inv_l);
+              *reinterpret_cast<uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        if (half16 == 1) {  // every read of the buffer is done
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(C::B_OFREE + ob));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16 / RPI; ++i) {
+          const int q = i * RPI + lane / CPR, c = lane % CPR;
+          const int rr = half16 * 16 + q;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
+          if (quarter * 32 + rr < qn) *reinterpret_cast<uint4*>(obase + size_t(rr) * rstride + 8 * c) = val;
+        }
+        __syncwarp();
+      }
+      if (r < qn)
+        p.lse[size_t(it.h) * p.T + it.s0 + it.qi0 + r] =
+            lt > 0.f ? (m + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
+    }
+   }
+  } else {
+    ptx::regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     // Two threads per query row: warps 0-3 take score columns 0-63 of every
     // k-tile, warps 4-7 columns 64-127.  Both halves keep the same exponent
@@ -467,14 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     constexpr int DH = D / 2;                  // O columns this half rescales and writes
-    const uint32_t col_oh = C::COL_O + uint32_t(DH * hf);
+    const uint32_t col_oh0 = C::col_o(0) + uint32_t(DH * hf);  // this half's O columns, buffer 0
     const float c2 = p.scale_log2;
     const float2 c22 = make_float2(c2, c2);
     float* xmax = reinterpret_cast<float*>(sbase + C::OFF_XMAX);  // [entry parity][half][row]
-    float* xsum = reinterpret_cast<float*>(sbase + C::OFF_XSUM);  // [item parity][half][row]
-    int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % 3
+    float* stats = reinterpret_cast<float*>(sbase + C::OFF_STATS);  // [item parity][l0, l1, m][row]
+    int nsf = 0;     // k-tile entries processed (all items): S buffer nsf % NS
     int up = 0;      // PARTIAL entries with key codes (all items): code buffer up % NCODE
-    int nodone = 0;  // items whose final O this warp has waited for
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -507,10 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (64 * hf + 32 * q < kn) dwords[q] = dense_word(p.mask, it.b, L, il, ((j0 + 64 * hf) >> 5) + q);
           }
         }
-        const int sb = nsf % 3, xb = nsf & 1;
+        const int sb = nsf % C::NS, xb = nsf & 1;
         const uint32_t col_s = C::col_s(sb) + 64u * hf;  // this half's 64 score columns; its P goes
                                                          // over the first 32 of them
-        if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(nsf / 3) & 1u, abort_flag, err, 8)) { ok = false; break; }
+        if (!warp_wait(bar(C::B_SFULL + sb), uint32_t(nsf / C::NS) & 1u, abort_flag, err, 8)) { ok = false; break; }
         ptx::tc_fence_after();
         float s[64];
         {
@@ -632,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O must hold exactly the P.V of the earlier entries: wait for the
             // last of them.  Each half rescales its half of the O columns.
             const int pl = nsf - 1;
-            if (!warp_wait(bar(C::B_PDONE + pl % 3), uint32_t(pl / 3) & 1u, abort_flag, err, 12)) {
+            if (!warp_wait(bar(C::B_PDONE + pl % C::NS), uint32_t(pl / C::NS) & 1u, abort_flag, err, 12)) {
               ok = false;
               break;
             }
@@ -641,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int q = 0; q < DH / 16; ++q) {
               uint32_t v[16];
-              ptx::tmem_ld16(lane_base + col_oh + q * 16, v);
+              ptx::tmem_ld16(lane_base + col_oh0 + 128u * uint32_t(k & 1) + q * 16, v);
               ptx::tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < 16; c += 2) {
@@ -649,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[c] = __float_as_uint(x.x);
                 v[c + 1] = __float_as_uint(x.y);
               }
-              ptx::tmem_st16(lane_base + col_oh + q * 16, v);
+              ptx::tmem_st16(lane_base + col_oh0 + 128u * uint32_t(k & 1) + q * 16, v);
             }
           }
           l *= alpha;
@@ -664,80 +759,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++cnt_item;
       }
       if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      // Swap the partial row sums; each half writes its half of the O columns.
+      // ---------------------------------------------------------- row statistics
+      // Post this half's row sum (and, from the first half, the reference m)
+      // for the epilogue warps, once they have read the same buffer two items
+      // ago; then straight on to the next item.
       {
-        float* xs = xsum + (k & 1) * (2 * kTile);
-        xs[hf * kTile + r] = l;
-        ptx::mbar_arrive(bar(C::B_XSUM + (k & 1)));
-        if (!warp_wait(bar(C::B_XSUM + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 17)) break;
+        const int ob = k & 1;
+        if (k >= 2 && !warp_wait(bar(C::B_OFREE + ob), uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 19)) break;
+        float* st = stats + ob * 3 * kTile;
+        st[hf * kTile + r] = l;
+        if (hf == 0) st[2 * kTile + r] = m_ref;
+        ptx::mbar_arrive(bar(C::B_STATS + ob));
       }
-      const float* xs = xsum + (k & 1) * (2 * kTile);
-      const float lt = xs[r] + xs[kTile + r];  // the same order in both halves
-      if (cnt_item > 0) {
-        if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
-        ++nodone;
-      }
-      ptx::tc_fence_after();
-      // All of this half's O columns into registers at once (one wait), and O
-      // is released for the next item's P.V before the stores to global memory.
-      uint32_t ov[DH];
-      if (cnt_item > 0) {
-        if constexpr (DH >= 32) {
-#pragma unroll
-          for (int q = 0; q < DH / 32; ++q)
-            ptx::tmem_ld32(lane_base + col_oh + q * 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32 * q));
-        } else {
-          ptx::tmem_ld16(lane_base + col_oh, *reinterpret_cast<uint32_t(*)[16]>(ov));
-        }
-        ptx::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int c = 0; c < DH; ++c) ov[c] = 0u;
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE));
-      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      // Stores of whole 128-byte row segments: the warp's rows pass through
-      // shared memory 16 at a time (chunk c of row q at slot c ^ (q & 7), so
-      // neither side conflicts on banks), then 8 lanes write each row's DH
-      // columns as consecutive 16-byte pieces.
-      {
-        constexpr int CPR = DH / 8;              // 16-byte chunks per row half (8, 4 or 2)
-        constexpr int RPI = 32 / CPR;            // rows per store instruction
-        uint8_t* stage = sbase + C::OFF_OSTAGE + warp * C::OSTAGE_WARP;
-        __nv_bfloat16* obase = p.o + (size_t(s0 + it.qi0 + quarter * 32) * p.H + it.h) * D + DH * hf;
-        const size_t rstride = size_t(p.H) * D;  // elements between consecutive tokens
-#pragma unroll
-        for (int half16 = 0; half16 < 2; ++half16) {
-          if ((lane >> 4) == half16) {
-            const int q = lane & 15;
-#pragma unroll
-            for (int c = 0; c < CPR; ++c) {
-              uint32_t w[4];
-#pragma unroll
-              for (int x = 0; x < 4; ++x)
-                w[x] = ptx::pack_bf16(__uint_as_float(ov[8 * c + 2 * x]) * inv_l,
-                                      __uint_as_float(ov[8 * c + 2 * x + 1]) * inv_l);
-              *reinterpret_cast<uint4*>(stage + q * 128 + ((c ^ (q & 7)) & (CPR - 1)) * 16) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 16 / RPI; ++i) {
-            const int q = i * RPI + lane / CPR, c = lane % CPR;  // row within these 16, chunk
-            const int rr = half16 * 16 + q;                       // row within the warp's 32
-            const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 128 + ((c ^ (q & 7)) & (CPR - 1)) * 16);
-            if (quarter * 32 + rr < qn)
-              *reinterpret_cast<uint4*>(obase + size_t(rr) * rstride + 8 * c) = val;
-          }
-          __syncwarp();
-        }
-      }
-      if (row_in && hf == 0)
-        p.lse[size_t(it.h) * p.T + s0 + il] =
-            lt > 0.f ? (m_ref + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
