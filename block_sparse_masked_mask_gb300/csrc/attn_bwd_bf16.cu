@@ -38,25 +38,32 @@ constexpr int kPlist = 256;
 constexpr int kWarpLoad = 4, kWarpMma = 5;
 
 // ---------------------------------------------------------------------------
-// D = rowsum(dO * O): one warp per (token, head) row.
+// D = rowsum(dO * O): D / 8 lanes per (token, head) row, 16 bytes of O and of
+// dO per lane (eight bf16 each), so that every load moves whole sectors.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         float* __restrict__ delta, int T, int H) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + warp;  // t * H + h
-  if (row >= (long long)T * H) return;
-  const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(o + row * D);
-  const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(dout + row * D);
+  constexpr int LPR = D / 8;                      // lanes per row: 16, 8 or 4
+  constexpr int RPB = 256 / LPR;                  // rows per block
+  const int sub = threadIdx.x % LPR;
+  const long long row = (long long)blockIdx.x * RPB + threadIdx.x / LPR;  // t * H + h
+  const bool in = row < (long long)T * H;
   float acc = 0.f;
+  if (in) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + 8 * sub);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + 8 * sub);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-  for (int c = lane; c < D / 2; c += 32) {
-    const float2 a = __bfloat1622float2(po[c]), b = __bfloat1622float2(pd[c]);
-    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
+  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && sub == 0) {
     const int t = int(row / H), h = int(row % H);
     delta[size_t(h) * T + t] = acc;
   }
@@ -1102,7 +1109,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   float* delta = reinterpret_cast<float*>(ws + a.ws.delta);
   int32_t* kpos = reinterpret_cast<int32_t*>(ws + a.ws.kpos);
   const long long rows = (long long)a.total_tokens * a.num_heads;
-  bwd_delta_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, s>>>(
+  bwd_delta_kernel<D><<<unsigned((rows + (2048 / D) - 1) / (2048 / D)), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), delta, a.total_tokens,
       a.num_heads);
   cudaError_t e = cudaGetLastError();
