@@ -6,19 +6,23 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // The xorl issue (Verified FA4 gaps, items 1-3) asks for this backward over
 // the block-sparse masks, walking the transposed (k-major) lists for dK and
-// dV, and with a deterministic dQ.  Three kernels:
+// dV, and with a deterministic dQ.  Four kernels:
 //   * delta: D = rowsum(dO * O) per (token, head), fp32;
+//   * kpos: for every q-major entry, its position in the k-major lists;
 //   * dK/dV: one work item per (k-tile, head) walks its k-major list of
-//     q-tiles, accumulating dK and dV in TMEM (K, V stay in shared memory);
-//   * dQ: one work item per (q-tile, head) walks its q-major list of k-tiles,
-//     accumulating dQ in TMEM.  dQ is a sum over k-tiles in a fixed order
-//     inside one CTA, so it is bit-reproducible, with no atomics.
-// Both list-walking kernels recompute S and dP (seven GEMMs where a dQ with
-// atomics would need five); the masks are applied on PARTIAL tiles only and
-// EMPTY tiles are never loaded.  Warp roles (256 threads): warps 0-3 one
-// thread per TMEM lane (a query row for dQ, a key row for dK/dV), warp 4 the
-// TMA producer, warp 5 the tcgen05 issuer (one thread, TMEM owner), warps 6-7
-// idle.  Every mbarrier wait is bounded as in the forward.
+//     q-tiles, recomputing S^T and dP^T, accumulating dK and dV in TMEM (K, V
+//     stay in shared memory), and stores every dS tile once as a 32 KB bf16
+//     block in the caller's workspace;
+//   * dQ: one work item per (q-tile, head) walks its q-major list of k-tiles
+//     and accumulates dQ = scale dS K in TMEM from the stored blocks.  dQ is a
+//     sum over k-tiles in a fixed order inside one CTA, so it is
+//     bit-reproducible, with no atomics.
+// Five products per tile pair (S, dP, dV, dK, dQ); the masks are applied on
+// PARTIAL tiles only and EMPTY tiles are never loaded.  Warp roles: dK/dV
+// (384 threads) eight row warps (two per TMEM lane quarter, one per half of
+// the queries), the TMA producer, the tcgen05 issuer, two idle; dQ (256
+// threads) four epilogue warps, the producer and the issuer.  Every mbarrier
+// wait is bounded as in the forward.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -219,34 +223,15 @@ __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint3
   }
 }
 
-// A stored dS block is the image, in shared memory, of a 128-key x 128-query
-// bf16 MN-major SW128 operand: two 16 KB chunks of 64 queries, key row r of a
-// chunk at r * 128 bytes with its eight 16-byte pieces XOR-swizzled by r & 7,
-// so one bulk copy of the 32 KB gives the dQ kernel its A operand.  This
-// writes this warp's 32 key rows (row0 ..) of one chunk (32 packed words per
-// lane), 16 rows at a time through a 2 KB stage, as whole 128-byte lines.
-__device__ __forceinline__ void store_ds_half(uint8_t* stage, int lane, const uint32_t (&w)[32], uint8_t* chunk,
-                                              int row0) {
-#pragma unroll
-  for (int half16 = 0; half16 < 2; ++half16) {
-    if ((lane >> 4) == half16) {
-      const int q = lane & 15;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(stage + q * 128 + ((u ^ q) & 7) * 16) =
-            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int q = 4 * i + (lane >> 3), u = lane & 7;  // row q of the 16, piece u of its 128 bytes
-      const uint4 val = *reinterpret_cast<const uint4*>(stage + q * 128 + ((u ^ q) & 7) * 16);
-      const int r = row0 + half16 * 16 + q;
-      *reinterpret_cast<uint4*>(chunk + r * 128 + ((u ^ (r & 7)) * 16)) = val;
-    }
-    __syncwarp();
-  }
-}
+// A stored dS block is the image, in shared memory, of a 128-query x 128-key
+// bf16 operand in the MN-major layout without swizzle: sixteen 2 KB chunks of
+// eight queries; in chunk c, key k's eight queries q = 8c .. 8c+7 are the 16
+// bytes at k * 16.  One bulk copy of the 32 KB gives the dQ kernel its A
+// operand (8-key core matrices 128 bytes apart along K, chunks 2 KB apart
+// along M), and a thread that holds one key's dS for 64 queries writes it
+// straight from registers: for each chunk the 32 lanes of a warp (32
+// consecutive keys) write 512 contiguous bytes.
+constexpr int kDsChunk = 2048;  // bytes per eight-query chunk of a dS block
 
 // TMEM -> registers: D fp32 columns of this thread's lane from `taddr`, times
 // `mul`, rounded to bf16 pairs (zeros when `have` is false).
@@ -367,7 +352,7 @@ struct DqCfg : TileLayout<D> {
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t DQ_COLS = D;                          // one dQ buffer
   static constexpr uint32_t TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;  // two buffers
-  // dS as the A operand: M = 128 queries (two 64-column chunks), K = keys
+  // dS as the A operand: M = 128 queries (sixteen 8-query chunks), K = keys
   static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16_f32(128, D, true, true);
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -513,7 +498,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int nload = 0;
       bool ok = true;
-      const uint64_t ds0 = ptx::smem_desc(sRing, kDsBlock / 2, 1024u, ptx::kSwizzle128B);
+      // dS: MN-major without swizzle, where the stride between eight-key core
+      // matrices (K, 128 bytes) is the leading offset and the stride between
+      // eight-query chunks (M, kDsChunk) the stride offset
+      const uint64_t ds0 = ptx::smem_desc(sRing, 128u, kDsChunk, ptx::kSwizzleNone);
       const uint64_t k0 = v_base<D>(sRing + kDsBlock);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -535,7 +523,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint64_t so = uint64_t(slot) * (C::SLOT >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            ptx::mma_ss(dq_t, ds0 + so + uint64_t(kk * 16 * 128 >> 4), k0 + so + v_step<D>(kk), C::IDESC_DQ,
+            ptx::mma_ss(dq_t, ds0 + so + uint64_t(kk * 16 * 16 >> 4), k0 + so + v_step<D>(kk), C::IDESC_DQ,
                         (j > 0 || kk > 0) ? 1u : 0u);
           ptx::mma_commit(bar(C::B_EMPTY + slot));
           ++nload;
@@ -1042,8 +1030,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           // this half's dS, from registers (its TMEM columns may already be
           // the next entry's dP by now), to its chunk of the block the dQ
           // kernel multiplies by K
-          uint8_t* blk = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock;
-          store_ds_half(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, dsw, blk + hf * (kDsBlock / 2), qd * 32);
+          uint8_t* kr = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock +
+                        size_t(qd * 32 + lane) * 16;  // this key's piece of every chunk
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(kr + (8 * hf + u) * kDsChunk) =
+                make_uint4(dsw[4 * u], dsw[4 * u + 1], dsw[4 * u + 2], dsw[4 * u + 3]);
         }
         ++nent;
       }
