@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpS) {
     // ------------------------------------------------------------ S issuer
-    // S(j) into S buffer j % 3 once P.V(j-3) has read the P written over
-    // S(j-3) there.
+    // S(j) into S buffer j % NS once P.V(j - NS) has read the P written over
+    // S(j - NS) there.
     if (lane == 0) {
       int nkc = 0, ns = 0;  // K loads consumed, S issued (all items)
       bool ok = true;
