@@ -325,16 +325,19 @@ def attention_backward_sampled(q, k, v, do, kind: str, cu_seqlens, meta=None, sc
         sk = kr[(kr >= start) & (kr < end)]
         if len(sq) == 0 and len(sk) == 0:
             continue
-        # LSE and O of every query row of this sequence (the forward oracle)
-        need = np.arange(start, end) if len(sk) else sq
+        tok = np.arange(start, end)
+        # The query rows that see at least one sampled key: every other row has
+        # P = 0 on all of them and adds exactly nothing to their dK and dV.
+        vis_k = visible(kind, cu, b, meta, tok - start, sk - start) if len(sk) else None
+        rows_k = tok[vis_k.any(axis=1)] if len(sk) else tok[:0]
+        # LSE and O of the query rows used below (the forward oracle)
+        need = np.union1d(sq, rows_k)
         O, LSE = attention(q, k, v, kind, cu, meta, scale, heads=heads, rows=need,
                            row_block=row_block)
-        tok = np.arange(start, end)
         for h in heads:
             qh, kh, vh, doh = (_as_f64(x[start:end, h]) for x in (q, k, v, do))
             lse_h = LSE[h, start:end]
             lse_safe = np.where(np.isfinite(lse_h), lse_h, 0.0)  # rows with no key have P = 0
-            dlt = (doh * O[start:end, h]).sum(axis=1) if len(sk) else None
             if len(sq):
                 li = sq - start
                 vis = visible(kind, cu, b, meta, sq - start, tok - start)
@@ -344,13 +347,14 @@ def attention_backward_sampled(q, k, v, do, kind: str, cu_seqlens, meta=None, sc
                 ds = p * ((doh[li] @ vh.T) - d_i[:, None])
                 dQ[sq, h] = (ds @ kh) * scale
             if len(sk):
-                lj = sk - start
-                vis = visible(kind, cu, b, meta, tok - start, sk - start)
-                s = (qh @ kh[lj].T) * scale
-                p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[:, None]), 0.0)
-                ds = p * ((doh @ vh[lj].T) - dlt[:, None])
-                dV[sk, h] = p.T @ doh
-                dK[sk, h] = (ds.T @ qh) * scale
+                lj, li = sk - start, rows_k - start
+                vis = vis_k[li]
+                dlt = (doh[li] * O[rows_k, h]).sum(axis=1)
+                s = (qh[li] @ kh[lj].T) * scale
+                p = np.where(vis, np.exp(np.where(vis, s, 0.0) - lse_safe[li, None]), 0.0)
+                ds = p * ((doh[li] @ vh[lj].T) - dlt[:, None])
+                dV[sk, h] = p.T @ doh[li]
+                dK[sk, h] = (ds.T @ qh[li]) * scale
     return dQ, dK, dV
 
 

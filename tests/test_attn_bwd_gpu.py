@@ -149,6 +149,27 @@ def test_full_size_workloads_sampled(c, form, heads):
         check(f"{w.name} {name}", g, r, rows=rows, heads=list(heads))
 
 
+def test_longest_single_sequence_sampled():
+    """The largest backward case: one 65536-token causal sequence (512 k-tiles,
+    131328 tile pairs, a 4.3 GB dS workspace); dQ on sampled query rows, dK and
+    dV on sampled keys of the last eight k-tiles (few rows see those, which
+    keeps the oracle quick)."""
+    L = 65536
+    w = W.random_workload(12, "causal", [L], num_heads=1, head_dim=128)
+    do = W.grad_output(w, seed=12)
+    got = run_bwd(w, do)
+    for g in got:
+        assert torch.isfinite(g.float()).all()
+    q_rows = sample_rows(w, seed=12)
+    rng = np.random.default_rng(12)
+    k_rows = sorted(set(rng.integers(L - 1024, L, 24).tolist()) | {L - 1024, L - 897, L - 896, L - 1})
+    ref = oracle.attention_backward_sampled(w.q, w.k, w.v, do, w.kind, w.cu_seqlens, w.meta(),
+                                            heads=[0], q_rows=q_rows, k_rows=k_rows)
+    check(f"{w.name} dQ", got[0], ref[0], rows=q_rows, heads=[0])
+    check(f"{w.name} dK", got[1], ref[1], rows=k_rows, heads=[0])
+    check(f"{w.name} dV", got[2], ref[2], rows=k_rows, heads=[0])
+
+
 def test_small_config_fp32_inputs_rounded_to_bf16():
     """The 64-token fp32 workload, rounded to bf16 for the backward (the
     backward has no fp32 path): every element against the oracle on the

@@ -132,6 +132,16 @@ def test_full_size_workloads_sampled(c, form):
     assert not torch.isnan(lse).any() and not (lse == float("inf")).any()
 
 
+def test_longest_single_sequence_sampled():
+    """The largest case: one 131072-token causal sequence (1024 q-tiles, 524800
+    listed tile pairs per head), compared on sampled rows; the last row sees
+    all 131072 keys."""
+    w = W.random_workload(11, "causal", [131072], num_heads=2, head_dim=128)
+    o, lse = run_gpu(w)
+    compare(w, o, lse, rows=sample_rows(w, n=24, seed=11), heads=[0, 1])
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
 def test_deterministic_repeats_bit_identical():
     w = full_workload(3)
     o1, l1 = run_gpu(w)
