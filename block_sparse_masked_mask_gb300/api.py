@@ -44,6 +44,40 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _need(t, name: str, where: str, dtypes=None, shape=None, device=None) -> None:
+    """Refuse, before any library call, a tensor the C side would misread: not
+    on a CUDA device (a host pointer would reach a kernel), on another device
+    than the rest, not contiguous (the layouts are dense row-major), of the
+    wrong element type or shape."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise AttnError(1, f"{where}: {name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise AttnError(1, f"{where}: {name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise AttnError(1, f"{where}: {name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise AttnError(1, f"{where}: {name} has dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise AttnError(1, f"{where}: {name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _need_meta(where, cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets, device=None):
+    """cu_seqlens int32; seg_id / turn int32, role int8 (one value per token);
+    the dense kind's words (32-bit) and int64 offsets."""
+    _need(cu_seqlens, "cu_seqlens", where, (torch.int32,), device=device)
+    dev = cu_seqlens.device
+    _need(seg_id, "seg_id", where, (torch.int32,), device=dev)
+    _need(role, "role", where, (torch.int8, torch.uint8), device=dev)
+    _need(turn, "turn", where, (torch.int32,), device=dev)
+    _need(dense_bits, "dense_bits", where, _WORD_DTYPES, device=dev)
+    _need(dense_offsets, "dense_offsets", where, (torch.int64,), device=dev)
+
+
+_WORD_DTYPES = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -137,6 +171,8 @@ def attn_block_mask_build(kind, cu_seqlens: torch.Tensor, total_tokens: int, max
                           dense_bits: Optional[torch.Tensor] = None,
                           dense_offsets: Optional[torch.Tensor] = None) -> BlockMask:
     """Build the block mask on the device (asynchronous on ``stream``)."""
+    _need_meta("attn_block_mask_build", cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets)
+    _need(workspace, "workspace", "attn_block_mask_build", device=cu_seqlens.device)
     batch = cu_seqlens.numel() - 1
     need = attn_block_mask_workspace_size(batch, total_tokens, max_seqlen)
     if workspace is None:
@@ -167,6 +203,9 @@ def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: 
     one-time address lookup and should come before any stream capture.  Only
     the arrays the forward reads are stored (``labels`` is not).
     """
+    _need_meta("attn_block_mask_build_noalloc", cu_seqlens, seg_id, role, turn, dense_bits,
+               dense_offsets)
+    _need(workspace, "workspace", "attn_block_mask_build_noalloc", device=cu_seqlens.device)
     batch = cu_seqlens.numel() - 1
     params = _params(role_think, dense_bits, dense_offsets)
     out = _native.AttnBlockMask()
@@ -184,13 +223,19 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, k
              lse: Optional[torch.Tensor] = None, stream=None,
              dense_bits: Optional[torch.Tensor] = None, dense_offsets: Optional[torch.Tensor] = None):
     """Masked attention forward; returns (O [T, H, D], LSE [H, T] fp32)."""
+    where = "attn_fwd"
+    _need(q, "q", where, tuple(DTYPES))
+    if q.dim() != 3:
+        raise AttnError(1, f"{where}: q must be [T, H, D]")
     T, H, D = q.shape
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        _need(t, name, where, (q.dtype,), q.shape, q.device)
+    _need(lse, "lse", where, (torch.float32,), (H, T), q.device)
+    _need_meta(where, cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets, q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
-    if q.dtype not in DTYPES:
-        raise AttnError(1, "attn_fwd: dtype must be bfloat16 or float32")
     params = _params(role_think, dense_bits, dense_offsets)
     _check(_native.lib().attn_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), DTYPES[q.dtype], T, H, D, float(scale),
@@ -220,9 +265,20 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     ``workspace`` (uint8, device) defaults to a fresh buffer of
     attn_bwd_workspace_size(bm, H) bytes; a smaller one runs the heads in groups.
     """
+    where = "attn_bwd"
+    _need(q, "q", where, tuple(DTYPES))
+    if q.dim() != 3:
+        raise AttnError(1, f"{where}: q must be [T, H, D]")
     T, H, D = q.shape
     if q.dtype != torch.bfloat16:
         raise AttnError(2, "attn_bwd: dtype must be bfloat16")
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _need(t, name, where, (q.dtype,), q.shape, q.device)
+    if o is None or dout is None or lse is None:
+        raise AttnError(1, f"{where}: o, lse and dout are required")
+    _need(lse, "lse", where, (torch.float32,), (H, T), q.device)
+    _need(workspace, "workspace", where, device=q.device)
+    _need_meta(where, cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets, q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -202,3 +202,19 @@ def test_product_path_has_no_oracle_or_fallback():
             assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), fn
     native = open(os.path.join(pkg, "_native.py")).read()
     assert "raise RuntimeError" in native
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """A host tensor's pointer must never reach a kernel: the binding refuses
+    it (ATTN_ERR_INVALID_ARG) before calling into the library."""
+    import torch
+    from block_sparse_masked_mask_gb300 import api
+    q = torch.zeros((256, 2, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((2, 256))
+    cu = torch.tensor([0, 256], dtype=torch.int32)
+    for call in (lambda: api.attn_block_mask_build("causal", cu, 256, 256),
+                 lambda: api.attn_fwd(q, q, q, None, "causal", cu, 256),
+                 lambda: api.attn_bwd(q, q, q, q, lse, q, None, "causal", cu, 256)):
+        with pytest.raises(api.AttnError) as e:
+            call()
+        assert e.value.status == 1 and "CUDA tensor" in str(e.value)

@@ -257,6 +257,36 @@ def test_mask_mismatch_and_metadata_errors():
     assert e.value.status == 4
 
 
+def test_binding_refuses_misread_tensors():
+    """Views, wrong element types and wrong shapes are refused by the binding
+    (ATTN_ERR_INVALID_ARG) instead of being read as dense [T, H, D] data."""
+    w = W.random_workload(1, "shared_prefix", [300], num_heads=2, head_dim=64)
+    dm = w.device_meta()
+    bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], w.total_tokens, w.max_seqlen,
+                                   seg_id=dm["seg_id"])
+    q = w.q.cuda()
+    seg = dm["seg_id"]
+    bad = [
+        dict(q=q.transpose(0, 1).contiguous().transpose(0, 1)),   # a strided view
+        dict(k=q.float()),                                         # k's type differs from q's
+        dict(v=q[:, :1]),                                          # wrong shape
+        dict(seg_id=seg.long()),                                   # int64 ids
+        dict(lse=torch.empty((w.total_tokens, 2), device="cuda")),  # [T, H] instead of [H, T]
+    ]
+    for over in bad:
+        kw = dict(q=q, k=q, v=q, seg_id=seg)
+        kw.update(over)
+        extra = {"lse": kw.pop("lse")} if "lse" in kw else {}
+        with pytest.raises(api.AttnError) as e:
+            api.attn_fwd(kw["q"], kw["k"], kw["v"], bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                         seg_id=kw["seg_id"], **extra)
+        assert e.value.status == 1, over.keys()
+    with pytest.raises(api.AttnError) as e:
+        api.attn_block_mask_build(w.kind, dm["cu_seqlens"].long(), w.total_tokens, w.max_seqlen,
+                                  seg_id=seg)
+    assert e.value.status == 1
+
+
 def test_repeated_forwards_on_one_mask():
     """The forward's work counters return to zero after every launch, so a
     mask serves any number of forwards with different inputs."""
