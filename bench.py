@@ -3,15 +3,22 @@
 
 One step = one pass of the whole hot path over one batch: build the block
 mask (tile summaries, exact classification, compacted lists, longest-first
-order) and run the attention forward, on inputs already resident in HBM.
-Metric: effective TFLOP/s counting only unmasked score FLOPs, 4*D*H*nnz per
-step (2*D for q.k and 2*D for p.v per visible pair), and its fraction of the
-measured dense bf16 tensor peak.
+order) once, then run the attention forward of every layer of the step
+(``--layers``, default 64; the layers of a model share one mask, which is
+built once per step and reused, the xorl issue's "Proposed work", item 3), on
+inputs already resident in HBM.  Every layer reads the workload's Q, K, V
+(805 MB on the default workload, larger than L2).  Metric: effective TFLOP/s
+counting only unmasked score FLOPs, 4*D*H*nnz per forward (2*D for q.k and
+2*D for p.v per visible pair), and its fraction of the measured dense bf16
+tensor peak.
 
 After the forward's timed steps, the backward (dQ, dK, dV for a seeded
-upstream gradient, on the forward's own O and LSE) is timed over its own K
-steps and reported under "backward", in effective TFLOP/s (10*D*H*nnz, the
-usual 2.5x the forward's count); ``--no-backward`` skips it.
+upstream gradient, on the forward's own O and LSE) is timed back to back for
+at least a second and reported under "backward", in effective TFLOP/s
+(10*D*H*nnz, the usual 2.5x the forward's count); ``--no-backward`` skips it.
+``per_config`` times the forward (and backward) of the other block-mask
+workloads (2: varlen causal, 3: shared prefix, 4: strip thinking), each back
+to back for at least a second with its own clock samples.
 
 Default workload: the 32768-token causal+document mask (12 documents, H=32,
 D=128, bf16), the largest configuration.  ``--impl reference`` times the fp64
@@ -81,7 +88,7 @@ def barrier(ws):
 class ClockSampler:
     """nvidia-smi samples during the timed region (SM clock, reasons)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -111,19 +118,27 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self):
+    def summary(self, window=None):
+        """Median SM clock and the throttle reasons seen; ``window`` = (t0, t1)
+        in host wall-clock seconds keeps only the samples taken inside it (the
+        timed region)."""
+        import datetime
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in getattr(self, "lines", []):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, top = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            if window is not None and not (window[0] <= t <= window[1]):
+                continue
+            sm.append(clk)
+            mx = top
+            for name, val in zip(names, parts[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
@@ -155,6 +170,11 @@ UNMASKED_PAIRS = {1: 2080, 2: 8_172_171, 3: 20_976_640, 4: 17_699_328, 5: 67_979
 
 def count_pairs(w, c):
     return UNMASKED_PAIRS[c]
+
+
+# kernels the library launches: a block-mask build (five kernels) and the backward
+BUILD_LAUNCHES = 5
+BWD_KERNELS = ["bwd_delta_kernel", "bwd_kpos_kernel", "attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel"]
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_causal_document_32k_h8_full.md")
@@ -256,6 +276,82 @@ def run_reference(args):
     return 0
 
 
+def time_loop(fn, stream, dev, min_seconds: float, batch: int = 8):
+    """Run ``fn`` back to back for at least ``min_seconds`` of device time, in
+    batches bracketed by CUDA events on ``stream``; returns the per-call device
+    times (ms, one batch mean per entry), the call count and the host
+    wall-clock window of the timed calls."""
+    per_call, calls = [], 0
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    while True:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(batch):
+            fn()
+        e1.record(stream)
+        e1.synchronize()
+        per_call.append(e0.elapsed_time(e1) / batch)
+        calls += batch
+        if sum(per_call) * batch >= min_seconds * 1e3:
+            break
+    return per_call, calls, (t0, time.time())
+
+
+def time_workload(c, dev, stream, peak, min_seconds, backward=True):
+    """Forward (and backward) of workload ``c`` back to back for at least
+    ``min_seconds`` each, mask built once, with clock samples of each timed
+    region."""
+    from block_sparse_masked_mask_gb300 import api
+    from block_sparse_masked_mask_gb300 import workloads as W
+    w = W.make_workload(c, tensors=True)
+    nnz = count_pairs(w, c)
+    flops = 4 * w.head_dim * w.num_heads * nnz
+    dm = w.device_meta(dev)
+    mkw = w.api_kwargs(dm)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], w.total_tokens, w.max_seqlen, **mkw)
+    out, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **mkw)
+
+    def fwd():
+        api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, out=out, lse=lse, **mkw)
+
+    for _ in range(5):
+        fwd()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        ms, calls, win = time_loop(fwd, stream, dev, min_seconds)
+    fwd_ms = sum(ms) / len(ms)
+    res = {"workload": w.name, "kind": w.kind, "total_tokens": w.total_tokens,
+           "num_heads": w.num_heads, "head_dim": w.head_dim, "unmasked_pairs_per_head": nnz,
+           "fwd_ms_mean": fwd_ms, "fwd_calls_timed": calls,
+           "fwd_tflops": flops / fwd_ms / 1e9, "fwd_frac": flops / fwd_ms / 1e9 / peak,
+           "fwd_clocks": clk.summary(win)}
+    if backward:
+        do = W.grad_output(w, seed=1).to(dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(api.attn_bwd_workspace_size(bm, w.num_heads), dtype=torch.uint8, device=dev)
+
+        def bwd():
+            api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                         dq=gq, dk=gk, dv=gv, workspace=bws, **mkw)
+
+        for _ in range(3):
+            bwd()
+        with ClockSampler(dev.index) as clk:
+            time.sleep(0.3)
+            ms, calls, win = time_loop(bwd, stream, dev, min_seconds)
+        bwd_ms = sum(ms) / len(ms)
+        res.update({"bwd_ms_mean": bwd_ms, "bwd_calls_timed": calls,
+                    "bwd_tflops_effective": 2.5 * flops / bwd_ms / 1e9,
+                    "bwd_frac_effective": 2.5 * flops / bwd_ms / 1e9 / peak,
+                    "bwd_clocks": clk.summary(win)})
+    status = api.attn_get_status(bm)
+    if status != 0:
+        raise RuntimeError(f"workload {c}: device status {api.attn_status_string(status)}")
+    return res
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -271,7 +367,9 @@ def run_ours(args):
         w.num_heads = args.heads
         w.q, w.k, w.v = (t[:, :args.heads].contiguous() for t in (w.q, w.k, w.v))
     nnz = count_pairs(w, args.workload)
-    flops = 4 * w.head_dim * w.num_heads * nnz
+    flops_fwd = 4 * w.head_dim * w.num_heads * nnz
+    L = args.layers
+    flops = flops_fwd * L  # per step
     dm = w.device_meta(dev)
     q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
     T, H, D = q.shape
@@ -283,11 +381,13 @@ def run_ours(args):
     mkw = w.api_kwargs(dm)
 
     def step(ev=None):
+        """One mask build, then the forward of each of the step's layers."""
         bm = api.attn_block_mask_build(w.kind, dm["cu_seqlens"], T, w.max_seqlen,
                                        workspace=workspace, **mkw)
         if ev is not None:
             ev.record(stream)
-        api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, out=out, lse=lse, **mkw)
+        for _ in range(L):
+            api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, out=out, lse=lse, **mkw)
         return bm
 
     for _ in range(args.warmup):
@@ -304,15 +404,17 @@ def run_ours(args):
     barrier(ws)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        time.sleep(0.2)
+        time.sleep(0.3)
+        t_wall0 = time.time()
         for i in range(args.steps):
             starts[i].record(stream)
             step(mids[i])
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
+        t_wall1 = time.time()
     barrier(ws)
     total_ms = starts[0].elapsed_time(ends[-1])
-    fwd_ms = [mids[i].elapsed_time(ends[i]) for i in range(args.steps)]
+    fwd_ms = [mids[i].elapsed_time(ends[i]) / L for i in range(args.steps)]
     build_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
     sec_per_step = reduce_max(total_ms / 1e3 / args.steps, ws)
     value = aggregate_throughput(flops, ws, sec_per_step)
@@ -322,7 +424,7 @@ def run_ours(args):
 
     peaks, peak_kind = load_peaks()
     fwd_avg_s = sum(fwd_ms) / len(fwd_ms) / 1e3
-    achieved = flops / fwd_avg_s / 1e12
+    achieved = flops_fwd / fwd_avg_s / 1e12
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "kernel": "attn_fwd_bf16_kernel<128, false>", "achieved": achieved,
                 "peak": peak, "unit": UNIT, "frac": achieved / peak,
@@ -335,50 +437,49 @@ def run_ours(args):
         roofline["traffic_source"] = traffic_src
 
     # ---- the backward on the same workload: dQ, dK, dV of the forward just
-    # timed, for a seeded upstream gradient, inputs resident (its own K steps)
+    # timed, for a seeded upstream gradient, inputs resident, back to back for
+    # at least a second
     bwd = None
     if not args.no_backward:
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         bws = torch.empty(api.attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=dev)
-        kw = mkw
 
         def bwd_step():
             api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
-                         dq=gq, dk=gk, dv=gv, workspace=bws, **kw)
+                         dq=gq, dk=gk, dv=gv, workspace=bws, **mkw)
 
         for _ in range(args.warmup):
             bwd_step()
-        b0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        b1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        torch.cuda.synchronize(dev)
-        for i in range(args.steps):
-            b0[i].record(stream)
-            bwd_step()
-            b1[i].record(stream)
-        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as bclk:
+            time.sleep(0.3)
+            bwd_ms, bwd_calls, bwin = time_loop(bwd_step, stream, dev, args.min_seconds)
         status = api.attn_get_status(bm)
         if status != 0:
             raise RuntimeError(f"device status {api.attn_status_string(status)}")
-        bwd_ms = [b0[i].elapsed_time(b1[i]) for i in range(args.steps)]
         bwd_s = sum(bwd_ms) / len(bwd_ms) / 1e3
-        eff = 2.5 * flops / bwd_s / 1e12
-        bwd = {"ms_mean": bwd_s * 1e3, "ms_min": min(bwd_ms),
+        eff = 2.5 * flops_fwd / bwd_s / 1e12
+        bwd = {"ms_mean": bwd_s * 1e3, "ms_min_batch": min(bwd_ms), "calls_timed": bwd_calls,
                "tflops_effective": eff, "frac_effective": eff / peak,
-               "flops_effective_per_step": 2.5 * flops,
-               "flop_counting": "effective = 10*D*H*nnz (five GEMMs: the usual 2.5x the "
-                                "forward), which is also what the kernels execute (dS is "
-                                "stored once and read back for dQ)",
-               "kernels": ["bwd_delta_kernel", "bwd_kpos_kernel", "attn_bwd_dkdv_kernel",
-                           "attn_bwd_dq_kernel"],
+               "flops_effective_per_step": 2.5 * flops_fwd,
+               "flop_counting": "effective = 10*D*H*nnz (five products per visible tile pair: "
+                                "S, dP, dV, dK, dQ; the usual 2.5x the forward)",
+               "kernels": BWD_KERNELS,
                "workspace_bytes": bws.numel(),
-               "gpu_launches": 4 * args.steps}
+               "clocks": bclk.summary(bwin)}
+
+    # ---- the other block-mask workloads, each timed for at least a second
+    per_config = None
+    if rank == 0 and ws == 1 and not args.no_per_config and args.workload == 5 and not args.heads:
+        per_config = {str(c): time_workload(c, dev, stream, peak, args.min_seconds,
+                                            backward=not args.no_backward) for c in (2, 3, 4)}
 
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs (Q, K, V and the mask metadata) from pinned host memory and reads
     # O and LSE back.  Two streams and two device buffer sets: the host->device
     # copy of step i+1 runs while step i builds its mask, runs the forward and
-    # copies its result back.
+    # copies its result back.  (One forward per step: each layer of a real model
+    # has its own inputs.)
     pin = lambda t: t.pin_memory()
     hq, hk, hv = pin(w.q), pin(w.k), pin(w.v)
     hmeta = {k2: (None if t is None else pin(t.cpu())) for k2, t in dm.items()}
@@ -437,9 +538,10 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_sec = reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, ws)
-    e2e = {"value": aggregate_throughput(flops, ws, e2e_sec), "unit": UNIT,
+    e2e = {"value": aggregate_throughput(flops_fwd, ws, e2e_sec), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3,
-           "pipeline": "two streams: the host->device copy of step i+1 overlaps step i"}
+           "pipeline": "two streams: the host->device copy of step i+1 overlaps step i; "
+                       "one mask build and one forward per step"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -452,17 +554,22 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(w, nnz, {
                 "parallelism": f"replicas{ws}",
+                "layers_per_step": L,
+                "step": f"one block-mask build + {L} forward passes sharing it",
+                "flops_per_step": flops,
                 "tiles_empty_partial_full": hdr[4:7],
                 "skipped_tile_ratio": hdr[4] / max(1, sum(hdr[4:7])),
-                "fwd_ms_mean": sum(fwd_ms) / len(fwd_ms), "fwd_ms_min": min(fwd_ms),
+                "timed_region_s": total_ms / 1e3,
+                "fwd_ms_mean": sum(fwd_ms) / len(fwd_ms), "fwd_ms_min_step": min(fwd_ms),
                 "build_ms_mean": sum(build_ms) / len(build_ms),
                 "fwd_tflops": achieved, "pct_of_peak_fwd": 100 * achieved / peak}),
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "clocks": clk.summary(),
+            "clocks": clk.summary((t_wall0, t_wall1)),
             "e2e": e2e,
-            "gpu_launches": 6 * args.steps,
+            "gpu_launches": (BUILD_LAUNCHES + L) * args.steps,
             "backward": bwd,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -487,6 +594,12 @@ def main():
                     help="skip the backward measurement that follows the forward's")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the head count (a smaller case of the same mask for profiling)")
+    ap.add_argument("--layers", type=int, default=64,
+                    help="forward passes per step, all sharing the step's one mask build")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="least device time of each back-to-back timing (backward, per_config)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the timings of workloads 2-4")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

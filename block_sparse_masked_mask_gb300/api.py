@@ -112,10 +112,16 @@ def attn_block_mask_workspace_size(batch: int, total_tokens: int, max_seqlen: in
 class BlockMask:
     """A built block mask: the C struct plus the tensors it points into."""
 
-    def __init__(self, struct: _native.AttnBlockMask, workspace: torch.Tensor, keep: tuple):
+    # arrays attn_block_mask_build_noalloc keeps in its own scratch and does not
+    # write to the workspace
+    NOALLOC_UNWRITTEN = ("labels", "qt_off", "pair_off")
+
+    def __init__(self, struct: _native.AttnBlockMask, workspace: torch.Tensor, keep: tuple,
+                 noalloc: bool = False):
         self.struct = struct
         self.workspace = workspace
         self._keep = keep  # metadata tensors must outlive the mask
+        self.noalloc = noalloc
 
     # -- read-back helpers (copy device arrays to the host; synchronising) --
     def _array(self, off: int, count: int, dtype) -> torch.Tensor:
@@ -131,13 +137,15 @@ class BlockMask:
         return int(self.header()[0])
 
     def lists(self) -> dict:
-        """Device arrays copied back: q-tile descriptors, labels, CSR lists, order."""
+        """Device arrays copied back: q-tile descriptors, labels, CSR lists, order.
+        A mask from the no-allocation builder has no ``labels``, ``qt_off`` or
+        ``pair_off`` (never written to its workspace); they are left out."""
         s = self.struct
         n = self.n_qtiles
         hdr = self.header()
         nent = int(hdr[1])
         koff = self._array(s.off_koff, n + 1, torch.int32)
-        return {
+        out = {
             "header": hdr,
             "qt_seq": self._array(s.off_qt_seq, n, torch.int32),
             "qt_idx": self._array(s.off_qt_idx, n, torch.int32),
@@ -158,6 +166,10 @@ class BlockMask:
             "qlabel": self._array(s.off_qlabel, nent, torch.uint8),
             "korder": self._array(s.off_korder, n, torch.int32),
         }
+        if self.noalloc:
+            for name in self.NOALLOC_UNWRITTEN:
+                del out[name]
+        return out
 
 
 def _params(role_think: int, dense_bits, dense_offsets) -> "_native.AttnMaskParams":
@@ -201,7 +213,9 @@ def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: 
     fixed 4 MiB array inside the library, shared by every call on the device,
     so calls must not overlap on the GPU.  The first call on a device does a
     one-time address lookup and should come before any stream capture.  Only
-    the arrays the forward reads are stored (``labels`` is not).
+    the arrays the forward and backward read are stored (``labels``, ``qt_off``
+    and ``pair_off`` are not).  The scratch serves up to 259,968 tokens in
+    one sequence (2031 tiles); larger problems are refused.
     """
     _need_meta("attn_block_mask_build_noalloc", cu_seqlens, seg_id, role, turn, dense_bits,
                dense_offsets)
@@ -214,7 +228,8 @@ def attn_block_mask_build_noalloc(kind, cu_seqlens: torch.Tensor, total_tokens: 
         _ptr(seg_id), _ptr(role), _ptr(turn), BLOCK_M, BLOCK_N, _ptr(workspace),
         workspace.numel() * workspace.element_size(), ctypes.byref(out), _stream(stream)),
         "attn_block_mask_build_noalloc")
-    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets))
+    return BlockMask(out, workspace, (cu_seqlens, seg_id, role, turn, dense_bits, dense_offsets),
+                     noalloc=True)
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, kind,

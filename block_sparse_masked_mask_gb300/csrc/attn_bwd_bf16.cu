@@ -107,6 +107,7 @@ struct BwdCfg : TileLayout<D> {
 
 struct BwdParams {
   int32_t* header;
+  int sched;              // this launch's work-counter slot
   const int32_t* order;   // items' tile order (q-major for dQ, k-major for dK/dV)
   const int32_t* qt_seq;
   const int32_t* qt_idx;
@@ -177,7 +178,7 @@ __device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, 
                                            volatile int* ring, uint32_t iempty0, uint32_t ifull0,
                                            volatile uint32_t* abort_flag, int32_t* err) {
   int ticket = 0;
-  if (lane == 0) ticket = atomicAdd(p.header + kHdrTicket, 1);
+  if (lane == 0) ticket = take_ticket(p.sched);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   const bool valid = ticket < n_items;
   if (valid) it = bwd_decode(p, ticket, n_t);
@@ -564,13 +565,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
-      atomicExch(p.header + kHdrTicket, 0);
-      atomicExch(p.header + kHdrFinished, 0);
-    }
-  }
+  if (threadIdx.x == 0) finish_sched(p.sched);
 }
 
 // k-major position of every q-major entry: for the pair (q-tile i, k-tile j),
@@ -1063,13 +1058,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
-      atomicExch(p.header + kHdrTicket, 0);
-      atomicExch(p.header + kHdrFinished, 0);
-    }
-  }
+  if (threadIdx.x == 0) finish_sched(p.sched);
 }
 
 template <int D>
@@ -1081,20 +1070,17 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
       !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mdo, a.dout, a.total_tokens, a.num_heads))
     return record_cuda_error(cudaErrorInvalidValue, "attn_bwd tensor map encoding");
-  static bool configured = false;
-  if (!configured) {
+  // per launch, for the current device (the settings are per device and context)
+  {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Q::SMEM_ALLOC);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd configure");
-    configured = true;
   }
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  int num_sms = 0;
+  {
+    const cudaError_t e = current_sm_count(&num_sms);
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd device query");
   }
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -1139,6 +1125,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
     p.label = a.bm.qlabel;
     p.out0 = static_cast<__nv_bfloat16*>(a.dk);
     p.out1 = static_cast<__nv_bfloat16*>(a.dv);
+    p.sched = next_sched_slot();
     attn_bwd_dkdv_kernel<D><<<grid, kDkdvThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
@@ -1148,6 +1135,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
     p.label = a.bm.klabel;
     p.out0 = static_cast<__nv_bfloat16*>(a.dq);
     p.out1 = nullptr;
+    p.sched = next_sched_slot();
     attn_bwd_dq_kernel<D><<<grid, kBwdThreads, Q::SMEM_ALLOC, s>>>(mk, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dq launch");

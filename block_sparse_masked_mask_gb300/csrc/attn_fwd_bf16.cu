@@ -94,6 +94,7 @@ struct Cfg : TileLayout<D> {
 
 struct FwdParams {
   int32_t* header;
+  int sched;         // this launch's work-counter slot
   const int32_t* order;
   const int32_t* qt_seq;
   const int32_t* qt_idx;
@@ -158,7 +159,7 @@ __device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane,
                                             Item& it, volatile int* item_ring, uint32_t iempty0,
                                             uint32_t ifull0, volatile uint32_t* abort_flag, int32_t* err) {
   int ticket = 0;
-  if (lane == 0) ticket = atomicAdd(p.header + kHdrTicket, 1);
+  if (lane == 0) ticket = take_ticket(p.sched);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   const bool valid = ticket < n_items;
   if (valid) it = decode_item(p, ticket, n_qt);
@@ -177,8 +178,9 @@ __device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane,
 // longest work first).  The K producer takes the tickets, decodes them one item
 // ahead and passes them to the other roles through a two-slot ring in shared
 // memory.  Barrier phases run on across items: the next item's Q load and
-// first S MMAs overlap the current item's last P.V and O epilogue.  The last
-// CTA to finish returns the counters to zero for the next launch.
+// first S MMAs overlap the current item's last P.V and O epilogue.  The
+// counters are this launch's slot of the scheduler pool; the last CTA to
+// finish returns them to zero.
 // kDense: the instantiation for ATTN_MASK_DENSE; the others leave its code out
 // (the softmax loop is sensitive to its own size).
 template <int D, bool kDense>
@@ -780,15 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
-    // Every CTA has taken its last ticket before it counts itself finished, so
-    // the last one can return both counters to zero for the next launch.
-    __threadfence();
-    if (atomicAdd(p.header + kHdrFinished, 1) == int(gridDim.x) - 1) {
-      atomicExch(p.header + kHdrTicket, 0);
-      atomicExch(p.header + kHdrFinished, 0);
-    }
-  }
+  if (threadIdx.x == 0) finish_sched(p.sched);
 }
 
 
@@ -800,14 +794,13 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
       !make_map<D>(&mk, a.k, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads))
     return record_cuda_error(cudaErrorInvalidValue, "attn_fwd tensor map encoding");
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_ALLOC);
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
-    configured = true;
-  }
+  // per launch, for the current device (the setting is per device and context)
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel<D, kDense>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
+  int num_sms = 0;
+  e = current_sm_count(&num_sms);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd device query");
   FwdParams p;
   p.header = a.bm.header;
   p.order = a.bm.order;
@@ -823,20 +816,14 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.sched = next_sched_slot();
   // Persistent: one CTA per SM (the q-tile count is only known on the device;
   // max_qt * H bounds the item count).
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd device query");
-  }
   const long long items = (long long)a.bm.max_qt * a.num_heads;
   if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const long long grid = items < num_sms ? items : num_sms;
   attn_fwd_bf16_kernel<D, kDense><<<unsigned(grid), kThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, p);
-  const cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");
 }
 

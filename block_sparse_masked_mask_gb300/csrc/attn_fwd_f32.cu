@@ -129,13 +129,10 @@ template <int D>
 attn_status launch(const FwdArgs& a, cudaStream_t s) {
   const size_t smem = (size_t(kTile) * (D + 1) + 2 * kChunk * D + size_t(kTile) * (kChunk + 1)) * sizeof(float) +
                       kChunk * sizeof(int);
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(attn_fwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
-    configured = true;
-  }
+  // per launch, for the current device (the setting is per device and context)
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_fwd configure");
   F32Params p;
   p.header = a.bm.header;
   p.order = a.bm.order;
@@ -157,7 +154,7 @@ attn_status launch(const FwdArgs& a, cudaStream_t s) {
   const long long grid = (long long)a.bm.max_qt * a.num_heads;
   if (grid <= 0 || grid > INT_MAX) return ATTN_ERR_UNSUPPORTED;
   attn_fwd_f32_kernel<D><<<unsigned(grid), 128, smem, s>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : record_cuda_error(e, "attn_fwd launch");
 }
 

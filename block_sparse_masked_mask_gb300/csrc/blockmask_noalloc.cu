@@ -17,10 +17,14 @@
 //  * The scratch holds kNoallocScratchBytes (4 MiB).  A problem whose scratch
 //    would not fit (max_qtiles * max_ktiles + 32 * max_qtiles + 8 * (batch + 1)
 //    bytes, each part rounded up to 256 bytes) is rejected with
-//    ATTN_ERR_UNSUPPORTED before anything is launched.
+//    ATTN_ERR_UNSUPPORTED before anything is launched.  For one sequence that
+//    is up to 259,968 tokens (2031 tiles).
 //  * The first call on a device looks up the array's device address with that
 //    device current (a one-time set-up).  Make that first call before any
-//    stream capture.
+//    stream capture.  The address is kept for the life of the process: after
+//    cudaDeviceReset (or anything else that destroys and recreates the
+//    device's primary context) it names memory of the old context, so a
+//    process that resets a device must not call this entry point on it again.
 //  * Every call on a device shares the one array and leaves its contents in
 //    place.  Calls whose kernels overlap on the GPU (other streams, other host
 //    threads) race on it; serialise them.  Nothing in the scratch has to start

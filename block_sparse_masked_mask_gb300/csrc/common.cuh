@@ -26,11 +26,10 @@ enum : int32_t {
   kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong | kErrCapacity,
 };
 
-// kHdrTicket / kHdrFinished: the forward's work-item counter and finished-CTA
-// counter; zeroed by the build, returned to zero by the last CTA of every
-// forward launch.
+// Header words of the block-mask workspace (the kernels' work counters are
+// per launch, not here: words 7 and up are reserved and zeroed by the build).
 enum : int { kHdrQtiles = 0, kHdrEntries = 1, kHdrError = 2, kHdrPairs = 3, kHdrEmpty = 4,
-             kHdrPartial = 5, kHdrFull = 6, kHdrTicket = 8, kHdrFinished = 9, kHdrInts = 16 };
+             kHdrPartial = 5, kHdrFull = 6, kHdrInts = 16 };
 
 enum : int { kSumInts = 8 };  // ints per tile summary
 

@@ -4,17 +4,65 @@
 // products), tensor-map encoding, and the mask-code helpers.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
 
+// Bound on one pipeline wait.  A build may lower it (-DATTN_WAIT_TIMEOUT_NS=...)
+// to make ordinary waits run out and exercise the abort path; the library
+// itself uses 1 s, far above any legitimate wait.
+#ifndef ATTN_WAIT_TIMEOUT_NS
+#define ATTN_WAIT_TIMEOUT_NS 1000000000ull
+#endif
+
 namespace attnmask {
 namespace {
 
-constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: far above any legitimate wait
+constexpr uint64_t kWaitTimeoutNs = ATTN_WAIT_TIMEOUT_NS;
 constexpr uint64_t kDrainTimeoutNs = 200000000ull;  // bound on waiting for in-flight work
+
+// Work counters of the persistent kernels.  Each launch takes one slot of a
+// small per-device pool (file scope, so every translation unit that includes
+// this header has its own): [0] the next work ticket, [1] the CTAs that have
+// finished.  The last CTA of a launch returns its slot to zero.  Because the
+// counters belong to the launch, not to the block mask, launches that share a
+// mask may overlap on the GPU; two launches collide only if more than
+// kSchedSlots launches of one translation unit's kernels are in flight on a
+// device at once.
+constexpr int kSchedSlots = 256;
+__device__ int32_t g_sched[kSchedSlots][2] = {};
+
+// Host: the slot of the next launch (round robin).
+inline int next_sched_slot() {
+  static std::atomic<uint32_t> next{0};
+  return int(next.fetch_add(1u, std::memory_order_relaxed) % uint32_t(kSchedSlots));
+}
+
+__device__ __forceinline__ int take_ticket(int slot) { return atomicAdd(&g_sched[slot][0], 1); }
+
+// Called once per CTA (one thread) after its last ticket: every CTA has taken
+// its last ticket before it counts itself finished, so the last one can
+// return both counters to zero for the next launch using the slot.
+__device__ __forceinline__ void finish_sched(int slot) {
+  __threadfence();
+  if (atomicAdd(&g_sched[slot][1], 1) == int(gridDim.x) - 1) {
+    atomicExch(&g_sched[slot][0], 0);
+    atomicExch(&g_sched[slot][1], 0);
+  }
+}
+
+// Launch settings, queried on every launch for the current device (cheap
+// runtime calls): they then follow the caller across devices and threads.
+inline cudaError_t current_sm_count(int* n) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  return e;
+}
 
 // A 128-row x D bf16 tile as TMA writes it: D split into row chunks of 128 B
 // (64 B for D = 32), each chunk 128 rows with the matching swizzle.

@@ -1,9 +1,14 @@
 """Seeded synthetic inputs for the structured-mask attention forward.
 
-This module only *generates data*: sequence lengths, per-token segment / role /
-turn metadata and random Q, K, V.  It holds none of the method's arithmetic
-(no predicate, no softmax, no tiling), so both the CUDA path and the fp64
-oracle can be fed from it without sharing any code that computes a result.
+This module generates data: sequence lengths, per-token segment / role / turn
+metadata and random Q, K, V.  It holds none of the method's arithmetic (no
+softmax, no tiling, no tile classification), so both the CUDA path and the
+fp64 oracle can be fed from it without sharing any code that computes a
+result.  One generator composes a mask itself: the DENSE kind's input bits of
+workload 8 (``causal_document_padding_bits``), which a caller of that kind
+supplies by definition.  The library only reads those bits; the oracle pins
+the composition independently (its causal + document + padding equals the
+sequence with the padding removed).
 
 The six workloads follow the shapes the block-mask pages describe:
 
@@ -295,9 +300,12 @@ def pack_rows(rows: np.ndarray, pad_rng: Optional[np.random.Generator] = None) -
 
 
 def causal_document_padding_bits(seg: np.ndarray, block: int = 128):
-    """A caller's dense mask for one sequence composed as the pages' causal +
-    document + padding: key at or before the query, same document id, and
-    neither token padding (id < 0).  Returns (bits uint32, offsets int64 [2])."""
+    """The caller's input of the DENSE kind for workload 8: one sequence's bit
+    rows composed as the pages' causal + document + padding (key at or before
+    the query, same document id, neither token padding, id < 0).  This is input
+    data, like seg_id for the other kinds: the library reads the bits and the
+    oracle checks the composition on its own.  Returns (bits uint32, offsets
+    int64 [2])."""
     L = len(seg)
     rows = []
     for r0 in range(0, L, block):

@@ -61,6 +61,11 @@
  * Conventions
  *   - Every array argument is a DEVICE pointer owned by the caller unless the
  *     comment says otherwise.  The library allocates no device memory.
+ *   - The persistent kernels take their work counters from a small pool held
+ *     by the library on each device (256 slots per kernel family, handed out
+ *     round robin, each returned to zero by its launch's last CTA).  Up to
+ *     256 forward and 256 backward launches may therefore be in flight on a
+ *     device at once, on any streams; more than that could share a slot.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream) and return after host-side argument checks; a returned
  *     error means nothing was launched.
@@ -140,11 +145,11 @@ typedef struct attn_mask_params {
  * comments, with NQ = max_qtiles and NK = max_ktiles.
  *   off_header  int32[16]: [0] n_qtiles, [1] n_entries (sum of kcount),
  *               [2] error bits, [3] n_qpairs, [4] EMPTY, [5] PARTIAL,
- *               [6] FULL tile-pair totals, [8] [9] the work counters of
- *               the forward and backward kernels (zero between launches),
- *               others reserved.  Because of [8] and [9], attn_fwd and
- *               attn_bwd calls that share one block mask must not run
- *               concurrently (same stream, or ordered).
+ *               [6] FULL tile-pair totals, others reserved.  The kernels
+ *               only read the mask (their work counters belong to each
+ *               launch), so attn_fwd and attn_bwd calls that share one block
+ *               mask may run concurrently on different streams, as long as
+ *               no attn_block_mask_build rewrites the workspace meanwhile.
  *   off_qt_seq  int32[NQ]       sequence of each q-tile (q-tiles are numbered
  *                               sequence-major, ascending inside a sequence)
  *   off_qt_idx  int32[NQ]       index of the q-tile inside its sequence
@@ -299,8 +304,8 @@ ATTN_API attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t 
  * rounded to nearest even.  Deterministic: each output row is summed by one
  * CTA in a fixed tile order, with no atomics.  Inputs must be finite inside
  * each sequence.  Only ATTN_DTYPE_BF16 exists (ATTN_ERR_UNSUPPORTED
- * otherwise).  Launches that share one block mask must not run concurrently
- * with each other or with attn_fwd() (header [8], [9]).
+ * otherwise).  Launches that share one block mask may run concurrently with
+ * each other and with attn_fwd() on other streams.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -326,10 +331,13 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
  *     the library instead; they are not kept, so off_labels, off_summary,
  *     off_qt_off and off_pair_off name unwritten workspace regions.
  *   - Needs max_qtiles * max_ktiles + 32 * max_qtiles + 8 * (batch + 1) bytes
- *     of that array (each part rounded up to 256); larger problems return
- *     ATTN_ERR_UNSUPPORTED and launch nothing.
+ *     of that array (each part rounded up to 256): up to 259,968 tokens in one
+ *     sequence; larger problems return ATTN_ERR_UNSUPPORTED and launch
+ *     nothing.
  *   - The first call on a device looks up the array's address with that device
- *     current; make that first call before any stream capture.
+ *     current; make that first call before any stream capture.  The address is
+ *     kept for the life of the process, so after cudaDeviceReset (which makes a
+ *     new context) this entry point must not be called on that device again.
  *   - All calls on a device share the array: calls whose kernels overlap on the
  *     GPU race and must be serialised by the caller.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.

@@ -293,3 +293,39 @@ def test_head_groups_match_one_pass_bit_exact():
         api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
                      workspace=torch.empty(base + head - 256, dtype=torch.uint8, device="cuda"), **kw)
     assert e.value.status == 3
+
+
+def test_one_mask_serves_overlapping_forward_and_backward():
+    """One block mask, built once, serves forwards on one stream while backwards
+    run on another (the reuse across layers the xorl issue asks for, Proposed
+    work, item 3): the kernels only read the mask, their work counters belong
+    to each launch.  Every result matches the oracle and equals the serial run
+    bit for bit."""
+    w = W.random_workload(81, "strip_thinking", [1500, 700, 257], num_heads=4, head_dim=128)
+    do = W.grad_output(w, seed=81)
+    dm = w.device_meta()
+    bm = build_mask(w, dm)
+    kw = w.api_kwargs(dm)
+    q, k, v, dod = w.q.cuda(), w.k.cuda(), w.v.cuda(), do.cuda()
+    o, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+    g_ser = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    fwd_out, bwd_out = [], []
+    for _ in range(4):
+        with torch.cuda.stream(sa):
+            fwd_out.append(api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw))
+        with torch.cuda.stream(sb):
+            bwd_out.append(api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"],
+                                        w.max_seqlen, **kw))
+    torch.cuda.synchronize()
+    assert api.attn_get_status(bm) == api.ATTN_OK
+    for o2, l2 in fwd_out:
+        assert torch.equal(o2, o) and torch.equal(l2, lse)
+    for g in bwd_out:
+        for x, y in zip(g, g_ser):
+            assert torch.equal(x, y)
+    O, L = oracle.attention(w.q, w.k, w.v, w.kind, w.cu_seqlens, w.meta())
+    assert np.abs(o.float().cpu().numpy() - O).max() <= 2e-2
+    assert np.abs(lse.cpu().numpy() - L).max() <= 1e-3
+    compare_all(w, do, tuple(x.cpu() for x in g_ser))
