@@ -174,7 +174,7 @@ def count_pairs(w, c):
 
 # kernels the library launches: a block-mask build (five kernels) and the backward
 BUILD_LAUNCHES = 5
-BWD_KERNELS = ["bwd_delta_kernel", "bwd_kpos_kernel", "attn_bwd_dkdv_kernel", "attn_bwd_dq_kernel"]
+BWD_KERNELS = ["bwd_zero_kernel", "bwd_prep_kernel", "attn_bwd_kernel", "bwd_dq_convert_kernel"]
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_causal_document_32k_h8_full.md")
@@ -330,7 +330,7 @@ def time_workload(c, dev, stream, peak, min_seconds, backward=True):
     if backward:
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        bws = torch.empty(api.attn_bwd_workspace_size(bm, w.num_heads), dtype=torch.uint8, device=dev)
+        bws = torch.empty(api.attn_bwd_workspace_size(bm, w.num_heads, w.head_dim), dtype=torch.uint8, device=dev)
 
         def bwd():
             api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
@@ -443,7 +443,7 @@ def run_ours(args):
     if not args.no_backward:
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        bws = torch.empty(api.attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=dev)
+        bws = torch.empty(api.attn_bwd_workspace_size(bm, H, D), dtype=torch.uint8, device=dev)
 
         def bwd_step():
             api.attn_bwd(q, k, v, out, lse, do, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,

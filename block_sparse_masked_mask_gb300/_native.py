@@ -90,7 +90,7 @@ def lib() -> ctypes.CDLL:
         c_int32, ctypes.c_float, c_void_p, c_int32, c_int32, ctypes.c_int, P(AttnMaskParams),
         c_void_p, c_void_p, c_void_p, P(AttnBlockMask), c_void_p]
     L.attn_fwd.restype = ctypes.c_int
-    L.attn_bwd_workspace_size.argtypes = [P(AttnBlockMask), c_int32, P(ctypes.c_size_t)]
+    L.attn_bwd_workspace_size.argtypes = [P(AttnBlockMask), c_int32, c_int32, P(ctypes.c_size_t)]
     L.attn_bwd_workspace_size.restype = ctypes.c_int
     L.attn_bwd.argtypes = [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

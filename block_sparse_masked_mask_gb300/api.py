@@ -260,10 +260,12 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bm: BlockMask, k
     return out, lse
 
 
-def attn_bwd_workspace_size(bm: BlockMask, num_heads: int) -> int:
-    """Bytes of backward workspace that run all heads in one pass."""
+def attn_bwd_workspace_size(bm: BlockMask, num_heads: int, head_dim: int) -> int:
+    """Bytes of device workspace attn_bwd needs: D and ||dO_i|| per row and
+    head, per-sequence bound words and the int32 fixed-point dQ accumulator,
+    O(T H D)."""
     out = ctypes.c_size_t()
-    _check(_native.lib().attn_bwd_workspace_size(ctypes.byref(bm.struct), num_heads,
+    _check(_native.lib().attn_bwd_workspace_size(ctypes.byref(bm.struct), num_heads, head_dim,
                                                  ctypes.byref(out)), "attn_bwd_workspace_size")
     return int(out.value)
 
@@ -278,7 +280,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     """Masked attention backward (bf16); returns (dQ, dK, dV), each [T, H, D].
 
     ``workspace`` (uint8, device) defaults to a fresh buffer of
-    attn_bwd_workspace_size(bm, H) bytes; a smaller one runs the heads in groups.
+    attn_bwd_workspace_size(bm, H, D) bytes.
     """
     where = "attn_bwd"
     _need(q, "q", where, tuple(DTYPES))
@@ -298,7 +300,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(attn_bwd_workspace_size(bm, H), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(attn_bwd_workspace_size(bm, H, D), dtype=torch.uint8, device=q.device)
     params = _params(role_think, dense_bits, dense_offsets)
     _check(_native.lib().attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),

@@ -52,20 +52,17 @@ bool bm_layout(int batch, int total_tokens, int max_seqlen, BmLayout* out) {
   return true;
 }
 
-bool bwd_layout(int kind, int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out) {
-  BmLayout bl;
-  if (num_heads < 1 || !bm_layout(batch, total_tokens, max_seqlen, &bl)) return false;
-  const uint64_t nq = uint64_t(bl.max_qt), nk = uint64_t(bl.max_nt);
-  uint64_t e = kind_causal(kind) ? (nq * (nk + 1) + 1) / 2 : nq * nk;
-  if (e > nq * nk) e = nq * nk;
-  if (e > uint64_t(INT_MAX)) return false;
+bool bwd_layout(int batch, int total_tokens, int num_heads, int head_dim, int max_qt, BwdLayout* out) {
+  if (batch < 1 || total_tokens < 0 || num_heads < 1 || head_dim < 1 || max_qt < 0) return false;
+  const uint64_t H = uint64_t(num_heads), T = uint64_t(total_tokens);
   BwdLayout l;
-  l.e_bound = int(e);
-  l.delta = 0;
-  l.kpos = align256(uint64_t(num_heads) * uint64_t(total_tokens) * 4u);
-  l.ds = align256(l.kpos + 4u * (e ? e : 1));
-  l.ds_per_head = e * uint64_t(kTile) * kTile * 2u;
-  l.total = l.ds + uint64_t(num_heads) * l.ds_per_head;
+  uint64_t p = 0;
+  auto take = [&](uint64_t bytes) { uint64_t at = p; p = align256(p + (bytes ? bytes : 1)); return at; };
+  l.side = take(4 * H * uint64_t(max_qt) * kBwdSideFloats);
+  l.dnorm = take(4 * H * T);
+  l.bounds = take(4 * uint64_t(batch) * H * 4);
+  l.dqacc = take(4 * T * H * uint64_t(head_dim));
+  l.total = p;
   *out = l;
   return true;
 }
@@ -274,10 +271,12 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   return dtype == ATTN_DTYPE_BF16 ? launch_attn_fwd_bf16(a, s) : launch_attn_fwd_f32(a, s);
 }
 
-attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads, size_t* bytes) {
+attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads, int32_t head_dim,
+                                    size_t* bytes) {
   if (bm == nullptr || bytes == nullptr || num_heads < 1) return ATTN_ERR_INVALID_ARG;
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
   BwdLayout l;
-  if (!bwd_layout(bm->kind, bm->batch, bm->total_tokens, bm->max_seqlen, num_heads, &l))
+  if (!bwd_layout(bm->batch, bm->total_tokens, num_heads, head_dim, bm->max_qtiles, &l))
     return ATTN_ERR_INVALID_ARG;
   if (l.total > uint64_t(SIZE_MAX)) return ATTN_ERR_INVALID_ARG;
   *bytes = size_t(l.total);
@@ -313,8 +312,8 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (uint64_t(total_tokens) * uint64_t(num_heads) * uint64_t(head_dim) > (uint64_t(1) << 40))
     return ATTN_ERR_UNSUPPORTED;
   BwdLayout l;
-  if (!bwd_layout(kind, batch, total_tokens, max_seqlen, num_heads, &l)) return ATTN_ERR_INVALID_ARG;
-  if (uint64_t(workspace_bytes) < l.ds + l.ds_per_head) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  if (!bwd_layout(batch, total_tokens, num_heads, head_dim, bm->max_qtiles, &l)) return ATTN_ERR_INVALID_ARG;
+  if (uint64_t(workspace_bytes) < l.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   if (total_tokens == 0) return ATTN_OK;
 
   BwdArgs a;
@@ -329,8 +328,6 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.dv = dv;
   a.workspace = workspace;
   a.ws = l;
-  const uint64_t fit = (uint64_t(workspace_bytes) - l.ds) / (l.ds_per_head ? l.ds_per_head : 1);
-  a.heads_per_pass = int(fit < uint64_t(num_heads) ? fit : uint64_t(num_heads));
   a.total_tokens = total_tokens;
   a.num_heads = num_heads;
   a.head_dim = head_dim;

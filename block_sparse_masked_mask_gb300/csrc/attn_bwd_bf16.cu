@@ -6,23 +6,60 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // The xorl issue (Verified FA4 gaps, items 1-3) asks for this backward over
 // the block-sparse masks, walking the transposed (k-major) lists for dK and
-// dV, and with a deterministic dQ.  Four kernels:
-//   * delta: D = rowsum(dO * O) per (token, head), fp32;
-//   * kpos: for every q-major entry, its position in the k-major lists;
-//   * dK/dV: one work item per (k-tile, head) walks its k-major list of
-//     q-tiles, recomputing S^T and dP^T, accumulating dK and dV in TMEM (K, V
-//     stay in shared memory), and stores every dS tile once as a 32 KB bf16
-//     block in the caller's workspace;
-//   * dQ: one work item per (q-tile, head) walks its q-major list of k-tiles
-//     and accumulates dQ = scale dS K in TMEM from the stored blocks.  dQ is a
-//     sum over k-tiles in a fixed order inside one CTA, so it is
-//     bit-reproducible, with no atomics.
-// Five products per tile pair (S, dP, dV, dK, dQ); the masks are applied on
-// PARTIAL tiles only and EMPTY tiles are never loaded.  Warp roles: dK/dV
-// (384 threads) eight row warps (two per TMEM lane quarter, one per half of
-// the queries), the TMA producer, the tcgen05 issuer, two idle; dQ (256
-// threads) four epilogue warps, the producer and the issuer.  Every mbarrier
-// wait is bounded as in the forward.
+// dV, and with a deterministic dQ.  Kernels:
+//   * zero: clears the per-(sequence, head) bound words;
+//   * prep: per (q-tile, head): D = rowsum(dO * O) and ||dO_i|| of every row
+//     in fp32, the largest ||V_j|| and |K_jd| of each (sequence, head), and
+//     zeroes the q-tile's rows of the dQ accumulator;
+//   * main: one work item per (k-tile, head) walks its k-major list of
+//     q-tiles.  Per entry it forms S^T and dP^T in TMEM, P^T and dS^T in the
+//     row warps, then dV += P^T dO and dK += dS^T Q (K, V stay in shared
+//     memory for the item) and dQ_i^T = K^T dS^T (dS kept in shared memory,
+//     never in HBM).  Four reducer warps add each dQ^T tile into the
+//     accumulator in HBM;
+//   * convert: dQ = scale * accumulator * quantum, rounded to bf16.
+// Five products per tile pair (S, dP, dV, dK, dQ), no per-pair HBM traffic:
+// the workspace is O(T H D).
+//
+// Deterministic dQ without ordering: the accumulator is exact int32 fixed
+// point.  Row i's contribution from one k-tile is added in quanta q_i =
+// B_i 2^-30, where B_i bounds every partial sum of the row: with P_ij <= 1,
+// sum_j P_ij = 1, |dP_ij| <= ||dO_i|| ||V_j|| and |D_i| = |sum_j P_ij dP_ij|
+// <= ||dO_i|| max_j ||V_j||, every partial sum of dS_ij K_jd over keys j is
+// at most 2 ||dO_i|| max_j ||V_j|| max_jd |K_jd| in magnitude, and B_i is
+// twice that (headroom for the rounding of P and dS to bf16).  So the
+// integer sums stay below 2^29 in magnitude, integer addition is exact and
+// order-independent, and every call gives the same bits whatever order the
+// CTAs add in (no atomics on floats, no turn-taking).  The quantum follows
+// the row's own ||dO_i|| (rows with a small upstream gradient get a fine
+// one) and is at most 2^-29 of the largest value the row's sum can reach;
+// the rounding adds at most q_i / 2 per contribution.  The row warps scale
+// the bf16 copy of dS that feeds dQ^T by m_i = 1 / q_i (rounded to bf16;
+// the convert kernel divides by the same value), so the product comes out
+// of the tensor cores already in quanta and the reducers only round and
+// add.  The maxima over V and K use only the sequence's own tokens, so the
+// result does not depend on what else is packed with it.
+//
+// Items are taken head-major (all k-tiles of head 0 longest list first, then
+// head 1, ...), so at any time the CTAs add into the accumulator rows of one
+// or two heads (17 MB per head on the 32k workload), which stay in L2.
+//
+// Each entry (q-tile) runs as two units of 64 queries, one per TMEM buffer,
+// so that the tensor pipe works on one unit while the row warps work on the
+// other.  Two threads issue the products: one the scores of each unit, the
+// other (once the row warps are done with a unit) its dV, dK and dQ^T, so
+// that the tensor pipe has work from one while the other waits for a buffer.
+// Warp roles of the main kernel (512 threads): warps 0-7 the row warps (warp
+// w owns TMEM lanes, i.e. keys, 32 (w % 4) .. +31 and, in each unit, query
+// columns 32 (w / 4) .. +31), warp 8 the TMA producer, warps 9 and 10 the
+// tcgen05 issuers (scores; dV, dK and dQ^T), warps 12-19 the dQ reducers (warp
+// 12 + r + 4 c owns TMEM lanes, i.e. head dims, 32 r .. +31 and query columns
+// 32 c .. +31 of each unit), warp 11 idle.  The row warpgroups run with kRegsRow
+// registers a thread, the other two with kRegsLoad and kRegsRed (setmaxnreg,
+// within the 128 x 512 of the launch).
+// TMEM: dV [0, D), dK [128, 128 + D), then per buffer h: S^T [256 + 128 h,
+// +64) (then P^T and dS^T in bf16 over it) and dP^T [320 + 128 h, +64) (then
+// dQ^T over it).  Every mbarrier wait is bounded as in the forward.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -33,48 +70,199 @@
 namespace attnmask {
 namespace {
 
-constexpr int kBwdThreads = 256;                        // dQ kernel: 4 epilogue warps, producer, MMA
-constexpr int kDkdvThreads = 384;                       // dK/dV kernel: 8 row warps, producer, MMA, 2 idle
-constexpr int kDkdvLoad = 8, kDkdvMma = 9;
-// The producers copy an item's list to shared memory this many entries at a
-// time, so that no list read sits between a free slot and the next copy.
-constexpr int kPlist = 256;
-constexpr int kWarpLoad = 4, kWarpMma = 5;
+constexpr int kBwdThreads = 640;
+constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpTail = 10, kWarpRed = 12;  // reducers: warps 12-19
+// registers a thread per warpgroup: rows (two warpgroups), producer + MMA,
+// reducers (two warpgroups); the launch gives 96 a thread (640 x 96 <= 65536),
+// 2 x 128 x kRegsRow + 128 x kRegsLoad + 2 x 128 x kRegsRed <= 640 x 96
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsRow = 136, kRegsLoad = 80, kRegsRed = 64;
+static_assert(2 * kRegsRow + kRegsLoad + 2 * kRegsRed <= 5 * kRegsLaunch, "register budget of the launch");
+static_assert(kRegsRow > kRegsLaunch && kRegsLoad < kRegsLaunch && kRegsRed < kRegsLaunch,
+              "the row warps grow, the others shrink");
+constexpr int kItemInts = 12;
+// dS of one entry as it sits in shared memory: 128 keys x 128 queries bf16,
+// in sixteen 2 KB chunks of eight queries; in chunk c, key k's eight queries
+// q = 8c .. 8c+7 are the 16 bytes at k * 16 (the MN-major operand layout
+// without swizzle: eight-key core matrices 128 bytes apart along K, chunks
+// 2 KB apart along N).  A row-warp thread, which holds one key's dS for 32
+// queries at a time, writes it as four 16-byte pieces, and the 32 lanes of a
+// warp (32 consecutive keys) write 512 contiguous bytes per chunk.
+constexpr int kDsBlock = kTile * kTile * 2;
+constexpr int kDsChunk = 2048;
+// Bound words per (sequence, head): max ||V_j||, max |K_jd| (non-negative
+// floats, so their bit patterns order like ints), two words unused.
+constexpr int kBoundWords = 4;
+constexpr float kFixScale = 1073741824.0f;  // 2^30: the quantum is B_i / 2^30
+
+// B_i / ||dO_i|| of a (sequence, head) from its bound words.
+__device__ __forceinline__ float fixed_base(const float* w) { return 4.0f * (w[0] * w[1]); }
+
+// Row i's fixed-point multiplier m_i = 1 / quantum_i = 2^30 / B_i, rounded to
+// bf16 (the row warps scale the bf16 dS that feeds dQ^T by it, so that the
+// product comes out in quanta), zero for a row whose dO is zero (its dS is
+// zero too) and capped at 2^100 (a smaller multiplier only coarsens the
+// quantum).  The producer and the convert kernel compute it the same way.
+__device__ __forceinline__ float row_multiplier(const float* bound_words, float dnorm_i) {
+  const float fb = fixed_base(bound_words) * dnorm_i;
+  const float m = fb > 0.f ? fminf(kFixScale / fb, 0x1p100f) : 0.f;
+  return __bfloat162float(__float2bfloat16_rn(m));
+}
 
 // ---------------------------------------------------------------------------
-// D = rowsum(dO * O): D / 8 lanes per (token, head) row, 16 bytes of O and of
-// dO per lane (eight bf16 each), so that every load moves whole sectors.
+__global__ void __launch_bounds__(256) bwd_zero_kernel(int32_t* __restrict__ x, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) x[i] = 0;
+}
+
+// Per (q-tile, head): the tile's side values LSE * log2 e and D = rowsum(dO *
+// O), ||dO_i|| (D / 8 lanes per row, 16 bytes of each tensor per lane), the
+// tile's largest ||V_i|| and |K_id| folded into its sequence's bound words,
+// and the tile's rows of the dQ accumulator zeroed.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                                        const __nv_bfloat16* __restrict__ dout,
-                                                        float* __restrict__ delta, int T, int H) {
-  constexpr int LPR = D / 8;                      // lanes per row: 16, 8 or 4
-  constexpr int RPB = 256 / LPR;                  // rows per block
-  const int sub = threadIdx.x % LPR;
-  const long long row = (long long)blockIdx.x * RPB + threadIdx.x / LPR;  // t * H + h
-  const bool in = row < (long long)T * H;
-  float acc = 0.f;
-  if (in) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + 8 * sub);
-    const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + 8 * sub);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const int32_t* __restrict__ header,
+                                                       const int32_t* __restrict__ qt_seq,
+                                                       const int32_t* __restrict__ qt_idx,
+                                                       const int32_t* __restrict__ cu,
+                                                       const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       const __nv_bfloat16* __restrict__ k,
+                                                       const __nv_bfloat16* __restrict__ v,
+                                                       const float* __restrict__ lse, float* __restrict__ side,
+                                                       float* __restrict__ dnorm, float* __restrict__ bounds,
+                                                       int32_t* __restrict__ dqacc, int T, int H, int G) {
+  constexpr int LPR = D / 8;        // lanes per row: 16, 8 or 4
+  constexpr int RPP = 256 / LPR;    // rows per pass
+  __shared__ float s_max[8][2];
+  const int g = blockIdx.x, h = blockIdx.y;
+  if (g >= header[kHdrQtiles]) return;
+  const int b = qt_seq[g];
+  const int s0 = cu[b], L = cu[b + 1] - s0;
+  const int a0 = qt_idx[g] * kTile;
+  const int qn = min(kTile, L - a0);
+  const int sub = threadIdx.x % LPR, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the tile's side values; rows past the sequence end see no key
+  float* sd = side + (size_t(h) * G + g) * kBwdSideFloats;
+  for (int r = qn + int(threadIdx.x); r < kTile; r += blockDim.x) {
+    sd[r] = INFINITY;
+    sd[kTile + r] = 0.f;
+  }
+  float mv = 0.f, mk = 0.f;
+  for (int r0 = 0; r0 < qn; r0 += RPP) {
+    const int r = r0 + int(threadIdx.x) / LPR;
+    const bool in = r < qn;
+    float acc = 0.f, sdo = 0.f, sv = 0.f, ak = 0.f;
+    const size_t row = (size_t(s0 + a0 + r) * H + h) * D + 8 * sub;
+    if (in) {
+      const uint4 ow = *reinterpret_cast<const uint4*>(o + row);
+      const uint4 gw = *reinterpret_cast<const uint4*>(dout + row);
+      const uint4 kw = *reinterpret_cast<const uint4*>(k + row);
+      const uint4 vw = *reinterpret_cast<const uint4*>(v + row);
+      const uint32_t oa[4] = {ow.x, ow.y, ow.z, ow.w}, ga[4] = {gw.x, gw.y, gw.z, gw.w};
+      const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w}, va[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
-      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[i]));
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&oa[i]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ga[i]));
+        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ka[i]));
+        const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&va[i]));
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+        sdo = fmaf(y.x, y.x, fmaf(y.y, y.y, sdo));
+        sv = fmaf(vv.x, vv.x, fmaf(vv.y, vv.y, sv));
+        ak = fmaxf(ak, fmaxf(fabsf(kk.x), fabsf(kk.y)));
+      }
+      int32_t* z = dqacc + row;
+      *reinterpret_cast<uint4*>(z) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(z + 4) = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      sdo += __shfl_xor_sync(0xffffffffu, sdo, off);
+      sv += __shfl_xor_sync(0xffffffffu, sv, off);
+      ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, off));
+    }
+    if (in && sub == 0) {
+      const size_t at = size_t(h) * T + s0 + a0 + r;
+      const float l = __ldg(lse + at);
+      sd[r] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+      sd[kTile + r] = acc;
+      // norms rounded up by a relative 2^-20, so that the bound holds for the
+      // exact norms too
+      dnorm[at] = sqrtf(sdo) * 1.000001f;
+      mv = fmaxf(mv, sqrtf(sv) * 1.000001f);
+      mk = fmaxf(mk, ak);
     }
   }
 #pragma unroll
-  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (in && sub == 0) {
-    const int t = int(row / H), h = int(row % H);
-    delta[size_t(h) * T + t] = acc;
+  for (int off = 16; off > 0; off >>= 1) {
+    mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+    mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+  }
+  if (lane == 0) {
+    s_max[warp][0] = mv;
+    s_max[warp][1] = mk;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {
+    float m = 0.f;
+    for (int w = 0; w < 8; ++w) m = fmaxf(m, s_max[w][threadIdx.x]);
+    atomicMax(reinterpret_cast<int*>(bounds + (size_t(b) * H + h) * kBoundWords + threadIdx.x), __float_as_int(m));
+  }
+}
+
+// Per (q-tile, head), once every tile's bound words are in: the rows'
+// fixed-point multipliers m_i (zero past the sequence end) into the side
+// values.
+__global__ void __launch_bounds__(kTile) bwd_mult_kernel(const int32_t* __restrict__ header,
+                                                         const int32_t* __restrict__ qt_seq,
+                                                         const int32_t* __restrict__ qt_idx,
+                                                         const int32_t* __restrict__ cu,
+                                                         const float* __restrict__ bounds,
+                                                         const float* __restrict__ dnorm, float* __restrict__ side,
+                                                         int T, int H, int G) {
+  const int g = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  if (g >= header[kHdrQtiles]) return;
+  const int b = qt_seq[g];
+  const int s0 = cu[b], L = cu[b + 1] - s0;
+  const int a0 = qt_idx[g] * kTile;
+  const float* bw = bounds + (size_t(b) * H + h) * kBoundWords;
+  side[(size_t(h) * G + g) * kBwdSideFloats + 2 * kTile + c] =
+      a0 + c < L ? row_multiplier(bw, __ldg(dnorm + size_t(h) * T + s0 + a0 + c)) : 0.f;
+}
+
+// dQ = scale * accumulator / m_i in bf16, per (q-tile, head).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const int32_t* __restrict__ header,
+                                                             const int32_t* __restrict__ qt_seq,
+                                                             const int32_t* __restrict__ qt_idx,
+                                                             const int32_t* __restrict__ cu,
+                                                             const float* __restrict__ bounds,
+                                                             const float* __restrict__ dnorm,
+                                                             const int32_t* __restrict__ acc,
+                                                             __nv_bfloat16* __restrict__ dq, int T, int H,
+                                                             float scale) {
+  const int g = blockIdx.x, h = blockIdx.y;
+  if (g >= header[kHdrQtiles]) return;
+  const int b = qt_seq[g];
+  const int s0 = cu[b], L = cu[b + 1] - s0;
+  const int a0 = qt_idx[g] * kTile;
+  const int qn = min(kTile, L - a0);
+  const float* bw = bounds + (size_t(b) * H + h) * kBoundWords;
+  constexpr int V4 = D / 4;  // four-int pieces per row
+  for (int x = threadIdx.x; x < qn * V4; x += blockDim.x) {
+    const int r = x / V4, c = x % V4;
+    const float m = row_multiplier(bw, __ldg(dnorm + size_t(h) * T + s0 + a0 + r));
+    const float mul = m > 0.f ? scale / m : 0.f;
+    const size_t off = (size_t(s0 + a0 + r) * H + h) * D + 4 * c;
+    const int4 v = __ldcg(reinterpret_cast<const int4*>(acc + off));
+    uint2 w;
+    w.x = ptx::pack_bf16(float(v.x) * mul, float(v.y) * mul);
+    w.y = ptx::pack_bf16(float(v.z) * mul, float(v.w) * mul);
+    *reinterpret_cast<uint2*>(dq + off) = w;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Shared layout of the two list-walking kernels.
 template <int D>
 struct BwdCfg : TileLayout<D> {
   using TileLayout<D>::TILE;
@@ -82,72 +270,85 @@ struct BwdCfg : TileLayout<D> {
   using TileLayout<D>::CE;
   using TileLayout<D>::NCH;
   using TileLayout<D>::ROWB;
-  static constexpr int NSLOT = 4;  // ring of streamed tiles (two per list entry)
-  // fixed tiles (Q and dO for dQ; K and V for dK/dV), then the ring
-  static constexpr int OFF_A = 0, OFF_B = TILE, OFF_RING = 2 * TILE;
-  static constexpr int B_FIX = 0, B_FIXFREE = 1, B_FULL = 2, B_EMPTY = 2 + NSLOT, B_VTMA = 2 + 2 * NSLOT,
-                       B_SFULL = B_VTMA + 1, B_PFULL = B_SFULL + 1, B_ODONE = B_PFULL + 2,
-                       B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, B_YFREE = B_DRAIN + 1, NBAR = B_YFREE + 1;
-  static constexpr int OFF_BAR = OFF_RING + NSLOT * TILE;
+  static constexpr int NSLOT = 4;  // ring of streamed tiles: Q and dO of two entries
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_RING = 2 * TILE;
+  static constexpr int OFF_DS = OFF_RING + NSLOT * TILE;  // dS of the entry; the dK/dV output stage
+  // barriers with two instances are per 64-query half (TMEM buffer) h
+  static constexpr int B_FIX = 0, B_FIXFREE = 1, B_KTAIL = 2, B_FULL = 3, B_EMPTY = B_FULL + NSLOT,
+                       B_QTAIL = B_EMPTY + NSLOT, B_SFULL = B_QTAIL + 1, B_PFULL = B_SFULL + 2,
+                       B_AFREE = B_PFULL + 2, B_DQFULL = B_AFREE + 2, B_DQFREE = B_DQFULL + 2,
+                       B_ODONE = B_DQFREE + 2, B_OFREE = B_ODONE + 1, B_IFULL = B_OFREE + 1,
+                       B_IEMPTY = B_IFULL + 2, B_DRAIN = B_IEMPTY + 2, B_DRAIN2 = B_DRAIN + 1,
+                       B_STAGE = B_DRAIN2 + 1, NBAR = B_STAGE + 1;
+  static constexpr int OFF_BAR = OFF_DS + kDsBlock;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_RINGI = OFF_MISC + 16;                 // two decoded work items, 8 ints each
-  // per ring slot: 128 ints of side data (key codes, or the q-tile's LSE, D and
-  // query codes: 3 x 128 words for the dK/dV kernel's Q slots)
-  static constexpr int OFF_SIDE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
-  static constexpr int SIDE_WORDS = 3 * kTile;
-  static constexpr int OFF_STAGE = OFF_SIDE + NSLOT * SIDE_WORDS * 4;  // per warp: 16 output rows
-  static constexpr int STAGE_WARP = 2048;                       // per row warp: output rows in rounds
-  static constexpr int OFF_PLIST = OFF_STAGE + 8 * STAGE_WARP;  // the producer's staged list
-  static constexpr int SMEM_USED = OFF_PLIST + 2 * kPlist * 4;
-  static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
+  static constexpr int OFF_RINGI = OFF_MISC + 16;  // two decoded work items
+  static constexpr int SMEM_USED = OFF_RINGI + 2 * kItemInts * 4;
+  static constexpr int SMEM_MAX = 232448;
+  // up to 1 KB of slack to align the base to 1024 bytes, within the limit; at
+  // least 116 KB so that one CTA holds an SM (and its 512 TMEM columns) alone
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > SMEM_MAX ? SMEM_MAX
+                                    : (SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024);
+  static constexpr int STAGE_WARP = 2048;  // per row warp: output rows in rounds (in the dS buffer)
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  // dV and dK accumulators, then per half h: S^T (64 columns, then P^T and
+  // dS^T in bf16 over it) and dP^T (64 columns, then dQ^T over it)
+  static constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_BUF = 256;
+  static constexpr uint32_t col_s(int h) { return COL_BUF + 128u * uint32_t(h); }
+  static constexpr uint32_t col_p(int h) { return COL_BUF + 128u * uint32_t(h) + 64u; }
+  // S^T = K Q_h^T and dP^T = V dO_h^T: M = 128 keys, N = 64 queries, K-major
+  static constexpr uint32_t IDESC_S64 = ptx::idesc_bf16_f32(128, 64, false, false);
+  // dQ_h^T = K^T dS_h^T: M = 128 head-dim rows (for D < 128 the rows past D
+  // read other shared memory and land in TMEM lanes nobody reads), N = 64
+  // queries, K = 128 keys, both operands MN-major
+  static constexpr uint32_t IDESC_DQT64 = ptx::idesc_bf16_f32(128, 64, true, true);
+  // byte offset of a streamed tile's rows 64 .. 127 (the second half)
+  static constexpr uint32_t HALF_ROWS = 64u * ROWB;
+  static_assert(SMEM_USED <= SMEM_MAX, "shared memory budget");
+  static_assert(8 * STAGE_WARP <= kDsBlock, "output stage");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_RING % 1024 == 0 && TILE % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
 };
 
 struct BwdParams {
   int32_t* header;
-  int sched;              // this launch's work-counter slot
-  const int32_t* order;   // items' tile order (q-major for dQ, k-major for dK/dV)
+  int sched;                // this launch's work-counter slot
+  const int32_t* korder;    // k-tiles by descending list length
   const int32_t* qt_seq;
   const int32_t* qt_idx;
-  const int32_t* off;     // CSR offsets of the walked lists
-  const int32_t* idx;     // tile index inside the sequence
-  const uint8_t* label;
+  const int32_t* qoff;      // k-major lists
+  const int32_t* qidx;
+  const uint8_t* qlabel;
   const int32_t* cu;
   MaskArgs mask;
-  const float* lse;       // [H, T]
-  const float* delta;     // [H, T]
-  __nv_bfloat16* out0;    // dQ, or dK
-  __nv_bfloat16* out1;    // unused, or dV
-  uint8_t* ds;            // dS blocks of heads h0 .. h0+G-1: [G][entries][128 x 128 bf16]
-  const int32_t* kpos;    // k-major position of every q-major entry
-  int H, T;
-  int h0, G;              // heads of this launch
-  int e_bound;            // entries the dS blocks were sized for
+  const float* side;        // [H][G][kBwdSideFloats]: LSE * log2 e, D, m_i of each q-tile's rows
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t* dqacc;           // [T, H, D] fixed point
+  int H, T, G;
   float scale;
   float scale_log2;
 };
 
-// Bytes of one stored dS block: 128 keys x 128 queries, bf16.
-constexpr int kDsBlock = kTile * kTile * 2;
-
-// One work item: a tile of one sequence and one head, and its list.
+// One work item: one k-tile of one sequence and one head, and its list.
 struct BwdItem {
-  int h, s0, L, i0, e0, e1, b;  // i0: first row of the item's tile, local to the sequence
+  int h, s0, L, i0, e0, e1, b, gbase;  // i0: first key of the tile (local); gbase: tile 0 of the sequence
 };
 
+// Items are head-major: every k-tile of head 0 (longest list first), then head 1, ...
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
   BwdItem it;
-  it.h = p.h0 + item / n_t;
-  const int g = p.order[item % n_t];
+  it.h = item / n_t;
+  const int g = p.korder[item % n_t];
   const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
   it.L = p.cu[b + 1] - it.s0;
-  it.i0 = p.qt_idx[g] * kTile;
-  it.e0 = p.off[g];
-  it.e1 = p.off[g + 1];
+  const int m = p.qt_idx[g];
+  it.i0 = m * kTile;
+  it.e0 = p.qoff[g];
+  it.e1 = p.qoff[g + 1];
   it.b = b;
+  it.gbase = g - m;
   return it;
 }
 
@@ -160,6 +361,7 @@ __device__ __forceinline__ void bwd_store(volatile int* d, const BwdItem& it, bo
   d[5] = it.e0;
   d[6] = it.e1;
   d[7] = it.b;
+  d[8] = it.gbase;
 }
 __device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
   if (!d[0]) return false;
@@ -170,6 +372,7 @@ __device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
   it.e0 = d[5];
   it.e1 = d[6];
   it.b = d[7];
+  it.gbase = d[8];
   return true;
 }
 
@@ -185,7 +388,7 @@ __device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, 
   const int slot_i = k & 1;
   if (k >= 2 && !warp_wait(iempty0 + 8u * slot_i, uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 15)) return -1;
   if (lane == 0) {
-    bwd_store(ring + 8 * slot_i, it, valid);
+    bwd_store(ring + kItemInts * slot_i, it, valid);
     ptx::mbar_arrive(ifull0 + 8u * slot_i);
   }
   return valid ? 1 : 0;
@@ -223,16 +426,6 @@ __device__ __forceinline__ void store_rows(uint8_t* stage, int lane, const uint3
     __syncwarp();
   }
 }
-
-// A stored dS block is the image, in shared memory, of a 128-query x 128-key
-// bf16 operand in the MN-major layout without swizzle: sixteen 2 KB chunks of
-// eight queries; in chunk c, key k's eight queries q = 8c .. 8c+7 are the 16
-// bytes at k * 16.  One bulk copy of the 32 KB gives the dQ kernel its A
-// operand (8-key core matrices 128 bytes apart along K, chunks 2 KB apart
-// along M), and a thread that holds one key's dS for 64 queries writes it
-// straight from registers: for each chunk the 32 lanes of a warp (32
-// consecutive keys) write 512 contiguous bytes.
-constexpr int kDsChunk = 2048;  // bytes per eight-query chunk of a dS block
 
 // TMEM -> registers: D fp32 columns of this thread's lane from `taddr`, times
 // `mul`, rounded to bf16 pairs (zeros when `have` is false).
@@ -309,357 +502,147 @@ __device__ __forceinline__ bool load_pair(const CUtensorMap* ma, const CUtensorM
   return true;
 }
 
-// Half `hf` of a product over the 128 rows of a streamed tile: k-steps
-// 4hf .. 4hf+3 of issue_pv (rows 64hf .. 64hf+63), so that the first half can
-// run while the row threads still produce the second.
+// The issuing thread's loops are unrolled with compile-time descriptor
+// offsets and accumulate flags: the tensor pipe finishes a 128 x 64 x 16
+// product in ~48 cycles, so a few instructions more per issue would leave it
+// idle.
+//
+// Half h of a product over the 128 rows of a streamed tile (dV += P^T dO or
+// dK += dS^T Q over rows 64h .. 64h+63, four k-steps of 16; b_desc already
+// points at row 64h).  The A operand (P^T or dS^T, bf16) sits over buffer h's
+// S^T columns: the row warps write each 32-query group g over its own 32
+// score columns, P^T in the first 16, dS^T in the next 16 (a_tmem is the
+// buffer's first column for P^T, that + 16 for dS^T), so k-step k4 is at
+// column 32 (k4 / 2) + 8 (k4 % 2).
 template <int D>
-__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, int hf, bool acc) {
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool acc) {
   using C = BwdCfg<D>;
+  ptx::mma_ts(d_tmem, a_tmem, b_desc, C::IDESC_PV, acc ? 1u : 0u);
 #pragma unroll
-  for (int k4 = 0; k4 < 4; ++k4) {
-    const int kk = 4 * hf + k4;
-    ptx::mma_ts(d_tmem, a_tmem + uint32_t(hf) * 64u + uint32_t(k4) * 8u, b_desc + v_step<D>(kk), C::IDESC_PV,
-                (acc || kk > 0) ? 1u : 0u);
+  for (int k4 = 1; k4 < 4; ++k4)
+    ptx::mma_ts_c<true>(d_tmem, a_tmem + uint32_t(k4 >> 1) * 32u + uint32_t(k4 & 1) * 8u, b_desc + v_step<D>(k4),
+                        C::IDESC_PV);
+}
+
+// Scores-like product D = A B^T over K = D, N = 64 (both operands K-major).
+template <int D>
+__device__ __forceinline__ void issue_scores64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  using C = BwdCfg<D>;
+  ptx::mma_ss_c<false>(d_tmem, a_desc, b_desc, C::IDESC_S64);
+#pragma unroll
+  for (int kk = 1; kk < D / 16; ++kk)
+    ptx::mma_ss_c<true>(d_tmem, a_desc + kmajor_step<D>(kk), b_desc + kmajor_step<D>(kk), C::IDESC_S64);
+}
+
+// dQ_h^T = K^T dS_h^T over the k-tile's 128 keys (eight k-steps of 16 keys).
+template <int D>
+__device__ __forceinline__ void issue_dqt64(uint32_t d_tmem, uint64_t kt_desc, uint64_t ds_desc) {
+  using C = BwdCfg<D>;
+  ptx::mma_ss_c<false>(d_tmem, kt_desc, ds_desc, C::IDESC_DQT64);
+#pragma unroll
+  for (int kk = 1; kk < kTile / 16; ++kk)
+    ptx::mma_ss_c<true>(d_tmem, kt_desc + v_step<D>(kk), ds_desc + uint64_t((kk * 256) >> 4), C::IDESC_DQT64);
+}
+
+// The products of one unit after its P^T and dS^T are in TMEM: dV and dK
+// (starting the accumulators when the unit opens its item), then dQ_h^T into
+// buffer h's dP^T columns.  Returns false when the CTA is aborting.
+template <int D>
+__device__ __forceinline__ bool bwd_tail(uint32_t tmem, uint32_t bars, int h, int ent, int qs, int ds, bool first,
+                                         int nitem, uint64_t rv0, uint64_t ktdesc, uint64_t dsdesc0,
+                                         volatile uint32_t* abort_flag, int32_t* err) {
+  using C = BwdCfg<D>;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  if (!wait_bar(bar(C::B_PFULL + h), uint32_t(ent) & 1u, abort_flag, err, 5)) return false;
+  // an item's first products overwrite dV and dK: the previous item's
+  // epilogue has read them out (it precedes this unit's P^T in every row
+  // warp, so this wait never holds)
+  if (first && nitem > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(nitem - 1) & 1u, abort_flag, err, 14)) return false;
+  ptx::tc_fence_after();
+  const uint32_t ts = tmem + C::col_s(h);
+  const uint64_t hrow = uint64_t(h) * (C::HALF_ROWS >> 4);  // rows 64h .. of a slot
+  issue_pv_half<D>(tmem + C::COL_DV, ts, rv0 + uint64_t(ds) * (C::TILE >> 4) + hrow, !first);
+  issue_pv_half<D>(tmem + C::COL_DK, ts + 16u, rv0 + uint64_t(qs) * (C::TILE >> 4) + hrow, !first);
+  ptx::mma_commit(bar(C::B_AFREE + h));
+  if (h == 1) {  // the entry's last products that read Q and dO
+    ptx::mma_commit(bar(C::B_EMPTY + qs));
+    ptx::mma_commit(bar(C::B_EMPTY + ds));
   }
+  // dQ_h^T over this k-tile into dP^T's columns (every row warp has read them
+  // before it signalled the unit)
+  issue_dqt64<D>(tmem + C::col_p(h), ktdesc, dsdesc0 + uint64_t(h) * uint64_t((kDsBlock / 2) >> 4));
+  ptx::mma_commit(bar(C::B_DQFULL + h));
+  return true;
 }
 
 // ---------------------------------------------------------------------------
-// dQ from the stored dS blocks: one item per (q-tile, head); per listed k-tile
-// j, dQ += dS(i, j) K_j, with dS(i, j) the block the dK/dV kernel wrote for the
-// pair (bulk-copied as the MN-major A operand) and K_j the MN-major B operand.
-// Warps 0-3 are the epilogue (one thread per query row), warp 4 the producer,
-// warp 5 the MMA issuer; dQ is double-buffered in TMEM so one item's epilogue
-// runs under the next item's products.  Each dQ row is a sum over its k-tiles
-// in ascending order inside one CTA: deterministic.
-template <int D>
-struct DqCfg : TileLayout<D> {
-  using TileLayout<D>::TILE;
-  using TileLayout<D>::CHUNK;
-  using TileLayout<D>::CE;
-  using TileLayout<D>::NCH;
-  using TileLayout<D>::ROWB;
-  static constexpr int SLOT = kDsBlock + TILE;  // dS block, then the K tile
-  static constexpr int NSLOT = D == 128 ? 3 : 4;
-  static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_TAIL = 2 * NSLOT, B_ODONE = B_TAIL + 1,
-                       B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
-                       B_DRAIN = B_IEMPTY + 2, NBAR = B_DRAIN + 1;
-  static constexpr int OFF_BAR = NSLOT * SLOT;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_RINGI = OFF_MISC + 16;
-  static constexpr int OFF_STAGE = (OFF_RINGI + 2 * 8 * 4 + 15) & ~15;
-  static constexpr int STAGE_WARP = 16 * 2 * D;
-  static constexpr int OFF_PLIST = OFF_STAGE + 4 * STAGE_WARP;  // the producer's staged list
-  static constexpr int SMEM_USED = OFF_PLIST + 2 * kPlist * 4;
-  static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
-  static constexpr uint32_t DQ_COLS = D;                          // one dQ buffer
-  static constexpr uint32_t TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;  // two buffers
-  // dS as the A operand: M = 128 queries (sixteen 8-query chunks), K = keys
-  static constexpr uint32_t IDESC_DQ = ptx::idesc_bf16_f32(128, D, true, true);
-  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-};
-
+// dK, dV and the dQ contributions: one item per (k-tile, head); per listed
+// q-tile i, in two units of 64 queries (h = 0, 1; TMEM buffer h):
+//   S^T = K Q_ih^T, dP^T = V dO_ih^T (TMEM, TMEM lane = key),
+//   P^T = 2^(S^T c2 - LSE_i log2 e), dS^T = P^T (dP^T - D_i),
+//   dV += P^T dO_ih, dK += dS^T Q_ih, dQ_ih^T (+)= K^T dS^T (over this k-tile).
+// The tensor pipe runs one unit ahead of the row warps: while they turn unit
+// u's scores into P^T and dS^T, it runs unit u-1's dV, dK and dQ^T products
+// and unit u+1's scores, each in the other buffer.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmK, const BwdParams p) {
-  using C = DqCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = p.header[kHdrQtiles];
-  const int n_entries = p.header[kHdrEntries];
-  const int n_items = n_t * p.G;
+  const int n_items = n_t * p.H;
   int32_t* err = p.header + kHdrError;
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sRing = base;
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sRing = base + C::OFF_RING, sDS = base + C::OFF_DS;
   const uint32_t bars = base + C::OFF_BAR;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
   volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
+  // the aligned layout must fit the allocation (it always does when the
+  // dynamic shared memory starts 1024-byte aligned); otherwise fail closed
+  if (base - raw + uint32_t(C::SMEM_USED) > uint32_t(C::SMEM_ALLOC)) {
+    if (threadIdx.x == 0) {
+      atomicOr(err, kErrTimeout | (31 << 9));
+      finish_sched(p.sched);
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(C::B_FIX), 1);
+    ptx::mbar_init(bar(C::B_FIXFREE), 2);  // tails issuer's commit + scores issuer's arrival
+    ptx::mbar_init(bar(C::B_KTAIL), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(C::B_FULL + s), 1);
       ptx::mbar_init(bar(C::B_EMPTY + s), 1);
     }
-    ptx::mbar_init(bar(C::B_TAIL), 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar(C::B_ODONE + i), 1);
-      ptx::mbar_init(bar(C::B_OFREE + i), 128);
-      ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 128 + 1);  // epilogue threads, MMA thread
+    ptx::mbar_init(bar(C::B_QTAIL), 1);
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(bar(C::B_SFULL + h), 1);
+      ptx::mbar_init(bar(C::B_PFULL + h), 256);
+      ptx::mbar_init(bar(C::B_AFREE + h), 1);
+      ptx::mbar_init(bar(C::B_DQFULL + h), 1);
+      ptx::mbar_init(bar(C::B_DQFREE + h), 256);
     }
-    ptx::mbar_init(bar(C::B_DRAIN), 1);
-    *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & (kErrTimeout | kErrCapacity)) ? 1u : 0u;
-    if (n_entries > p.e_bound) {
-      atomicOr(err, kErrCapacity);
-      *abort_flag = 1u;
-    }
-    ptx::fence_mbar_init();
-  }
-  if (warp == kWarpMma) {
-    ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = misc[0];
-  const bool skip = *abort_flag != 0u;
-
-  if (skip) {
-  } else if (warp == kWarpLoad) {
-    // ---------------------------------------------------------- producer
-    int nload = 0, ntail = 0;
-    bool tail_pending = false, ok = true;
-    BwdItem it_next;
-    int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
-                              abort_flag, err);
-    for (int k = 0; ok && st_next == 1; ++k) {
-      const BwdItem it = it_next;
-      st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
-                            abort_flag, err);
-      if (st_next < 0) break;
-      const uint8_t* ds_head = p.ds + size_t(it.h - p.h0) * size_t(n_entries) * kDsBlock;
-      int* s_idx = reinterpret_cast<int*>(sbase + C::OFF_PLIST);
-      int* s_pos = s_idx + kPlist;
-      for (int e = it.e0; e < it.e1; ++e) {
-        const int r = (e - it.e0) & (kPlist - 1);
-        if (r == 0) {  // the next kPlist entries of the list and their dS block positions
-          __syncwarp();
-          for (int x = lane; x < kPlist && e + x < it.e1; x += 32) {
-            s_idx[x] = __ldg(p.idx + e + x);
-            s_pos[x] = __ldg(p.kpos + e + x);
-          }
-          __syncwarp();
-        }
-        const int j0 = s_idx[r] * kTile, kn = min(kTile, it.L - j0);
-        const uint8_t* blk = ds_head + size_t(s_pos[r]) * kDsBlock;
-        const int slot = nload % C::NSLOT;
-        if (nload >= C::NSLOT &&
-            !warp_wait(bar(C::B_EMPTY + slot), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t dst = sRing + uint32_t(slot) * C::SLOT, kdst = dst + kDsBlock;
-        const uint32_t full = bar(C::B_FULL + slot);
-        if (kn == kTile) {
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full, kDsBlock + C::TILE);
-            ptx::bulk_load(dst, blk, kDsBlock, full);
-            for (int c = 0; c < C::NCH; ++c)
-              ptx::tma_load_3d(kdst + c * C::CHUNK, &tmK, full, c * C::CE, it.h, it.s0 + j0);
-          }
-        } else {
-          // K rows past the sequence end are zeroed before FULL opens: their dS
-          // is zero, but an inf there would make the product NaN
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar(C::B_TAIL), C::TILE);
-            for (int c = 0; c < C::NCH; ++c)
-              ptx::tma_load_3d(kdst + c * C::CHUNK, &tmK, bar(C::B_TAIL), c * C::CE, it.h, it.s0 + j0);
-          }
-          tail_pending = true;
-          if (!warp_wait(bar(C::B_TAIL), uint32_t(ntail) & 1u, abort_flag, err, 2)) {
-            ok = false;
-            break;
-          }
-          tail_pending = false;
-          ++ntail;
-          uint8_t* kgen = sbase + size_t(slot) * C::SLOT + kDsBlock;
-          for (int rr = kn + lane; rr < kTile; rr += 32) {
-#pragma unroll
-            for (int c = 0; c < C::NCH; ++c) {
-              uint4* row = reinterpret_cast<uint4*>(kgen + c * C::CHUNK + rr * C::ROWB);
-#pragma unroll
-              for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(full, kDsBlock);
-            ptx::bulk_load(dst, blk, kDsBlock, full);
-          }
-        }
-        ++nload;
-      }
-    }
-    if (lane == 0) {
-      for (int s = 0; s < C::NSLOT; ++s) {
-        if (nload <= s) continue;
-        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
-        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
-      }
-      if (tail_pending) drain_bar(bar(C::B_TAIL), uint32_t(ntail) & 1u, err);
-    }
-    __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int nload = 0;
-      bool ok = true;
-      // dS: MN-major without swizzle, where the stride between eight-key core
-      // matrices (K, 128 bytes) is the leading offset and the stride between
-      // eight-query chunks (M, kDsChunk) the stride offset
-      const uint64_t ds0 = ptx::smem_desc(sRing, 128u, kDsChunk, ptx::kSwizzleNone);
-      const uint64_t k0 = v_base<D>(sRing + kDsBlock);
-      for (int k = 0; ok; ++k) {
-        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
-        BwdItem it;
-        const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
-        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
-        if (!valid) break;
-        const int b = k & 1;
-        if (k >= 2 && !wait_bar(bar(C::B_OFREE + b), uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 14)) break;
-        const uint32_t dq_t = tmem + uint32_t(b) * C::DQ_COLS;
-        const int n = it.e1 - it.e0;
-        for (int j = 0; j < n; ++j) {
-          const int slot = nload % C::NSLOT;
-          if (!wait_bar(bar(C::B_FULL + slot), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint64_t so = uint64_t(slot) * (C::SLOT >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            ptx::mma_ss(dq_t, ds0 + so + uint64_t(kk * 16 * 16 >> 4), k0 + so + v_step<D>(kk), C::IDESC_DQ,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(C::B_EMPTY + slot));
-          ++nload;
-        }
-        if (!ok) break;
-        ptx::mma_commit(bar(C::B_ODONE + b));
-      }
-      ptx::mma_commit(bar(C::B_DRAIN));
-      drain_bar(bar(C::B_DRAIN), 0, err);
-    }
-    __syncwarp();
-  } else if (warp < 4) {
-    // ---------------------------------------------------------- epilogue
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-    for (int k = 0;; ++k) {
-      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
-      BwdItem it;
-      const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
-      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
-      if (!valid) break;
-      const int b = k & 1;
-      if (!warp_wait(bar(C::B_ODONE + b), uint32_t(k >> 1) & 1u, abort_flag, err, 11)) break;
-      ptx::tc_fence_after();
-      uint32_t w[D / 2];
-      tmem_row_bf16<D>(lane_base + uint32_t(b) * C::DQ_COLS, p.scale, it.e1 > it.e0, w);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE + b));
-      const int qn = min(kTile, it.L - it.i0);
-      store_rows<D, C::STAGE_WARP>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
-                    p.out0 + (size_t(it.s0 + it.i0 + warp * 32) * p.H + it.h) * D, size_t(p.H) * D,
-                    qn - warp * 32);
-    }
-  }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-  if (threadIdx.x == 0) finish_sched(p.sched);
-}
-
-// k-major position of every q-major entry: for the pair (q-tile i, k-tile j),
-// the rank of i in k-tile j's ascending list (one block per q-tile).
-__global__ void __launch_bounds__(128) bwd_kpos_kernel(const int32_t* __restrict__ header,
-                                                       const int32_t* __restrict__ qt_idx,
-                                                       const int32_t* __restrict__ koff,
-                                                       const int32_t* __restrict__ kidx,
-                                                       const int32_t* __restrict__ qoff,
-                                                       const int32_t* __restrict__ qidx, int32_t* kpos) {
-  const int g = blockIdx.x;
-  if (g >= header[kHdrQtiles]) return;
-  const int i = qt_idx[g], g0 = g - i;  // tiles of one sequence are numbered contiguously
-  for (int e = koff[g] + threadIdx.x; e < koff[g + 1]; e += blockDim.x) {
-    const int gj = g0 + kidx[e];
-    int lo = qoff[gj], hi = qoff[gj + 1];
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (qidx[mid] < i) lo = mid + 1;
-      else hi = mid;
-    }
-    kpos[e] = lo;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// dK, dV: one item per (k-tile, head); per listed q-tile i:
-//   S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, TMEM lane = key),
-//   P^T = 2^(S^T c2 - LSE_i log2 e), dS^T = P^T (dP^T - D_i),
-//   dV += P^T dO_i, dK += dS^T Q_i.
-// TMEM: dV [0, D), dK [128, 128+D), and two 128-column regions [256,384),
-// [384,512) that alternate by entry: S^T of entry j goes to region j % 2 and
-// dP^T to the other; the row warps write bf16 P^T and dS^T over S^T's region
-// (P^T over the first 32 columns of each 64-column half, dS^T over the other
-// 32), so dP^T's region is free once they have read it, and S^T of entry j+1
-// goes there while they are still working on entry j.
-// Warps 0-7 are the row warps: warp w owns TMEM lanes (keys) 32 (w % 4) ..
-// +31 and query columns 64 (w / 4) .. +63, so each half of the queries has its
-// own four warps (two warps per SM sub-partition hide each other's latency);
-// at the end of an item the first four store dV and the other four dK.  Warp 8
-// is the TMA producer, warp 9 the tcgen05 issuer, warps 10-11 idle; the row
-// warpgroups run with 192 registers a thread and the third with 112 (within
-// the 168 x 384 the block is launched with).
-template <int D>
-__global__ void __launch_bounds__(kDkdvThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                         const BwdParams p) {
-  using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_t = p.header[kHdrQtiles];
-  const int n_entries = p.header[kHdrEntries];
-  const int n_items = n_t * p.G;
-  int32_t* err = p.header + kHdrError;
-  const uint32_t raw = ptx::smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sK = base + C::OFF_A, sV = base + C::OFF_B, sRing = base + C::OFF_RING;
-  const uint32_t bars = base + C::OFF_BAR;
-  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + C::OFF_MISC);
-  volatile uint32_t* abort_flag = misc + 1;
-  volatile int* item_ring = reinterpret_cast<volatile int*>(sbase + C::OFF_RINGI);
-  int* side = reinterpret_cast<int*>(sbase + C::OFF_SIDE);
-  constexpr uint32_t COL_DV = 0, COL_DK = 128, COL_R0 = 256;
-
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(C::B_FIX), 1);
-    ptx::mbar_init(bar(C::B_FIXFREE), 1);
-    for (int s = 0; s < C::NSLOT; ++s) {
-      ptx::mbar_init(bar(C::B_FULL + s), (s & 1) ? 1 : 2);  // Q slots: copy + side words
-      ptx::mbar_init(bar(C::B_EMPTY + s), 1);
-    }
-    ptx::mbar_init(bar(C::B_VTMA), 1);
-    ptx::mbar_init(bar(C::B_SFULL), 1);
-    ptx::mbar_init(bar(C::B_PFULL), 128);
-    ptx::mbar_init(bar(C::B_PFULL + 1), 128);
     ptx::mbar_init(bar(C::B_ODONE), 1);
     ptx::mbar_init(bar(C::B_OFREE), 256);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 1);  // row threads, MMA thread
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 2 + 256);  // row threads, two MMA threads, reducers
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
-    ptx::mbar_init(bar(C::B_YFREE), 256);
+    ptx::mbar_init(bar(C::B_DRAIN2), 1);
+    ptx::mbar_init(bar(C::B_STAGE), 256);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
-    if (n_entries > p.e_bound) {  // the dS blocks cannot hold this mask's entries
-      atomicOr(err, kErrCapacity);
-      *abort_flag = 1u;
-    }
     ptx::fence_mbar_init();
   }
-  if (warp == kDkdvMma) {
+  if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_addr(misc), C::TMEM_COLS);
     ptx::tmem_relinquish();
   }
@@ -671,208 +654,269 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   if (skip) {
   } else if (warp >= 8) {
-    ptx::regs_dec<112>();
-    if (warp == kDkdvLoad) {
-    // ---------------------------------------------------------- producer
-    int nload = 0, ntail = 0, nfix = 0;
-    bool tail_pending = false, ok = true;
-    BwdItem it_next;
-    int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+    if (warp < kWarpRed) ptx::regs_dec<kRegsLoad>();
+    else ptx::regs_dec<kRegsRed>();
+    if (warp == kWarpLoad) {
+      // ---------------------------------------------------------- producer
+      int nload = 0, ntail = 0, nfix = 0, nktail = 0;
+      bool tail_pending = false, ktail_pending = false, ok = true;
+      BwdItem it_next;
+      int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
+                                abort_flag, err);
+      for (int k = 0; ok && st_next == 1; ++k) {
+        const BwdItem it = it_next;
+        st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
                               abort_flag, err);
-    for (int k = 0; ok && st_next == 1; ++k) {
-      const BwdItem it = it_next;
-      st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
-                            abort_flag, err);
-      if (st_next < 0) break;
-      // K and V of this k-tile, once the previous item's MMAs no longer read
-      // them (rows past the sequence end only reach their own dK, dV rows,
-      // which are not stored)
-      if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE);
-        for (int c = 0; c < C::NCH; ++c) {
-          ptx::tma_load_3d(sK + c * C::CHUNK, &tmK, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
-          ptx::tma_load_3d(sV + c * C::CHUNK, &tmV, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
-        }
-      }
-      ++nfix;
-      // Q(i) and dO(i) of every listed q-tile into two free slots.  Q's side
-      // words get the q-tile's LSE (times log2 e; +inf for rows that see no
-      // key or lie past the end), D and, on PARTIAL tiles, the query codes;
-      // those come from global memory one entry ahead of their use, and the
-      // list itself from the staged copy, so a free slot is refilled at once.
-      int* s_idx = reinterpret_cast<int*>(sbase + C::OFF_PLIST);
-      int* s_lab = s_idx + kPlist;
-      float nl[4], ng[4];
-      int nc[4];
-      int a0 = 0, an = 0, lab = 0;
-      auto fetch = [&](int e, int r) {  // list entry e (staged at r, if r >= 0) and its side values
-        const int ix = r >= 0 ? s_idx[r] : __ldg(p.idx + e);
-        lab = r >= 0 ? s_lab[r] : __ldg(p.label + e);
-        a0 = ix * kTile;
-        an = min(kTile, it.L - a0);
-        const bool codes = kind_codes(p.mask.kind) && lab == ATTN_TILE_PARTIAL;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int c = lane + 32 * m;
-          const size_t at = size_t(it.h) * p.T + it.s0 + a0 + c;
-          nl[m] = c < an ? __ldg(p.lse + at) : -INFINITY;
-          ng[m] = c < an ? __ldg(p.delta + at) : 0.f;
-          nc[m] = codes ? query_code(p.mask, it.s0 + a0 + min(c, an - 1)) : 0;
-        }
-      };
-      for (int e = it.e0; e < it.e1; ++e) {
-        const int r = (e - it.e0) & (kPlist - 1);
-        if (r == 0) {
-          __syncwarp();
-          for (int x = lane; x < kPlist && e + x < it.e1; x += 32) {
-            s_idx[x] = __ldg(p.idx + e + x);
-            s_lab[x] = __ldg(p.label + e + x);
+        if (st_next < 0) break;
+        // K and V of this k-tile, once the previous item's products no longer
+        // read them.  K rows past the sequence end are zeroed: their dS is
+        // zero, but an inf there would make dQ^T = K^T dS^T NaN.
+        if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
+        const int kn = min(kTile, it.L - it.i0);
+        if (kn == kTile) {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::B_FIX), 2 * C::TILE);
+            for (int c = 0; c < C::NCH; ++c) {
+              ptx::tma_load_3d(sK + c * C::CHUNK, &tmK, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+              ptx::tma_load_3d(sV + c * C::CHUNK, &tmV, bar(C::B_FIX), c * C::CE, it.h, it.s0 + it.i0);
+            }
           }
-          __syncwarp();
-          if (e == it.e0) fetch(e, 0);
-        }
-        const int ca0 = a0, can = an, clab = lab;
-        float cl[4], cg[4];
-        int cc[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          cl[m] = nl[m];
-          cg[m] = ng[m];
-          cc[m] = nc[m];
-        }
-        const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
-        if (nload >= C::NSLOT &&
-            (!warp_wait(bar(C::B_EMPTY + qs), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
-             !warp_wait(bar(C::B_EMPTY + ds), uint32_t((nload + 1) / C::NSLOT - 1) & 1u, abort_flag, err, 1))) {
-          ok = false;
-          break;
-        }
-        if (!load_pair<D>(&tmQ, &tmDO, it.h, it.s0 + ca0, can, sRing, sbase + C::OFF_RING, qs, ds, bar(C::B_FULL),
-                          bar(C::B_VTMA), ntail, tail_pending, lane, abort_flag, err)) {
-          ok = false;
-          break;
-        }
-        {
-          float* sl = reinterpret_cast<float*>(side + qs * C::SIDE_WORDS);
-          const bool codes = kind_codes(p.mask.kind) && clab == ATTN_TILE_PARTIAL;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int c = lane + 32 * m;
-            sl[c] = cl[m] == -INFINITY ? INFINITY : cl[m] * 1.4426950408889634f;
-            sl[kTile + c] = cg[m];
-            if (codes) side[qs * C::SIDE_WORDS + 2 * kTile + c] = cc[m];
+        } else {
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::B_KTAIL), 2 * C::TILE);
+            for (int c = 0; c < C::NCH; ++c) {
+              ptx::tma_load_3d(sK + c * C::CHUNK, &tmK, bar(C::B_KTAIL), c * C::CE, it.h, it.s0 + it.i0);
+              ptx::tma_load_3d(sV + c * C::CHUNK, &tmV, bar(C::B_KTAIL), c * C::CE, it.h, it.s0 + it.i0);
+            }
           }
+          ktail_pending = true;
+          if (!warp_wait(bar(C::B_KTAIL), uint32_t(nktail) & 1u, abort_flag, err, 12)) break;
+          ktail_pending = false;
+          ++nktail;
+          for (int rr = kn + lane; rr < kTile; rr += 32) {
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_K + c * C::CHUNK + rr * C::ROWB);
+#pragma unroll
+              for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          ptx::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(C::B_FULL + qs));
+          if (lane == 0) ptx::mbar_arrive(bar(C::B_FIX));
         }
-        nload += 2;
-        if (e + 1 < it.e1) fetch(e + 1, r + 1 < kPlist ? r + 1 : -1);
-      }
-    }
-    if (lane == 0) {
-      for (int s = 0; s < C::NSLOT; ++s) {
-        if (nload <= s) continue;
-        const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
-        drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
-      }
-      if (tail_pending) drain_bar(bar(C::B_VTMA), uint32_t(ntail) & 1u, err);
-      if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
-    }
-    __syncwarp();
-  } else if (warp == kDkdvMma) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int nload = 0, nent = 0;
-      bool ok = true;
-      const uint64_t kdesc = kmajor_base<D>(sK), vdesc = kmajor_base<D>(sV);
-      const uint64_t rk0 = kmajor_base<D>(sRing), rv0 = v_base<D>(sRing);
-      for (int k = 0; ok; ++k) {
-        if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
-        BwdItem it;
-        const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
-        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
-        if (!valid) break;
-        if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
-        const int n = it.e1 - it.e0;
-        bool s_early = false;  // S^T of the current entry was issued during the previous one
-        for (int j = 0; j < n; ++j) {
+        ++nfix;
+        // Q(i) and dO(i) of every listed q-tile into two free slots; the list
+        // entry comes from global memory one entry ahead of its use, so a free
+        // slot is refilled at once
+        int nx = it.e0 < it.e1 ? __ldg(p.qidx + it.e0) : 0;
+        for (int e = it.e0; e < it.e1; ++e) {
+          const int ca0 = nx * kTile, can = min(kTile, it.L - ca0);
+          if (e + 1 < it.e1) nx = __ldg(p.qidx + e + 1);
           const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
-          const uint32_t rs = tmem + COL_R0 + 128u * uint32_t(nent & 1);        // S^T, then P^T and dS^T
-          const uint32_t rp = tmem + COL_R0 + 128u * uint32_t((nent & 1) ^ 1);  // dP^T
-          if (!s_early) {
-            if (!wait_bar(bar(C::B_FULL + qs), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_s<D>(rs, kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4));  // S^T = K Q^T
-          }
-          if (!wait_bar(bar(C::B_FULL + ds), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+          if (nload >= C::NSLOT &&
+              (!warp_wait(bar(C::B_EMPTY + qs), uint32_t(nload / C::NSLOT - 1) & 1u, abort_flag, err, 1) ||
+               !warp_wait(bar(C::B_EMPTY + ds), uint32_t((nload + 1) / C::NSLOT - 1) & 1u, abort_flag, err, 1))) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          issue_s<D>(rp, vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4));  // dP^T = V dO^T
-          ptx::mma_commit(bar(C::B_SFULL));
-          if (j == 0 && k > 0 && !wait_bar(bar(C::B_OFREE), uint32_t(k - 1) & 1u, abort_flag, err, 14)) {
+          if (!load_pair<D>(&tmQ, &tmDO, it.h, it.s0 + ca0, can, sRing, sbase + C::OFF_RING, qs, ds,
+                            bar(C::B_FULL), bar(C::B_QTAIL), ntail, tail_pending, lane, abort_flag, err)) {
             ok = false;
             break;
           }
-          // dV += P^T dO and dK += dS^T Q (dO, Q read MN-major), one half of the
-          // queries at a time; between the halves, S^T of the next entry
-          s_early = false;
-          for (int hf = 0; hf < 2 && ok; ++hf) {
-            if (!wait_bar(bar(C::B_PFULL + hf), uint32_t(nent) & 1u, abort_flag, err, 5)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            issue_pv_half<D>(tmem + COL_DV, rs, rv0 + uint64_t(ds) * (C::TILE >> 4), hf, j > 0);
-            issue_pv_half<D>(tmem + COL_DK, rs + 32u, rv0 + uint64_t(qs) * (C::TILE >> 4), hf, j > 0);
-            if (hf == 0 && j + 1 < n) {
-              const int nq = (nload + 2) % C::NSLOT;
-              if (!wait_bar(bar(C::B_YFREE), uint32_t(nent) & 1u, abort_flag, err, 6) ||
-                  !wait_bar(bar(C::B_FULL + nq), uint32_t((nload + 2) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+          nload += 2;
+        }
+      }
+      if (lane == 0) {
+        for (int s = 0; s < C::NSLOT; ++s) {
+          if (nload <= s) continue;
+          const int last = s + C::NSLOT * ((nload - 1 - s) / C::NSLOT);
+          drain_bar(bar(C::B_FULL + s), uint32_t(last / C::NSLOT) & 1u, err);
+        }
+        if (tail_pending) drain_bar(bar(C::B_QTAIL), uint32_t(ntail) & 1u, err);
+        if (ktail_pending) drain_bar(bar(C::B_KTAIL), uint32_t(nktail) & 1u, err);
+        if (nfix > 0) drain_bar(bar(C::B_FIX), uint32_t(nfix - 1) & 1u, err);
+      }
+      __syncwarp();
+    } else if (warp == kWarpMma) {
+      // ---------------------------------------------------------- scores issuer
+      // Per unit u = (entry, half h): S^T and dP^T into buffer h.  The tails
+      // (dV, dK, dQ^T) come from a second issuing thread, so that the tensor
+      // pipe has work from one while the other waits for a buffer.
+      if (lane == 0) {
+        int nload = 0, nent = 0;
+        bool ok = true;
+        const uint64_t kdesc = kmajor_base<D>(sK), vdesc = kmajor_base<D>(sV);
+        const uint64_t rk0 = kmajor_base<D>(sRing);
+        for (int k = 0; ok; ++k) {
+          if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+          BwdItem it;
+          const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
+          ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+          if (!valid) break;
+          if (!wait_bar(bar(C::B_FIX), uint32_t(k) & 1u, abort_flag, err, 3)) { ok = false; break; }
+          const int n = it.e1 - it.e0;
+          for (int j = 0; j < n && ok; ++j) {
+            const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t hrow = uint64_t(h) * (C::HALF_ROWS >> 4);
+              // S^T into buffer h once the previous entry's dV and dK products
+              // of this half have read the P^T and dS^T written there
+              if (nent > 0 && !wait_bar(bar(C::B_AFREE + h), uint32_t(nent - 1) & 1u, abort_flag, err, 7)) {
+                ok = false;
+                break;
+              }
+              if (h == 0 && !wait_bar(bar(C::B_FULL + qs), uint32_t(nload / C::NSLOT) & 1u, abort_flag, err, 4)) {
                 ok = false;
                 break;
               }
               ptx::tc_fence_after();
-              issue_s<D>(rp, kdesc, rk0 + uint64_t(nq) * (C::TILE >> 4));
-              s_early = true;
+              issue_scores64<D>(tmem + C::col_s(h), kdesc, rk0 + uint64_t(qs) * (C::TILE >> 4) + hrow);
+              // dP^T into buffer h once the reducers have read the dQ^T there
+              if (nent > 0 && !wait_bar(bar(C::B_DQFREE + h), uint32_t(nent - 1) & 1u, abort_flag, err, 10)) {
+                ok = false;
+                break;
+              }
+              if (h == 0 &&
+                  !wait_bar(bar(C::B_FULL + ds), uint32_t((nload + 1) / C::NSLOT) & 1u, abort_flag, err, 4)) {
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              issue_scores64<D>(tmem + C::col_p(h), vdesc, rk0 + uint64_t(ds) * (C::TILE >> 4) + hrow);
+              ptx::mma_commit(bar(C::B_SFULL + h));
             }
+            nload += 2;
+            ++nent;
+          }
+          // done with this item's K and V (its products' completion is the
+          // tails issuer's half of the barrier): the next item's copy may only
+          // start after this thread has seen the present one, or a phase of
+          // the copy barrier could pass unseen
+          if (ok) ptx::mbar_arrive(bar(C::B_FIXFREE));
+        }
+        ptx::mma_commit(bar(C::B_DRAIN));
+        drain_bar(bar(C::B_DRAIN), 0, err);
+      }
+      __syncwarp();
+    } else if (warp == kWarpTail) {
+      // ---------------------------------------------------------- tails issuer
+      // Per unit, once the row warps have written its P^T and dS^T: dV, dK and
+      // dQ^T.  Its commits also free K and V (after the item's last unit) and
+      // close dV and dK for the epilogue; both cover the scores issuer's
+      // products too, which finished before the row warps signalled.
+      if (lane == 0) {
+        int nload = 0, nent = 0;
+        bool ok = true;
+        const uint64_t rv0 = v_base<D>(sRing);
+        // dQ^T operands: K^T (the K tile read MN-major, like V in P.V) and dS^T
+        // (MN-major without swizzle: 128 bytes between eight-key core matrices
+        // along K, 2 KB between eight-query chunks along N; half h starts at
+        // chunk 8h)
+        const uint64_t ktdesc = v_base<D>(sK);
+        const uint64_t dsdesc0 = ptx::smem_desc(sDS, 128u, kDsChunk, ptx::kSwizzleNone);
+        for (int k = 0; ok; ++k) {
+          if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+          BwdItem it;
+          const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
+          ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+          if (!valid) break;
+          const int n = it.e1 - it.e0;
+          for (int j = 0; j < n && ok; ++j) {
+            const int qs = nload % C::NSLOT, ds = (nload + 1) % C::NSLOT;
+            for (int h = 0; h < 2 && ok; ++h)
+              ok = bwd_tail<D>(tmem, bars, h, nent, qs, ds, j == 0 && h == 0, k, rv0, ktdesc, dsdesc0, abort_flag,
+                               err);
+            nload += 2;
+            ++nent;
           }
           if (!ok) break;
-          ptx::mma_commit(bar(C::B_EMPTY + qs));
-          ptx::mma_commit(bar(C::B_EMPTY + ds));
-          nload += 2;
+          // K and V are free and (with n > 0) dV and dK final once the item's
+          // products have finished; that includes the last dQ^T, so the dS
+          // buffer is free for the output stage too
+          ptx::mma_commit(bar(C::B_FIXFREE));
+          if (n > 0) ptx::mma_commit(bar(C::B_ODONE));
+        }
+        ptx::mma_commit(bar(C::B_DRAIN2));
+        drain_bar(bar(C::B_DRAIN2), 0, err);
+      }
+      __syncwarp();
+    } else if (warp >= kWarpRed) {
+      // ---------------------------------------------------------- dQ reducers
+      // Warps 12-19: warp 12 + rq + 4 ch owns TMEM lanes 32 rq .. +31 of dQ^T,
+      // i.e. head dims d = 32 rq + lane, and query columns 32 ch .. +31 of each
+      // unit (64 queries of buffer h): its 32 columns into registers, the
+      // buffer released at once, then for each of its query rows q,
+      // dQacc[q, h, d] += round(dQ^T[d, q]): the product already comes out in
+      // the row's quanta (its dS was scaled by m_q), so this is an exact
+      // integer add at L2, each warp instruction covering 128 contiguous bytes.
+      const int rq = (warp - kWarpRed) & 3, ch = (warp - kWarpRed) >> 2;
+      const bool active = 32 * rq < D;
+      const uint32_t lane_off = uint32_t(rq * 32) << 16;
+      int nent = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+        BwdItem it;
+        const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
+        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        if (!valid) break;
+        const size_t rstride = size_t(p.H) * D;
+        int nx = it.e0 < it.e1 ? __ldg(p.qidx + it.e0) : 0;
+        for (int e = it.e0; e < it.e1 && ok; ++e) {
+          const int a0 = nx * kTile, qn = min(kTile, it.L - a0);
+          if (e + 1 < it.e1) nx = __ldg(p.qidx + e + 1);  // one entry ahead
+          for (int h = 0; h < 2; ++h) {
+            if (!warp_wait(bar(C::B_DQFULL + h), uint32_t(nent) & 1u, abort_flag, err, 11)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            uint32_t v[32];
+            if (active) {
+              ptx::tmem_ld32(tmem + C::col_p(h) + lane_off + 32 * ch, v);
+              ptx::tmem_wait_ld();
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::B_DQFREE + h));
+            const int q0 = 64 * h + 32 * ch;  // first query row of this warp's columns
+            if (active && q0 < qn) {
+              int32_t* row = p.dqacc + (size_t(it.s0 + a0 + q0) * p.H + it.h) * D + 32 * rq + lane;
+              // rows past the sequence end hold zeros and are skipped by the
+              // instruction's predicate
+#pragma unroll
+              for (int q = 0; q < 32; ++q, row += rstride)
+                ptx::red_add_s32_if(row, __float2int_rn(__uint_as_float(v[q])), q0 + q < qn);
+            }
+          }
           ++nent;
         }
-        if (!ok) break;
-        ptx::mma_commit(bar(C::B_FIXFREE));
-        if (n > 0) ptx::mma_commit(bar(C::B_ODONE));
       }
-      ptx::mma_commit(bar(C::B_DRAIN));
-      drain_bar(bar(C::B_DRAIN), 0, err);
-    }
-    __syncwarp();
     }
   } else {
-    ptx::regs_inc<192>();
+    ptx::regs_inc<kRegsRow>();
     // ---------------------------------------------------------- P^T, dS^T (key rows)
-    const int qd = warp & 3, hf = warp >> 2;  // lane quarter, query half
+    // Warp w owns TMEM lanes (keys) 32 (w % 4) .. +31 and, in every unit, the
+    // unit's query columns 32 (w / 4) .. +31.
+    const int qd = warp & 3, cg = warp >> 2;  // lane quarter, column group
     const int r = qd * 32 + lane;
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
     const float c2 = p.scale_log2;
+    uint8_t* dsbuf = sbase + C::OFF_DS;
     int nent = 0, nodone = 0, nload = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
       BwdItem it;
-      const bool valid = bwd_load(item_ring + 8 * (k & 1), it);
+      const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
       ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
       if (!valid) break;
+      // the dS buffer doubles as the output stage of the item's epilogue: no
+      // warp writes this item's dS before every warp has stored the previous
+      // item's rows
+      if (k > 0 && !warp_wait(bar(C::B_STAGE), uint32_t(k - 1) & 1u, abort_flag, err, 6)) break;
       const int kn = min(kTile, it.L - it.i0);
       const bool row_in = r < kn;
       const int kl = it.i0 + r;  // local key index
@@ -884,153 +928,125 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const bool uniform_k = __all_sync(0xffffffffu, !row_in || kcode == kcode_w);
       const bool all_in = __all_sync(0xffffffffu, row_in);
       const int n = it.e1 - it.e0;
-      int nx_idx = n > 0 ? __ldg(p.idx + it.e0) : 0, nx_lab = n > 0 ? __ldg(p.label + it.e0) : 0;
-      for (int jj = 0; jj < n; ++jj) {
+      int nx_idx = n > 0 ? __ldg(p.qidx + it.e0) : 0, nx_lab = n > 0 ? __ldg(p.qlabel + it.e0) : 0;
+      for (int jj = 0; jj < n && ok; ++jj) {
         const int e = it.e0 + jj;
-        const int a0 = nx_idx * kTile, an = min(kTile, it.L - a0);
+        const int ti = nx_idx;  // the entry's q-tile within the sequence
+        const int a0 = ti * kTile, an = min(kTile, it.L - a0);
         const int lab = nx_lab;
         if (jj + 1 < n) {  // the next entry's list values, one entry ahead
-          nx_idx = __ldg(p.idx + e + 1);
-          nx_lab = __ldg(p.label + e + 1);
+          nx_idx = __ldg(p.qidx + e + 1);
+          nx_lab = __ldg(p.qlabel + e + 1);
         }
-        const int qs = nload % C::NSLOT;
         nload += 2;
-        // the dense kind: each lane loads the caller's word of query row
-        // a0 + 64 hf + 32 m + lane over the warp's 32 keys, before the wait
-        uint32_t dw[2] = {0u, 0u};
-        if (kind == ATTN_MASK_DENSE && lab == ATTN_TILE_PARTIAL && kbase < it.L) {
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int qrow = a0 + 64 * hf + 32 * m + lane;
-            if (qrow < it.L) dw[m] = dense_word(p.mask, it.b, it.L, qrow, kbase >> 5);
-          }
-        }
-        if (!warp_wait(bar(C::B_SFULL), uint32_t(nent) & 1u, abort_flag, err, 8)) { ok = false; break; }
-        ptx::tc_fence_after();
-        // the q-tile's LSE, D and codes came with Q(i): its load has landed
-        if (!warp_wait(bar(C::B_FULL + qs), uint32_t((nload - 2) / C::NSLOT) & 1u, abort_flag, err, 9)) {
-          ok = false;
-          break;
-        }
-        const float* sl = reinterpret_cast<const float*>(side + qs * C::SIDE_WORDS);
+        // the q-tile's side values (LSE * log2 e, D, m_i), from global memory:
+        // the tensor cores have priority on shared memory, global loads do not
+        // wait for them
+        const float* sl = p.side + (size_t(it.h) * p.G + it.gbase + ti) * kBwdSideFloats;
         // every pair of the warp's rows and columns visible: no masking at all
         const bool fast = lab == ATTN_TILE_FULL && an == kTile && all_in;
-        // bit c of vis[m]: query column 64 hf + 32 m + c sees this key.  Causal
-        // part and bounds: a0 + column >= kl and column < an.
-        uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
-        if (!fast) {
-          const int lo = kl - a0;  // first visible column
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int c0 = 64 * hf + 32 * m;
-            vis[m] = lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? ~prefix_bits(lo - c0) & prefix_bits(an - c0)
-                                                                   : prefix_bits(an - c0);
+        for (int h = 0; h < 2; ++h) {
+          const int cq = 64 * h + 32 * cg;  // the warp's first query column of the entry
+          // before the wait: the dense kind's word of query row a0 + cq + lane
+          // over the warp's 32 keys, or (code kinds) that query's code
+          uint32_t dw = 0u;
+          int qc = 0;
+          if (lab == ATTN_TILE_PARTIAL && kbase < it.L) {
+            const int qrow = a0 + cq + lane;
+            if (kind == ATTN_MASK_DENSE) {
+              if (qrow < it.L) dw = dense_word(p.mask, it.b, it.L, qrow, kbase >> 5);
+            } else if (kind_codes(kind)) {
+              qc = query_code(p.mask, it.s0 + min(qrow, a0 + an - 1));
+            }
           }
-          if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
-            // transpose the 32 x 32 bit block: ballot j gathers bit j (key
-            // lane j) of every lane's (query's) word, and lane j keeps it
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
+          if (!warp_wait(bar(C::B_SFULL + h), uint32_t(nent) & 1u, abort_flag, err, 8)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // bit c of vis: query column cq + c sees this key.  Causal part and
+          // bounds: a0 + column >= kl and column < an.
+          uint32_t vis = 0xffffffffu;
+          if (!fast) {
+            vis = lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? ~prefix_bits(kl - a0 - cq) & prefix_bits(an - cq)
+                                                                : prefix_bits(an - cq);
+            if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
+              // transpose the 32 x 32 bit block: ballot j gathers bit j (key
+              // lane j) of every lane's (query's) word, and lane j keeps it
               uint32_t mine = 0u;
 #pragma unroll 4
               for (int j = 0; j < 32; ++j) {
-                const uint32_t t = __ballot_sync(0xffffffffu, (dw[m] >> j) & 1u);
+                const uint32_t t = __ballot_sync(0xffffffffu, (dw >> j) & 1u);
                 mine = lane == j ? t : mine;
               }
-              vis[m] &= mine;
-            }
-          } else if (lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
-            const int* qc = side + qs * C::SIDE_WORDS + 2 * kTile + 64 * hf;
-            if (uniform_k) {
-#pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                vis[m] &= __ballot_sync(0xffffffffu, code_visible(kind, qc[32 * m + lane], kcode_w));
-              }
-            } else {
-#pragma unroll
-              for (int m = 0; m < 2; ++m) {
+              vis &= mine;
+            } else if (lab == ATTN_TILE_PARTIAL && kind_codes(kind)) {
+              if (uniform_k) {
+                vis &= __ballot_sync(0xffffffffu, code_visible(kind, qc, kcode_w));
+              } else {
                 uint32_t w = 0;
-                for (int c = 0; c < 32; ++c) w |= uint32_t(code_visible(kind, qc[32 * m + c], kcode)) << c;
-                vis[m] &= w;
+                for (int c = 0; c < 32; ++c)
+                  w |= uint32_t(code_visible(kind, __shfl_sync(0xffffffffu, qc, c), kcode)) << c;
+                vis &= w;
               }
             }
+            // a key past the sequence end: its P and dS are exactly zero
+            if (!row_in) vis = 0u;
           }
-          if (!row_in) {
-            // a key past the sequence end: its P and dS are exactly zero, so the
-            // stored dS block holds no value from another sequence
-            vis[0] = vis[1] = 0u;
-          }
-        }
-        // this warp's 64 columns: S^T (both quarters) and dP^T (first quarter)
-        // first; dP^T's second quarter loads while the first is computed, after
-        // which dP^T's region is released for the next entry's S^T.  Quarter m
-        // writes P^T to columns 64 hf + 16 m + [0,16) and dS^T to 64 hf + 32 +
-        // 16 m + [0,16) of the S^T region, all of which this warp has read.
-        const uint32_t rs = COL_R0 + 128u * uint32_t(nent & 1), rp = COL_R0 + 128u * uint32_t((nent & 1) ^ 1);
-        uint32_t sv[2][32], dv0[32], dv1[32];
-        uint32_t dsw[32];  // this half's dS (bf16 pairs), kept for the block store
-        ptx::tmem_ld32(lane_base + rs + 64 * hf, sv[0]);
-        ptx::tmem_ld32(lane_base + rs + 64 * hf + 32, sv[1]);
-        ptx::tmem_ld32(lane_base + rp + 64 * hf, dv0);
-        ptx::tmem_wait_ld();
-        ptx::tmem_ld32(lane_base + rp + 64 * hf + 32, dv1);
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int cq = 64 * hf + 32 * m;
-          if (m == 1) {
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::B_YFREE));
-          }
-          const uint32_t(&dv)[32] = m ? dv1 : dv0;
+          // the warp's 32 columns of S^T and dP^T in, then P^T over the first
+          // 16 and dS^T over the next 16 of its score columns
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(lane_base + C::col_s(h) + 32 * cg, sv);
+          ptx::tmem_ld32(lane_base + C::col_p(h) + 32 * cg, dv);
+          ptx::tmem_wait_ld();
+          // P^T and dS^T for TMEM; the copy of dS for the dQ^T product goes to
+          // shared memory scaled by each query's fixed-point multiplier m_i:
+          // this key's 32 queries as four 16-byte pieces, one per eight-query
+          // chunk (the dQ^T that last read these chunks, the previous entry's
+          // of this half, was issued before this unit's scores, whose
+          // completion this warp waited for)
+          // side values four columns per (broadcast) load
+          const float4* l4 = reinterpret_cast<const float4*>(sl + cq);
+          const float4* g4 = reinterpret_cast<const float4*>(sl + kTile + cq);
+          const float4* m4 = reinterpret_cast<const float4*>(sl + 2 * kTile + cq);
           uint32_t pp[16], pd[16];
-          if (fast) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
-              const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
-              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[m][c]), __uint_as_float(sv[m][c + 1])),
-                                          make_float2(c2, c2), make_float2(-l.x, -l.y));
-              const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-              pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
-              const float2 dd = ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                                          make_float2(-g.x, -g.y)));
-              pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
-            }
-          } else {
-            const uint32_t vw = vis[m];
+          for (int u = 0; u < 4; ++u) {
+            uint32_t ps[4];
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float2 l = *reinterpret_cast<const float2*>(sl + cq + c);
-              const float2 g = *reinterpret_cast<const float2*>(sl + kTile + cq + c);
-              const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[m][c]), __uint_as_float(sv[m][c + 1])),
-                                          make_float2(c2, c2), make_float2(-l.x, -l.y));
-              const bool v0 = (vw >> c) & 1u, v1 = (vw >> (c + 1)) & 1u;
-              const float p0 = v0 ? ptx::ex2(x.x) : 0.f, p1 = v1 ? ptx::ex2(x.y) : 0.f;
-              pp[c >> 1] = ptx::pack_bf16(p0, p1);
-              const float d0 = v0 ? p0 * (__uint_as_float(dv[c]) - g.x) : 0.f;
-              const float d1 = v1 ? p1 * (__uint_as_float(dv[c + 1]) - g.y) : 0.f;
-              pd[c >> 1] = ptx::pack_bf16(d0, d1);
+            for (int hq = 0; hq < 2; ++hq) {
+              const float4 lq = __ldg(l4 + 2 * u + hq), gq = __ldg(g4 + 2 * u + hq), mq = __ldg(m4 + 2 * u + hq);
+#pragma unroll
+              for (int e2 = 0; e2 < 2; ++e2) {
+                const int c = 8 * u + 4 * hq + 2 * e2;  // column pair (c, c + 1)
+                const float2 l = e2 ? make_float2(lq.z, lq.w) : make_float2(lq.x, lq.y);
+                const float2 g = e2 ? make_float2(gq.z, gq.w) : make_float2(gq.x, gq.y);
+                const float2 mf = e2 ? make_float2(mq.z, mq.w) : make_float2(mq.x, mq.y);
+                const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                            make_float2(c2, c2), make_float2(-l.x, -l.y));
+                // branch-free (vis is all ones on unmasked tiles), so that the
+                // compiler interleaves the independent column pairs; a hidden
+                // pair's P and dS are selected to exactly zero
+                const bool v0 = (vis >> c) & 1u, v1 = (vis >> (c + 1)) & 1u;
+                float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                float2 dd = ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                                      make_float2(-g.x, -g.y)));
+                pv = make_float2(v0 ? pv.x : 0.f, v1 ? pv.y : 0.f);
+                dd = make_float2(v0 ? dd.x : 0.f, v1 ? dd.y : 0.f);
+                pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
+                pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
+                const float2 dm = ptx::fmul2(dd, mf);
+                ps[(c >> 1) & 3] = ptx::pack_bf16(dm.x, dm.y);
+              }
             }
+            *reinterpret_cast<uint4*>(dsbuf + ((cq >> 3) + u) * kDsChunk + r * 16) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
           }
-          ptx::tmem_st16(lane_base + rs + 64 * hf + 16 * m, pp);
-          ptx::tmem_st16(lane_base + rs + 64 * hf + 32 + 16 * m, pd);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) dsw[16 * m + i] = pd[i];
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(C::B_PFULL + hf));  // queries 64 hf .. +63 are ready for the products
-        {
-          // this half's dS, from registers (its TMEM columns may already be
-          // the next entry's dP by now), to its chunk of the block the dQ
-          // kernel multiplies by K
-          uint8_t* kr = p.ds + (size_t(it.h - p.h0) * size_t(n_entries) + size_t(e)) * kDsBlock +
-                        size_t(qd * 32 + lane) * 16;  // this key's piece of every chunk
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(kr + (8 * hf + u) * kDsChunk) =
-                make_uint4(dsw[4 * u], dsw[4 * u + 1], dsw[4 * u + 2], dsw[4 * u + 3]);
+          ptx::tmem_st16(lane_base + C::col_s(h) + 32 * cg, pp);
+          ptx::tmem_st16(lane_base + C::col_s(h) + 32 * cg + 16, pd);
+          ptx::tmem_wait_st();
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(C::B_PFULL + h));  // unit (entry, h) is ready for its products
         }
         ++nent;
       }
@@ -1043,18 +1059,19 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       ptx::tc_fence_after();
       // the first four warps store dV, the other four dK (times the scale)
       uint32_t w[D / 2];
-      tmem_row_bf16<D>(lane_base + (hf ? COL_DK : COL_DV), hf ? p.scale : 1.f, n > 0, w);
+      tmem_row_bf16<D>(lane_base + (cg ? C::COL_DK : C::COL_DV), cg ? p.scale : 1.f, n > 0, w);
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE));
       const size_t row0 = (size_t(it.s0 + it.i0 + qd * 32) * p.H + it.h) * D;
-      store_rows<D, C::STAGE_WARP>(sbase + C::OFF_STAGE + warp * C::STAGE_WARP, lane, w,
-                                   (hf ? p.out0 : p.out1) + row0, size_t(p.H) * D, kn - qd * 32);
+      store_rows<D, C::STAGE_WARP>(dsbuf + warp * C::STAGE_WARP, lane, w, (cg ? p.dk : p.dv) + row0,
+                                   size_t(p.H) * D, kn - qd * 32);
+      ptx::mbar_arrive(bar(C::B_STAGE));
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kDkdvMma) {
+  if (warp == kWarpMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -1064,82 +1081,75 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 template <int D>
 attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
-  using Q = DqCfg<D>;
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map<D>(&mq, a.q, a.total_tokens, a.num_heads) || !make_map<D>(&mk, a.k, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mv, a.v, a.total_tokens, a.num_heads) ||
       !make_map<D>(&mdo, a.dout, a.total_tokens, a.num_heads))
     return record_cuda_error(cudaErrorInvalidValue, "attn_bwd tensor map encoding");
   // per launch, for the current device (the settings are per device and context)
-  {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Q::SMEM_ALLOC);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd configure");
-  }
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_ALLOC);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd configure");
   int num_sms = 0;
-  {
-    const cudaError_t e = current_sm_count(&num_sms);
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd device query");
-  }
+  e = current_sm_count(&num_sms);
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd device query");
+  const long long items = (long long)a.bm.max_qt * a.num_heads;
+  if (items <= 0 || items > INT_MAX || a.num_heads > 65535) return ATTN_ERR_UNSUPPORTED;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  float* delta = reinterpret_cast<float*>(ws + a.ws.delta);
-  int32_t* kpos = reinterpret_cast<int32_t*>(ws + a.ws.kpos);
-  const long long rows = (long long)a.total_tokens * a.num_heads;
-  bwd_delta_kernel<D><<<unsigned((rows + (2048 / D) - 1) / (2048 / D)), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), delta, a.total_tokens,
-      a.num_heads);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd delta launch");
-  bwd_kpos_kernel<<<unsigned(a.bm.max_qt), 128, 0, s>>>(a.bm.header, a.bm.qt_idx, a.bm.koff, a.bm.kidx,
-                                                          a.bm.qoff, a.bm.qidx, kpos);
+  float* side = reinterpret_cast<float*>(ws + a.ws.side);
+  float* dnorm = reinterpret_cast<float*>(ws + a.ws.dnorm);
+  float* bounds = reinterpret_cast<float*>(ws + a.ws.bounds);
+  int32_t* dqacc = reinterpret_cast<int32_t*>(ws + a.ws.dqacc);
+  const int G = a.bm.max_qt;
+
+  const int nbound = a.bm.batch * a.num_heads * kBoundWords;
+  bwd_zero_kernel<<<unsigned((nbound + 255) / 256 < 1024 ? (nbound + 255) / 256 : 1024), 256, 0, s>>>(
+      reinterpret_cast<int32_t*>(bounds), nbound);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd entry map launch");
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd zero launch");
+  const dim3 tiles(unsigned(a.bm.max_qt), unsigned(a.num_heads));
+  bwd_prep_kernel<D><<<tiles, 256, 0, s>>>(a.bm.header, a.bm.qt_seq, a.bm.qt_idx, a.bm.cu,
+                                           static_cast<const __nv_bfloat16*>(a.o),
+                                           static_cast<const __nv_bfloat16*>(a.dout),
+                                           static_cast<const __nv_bfloat16*>(a.k),
+                                           static_cast<const __nv_bfloat16*>(a.v), a.lse, side, dnorm, bounds, dqacc,
+                                           a.total_tokens, a.num_heads, G);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd prep launch");
+  bwd_mult_kernel<<<tiles, kTile, 0, s>>>(a.bm.header, a.bm.qt_seq, a.bm.qt_idx, a.bm.cu, bounds, dnorm, side,
+                                          a.total_tokens, a.num_heads, G);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd multiplier launch");
+
   BwdParams p;
   p.header = a.bm.header;
+  p.korder = a.bm.korder;
   p.qt_seq = a.bm.qt_seq;
   p.qt_idx = a.bm.qt_idx;
+  p.qoff = a.bm.qoff;
+  p.qidx = a.bm.qidx;
+  p.qlabel = a.bm.qlabel;
   p.cu = a.bm.cu;
   p.mask = a.mask;
-  p.lse = a.lse;
-  p.delta = delta;
-  p.ds = ws + a.ws.ds;
-  p.kpos = kpos;
-  p.e_bound = a.ws.e_bound;
+  p.side = side;
+  p.G = G;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.dqacc = dqacc;
   p.H = a.num_heads;
   p.T = a.total_tokens;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  // head groups whose dS blocks fit the workspace: dK, dV over the k-major
-  // lists (writing dS), then dQ over the q-major lists (reading it)
-  for (int h0 = 0; h0 < a.num_heads; h0 += a.heads_per_pass) {
-    p.h0 = h0;
-    p.G = a.num_heads - h0 < a.heads_per_pass ? a.num_heads - h0 : a.heads_per_pass;
-    const long long items = (long long)a.bm.max_qt * p.G;
-    if (items <= 0 || items > INT_MAX) return ATTN_ERR_UNSUPPORTED;
-    const unsigned grid = unsigned(items < num_sms ? items : num_sms);
-    p.order = a.bm.korder;
-    p.off = a.bm.qoff;
-    p.idx = a.bm.qidx;
-    p.label = a.bm.qlabel;
-    p.out0 = static_cast<__nv_bfloat16*>(a.dk);
-    p.out1 = static_cast<__nv_bfloat16*>(a.dv);
-    p.sched = next_sched_slot();
-    attn_bwd_dkdv_kernel<D><<<grid, kDkdvThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dk/dv launch");
-    p.order = a.bm.order;
-    p.off = a.bm.koff;
-    p.idx = a.bm.kidx;
-    p.label = a.bm.klabel;
-    p.out0 = static_cast<__nv_bfloat16*>(a.dq);
-    p.out1 = nullptr;
-    p.sched = next_sched_slot();
-    attn_bwd_dq_kernel<D><<<grid, kBwdThreads, Q::SMEM_ALLOC, s>>>(mk, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dq launch");
-  }
+  p.sched = next_sched_slot();
+  const unsigned grid = unsigned(items < num_sms ? items : num_sms);
+  attn_bwd_kernel<D><<<grid, kBwdThreads, C::SMEM_ALLOC, s>>>(mq, mk, mv, mdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd launch");
+  bwd_dq_convert_kernel<D><<<tiles, 256, 0, s>>>(a.bm.header, a.bm.qt_seq, a.bm.qt_idx, a.bm.cu, bounds, dnorm,
+                                                 dqacc, static_cast<__nv_bfloat16*>(a.dq), a.total_tokens,
+                                                 a.num_heads, a.scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd dq convert launch");
   return ATTN_OK;
 }
 

@@ -21,9 +21,8 @@ enum : int32_t {
   kErrCuOrder = 1 << 1,      // cu_seqlens decreases somewhere
   kErrCuLast = 1 << 2,       // cu_seqlens[batch] != total_tokens
   kErrSeqTooLong = 1 << 3,   // a sequence is longer than max_seqlen
-  kErrCapacity = 1 << 4,     // more tile entries than the backward's dS blocks were sized for
   kErrTimeout = 1 << 8,      // a pipeline wait gave up (bits 9.. hold the wait site)
-  kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong | kErrCapacity,
+  kErrInputMask = kErrCuFirst | kErrCuOrder | kErrCuLast | kErrSeqTooLong,
 };
 
 // Header words of the block-mask workspace (the kernels' work counters are
@@ -177,17 +176,17 @@ struct FwdArgs {
 attn_status launch_attn_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 attn_status launch_attn_fwd_f32(const FwdArgs& a, cudaStream_t s);
 
-// Byte layout of the backward's workspace: D = rowsum(dO * O) as fp32 [H, T],
-// the k-major position of every q-major tile entry, then the dS blocks
-// (128 x 128 bf16 per entry and head) of as many heads as fit.  e_bound bounds
-// the entries of any mask of these sizes and kind: a causal kind keeps only
-// keys at or before the query, so a sequence of n tiles has at most
-// n (n + 1) / 2 pairs; the others up to n^2.
+// Byte layout of the backward's workspace: per q-tile and head the side values
+// of its 128 rows, fp32 [H][max_qtiles][kBwdSideFloats] (LSE * log2 e, +inf
+// for rows that see no key or lie past the sequence end; D = rowsum(dO * O);
+// the fixed-point multiplier m_i), ||dO_i|| fp32 [H, T], the bound words of
+// every (sequence, head) (fp32 [batch][H][4]), and the dQ accumulator, int32
+// fixed point [T, H, D].
+constexpr int kBwdSideFloats = 3 * kTile;
 struct BwdLayout {
-  uint64_t delta = 0, kpos = 0, ds = 0, ds_per_head = 0, total = 0;
-  int e_bound = 0;
+  uint64_t side = 0, dnorm = 0, bounds = 0, dqacc = 0, total = 0;
 };
-bool bwd_layout(int kind, int batch, int total_tokens, int max_seqlen, int num_heads, BwdLayout* out);
+bool bwd_layout(int batch, int total_tokens, int num_heads, int head_dim, int max_qt, BwdLayout* out);
 
 struct BwdArgs {
   const void* q;
@@ -201,7 +200,6 @@ struct BwdArgs {
   void* dv;
   void* workspace;
   BwdLayout ws;
-  int heads_per_pass;
   int total_tokens, num_heads, head_dim;
   float scale;
   BmView bm;

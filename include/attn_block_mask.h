@@ -103,8 +103,7 @@ typedef enum attn_status {
   ATTN_ERR_MASK_MISMATCH = 4,        /* block mask built for another kind / cu_seqlens / sizes */
   ATTN_ERR_CUDA = 5,                 /* a CUDA runtime or driver call failed */
   ATTN_ERR_DEVICE_TIMEOUT = 6,       /* a kernel gave up on a pipeline wait (reported later) */
-  ATTN_ERR_DEVICE_INVALID_INPUT = 7  /* the device found cu_seqlens malformed, or more tile entries
-                                        than the backward workspace was sized for (reported later) */
+  ATTN_ERR_DEVICE_INVALID_INPUT = 7  /* the device found cu_seqlens malformed (reported later) */
 } attn_status;
 
 typedef enum attn_mask_kind {
@@ -263,20 +262,22 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_stream_t stream);
 
 /*
- * Bytes of device workspace attn_bwd() needs to run all `num_heads` heads in
- * one pass over the mask `bm` (built by attn_block_mask_build()).  Pure host
- * function.  The workspace holds, 256-byte aligned:
+ * Bytes of device workspace attn_bwd() needs for `num_heads` heads of
+ * `head_dim` (32, 64 or 128) over the mask `bm` (built by
+ * attn_block_mask_build()).  Pure host function.  The workspace holds,
+ * 256-byte aligned:
  *   D = rowsum(dout * o)        fp32 [num_heads, total_tokens]
- *   entry map                   int32 per tile entry: the position of each
- *                               q-major entry in the k-major lists
- *   dS blocks                   128 x 128 bf16 per tile entry and head
- * The entry count is bounded on the host from the mask's sizes and kind (a
- * sequence of n tiles has at most n (n + 1) / 2 tile pairs with keys at or
- * before the query under the causal kinds, n^2 under NONE and DENSE); only
- * the entries the mask keeps are written and read.
+ *   ||dout_i||                  fp32 [num_heads, total_tokens]
+ *   bound words                 fp32 [batch][num_heads][4]: the largest
+ *                               ||v_j|| and |k_jd| of each sequence and
+ *                               head (two words unused)
+ *   dQ accumulator              int32 [total_tokens, num_heads, head_dim],
+ *                               fixed point
+ * i.e. O(total_tokens * num_heads * head_dim); nothing is kept per tile pair.
+ * Returns ATTN_ERR_UNSUPPORTED for another head_dim.
  */
 ATTN_API attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t num_heads,
-                                             size_t* bytes);
+                                             int32_t head_dim, size_t* bytes);
 
 /*
  * Attention backward with the structured mask: the gradients of attn_fwd()'s
@@ -290,22 +291,28 @@ ATTN_API attn_status attn_bwd_workspace_size(const attn_block_mask* bm, int32_t 
  *             written; nothing else is touched)
  *   head_dim, scale, cu_seqlens, batch, max_seqlen, kind, params, seg_id,
  *             role, turn, bm: as for attn_fwd(), with the same checks; the
- *             block mask's transposed (k-major) lists drive dk and dv
- *   workspace device, 256-byte aligned, caller-owned scratch (layout above);
- *             workspace_bytes below attn_bwd_workspace_size() for one head
- *             gives ATTN_ERR_WORKSPACE_TOO_SMALL, and a size between the
- *             one-head and all-head figures runs the heads in groups
+ *             block mask's transposed (k-major) lists drive the work
+ *   workspace device, 256-byte aligned, caller-owned scratch of at least
+ *             attn_bwd_workspace_size() bytes (layout above), else
+ *             ATTN_ERR_WORKSPACE_TOO_SMALL
  * Math: P = exp(scale q k^T - LSE) over the visible pairs, dV = P^T dO,
  * dP = dO V^T, dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q.  One
- * kernel walks every k-tile's list (dK, dV, and dS stored as bf16 blocks), a
- * second walks every q-tile's list (dQ from the stored dS blocks): five
- * products per visible tile pair.  P and dS are rounded to bf16 for the
+ * persistent kernel walks every (k-tile, head)'s list: five tensor-core
+ * products per visible tile pair (S^T, dP^T, dV, dK and dQ^T = K^T dS^T), with
+ * dS kept on chip.  Each k-tile's dQ^T contribution is added into an int32
+ * fixed-point accumulator whose quantum, per query row i and head, is 2^-30
+ * of 4 ||dout_i|| max_j||v_j|| max_jd|k_jd| (the maxima over the row's
+ * sequence; twice a bound on every partial sum of the row, so the sums never
+ * overflow); integer addition is exact, so the backward is deterministic
+ * (bit-identical repeats, whatever the order of the adds) without per-pair
+ * storage.  P and dS are rounded to bf16 for the
  * tensor-core products, accumulation is fp32 in tensor memory, outputs are
- * rounded to nearest even.  Deterministic: each output row is summed by one
- * CTA in a fixed tile order, with no atomics.  Inputs must be finite inside
- * each sequence.  Only ATTN_DTYPE_BF16 exists (ATTN_ERR_UNSUPPORTED
- * otherwise).  Launches that share one block mask may run concurrently with
- * each other and with attn_fwd() on other streams.
+ * rounded to nearest even.  `lse` must be the forward's (the bound assumes
+ * each row's weights sum to one).  Inputs must be finite inside each
+ * sequence.  Only ATTN_DTYPE_BF16 exists
+ * (ATTN_ERR_UNSUPPORTED otherwise).  Launches that share one block mask may
+ * run concurrently with each other and with attn_fwd() on other streams, each
+ * with its own workspace.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                               const void* dout, const float* lse, void* dq, void* dk, void* dv,

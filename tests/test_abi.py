@@ -164,26 +164,24 @@ def test_bwd_rejects_bad_arguments_before_any_launch(native_lib):
     bm2.block_m = bm2.block_n = 128
     bm2.cu_seqlens = 0x30000
     assert call(bmref=bm2, maxL=128) == 4
-    # workspace sizes: all heads, and below one head's dS blocks
+    # workspace size: the side values of each q-tile and head (3 x 128 fp32),
+    # ||dO_i|| [H, T] fp32, the bound words [batch][H][4] fp32 and the dQ
+    # accumulator [T, H, D] int32, each 256-byte aligned; nothing per tile pair
+    bm2.max_qtiles = 3
     out = ctypes.c_size_t()
-    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, ctypes.byref(out)) == 0
-    full = out.value
-    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 1, ctypes.byref(out)) == 0
-    one = out.value
-    # 256 tokens in one sequence: 2 tiles and 3 tile pairs, but the host bound
-    # is nq (nk + 1) / 2 with nq = ceil(T / 128) + batch = 3 and nk = 2, i.e. 5
-    # pairs of 32 KB per head, plus D's [H, T] fp32 (256-byte aligned)
-    assert full - one == 5 * 128 * 128 * 2 + 1024
-    assert call(bmref=bm2, wsb=one - 1) == 3
-    # without a causal restriction (the none and dense kinds) the bound is nq x nk
-    bm2.kind = 5
-    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, ctypes.byref(out)) == 0
-    full5 = out.value
-    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 1, ctypes.byref(out)) == 0
-    assert full5 - out.value == 6 * 128 * 128 * 2 + 1024
+    a256 = lambda x: (x + 255) // 256 * 256
+    for kind in (0, 5):
+        bm2.kind = kind
+        for H, D in ((2, 128), (1, 64), (3, 32)):
+            assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), H, D, ctypes.byref(out)) == 0
+            want = a256(4 * H * 3 * 384) + a256(4 * H * 256) + a256(16 * H) + a256(4 * 256 * H * D)
+            assert out.value == want, (kind, H, D)
     bm2.kind = 0
-    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 0, ctypes.byref(out)) == 1
-    assert lib.attn_bwd_workspace_size(None, 2, ctypes.byref(out)) == 1
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, 128, ctypes.byref(out)) == 0
+    assert call(bmref=bm2, wsb=out.value - 1) == 3
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 2, 96, ctypes.byref(out)) == 2
+    assert lib.attn_bwd_workspace_size(ctypes.byref(bm2), 0, 128, ctypes.byref(out)) == 1
+    assert lib.attn_bwd_workspace_size(None, 2, 128, ctypes.byref(out)) == 1
 
 
 def test_get_status_rejects_unbuilt_mask(native_lib):

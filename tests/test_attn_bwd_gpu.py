@@ -151,7 +151,7 @@ def test_full_size_workloads_sampled(c, form, heads):
 
 def test_longest_single_sequence_sampled():
     """The largest backward case: one 65536-token causal sequence (512 k-tiles,
-    131328 tile pairs, a 4.3 GB dS workspace); dQ on sampled query rows, dK and
+    131328 tile pairs; the last q-tile's dQ sums 512 k-tiles); dQ on sampled query rows, dK and
     dV on sampled keys of the last eight k-tiles (few rows see those, which
     keeps the oracle quick)."""
     L = 65536
@@ -179,6 +179,28 @@ def test_small_config_fp32_inputs_rounded_to_bf16():
                     q=w.q.bfloat16(), k=w.k.bfloat16(), v=w.v.bfloat16())
     do = W.grad_output(wb, seed=11)
     compare_all(wb, do, run_bwd(wb, do))
+
+
+def test_dq_follows_each_rows_upstream_scale():
+    """dO rows spanning twenty binary orders of magnitude, and a tenth of them
+    zero (as under a loss mask): the dQ of the smallest rows meets the bar
+    relative to their own size, not to the largest row's (the fixed-point
+    quantum follows each row's ||dO_i||), and zero rows get exactly zero."""
+    w = W.random_workload(91, "causal_document", [700, 1300, 129], num_heads=2, head_dim=128)
+    rng = np.random.default_rng(91)
+    e = rng.integers(0, 21, w.total_tokens)
+    f = 2.0 ** -e.astype(np.float64)
+    f[rng.random(w.total_tokens) < 0.1] = 0.0
+    do = (W.grad_output(w, seed=91).float() * torch.from_numpy(f).float()[:, None, None]).bfloat16()
+    got = run_bwd(w, do)
+    ref = oracle.attention_backward(w.q, w.k, w.v, do, w.kind, w.cu_seqlens, w.meta())
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        check(name, g, r)
+    small = np.flatnonzero((e >= 16) & (f > 0)).tolist()
+    zero = np.flatnonzero(f == 0).tolist()
+    assert len(small) > 50 and len(zero) > 50
+    check("dQ of the rows scaled by 2^-16 .. 2^-20", got[0], ref[0], rows=small)
+    assert torch.count_nonzero(got[0][zero]).item() == 0
 
 
 def test_deterministic_repeats_bit_identical():
@@ -259,40 +281,50 @@ def test_invalid_dtype_and_mask_mismatch():
     assert e.value.status == 4
 
 
-def _align256(x):
-    return (x + 255) // 256 * 256
-
-
-def test_head_groups_match_one_pass_bit_exact():
-    """A workspace that holds the dS blocks of fewer heads runs the heads in
-    groups; every gradient is bit-identical to the one-pass run."""
-    w = W.random_workload(72, "shared_prefix", [700, 255, 1000], num_heads=3, head_dim=64)
-    do = W.grad_output(w, seed=72)
+def test_workspace_is_linear_in_tokens_heads_and_dims():
+    """The backward's workspace holds per-row side values (LSE, D, the
+    fixed-point multiplier) and ||dO_i||, the int32 dQ accumulator and
+    per-sequence bound words, O(T H D); no storage per tile pair (the 32k
+    workload's 32 heads take about 0.56 GB)."""
+    w = full_workload(5)
     dm = w.device_meta()
     bm = build_mask(w, dm)
-    q, k, v, dod = w.q.cuda(), w.k.cuda(), w.v.cuda(), do.cuda()
-    kw = dict(seg_id=dm["seg_id"], role=dm["role"], turn=dm["turn"], role_think=w.role_think)
-    o, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
-    ref = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
-    # the documented layout: D [H, T] fp32, the entry map, then e_bound blocks per head
-    H, T = w.num_heads, w.total_tokens
-    nq = -(-T // 128) + w.batch
-    nk = -(-w.max_seqlen // 128)
-    e_bound = min(nq * nk, (nq * (nk + 1) + 1) // 2)
-    head = e_bound * 128 * 128 * 2
-    base = _align256(_align256(H * T * 4) + 4 * e_bound)
-    assert api.attn_bwd_workspace_size(bm, H) == base + H * head
-    for heads_per_pass in (1, 2):
-        ws = torch.empty(base + heads_per_pass * head, dtype=torch.uint8, device="cuda")
-        got = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
-                           workspace=ws, **kw)
-        assert api.attn_get_status(bm) == api.ATTN_OK
-        for x, y in zip(ref, got):
-            assert torch.equal(x, y)
+    T, H, D = w.total_tokens, w.num_heads, w.head_dim
+    size = api.attn_bwd_workspace_size(bm, H, D)
+    side = 4 * H * bm.struct.max_qtiles * 3 * 128
+    assert side + 4 * T * H * (D + 1) <= size < side + 4 * T * H * (D + 1) + (1 << 20)
+    # a too small workspace is refused before any launch
     with pytest.raises(api.AttnError) as e:
-        api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
-                     workspace=torch.empty(base + head - 256, dtype=torch.uint8, device="cuda"), **kw)
+        api.attn_bwd(w.q.cuda(), w.k.cuda(), w.v.cuda(), w.q.cuda(), torch.zeros((H, T), device="cuda"),
+                     w.q.cuda(), bm, w.kind, dm["cu_seqlens"], w.max_seqlen,
+                     workspace=torch.empty(size - 256, dtype=torch.uint8, device="cuda"), **w.api_kwargs(dm))
     assert e.value.status == 3
+
+
+def test_dq_is_bit_identical_under_other_work():
+    """dQ is the same bit for bit when the backward shares the GPU with other
+    kernels (its CTAs then start at other times, take other items and add
+    into the accumulator in another order): the fixed-point sums do not
+    depend on the order of the adds."""
+    w = W.random_workload(82, "causal_document", [3000, 2500, 700], num_heads=8, head_dim=128)
+    do = W.grad_output(w, seed=82)
+    ref = run_bwd(w, do)
+    dm = w.device_meta()
+    bm = build_mask(w, dm)
+    kw = w.api_kwargs(dm)
+    q, k, v, dod = w.q.cuda(), w.k.cuda(), w.v.cuda(), do.cuda()
+    o, lse = api.attn_fwd(q, k, v, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+    side = torch.cuda.Stream()
+    big = torch.randn(4096, 4096, device="cuda")
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            for _ in range(4):
+                big = big @ big * 1e-3
+        got = api.attn_bwd(q, k, v, o, lse, dod, bm, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
+        torch.cuda.synchronize()
+        assert api.attn_get_status(bm) == api.ATTN_OK
+        for x, y in zip(got, ref):
+            assert torch.equal(x.cpu(), y)
 
 
 def test_one_mask_serves_overlapping_forward_and_backward():

@@ -7,8 +7,9 @@ fixed array inside the library, so such a caller only passes the metadata and
 the output buffer it owns.  These tests call it through the C ABI twice in a
 row, on different masks that share that array, and check that its output
 equals the regular builder's (the lists bit-exact, as every block-mask test
-requires) and that the forward gives the same O and LSE from either mask
-(within the forward tolerances, O 2e-2 and LSE 1e-3).
+requires) and that the forward and backward give the same results from
+either mask (bit for bit, as the same lists drive the same deterministic
+kernels, so well within the forward tolerances, O 2e-2 and LSE 1e-3).
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test; it also passes when run alone.
@@ -63,8 +64,11 @@ def test_noalloc_build_matches_regular_build_twice_in_a_row():
         o_ref, l_ref = api.attn_fwd(q, k, v, ref, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
         o_na, l_na = api.attn_fwd(q, k, v, na, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
         assert api.attn_get_status(na) == api.ATTN_OK
-        assert (o_na.float() - o_ref.float()).abs().max().item() <= 2e-2
-        assert (l_na - l_ref).abs().max().item() <= 1e-3
+        # identical lists drive the same deterministic kernels: the outputs are
+        # equal bit for bit (well inside the forward tolerances, O 2e-2 and LSE
+        # 1e-3; rows that see no key have LSE = -inf on both sides)
+        assert torch.equal(o_na, o_ref)
+        assert torch.equal(l_na, l_ref)
         do = W.grad_output(w, seed=3).cuda()
         g_ref = api.attn_bwd(q, k, v, o_ref, l_ref, do, ref, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
         g_na = api.attn_bwd(q, k, v, o_ref, l_ref, do, na, w.kind, dm["cu_seqlens"], w.max_seqlen, **kw)
