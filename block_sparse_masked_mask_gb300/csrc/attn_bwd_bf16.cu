@@ -669,8 +669,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               abort_flag, err);
         if (st_next < 0) break;
         // K and V of this k-tile, once the previous item's products no longer
-        // read them.  K rows past the sequence end are zeroed: their dS is
-        // zero, but an inf there would make dQ^T = K^T dS^T NaN.
+        // read them.  K and V rows past the sequence end are zeroed: their P
+        // and dS are zero, but an inf there would make dQ^T = K^T dS^T or dP
+        // (hence 0 * dP) NaN.
         if (nfix > 0 && !warp_wait(bar(C::B_FIXFREE), uint32_t(nfix - 1) & 1u, abort_flag, err, 13)) break;
         const int kn = min(kTile, it.L - it.i0);
         if (kn == kTile) {
@@ -696,9 +697,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int rr = kn + lane; rr < kTile; rr += 32) {
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
-              uint4* row = reinterpret_cast<uint4*>(sbase + C::OFF_K + c * C::CHUNK + rr * C::ROWB);
+              uint4* krow = reinterpret_cast<uint4*>(sbase + C::OFF_K + c * C::CHUNK + rr * C::ROWB);
+              uint4* vrow = reinterpret_cast<uint4*>(sbase + C::OFF_V + c * C::CHUNK + rr * C::ROWB);
 #pragma unroll
-              for (int x = 0; x < C::ROWB / 16; ++x) row[x] = make_uint4(0u, 0u, 0u, 0u);
+              for (int x = 0; x < C::ROWB / 16; ++x) {
+                krow[x] = make_uint4(0u, 0u, 0u, 0u);
+                vrow[x] = make_uint4(0u, 0u, 0u, 0u);
+              }
             }
           }
           ptx::fence_proxy_async_smem();
@@ -929,6 +934,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool all_in = __all_sync(0xffffffffu, row_in);
       const int n = it.e1 - it.e0;
       int nx_idx = n > 0 ? __ldg(p.qidx + it.e0) : 0, nx_lab = n > 0 ? __ldg(p.qlabel + it.e0) : 0;
+      // the side values of a q-tile (1.5 KB, twelve lines) go into L1 one entry
+      // ahead of their loads, which then do not wait for L2
+      const float* side_h = p.side + (size_t(it.h) * p.G + it.gbase) * kBwdSideFloats;
+      if (warp == 0 && lane < kBwdSideFloats / 32 && n > 0) ptx::prefetch_l1(side_h + size_t(nx_idx) * kBwdSideFloats + 32 * lane);
       for (int jj = 0; jj < n && ok; ++jj) {
         const int e = it.e0 + jj;
         const int ti = nx_idx;  // the entry's q-tile within the sequence
@@ -937,12 +946,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (jj + 1 < n) {  // the next entry's list values, one entry ahead
           nx_idx = __ldg(p.qidx + e + 1);
           nx_lab = __ldg(p.qlabel + e + 1);
+          if (warp == 0 && lane < kBwdSideFloats / 32)
+            ptx::prefetch_l1(side_h + size_t(nx_idx) * kBwdSideFloats + 32 * lane);
         }
         nload += 2;
         // the q-tile's side values (LSE * log2 e, D, m_i), from global memory:
         // the tensor cores have priority on shared memory, global loads do not
         // wait for them
-        const float* sl = p.side + (size_t(it.h) * p.G + it.gbase + ti) * kBwdSideFloats;
+        const float* sl = side_h + size_t(ti) * kBwdSideFloats;
         // every pair of the warp's rows and columns visible: no masking at all
         const bool fast = lab == ATTN_TILE_FULL && an == kTile && all_in;
         for (int h = 0; h < 2; ++h) {
@@ -959,6 +970,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               qc = query_code(p.mask, it.s0 + min(qrow, a0 + an - 1));
             }
           }
+          // lane c holds column cq + c's side values; the math below takes
+          // each column's from its lane by shuffle (loads that hit L1 wait
+          // behind the tensor cores' shared-memory reads, shuffles do not)
+          const float sl_l = __ldg(sl + cq + lane), sl_g = __ldg(sl + kTile + cq + lane),
+                      sl_m = __ldg(sl + 2 * kTile + cq + lane);
           if (!warp_wait(bar(C::B_SFULL + h), uint32_t(nent) & 1u, abort_flag, err, 8)) {
             ok = false;
             break;
@@ -1005,34 +1021,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // chunk (the dQ^T that last read these chunks, the previous entry's
           // of this half, was issued before this unit's scores, whose
           // completion this warp waited for)
-          // side values four columns per (broadcast) load
-          const float4* l4 = reinterpret_cast<const float4*>(sl + cq);
-          const float4* g4 = reinterpret_cast<const float4*>(sl + kTile + cq);
-          const float4* m4 = reinterpret_cast<const float4*>(sl + 2 * kTile + cq);
           uint32_t pp[16], pd[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint32_t ps[4];
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
-              const float4 lq = __ldg(l4 + 2 * u + hq), gq = __ldg(g4 + 2 * u + hq), mq = __ldg(m4 + 2 * u + hq);
 #pragma unroll
               for (int e2 = 0; e2 < 2; ++e2) {
                 const int c = 8 * u + 4 * hq + 2 * e2;  // column pair (c, c + 1)
-                const float2 l = e2 ? make_float2(lq.z, lq.w) : make_float2(lq.x, lq.y);
-                const float2 g = e2 ? make_float2(gq.z, gq.w) : make_float2(gq.x, gq.y);
-                const float2 mf = e2 ? make_float2(mq.z, mq.w) : make_float2(mq.x, mq.y);
-                const float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                            make_float2(c2, c2), make_float2(-l.x, -l.y));
+                const float2 l = make_float2(__shfl_sync(0xffffffffu, sl_l, c), __shfl_sync(0xffffffffu, sl_l, c + 1));
+                const float2 g = make_float2(__shfl_sync(0xffffffffu, sl_g, c), __shfl_sync(0xffffffffu, sl_g, c + 1));
+                const float2 mf = make_float2(__shfl_sync(0xffffffffu, sl_m, c), __shfl_sync(0xffffffffu, sl_m, c + 1));
+                float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                      make_float2(c2, c2), make_float2(-l.x, -l.y));
                 // branch-free (vis is all ones on unmasked tiles), so that the
-                // compiler interleaves the independent column pairs; a hidden
-                // pair's P and dS are selected to exactly zero
-                const bool v0 = (vis >> c) & 1u, v1 = (vis >> (c + 1)) & 1u;
-                float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-                float2 dd = ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                                      make_float2(-g.x, -g.y)));
-                pv = make_float2(v0 ? pv.x : 0.f, v1 ? pv.y : 0.f);
-                dd = make_float2(v0 ? dd.x : 0.f, v1 ? dd.y : 0.f);
+                // compiler interleaves the independent column pairs: a hidden
+                // pair's exponent is -inf, so its P is exactly zero, and so is
+                // its dS = P (dP - D) (dP and D are finite)
+                x = make_float2((vis >> c) & 1u ? x.x : -INFINITY, (vis >> (c + 1)) & 1u ? x.y : -INFINITY);
+                const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                const float2 dd =
+                    ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                              make_float2(-g.x, -g.y)));
                 pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
                 pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
                 const float2 dm = ptx::fmul2(dd, mf);

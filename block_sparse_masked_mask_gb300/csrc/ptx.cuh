@@ -69,6 +69,11 @@ __device__ __forceinline__ void red_add_s32_if(int32_t* p, int32_t v, bool on) {
       : "memory");
 }
 
+// Bring a line of global memory into L1 ahead of its loads.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
