@@ -40,9 +40,9 @@
 // add.  The maxima over V and K use only the sequence's own tokens, so the
 // result does not depend on what else is packed with it.
 //
-// Items are taken head-major (all k-tiles of head 0 longest list first, then
-// head 1, ...), so at any time the CTAs add into the accumulator rows of one
-// or two heads (17 MB per head on the 32k workload), which stay in L2.
+// Items are taken by groups of eight heads, longest list first inside a
+// group, so at any time the CTAs add into the accumulator rows of a few heads
+// (17 MB per head on the 32k workload).
 //
 // Each entry (q-tile) runs as two units of 64 queries, one per TMEM buffer,
 // so that the tensor pipe works on one unit while the row warps work on the
@@ -335,11 +335,19 @@ struct BwdItem {
   int h, s0, L, i0, e0, e1, b, gbase;  // i0: first key of the tile (local); gbase: tile 0 of the sequence
 };
 
-// Items are head-major: every k-tile of head 0 (longest list first), then head 1, ...
+// Items go by groups of kHeadGroup heads: inside a group, k-tiles longest list
+// first, each k-tile for every head of the group in turn.  A group keeps the
+// accumulator rows and Q / dO tiles that the CTAs touch at once to a few
+// heads (L2 locality), and the longest lists of the last group still start
+// well before the end (a purely head-major order would start the last
+// head's longest lists last and leave a tail of one list's duration).
+constexpr int kHeadGroup = 8;
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
   BwdItem it;
-  it.h = item / n_t;
-  const int g = p.korder[item % n_t];
+  const int grp = item / (n_t * kHeadGroup), r = item - grp * (n_t * kHeadGroup);
+  const int hg = min(kHeadGroup, p.H - grp * kHeadGroup);  // heads in this group
+  it.h = grp * kHeadGroup + r % hg;
+  const int g = p.korder[r / hg];
   const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
   it.L = p.cu[b + 1] - it.s0;

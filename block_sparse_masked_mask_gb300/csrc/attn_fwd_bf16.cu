@@ -115,10 +115,18 @@ struct Item {
   int h, s0, L, qi0, e0, e1, b;
 };
 
+// Items go by groups of kHeadGroup heads: inside a group, q-tiles longest
+// list first, each q-tile for every head of the group in turn.  The group
+// keeps the K / V tiles the CTAs read at once to a few heads (L2 locality),
+// and the longest lists of the last group still start well before the end (a
+// purely head-major order starts the last head's longest lists last).
+constexpr int kHeadGroup = 8;
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, int n_qt) {
   Item it;
-  it.h = item / n_qt;
-  const int g = p.order[item % n_qt];
+  const int grp = item / (n_qt * kHeadGroup), r = item - grp * (n_qt * kHeadGroup);
+  const int hg = min(kHeadGroup, p.H - grp * kHeadGroup);  // heads in this group
+  it.h = grp * kHeadGroup + r % hg;
+  const int g = p.order[r / hg];
   const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
   it.L = p.cu[b + 1] - it.s0;
@@ -174,8 +182,8 @@ __device__ __forceinline__ int publish_item(const FwdParams& p, int k, int lane,
 }
 
 // Persistent: each CTA takes work items from a global ticket counter (items
-// are head-major, longest q-tile first inside a head, so tickets hand out the
-// longest work first).  The K producer takes the tickets, decodes them one item
+// go by groups of heads, longest q-tile first inside a group, so tickets hand
+// out the longest work first).  The K producer takes the tickets, decodes them one item
 // ahead and passes them to the other roles through a two-slot ring in shared
 // memory.  Barrier phases run on across items: the next item's Q load and
 // first S MMAs overlap the current item's last P.V and O epilogue.  The
