@@ -5,6 +5,7 @@ library.  There is no fallback: if the library is missing this module raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -63,17 +64,7 @@ class AttnBlockMask(ctypes.Structure):
 _lib = None
 
 
-def lib() -> ctypes.CDLL:
-    """The loaded library; raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(
-            f"{LIB_PATH} is missing: build it first with "
-            "`python -c 'import __graft_entry__ as g; g.build()'` "
-            "(or block_sparse_masked_mask_gb300.build.build()).")
-    L = ctypes.CDLL(LIB_PATH)
+def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     P = ctypes.POINTER
     L.attn_block_mask_workspace_size.argtypes = [c_int32, c_int32, c_int32, c_int32, c_int32,
                                                  P(ctypes.c_size_t)]
@@ -106,5 +97,31 @@ def lib() -> ctypes.CDLL:
     L.attn_last_error_message.restype = ctypes.c_char_p
     L.attn_version.argtypes = []
     L.attn_version.restype = c_int32
-    _lib = L
     return L
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it first with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or block_sparse_masked_mask_gb300.build.build()).")
+    _lib = _configure(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Run the binding's calls through another build of the library (a copy
+    compiled with other settings) inside the ``with`` block."""
+    global _lib
+    saved = lib()
+    _lib = _configure(ctypes.CDLL(path))
+    try:
+        yield _lib
+    finally:
+        _lib = saved

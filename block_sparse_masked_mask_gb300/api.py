@@ -14,6 +14,8 @@ import torch
 from . import _native
 
 ATTN_OK = 0
+(ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_MASK_MISMATCH,
+ ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_DEVICE_INVALID_INPUT) = range(1, 8)
 STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
     3: "ATTN_ERR_WORKSPACE_TOO_SMALL", 4: "ATTN_ERR_MASK_MISMATCH", 5: "ATTN_ERR_CUDA",

@@ -51,15 +51,12 @@ def _stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Build the library if missing or out of date; return its path."""
-    if not force and not _stale():
-        return LIB_PATH
+def _compile_and_link(out_path: str, obj_dir: str, extra_flags=(), verbose: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -70,14 +67,32 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = out_path + ".tmp"
     cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs,
            "-lcudart"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Build the library if missing or out of date; return its path."""
+    if not force and not _stale():
+        return LIB_PATH
+    return _compile_and_link(LIB_PATH, BUILD, extra_flags, verbose)
+
+
+def build_variant(tag: str, defines: dict) -> str:
+    """Build a copy of the library with extra preprocessor definitions (for
+    tests of compile-time settings, e.g. a short pipeline-wait bound) as
+    ``lib<name>_<tag>.so`` next to the regular one; return its path."""
+    out = os.path.join(PKG, f"{os.path.splitext(LIB_NAME)[0]}_{tag}.so")
+    if os.path.exists(out) and all(os.path.getmtime(p) <= os.path.getmtime(out) for p in _inputs()):
+        return out
+    flags = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    return _compile_and_link(out, os.path.join(BUILD, tag), flags)
 
 
 def ensure_built() -> str:
