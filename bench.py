@@ -174,7 +174,7 @@ def count_pairs(w, c):
 
 # kernels the library launches: a block-mask build (five kernels) and the backward
 BUILD_LAUNCHES = 5
-BWD_KERNELS = ["bwd_zero_kernel", "bwd_prep_kernel", "attn_bwd_kernel", "bwd_dq_convert_kernel"]
+BWD_KERNELS = ["bwd_zero_kernel", "bwd_prep_kernel", "bwd_mult_kernel", "attn_bwd_kernel", "bwd_dq_convert_kernel"]
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_fwd_bf16_causal_document_32k_h8_full.md")
