@@ -70,14 +70,15 @@
 namespace attnmask {
 namespace {
 
-constexpr int kBwdThreads = 640;
-constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpTail = 10, kWarpRed = 12;  // reducers: warps 12-19
-// registers a thread per warpgroup: rows (two warpgroups), producer + MMA,
-// reducers (two warpgroups); the launch gives 96 a thread (640 x 96 <= 65536),
-// 2 x 128 x kRegsRow + 128 x kRegsLoad + 2 x 128 x kRegsRed <= 640 x 96
-constexpr int kRegsLaunch = 96;
-constexpr int kRegsRow = 136, kRegsLoad = 80, kRegsRed = 64;
-static_assert(2 * kRegsRow + kRegsLoad + 2 * kRegsRed <= 5 * kRegsLaunch, "register budget of the launch");
+constexpr int kBwdThreads = 896;
+constexpr int kRowWarps = 16;
+constexpr int kWarpLoad = 16, kWarpMma = 17, kWarpTail = 18, kWarpRed = 20;  // reducers: warps 20-27
+// registers a thread per warpgroup: rows (four warpgroups), producer + MMA,
+// reducers (two warpgroups); the launch gives 72 a thread (896 x 72 <= 65536),
+// 4 x 128 x kRegsRow + 128 x kRegsLoad + 2 x 128 x kRegsRed <= 896 x 72
+constexpr int kRegsLaunch = 72;
+constexpr int kRegsRow = 80, kRegsLoad = 64, kRegsRed = 56;
+static_assert(4 * kRegsRow + kRegsLoad + 2 * kRegsRed <= 7 * kRegsLaunch, "register budget of the launch");
 static_assert(kRegsRow > kRegsLaunch && kRegsLoad < kRegsLaunch && kRegsRed < kRegsLaunch,
               "the row warps grow, the others shrink");
 constexpr int kItemInts = 12;
@@ -518,18 +519,17 @@ __device__ __forceinline__ bool load_pair(const CUtensorMap* ma, const CUtensorM
 // Half h of a product over the 128 rows of a streamed tile (dV += P^T dO or
 // dK += dS^T Q over rows 64h .. 64h+63, four k-steps of 16; b_desc already
 // points at row 64h).  The A operand (P^T or dS^T, bf16) sits over buffer h's
-// S^T columns: the row warps write each 32-query group g over its own 32
-// score columns, P^T in the first 16, dS^T in the next 16 (a_tmem is the
-// buffer's first column for P^T, that + 16 for dS^T), so k-step k4 is at
-// column 32 (k4 / 2) + 8 (k4 % 2).
+// S^T columns: the row warps write each 16-query group g over its own 16
+// score columns, P^T in the first 8, dS^T in the next 8 (a_tmem is the
+// buffer's first column for P^T, that + 8 for dS^T), so k-step k4 is at
+// column 16 k4.
 template <int D>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool acc) {
   using C = BwdCfg<D>;
   ptx::mma_ts(d_tmem, a_tmem, b_desc, C::IDESC_PV, acc ? 1u : 0u);
 #pragma unroll
   for (int k4 = 1; k4 < 4; ++k4)
-    ptx::mma_ts_c<true>(d_tmem, a_tmem + uint32_t(k4 >> 1) * 32u + uint32_t(k4 & 1) * 8u, b_desc + v_step<D>(k4),
-                        C::IDESC_PV);
+    ptx::mma_ts_c<true>(d_tmem, a_tmem + uint32_t(k4) * 16u, b_desc + v_step<D>(k4), C::IDESC_PV);
 }
 
 // Scores-like product D = A B^T over K = D, N = 64 (both operands K-major).
@@ -570,7 +570,7 @@ __device__ __forceinline__ bool bwd_tail(uint32_t tmem, uint32_t bars, int h, in
   const uint32_t ts = tmem + C::col_s(h);
   const uint64_t hrow = uint64_t(h) * (C::HALF_ROWS >> 4);  // rows 64h .. of a slot
   issue_pv_half<D>(tmem + C::COL_DV, ts, rv0 + uint64_t(ds) * (C::TILE >> 4) + hrow, !first);
-  issue_pv_half<D>(tmem + C::COL_DK, ts + 16u, rv0 + uint64_t(qs) * (C::TILE >> 4) + hrow, !first);
+  issue_pv_half<D>(tmem + C::COL_DK, ts + 8u, rv0 + uint64_t(qs) * (C::TILE >> 4) + hrow, !first);
   ptx::mma_commit(bar(C::B_AFREE + h));
   if (h == 1) {  // the entry's last products that read Q and dO
     ptx::mma_commit(bar(C::B_EMPTY + qs));
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_QTAIL), 1);
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(bar(C::B_SFULL + h), 1);
-      ptx::mbar_init(bar(C::B_PFULL + h), 256);
+      ptx::mbar_init(bar(C::B_PFULL + h), 32 * kRowWarps);
       ptx::mbar_init(bar(C::B_AFREE + h), 1);
       ptx::mbar_init(bar(C::B_DQFULL + h), 1);
       ptx::mbar_init(bar(C::B_DQFREE + h), 256);
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_OFREE), 256);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 256 + 2 + 256);  // row threads, two MMA threads, reducers
+      ptx::mbar_init(bar(C::B_IEMPTY + i), 32 * kRowWarps + 2 + 256);  // row threads, two MMA threads, reducers
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::mbar_init(bar(C::B_DRAIN2), 1);
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const bool skip = *abort_flag != 0u;
 
   if (skip) {
-  } else if (warp >= 8) {
+  } else if (warp >= kRowWarps) {
     if (warp < kWarpRed) ptx::regs_dec<kRegsLoad>();
     else ptx::regs_dec<kRegsRed>();
     if (warp == kWarpLoad) {
@@ -911,14 +911,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::regs_inc<kRegsRow>();
     // ---------------------------------------------------------- P^T, dS^T (key rows)
     // Warp w owns TMEM lanes (keys) 32 (w % 4) .. +31 and, in every unit, the
-    // unit's query columns 32 (w / 4) .. +31.
-    const int qd = warp & 3, cg = warp >> 2;  // lane quarter, column group
+    // unit's query columns 16 (w / 4) .. +15; the first eight warps also write
+    // the item's dV (w / 4 = 0) or dK (w / 4 = 1) rows.
+    const int qd = warp & 3, cg = warp >> 2;  // lane quarter, 16-column group
     const int r = qd * 32 + lane;
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
     const float c2 = p.scale_log2;
     uint8_t* dsbuf = sbase + C::OFF_DS;
-    int nent = 0, nodone = 0, nload = 0;
+    const bool epi = cg < 2;
+    int nent = 0, nodone = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
@@ -927,8 +929,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
       if (!valid) break;
       // the dS buffer doubles as the output stage of the item's epilogue: no
-      // warp writes this item's dS before every warp has stored the previous
-      // item's rows
+      // warp writes this item's dS before every epilogue warp has stored the
+      // previous item's rows
       if (k > 0 && !warp_wait(bar(C::B_STAGE), uint32_t(k - 1) & 1u, abort_flag, err, 6)) break;
       const int kn = min(kTile, it.L - it.i0);
       const bool row_in = r < kn;
@@ -943,9 +945,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int n = it.e1 - it.e0;
       int nx_idx = n > 0 ? __ldg(p.qidx + it.e0) : 0, nx_lab = n > 0 ? __ldg(p.qlabel + it.e0) : 0;
       // the side values of a q-tile (1.5 KB, twelve lines) go into L1 one entry
-      // ahead of their loads, which then do not wait for L2
+      // ahead of their loads
       const float* side_h = p.side + (size_t(it.h) * p.G + it.gbase) * kBwdSideFloats;
-      if (warp == 0 && lane < kBwdSideFloats / 32 && n > 0) ptx::prefetch_l1(side_h + size_t(nx_idx) * kBwdSideFloats + 32 * lane);
+      if (warp == 0 && lane < kBwdSideFloats / 32 && n > 0)
+        ptx::prefetch_l1(side_h + size_t(nx_idx) * kBwdSideFloats + 32 * lane);
       for (int jj = 0; jj < n && ok; ++jj) {
         const int e = it.e0 + jj;
         const int ti = nx_idx;  // the entry's q-tile within the sequence
@@ -957,7 +960,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (warp == 0 && lane < kBwdSideFloats / 32)
             ptx::prefetch_l1(side_h + size_t(nx_idx) * kBwdSideFloats + 32 * lane);
         }
-        nload += 2;
         // the q-tile's side values (LSE * log2 e, D, m_i), from global memory:
         // the tensor cores have priority on shared memory, global loads do not
         // wait for them
@@ -965,38 +967,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // every pair of the warp's rows and columns visible: no masking at all
         const bool fast = lab == ATTN_TILE_FULL && an == kTile && all_in;
         for (int h = 0; h < 2; ++h) {
-          const int cq = 64 * h + 32 * cg;  // the warp's first query column of the entry
-          // before the wait: the dense kind's word of query row a0 + cq + lane
+          const int cq = 64 * h + 16 * cg;  // the warp's first query column of the entry
+          const int cl = lane & 15;         // lanes 16-31 repeat lanes 0-15
+          // before the wait: the dense kind's word of query row a0 + cq + cl
           // over the warp's 32 keys, or (code kinds) that query's code
           uint32_t dw = 0u;
           int qc = 0;
           if (lab == ATTN_TILE_PARTIAL && kbase < it.L) {
-            const int qrow = a0 + cq + lane;
+            const int qrow = a0 + cq + cl;
             if (kind == ATTN_MASK_DENSE) {
-              if (qrow < it.L) dw = dense_word(p.mask, it.b, it.L, qrow, kbase >> 5);
+              if (qrow < it.L && lane < 16) dw = dense_word(p.mask, it.b, it.L, qrow, kbase >> 5);
             } else if (kind_codes(kind)) {
               qc = query_code(p.mask, it.s0 + min(qrow, a0 + an - 1));
             }
           }
           // lane c holds column cq + c's side values; the math below takes
-          // each column's from its lane by shuffle (loads that hit L1 wait
-          // behind the tensor cores' shared-memory reads, shuffles do not)
-          const float sl_l = __ldg(sl + cq + lane), sl_g = __ldg(sl + kTile + cq + lane),
-                      sl_m = __ldg(sl + 2 * kTile + cq + lane);
+          // each column's from its lane by shuffle
+          const float sl_l = __ldg(sl + cq + cl), sl_g = __ldg(sl + kTile + cq + cl),
+                      sl_m = __ldg(sl + 2 * kTile + cq + cl);
           if (!warp_wait(bar(C::B_SFULL + h), uint32_t(nent) & 1u, abort_flag, err, 8)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          // bit c of vis: query column cq + c sees this key.  Causal part and
-          // bounds: a0 + column >= kl and column < an.
-          uint32_t vis = 0xffffffffu;
+          // bit c of vis: query column cq + c sees this key (bits 0-15).
+          // Causal part and bounds: a0 + column >= kl and column < an.
+          uint32_t vis = 0xffffu;
           if (!fast) {
-            vis = lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? ~prefix_bits(kl - a0 - cq) & prefix_bits(an - cq)
-                                                                : prefix_bits(an - cq);
+            vis = (lab == ATTN_TILE_PARTIAL && kind_causal(kind) ? ~prefix_bits(kl - a0 - cq) & prefix_bits(an - cq)
+                                                                 : prefix_bits(an - cq)) &
+                  0xffffu;
             if (lab == ATTN_TILE_PARTIAL && kind == ATTN_MASK_DENSE) {
-              // transpose the 32 x 32 bit block: ballot j gathers bit j (key
-              // lane j) of every lane's (query's) word, and lane j keeps it
+              // transpose the 32-key x 16-query bit block: ballot j gathers bit
+              // j (key lane j) of every lane's (query's) word, and lane j keeps it
               uint32_t mine = 0u;
 #pragma unroll 4
               for (int j = 0; j < 32; ++j) {
@@ -1009,7 +1012,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 vis &= __ballot_sync(0xffffffffu, code_visible(kind, qc, kcode_w));
               } else {
                 uint32_t w = 0;
-                for (int c = 0; c < 32; ++c)
+                for (int c = 0; c < 16; ++c)
                   w |= uint32_t(code_visible(kind, __shfl_sync(0xffffffffu, qc, c), kcode)) << c;
                 vis &= w;
               }
@@ -1017,51 +1020,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // a key past the sequence end: its P and dS are exactly zero
             if (!row_in) vis = 0u;
           }
-          // the warp's 32 columns of S^T and dP^T in, then P^T over the first
-          // 16 and dS^T over the next 16 of its score columns
-          uint32_t sv[32], dv[32];
-          ptx::tmem_ld32(lane_base + C::col_s(h) + 32 * cg, sv);
-          ptx::tmem_ld32(lane_base + C::col_p(h) + 32 * cg, dv);
+          // the warp's 16 columns of S^T and dP^T in, then P^T over the first
+          // 8 and dS^T over the next 8 of its score columns
+          uint32_t sv[16], dv[16];
+          ptx::tmem_ld16(lane_base + C::col_s(h) + 16 * cg, sv);
+          ptx::tmem_ld16(lane_base + C::col_p(h) + 16 * cg, dv);
           ptx::tmem_wait_ld();
           // P^T and dS^T for TMEM; the copy of dS for the dQ^T product goes to
           // shared memory scaled by each query's fixed-point multiplier m_i:
-          // this key's 32 queries as four 16-byte pieces, one per eight-query
+          // this key's 16 queries as two 16-byte pieces, one per eight-query
           // chunk (the dQ^T that last read these chunks, the previous entry's
           // of this half, was issued before this unit's scores, whose
           // completion this warp waited for)
-          uint32_t pp[16], pd[16];
+          uint32_t pp[8], pd[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 2; ++u) {
             uint32_t ps[4];
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-#pragma unroll
-              for (int e2 = 0; e2 < 2; ++e2) {
-                const int c = 8 * u + 4 * hq + 2 * e2;  // column pair (c, c + 1)
-                const float2 l = make_float2(__shfl_sync(0xffffffffu, sl_l, c), __shfl_sync(0xffffffffu, sl_l, c + 1));
-                const float2 g = make_float2(__shfl_sync(0xffffffffu, sl_g, c), __shfl_sync(0xffffffffu, sl_g, c + 1));
-                const float2 mf = make_float2(__shfl_sync(0xffffffffu, sl_m, c), __shfl_sync(0xffffffffu, sl_m, c + 1));
-                float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                      make_float2(c2, c2), make_float2(-l.x, -l.y));
-                // branch-free (vis is all ones on unmasked tiles), so that the
-                // compiler interleaves the independent column pairs: a hidden
-                // pair's exponent is -inf, so its P is exactly zero, and so is
-                // its dS = P (dP - D) (dP and D are finite)
-                x = make_float2((vis >> c) & 1u ? x.x : -INFINITY, (vis >> (c + 1)) & 1u ? x.y : -INFINITY);
-                const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-                const float2 dd =
-                    ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
-                                              make_float2(-g.x, -g.y)));
-                pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
-                pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
-                const float2 dm = ptx::fmul2(dd, mf);
-                ps[(c >> 1) & 3] = ptx::pack_bf16(dm.x, dm.y);
-              }
+            for (int c = 8 * u; c < 8 * u + 8; c += 2) {  // column pair (c, c + 1)
+              const float2 l = make_float2(__shfl_sync(0xffffffffu, sl_l, c), __shfl_sync(0xffffffffu, sl_l, c + 1));
+              const float2 g = make_float2(__shfl_sync(0xffffffffu, sl_g, c), __shfl_sync(0xffffffffu, sl_g, c + 1));
+              const float2 mf = make_float2(__shfl_sync(0xffffffffu, sl_m, c), __shfl_sync(0xffffffffu, sl_m, c + 1));
+              float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                    make_float2(c2, c2), make_float2(-l.x, -l.y));
+              // branch-free (vis is all ones on unmasked tiles), so that the
+              // compiler interleaves the independent column pairs: a hidden
+              // pair's exponent is -inf, so its P is exactly zero, and so is
+              // its dS = P (dP - D) (dP and D are finite)
+              x = make_float2((vis >> c) & 1u ? x.x : -INFINITY, (vis >> (c + 1)) & 1u ? x.y : -INFINITY);
+              const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+              const float2 dd =
+                  ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                            make_float2(-g.x, -g.y)));
+              pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
+              pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
+              const float2 dm = ptx::fmul2(dd, mf);
+              ps[(c >> 1) & 3] = ptx::pack_bf16(dm.x, dm.y);
             }
             *reinterpret_cast<uint4*>(dsbuf + ((cq >> 3) + u) * kDsChunk + r * 16) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
           }
-          ptx::tmem_st16(lane_base + C::col_s(h) + 32 * cg, pp);
-          ptx::tmem_st16(lane_base + C::col_s(h) + 32 * cg + 16, pd);
+          ptx::tmem_st8(lane_base + C::col_s(h) + 16 * cg, pp);
+          ptx::tmem_st8(lane_base + C::col_s(h) + 16 * cg + 8, pd);
           ptx::tmem_wait_st();
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
@@ -1070,20 +1069,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ++nent;
       }
       if (!ok) break;
+      if (!epi) continue;
       // ---------------------------------------------------------- epilogue
       if (n > 0) {
         if (!warp_wait(bar(C::B_ODONE), uint32_t(nodone) & 1u, abort_flag, err, 11)) break;
         ++nodone;
       }
       ptx::tc_fence_after();
-      // the first four warps store dV, the other four dK (times the scale)
-      uint32_t w[D / 2];
-      tmem_row_bf16<D>(lane_base + (cg ? C::COL_DK : C::COL_DV), cg ? p.scale : 1.f, n > 0, w);
+      // warps 0-3 store dV, warps 4-7 dK (times the scale), 64 columns at a
+      // time (the row warps' register budget holds half a row)
+      constexpr int PART = D < 64 ? D : 64;
+      const size_t row0 = (size_t(it.s0 + it.i0 + qd * 32) * p.H + it.h) * D;
+#pragma unroll 1
+      for (int pc = 0; pc < D; pc += PART) {
+        uint32_t w[PART / 2];
+        tmem_row_bf16<PART>(lane_base + (cg ? C::COL_DK : C::COL_DV) + pc, cg ? p.scale : 1.f, n > 0, w);
+        store_rows<PART, C::STAGE_WARP>(dsbuf + warp * C::STAGE_WARP, lane, w, (cg ? p.dk : p.dv) + row0 + pc,
+                                        size_t(p.H) * D, kn - qd * 32);
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(C::B_OFREE));
-      const size_t row0 = (size_t(it.s0 + it.i0 + qd * 32) * p.H + it.h) * D;
-      store_rows<D, C::STAGE_WARP>(dsbuf + warp * C::STAGE_WARP, lane, w, (cg ? p.dk : p.dv) + row0,
-                                   size_t(p.H) * D, kn - qd * 32);
       ptx::mbar_arrive(bar(C::B_STAGE));
     }
   }

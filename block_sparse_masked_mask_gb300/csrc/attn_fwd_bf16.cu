@@ -61,14 +61,19 @@ struct Cfg : TileLayout<D> {
   using TileLayout<D>::CE;
   using TileLayout<D>::NCH;
   using TileLayout<D>::ROWB;
-  static constexpr int NK = 3;                        // K ring slots
+  // Q slots and K ring slots: a second Q slot (the next item's Q loaded under
+  // this item's last k-tiles) in place of the third K slot measured slower
+  // on every workload (0.950 vs 0.934 ms on the 32k mask, 0.108 vs 0.104 ms
+  // on the 8-sequence varlen batch)
+  static constexpr int NQ = 1;
+  static constexpr int NK = 3;
   static constexpr int NV = 2;                        // V ring slots
   static constexpr int NCODE = 6;                     // key-code buffers (entries in flight)
-  static constexpr int OFF_Q = 0, OFF_K = TILE, OFF_V = OFF_K + NK * TILE;
+  static constexpr int OFF_Q = 0, OFF_K = NQ * TILE, OFF_V = OFF_K + NK * TILE;
   static constexpr int NS = 2;                        // S buffers in TMEM
   // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; ODONE, OFREE,
   // STATS: per O buffer (item parity)
-  static constexpr int B_Q = 0, B_QFREE = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
+  static constexpr int B_Q = 0, B_QFREE = NQ, B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
                        B_VEMPTY = B_VFULL + NV, B_VTMA = B_VEMPTY + NV, B_SFULL = B_VTMA + 1,
                        B_PFULL = B_SFULL + NS, B_PDONE = B_PFULL + NS, B_ODONE = B_PDONE + NS,
                        B_OFREE = B_ODONE + 2, B_IFULL = B_OFREE + 2, B_IEMPTY = B_IFULL + 2,
@@ -216,8 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* key_codes = reinterpret_cast<int*>(sbase + C::OFF_CODES);
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(C::B_Q), 1);
-    ptx::mbar_init(bar(C::B_QFREE), 1);
+    for (int q = 0; q < C::NQ; ++q) {
+      ptx::mbar_init(bar(C::B_Q + q), 1);
+      ptx::mbar_init(bar(C::B_QFREE + q), 1);
+    }
     for (int s = 0; s < C::NK; ++s) {
       ptx::mbar_init(bar(C::B_KFULL + s), 1);
       ptx::mbar_init(bar(C::B_KEMPTY + s), 1);
@@ -281,12 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       st_next = publish_item(p, k + 1, lane, n_items, n_qt, it_next, item_ring, bar(C::B_IEMPTY),
                              bar(C::B_IFULL), abort_flag, err);
       if (st_next < 0) break;
-      // Q of this item, once the previous item's S MMAs no longer read Q.
-      if (nq > 0 && !warp_wait(bar(C::B_QFREE), uint32_t(nq - 1) & 1u, abort_flag, err, 13)) break;
+      // Q of this item into slot nq % NQ, once the S MMAs of the item that
+      // last used the slot no longer read it.
+      const int qsl = nq % C::NQ;
+      if (nq >= C::NQ &&
+          !warp_wait(bar(C::B_QFREE + qsl), uint32_t(nq / C::NQ - 1) & 1u, abort_flag, err, 13))
+        break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(C::B_Q), C::TILE);
+        ptx::mbar_arrive_expect_tx(bar(C::B_Q + qsl), C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          ptx::tma_load_3d(sQ + c * C::CHUNK, &tmQ, bar(C::B_Q), c * C::CE, it.h, it.s0 + it.qi0);
+          ptx::tma_load_3d(sQ + uint32_t(qsl) * C::TILE + c * C::CHUNK, &tmQ, bar(C::B_Q + qsl), c * C::CE,
+                           it.h, it.s0 + it.qi0);
       }
       ++nq;
       for (int e = it.e0; e < it.e1; ++e) {
@@ -330,7 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int last = s + C::NK * ((nk - 1 - s) / C::NK);  // last load into slot s
         drain_bar(bar(C::B_KFULL + s), uint32_t(last / C::NK) & 1u, err);
       }
-      if (nq > 0) drain_bar(bar(C::B_Q), uint32_t(nq - 1) & 1u, err);
+      for (int q = 0; q < C::NQ; ++q) {
+        if (nq <= q) continue;
+        const int last = q + C::NQ * ((nq - 1 - q) / C::NQ);  // last load into slot q
+        drain_bar(bar(C::B_Q + q), uint32_t(last / C::NQ) & 1u, err);
+      }
     }
     __syncwarp();
   } else if (warp == kWarpVLoad) {
@@ -407,14 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int nkc = 0, ns = 0;  // K loads consumed, S issued (all items)
       bool ok = true;
-      const uint64_t qdesc = kmajor_base<D>(sQ), kdesc0 = kmajor_base<D>(sK);
+      const uint64_t qdesc0 = kmajor_base<D>(sQ), kdesc0 = kmajor_base<D>(sK);
       for (int k = 0; ok; ++k) {
         if (!wait_bar(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
         Item it;
         const bool valid = load_item(item_ring + 8 * (k & 1), it);
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
-        if (!wait_bar(bar(C::B_Q), uint32_t(k) & 1u, abort_flag, err, 3)) break;
+        const int qsl = k % C::NQ;
+        if (!wait_bar(bar(C::B_Q + qsl), uint32_t(k / C::NQ) & 1u, abort_flag, err, 3)) break;
+        const uint64_t qdesc = qdesc0 + uint64_t(qsl) * (C::TILE >> 4);
         for (int e = it.e0; e < it.e1; ++e) {
           const int sb = ns % C::NS, ks = nkc % C::NK;
           if (ns >= C::NS && !wait_bar(bar(C::B_PDONE + sb), uint32_t(ns / C::NS - 1) & 1u, abort_flag, err, 7)) {
@@ -429,8 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ns;
           ++nkc;
         }
-        // every S of this item has been issued: Q may be replaced once they finish
-        ptx::mma_commit(bar(C::B_QFREE));
+        // every S of this item has been issued: its Q slot may be refilled once
+        // they finish
+        ptx::mma_commit(bar(C::B_QFREE + qsl));
       }
       // Every MMA this thread issued has finished once this commit arrives.
       ptx::mma_commit(bar(C::B_DRAIN));
