@@ -896,11 +896,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int q0 = 64 * h + 32 * ch;  // first query row of this warp's columns
             if (active && q0 < qn) {
               int32_t* row = p.dqacc + (size_t(it.s0 + a0 + q0) * p.H + it.h) * D + 32 * rq + lane;
-              // rows past the sequence end hold zeros and are skipped by the
-              // instruction's predicate
+              if (q0 + 32 <= qn) {
 #pragma unroll
-              for (int q = 0; q < 32; ++q, row += rstride)
-                ptx::red_add_s32_if(row, __float2int_rn(__uint_as_float(v[q])), q0 + q < qn);
+                for (int q = 0; q < 32; ++q, row += rstride)
+                  ptx::red_add_s32(row, __float2int_rn(__uint_as_float(v[q])));
+              } else {
+                // rows past the sequence end hold zeros and are skipped by the
+                // instruction's predicate
+#pragma unroll
+                for (int q = 0; q < 32; ++q, row += rstride)
+                  ptx::red_add_s32_if(row, __float2int_rn(__uint_as_float(v[q])), q0 + q < qn);
+              }
             }
           }
           ++nent;

@@ -58,7 +58,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---------------------------------------------------------------- global memory
 // Fire-and-forget integer add at the memory (exact, so sums do not depend on
-// order), issued only when `on` is set.  The predicate lives in the
+// order).
+__device__ __forceinline__ void red_add_s32(int32_t* p, int32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The same, issued only when `on` is set.  The predicate lives in the
 // instruction rather than in a branch around it, so that the values of a
 // loop of these can be computed ahead of the adds.
 __device__ __forceinline__ void red_add_s32_if(int32_t* p, int32_t v, bool on) {
