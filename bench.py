@@ -425,11 +425,20 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     fwd_avg_s = sum(fwd_ms) / len(fwd_ms) / 1e3
     achieved = flops_fwd / fwd_avg_s / 1e12
-    peak = float(peaks["bf16_tflops"])
+    # The forward is timed inside a long step (back-to-back launches over a
+    # second or more, under the power cap): the sustained tensor peak is its
+    # denominator; a short run (well under a second) is compared with the burst
+    # peak.  Both fractions are reported.
+    burst = float(peaks["bf16_tflops"])
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    long_step = total_ms >= 1000.0
+    peak = sustained if long_step else burst
     roofline = {"bound": "tensor", "kernel": "attn_fwd_bf16_kernel<128, false>", "achieved": achieved,
                 "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "peak_source": f"{peak_kind} bf16_tflops" + ("_sustained (timed region "
+                               f"{total_ms / 1e3:.2f} s)" if long_step else " (burst)"),
+                "frac_of_burst": achieved / burst,
+                "frac_of_sustained": achieved / sustained,
                 "traffic": None}
     traffic, traffic_src = profiled_traffic(args.workload, w.num_heads)
     if traffic is not None:
