@@ -49,14 +49,15 @@
 // other.  Two threads issue the products: one the scores of each unit, the
 // other (once the row warps are done with a unit) its dV, dK and dQ^T, so
 // that the tensor pipe has work from one while the other waits for a buffer.
-// Warp roles of the main kernel (512 threads): warps 0-7 the row warps (warp
+// Warp roles of the main kernel (896 threads): warps 0-15 the row warps (warp
 // w owns TMEM lanes, i.e. keys, 32 (w % 4) .. +31 and, in each unit, query
-// columns 32 (w / 4) .. +31), warp 8 the TMA producer, warps 9 and 10 the
-// tcgen05 issuers (scores; dV, dK and dQ^T), warps 12-19 the dQ reducers (warp
-// 12 + r + 4 c owns TMEM lanes, i.e. head dims, 32 r .. +31 and query columns
-// 32 c .. +31 of each unit), warp 11 idle.  The row warpgroups run with kRegsRow
-// registers a thread, the other two with kRegsLoad and kRegsRed (setmaxnreg,
-// within the 128 x 512 of the launch).
+// columns 16 (w / 4) .. +15; warps 0-7 also write dV and dK), warp 16 the TMA
+// producer, warps 17 and 18 the tcgen05 issuers (scores; dV, dK and dQ^T),
+// warps 20-27 the dQ reducers (warp 20 + r + 4 c owns TMEM lanes, i.e. head
+// dims, 32 r .. +31 and query columns 32 c .. +31 of each unit), warp 19
+// idle.  The row warpgroups run with kRegsRow registers a thread, the others
+// with kRegsLoad and kRegsRed (setmaxnreg, within the 896 x 72 of the
+// launch).
 // TMEM: dV [0, D), dK [128, 128 + D), then per buffer h: S^T [256 + 128 h,
 // +64) (then P^T and dS^T in bf16 over it) and dP^T [320 + 128 h, +64) (then
 // dQ^T over it).  Every mbarrier wait is bounded as in the forward.
@@ -857,7 +858,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
     } else if (warp >= kWarpRed) {
       // ---------------------------------------------------------- dQ reducers
-      // Warps 12-19: warp 12 + rq + 4 ch owns TMEM lanes 32 rq .. +31 of dQ^T,
+      // Warps 20-27: warp 20 + rq + 4 ch owns TMEM lanes 32 rq .. +31 of dQ^T,
       // i.e. head dims d = 32 rq + lane, and query columns 32 ch .. +31 of each
       // unit (64 queries of buffer h): its 32 columns into registers, the
       // buffer released at once, then for each of its query rows q,
