@@ -634,20 +634,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(C::B_QTAIL), 1);
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(bar(C::B_SFULL + h), 1);
-      ptx::mbar_init(bar(C::B_PFULL + h), 32 * kRowWarps);
+      ptx::mbar_init(bar(C::B_PFULL + h), kRowWarps);
       ptx::mbar_init(bar(C::B_AFREE + h), 1);
       ptx::mbar_init(bar(C::B_DQFULL + h), 1);
-      ptx::mbar_init(bar(C::B_DQFREE + h), 256);
+      ptx::mbar_init(bar(C::B_DQFREE + h), 8);
     }
     ptx::mbar_init(bar(C::B_ODONE), 1);
-    ptx::mbar_init(bar(C::B_OFREE), 256);
+    ptx::mbar_init(bar(C::B_OFREE), 8);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(C::B_IFULL + i), 1);
-      ptx::mbar_init(bar(C::B_IEMPTY + i), 32 * kRowWarps + 2 + 256);  // row threads, two MMA threads, reducers
+      ptx::mbar_init(bar(C::B_IEMPTY + i), kRowWarps + 2 + 8);  // row warps, two MMA threads, reducer warps
     }
     ptx::mbar_init(bar(C::B_DRAIN), 1);
     ptx::mbar_init(bar(C::B_DRAIN2), 1);
-    ptx::mbar_init(bar(C::B_STAGE), 256);
+    ptx::mbar_init(bar(C::B_STAGE), 8);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(err) & kErrTimeout) ? 1u : 0u;
     ptx::fence_mbar_init();
   }
@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
         BwdItem it;
         const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
-        ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+        warp_arrive(bar(C::B_IEMPTY + (k & 1)), lane);
         if (!valid) break;
         const size_t rstride = size_t(p.H) * D;
         int nx = it.e0 < it.e1 ? __ldg(p.qidx + it.e0) : 0;
@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               ptx::tmem_wait_ld();
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::B_DQFREE + h));
+            warp_arrive(bar(C::B_DQFREE + h), lane);
             const int q0 = 64 * h + 32 * ch;  // first query row of this warp's columns
             if (active && q0 < qn) {
               int32_t* row = p.dqacc + (size_t(it.s0 + a0 + q0) * p.H + it.h) * D + 32 * rq + lane;
@@ -933,7 +933,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
       BwdItem it;
       const bool valid = bwd_load(item_ring + kItemInts * (k & 1), it);
-      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      warp_arrive(bar(C::B_IEMPTY + (k & 1)), lane);
       if (!valid) break;
       // the dS buffer doubles as the output stage of the item's epilogue: no
       // warp writes this item's dS before every epilogue warp has stored the
@@ -1071,7 +1071,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_wait_st();
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(C::B_PFULL + h));  // unit (entry, h) is ready for its products
+          warp_arrive(bar(C::B_PFULL + h), lane);  // unit (entry, h) is ready for its products
         }
         ++nent;
       }
@@ -1095,8 +1095,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                         size_t(p.H) * D, kn - qd * 32);
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(C::B_OFREE));
-      ptx::mbar_arrive(bar(C::B_STAGE));
+      warp_arrive(bar(C::B_OFREE), lane);
+      warp_arrive(bar(C::B_STAGE), lane);
     }
   }
 

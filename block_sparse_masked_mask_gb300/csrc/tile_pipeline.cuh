@@ -106,6 +106,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err, site));
 }
 
+// One arrival for the whole warp: every lane's earlier memory and tensor-memory
+// operations are ordered before it by the warp barrier (each lane issues its
+// own fences first), and one shared-memory atomic replaces 32 on a word that
+// other warps arrive on too.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(bar);
+}
+
 // Bounded wait that ignores the abort flag: used to let copies and MMAs this
 // CTA issued finish before it frees shared and tensor memory.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, int32_t* err) {
