@@ -17,8 +17,9 @@ upstream gradient, on the forward's own O and LSE) is timed back to back for
 at least a second and reported under "backward", in effective TFLOP/s
 (10*D*H*nnz, the usual 2.5x the forward's count); ``--no-backward`` skips it.
 ``per_config`` times the forward (and backward) of the other block-mask
-workloads (2: varlen causal, 3: shared prefix, 4: strip thinking), each back
-to back for at least a second with its own clock samples.
+workloads (1: one 64-token causal sequence in fp32, forward only, on the
+CUDA-core path; 2: varlen causal, 3: shared prefix, 4: strip thinking), each
+back to back for at least a second with its own clock samples.
 
 Default workload: the 32768-token causal+document mask (12 documents, H=32,
 D=128, bf16), the largest configuration.  ``--impl reference`` times the fp64
@@ -172,6 +173,10 @@ def count_pairs(w, c):
     return UNMASKED_PAIRS[c]
 
 
+# the fp32 path runs on CUDA cores: 152 SMs x 128 fp32 lanes x 2 FLOP per FFMA x 2.07 GHz
+FP32_FFMA_PEAK = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 # kernels the library launches: a block-mask build (five kernels) and the backward
 BUILD_LAUNCHES = 5
 BWD_KERNELS = ["bwd_zero_kernel", "bwd_prep_kernel", "bwd_mult_kernel", "attn_bwd_kernel", "bwd_dq_convert_kernel"]
@@ -322,12 +327,18 @@ def time_workload(c, dev, stream, peak, min_seconds, backward=True):
         time.sleep(0.3)
         ms, calls, win = time_loop(fwd, stream, dev, min_seconds)
     fwd_ms = sum(ms) / len(ms)
-    res = {"workload": w.name, "kind": w.kind, "total_tokens": w.total_tokens,
+    fp32 = w.dtype == torch.float32
+    fpeak = FP32_FFMA_PEAK if fp32 else peak
+    res = {"workload": w.name, "kind": w.kind, "dtype": "f32" if fp32 else "bf16",
+           "total_tokens": w.total_tokens,
            "num_heads": w.num_heads, "head_dim": w.head_dim, "unmasked_pairs_per_head": nnz,
            "fwd_ms_mean": fwd_ms, "fwd_calls_timed": calls,
-           "fwd_tflops": flops / fwd_ms / 1e9, "fwd_frac": flops / fwd_ms / 1e9 / peak,
+           "fwd_tflops": flops / fwd_ms / 1e9, "fwd_frac": flops / fwd_ms / 1e9 / fpeak,
            "fwd_clocks": clk.summary(win)}
-    if backward:
+    if fp32:
+        res["fwd_peak"] = ("CUDA-core FFMA, derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz = "
+                           f"{FP32_FFMA_PEAK:.1f} TFLOP/s; one 64-token sequence is launch-latency bound")
+    if backward and not fp32:  # the backward is bf16 only
         do = W.grad_output(w, seed=1).to(dev)
         gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         bws = torch.empty(api.attn_bwd_workspace_size(bm, w.num_heads, w.head_dim), dtype=torch.uint8, device=dev)
@@ -481,7 +492,7 @@ def run_ours(args):
     per_config = None
     if rank == 0 and ws == 1 and not args.no_per_config and args.workload == 5 and not args.heads:
         per_config = {str(c): time_workload(c, dev, stream, peak, args.min_seconds,
-                                            backward=not args.no_backward) for c in (2, 3, 4)}
+                                            backward=not args.no_backward) for c in (1, 2, 3, 4)}
 
     # ---- end to end through the public API with host buffers.  Every step copies
     # its inputs (Q, K, V and the mask metadata) from pinned host memory and reads
