@@ -619,7 +619,7 @@ def main():
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="least device time of each back-to-back timing (backward, per_config)")
     ap.add_argument("--no-per-config", action="store_true",
-                    help="skip the timings of workloads 2-4")
+                    help="skip the timings of workloads 1-4")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
