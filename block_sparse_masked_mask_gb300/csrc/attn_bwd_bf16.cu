@@ -921,7 +921,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // unit's query columns 16 (w / 4) .. +15; the first eight warps also write
     // the item's dV (w / 4 = 0) or dK (w / 4 = 1) rows.
     const int qd = warp & 3, cg = warp >> 2;  // lane quarter, 16-column group
-    const int r = qd * 32 + lane;
+    const int r = qd * 32 + lane;             // the key whose mask word this lane works out
+    const int kg = lane >> 2, qi = lane & 3;  // the P and dS arithmetic: keys kg + 8k, columns 2 qi (+8)
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(qd * 32) << 16);
     const float c2 = p.scale_log2;
@@ -975,7 +976,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool fast = lab == ATTN_TILE_FULL && an == kTile && all_in;
         for (int h = 0; h < 2; ++h) {
           const int cq = 64 * h + 16 * cg;  // the warp's first query column of the entry
-          const int cl = lane & 15;         // lanes 16-31 repeat lanes 0-15
+          const int cl = lane & 15;         // the masking's query column: lanes 16-31 repeat 0-15
           // before the wait: the dense kind's word of query row a0 + cq + cl
           // over the warp's 32 keys, or (code kinds) that query's code
           uint32_t dw = 0u;
@@ -988,10 +989,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               qc = query_code(p.mask, it.s0 + min(qrow, a0 + an - 1));
             }
           }
-          // lane c holds column cq + c's side values; the math below takes
-          // each column's from its lane by shuffle
-          const float sl_l = __ldg(sl + cq + cl), sl_g = __ldg(sl + kTile + cq + cl),
-                      sl_m = __ldg(sl + 2 * kTile + cq + cl);
+          // the side values of this thread's four query columns, cq + 2 qi,
+          // cq + 2 qi + 1 and the same 8 columns on (the TMEM layout below)
+          const float* slc = sl + cq + 2 * qi;
+          const float2 l_a = __ldg(reinterpret_cast<const float2*>(slc)),
+                       l_b = __ldg(reinterpret_cast<const float2*>(slc + 8));
+          const float2 g_a = __ldg(reinterpret_cast<const float2*>(slc + kTile)),
+                       g_b = __ldg(reinterpret_cast<const float2*>(slc + kTile + 8));
+          const float2 m_a = __ldg(reinterpret_cast<const float2*>(slc + 2 * kTile)),
+                       m_b = __ldg(reinterpret_cast<const float2*>(slc + 2 * kTile + 8));
           if (!warp_wait(bar(C::B_SFULL + h), uint32_t(nent) & 1u, abort_flag, err, 8)) {
             ok = false;
             break;
@@ -1027,47 +1033,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // a key past the sequence end: its P and dS are exactly zero
             if (!row_in) vis = 0u;
           }
-          // the warp's 16 columns of S^T and dP^T in, then P^T over the first
-          // 8 and dS^T over the next 8 of its score columns
-          uint32_t sv[16], dv[16];
-          ptx::tmem_ld16(lane_base + C::col_s(h) + 16 * cg, sv);
-          ptx::tmem_ld16(lane_base + C::col_p(h) + 16 * cg, dv);
+          // The warp's 32 keys x 16 query columns of S^T and dP^T, read by
+          // halves of 16 TMEM lanes: this thread takes keys kg, kg + 8 (first
+          // half) and kg + 16, kg + 24 (second) at the query columns 2 qi,
+          // 2 qi + 1, 8 + 2 qi, 9 + 2 qi, so it needs the side values of four
+          // columns only.  vk[k]: the visibility word of its key k.
+          uint32_t vk[4] = {vis, vis, vis, vis};
+          if (!fast) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) vk[k] = __shfl_sync(0xffffffffu, vis, kg + 8 * k);
+          }
+          const uint32_t half2 = 16u << 16;  // TMEM lane offset of the second half
+          uint32_t sa[8], sb[8], da[8], db[8];
+          ptx::tmem_ld16x256_x2(lane_base + C::col_s(h) + 16 * cg, sa);
+          ptx::tmem_ld16x256_x2(lane_base + half2 + C::col_s(h) + 16 * cg, sb);
+          ptx::tmem_ld16x256_x2(lane_base + C::col_p(h) + 16 * cg, da);
+          ptx::tmem_ld16x256_x2(lane_base + half2 + C::col_p(h) + 16 * cg, db);
           ptx::tmem_wait_ld();
-          // P^T and dS^T for TMEM; the copy of dS for the dQ^T product goes to
-          // shared memory scaled by each query's fixed-point multiplier m_i:
-          // this key's 16 queries as two 16-byte pieces, one per eight-query
-          // chunk (the dQ^T that last read these chunks, the previous entry's
-          // of this half, was issued before this unit's scores, whose
-          // completion this warp waited for)
-          uint32_t pp[8], pd[8];
+          // P^T and dS^T back to TMEM, packed bf16 pairs over the first 8 and
+          // the next 8 of the warp's score columns: column j holds query
+          // columns 2j, 2j + 1, so this thread's pairs land at columns qi and
+          // 4 + qi of its keys.  The copy of dS for the dQ^T product goes to
+          // shared memory scaled by each query's fixed-point multiplier m_i,
+          // 4 bytes per (key, column pair) in the key's 16-byte row of the
+          // eight-query chunk (the dQ^T that last read these chunks, the
+          // previous entry's of this half, was issued before this unit's
+          // scores, whose completion this warp waited for).
+          uint32_t pa[4], pb[4], qa[4], qb[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            uint32_t ps[4];
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int c = 8 * u; c < 8 * u + 8; c += 2) {  // column pair (c, c + 1)
-              const float2 l = make_float2(__shfl_sync(0xffffffffu, sl_l, c), __shfl_sync(0xffffffffu, sl_l, c + 1));
-              const float2 g = make_float2(__shfl_sync(0xffffffffu, sl_g, c), __shfl_sync(0xffffffffu, sl_g, c + 1));
-              const float2 mf = make_float2(__shfl_sync(0xffffffffu, sl_m, c), __shfl_sync(0xffffffffu, sl_m, c + 1));
-              float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+            for (int u = 0; u < 2; ++u) {  // column pair (c, c + 1), c = 8 u + 2 qi
+              const uint32_t* sv = k < 2 ? sa : sb;
+              const uint32_t* dv = k < 2 ? da : db;
+              const int ri = (k & 1) * 2 + u * 4;  // the pair's registers
+              const int c = 8 * u + 2 * qi;
+              const float2 l = u ? l_b : l_a, g = u ? g_b : g_a, mf = u ? m_b : m_a;
+              float2 x = ptx::ffma2(make_float2(__uint_as_float(sv[ri]), __uint_as_float(sv[ri + 1])),
                                     make_float2(c2, c2), make_float2(-l.x, -l.y));
-              // branch-free (vis is all ones on unmasked tiles), so that the
-              // compiler interleaves the independent column pairs: a hidden
-              // pair's exponent is -inf, so its P is exactly zero, and so is
-              // its dS = P (dP - D) (dP and D are finite)
-              x = make_float2((vis >> c) & 1u ? x.x : -INFINITY, (vis >> (c + 1)) & 1u ? x.y : -INFINITY);
+              // branch-free (vk is all ones on unmasked tiles), so that the
+              // compiler interleaves the independent pairs: a hidden pair's
+              // exponent is -inf, so its P is exactly zero, and so is its
+              // dS = P (dP - D) (dP and D are finite)
+              x = make_float2((vk[k] >> c) & 1u ? x.x : -INFINITY, (vk[k] >> (c + 1)) & 1u ? x.y : -INFINITY);
               const float2 pv = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
               const float2 dd =
-                  ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                  ptx::fmul2(pv, ptx::fadd2(make_float2(__uint_as_float(dv[ri]), __uint_as_float(dv[ri + 1])),
                                             make_float2(-g.x, -g.y)));
-              pp[c >> 1] = ptx::pack_bf16(pv.x, pv.y);
-              pd[c >> 1] = ptx::pack_bf16(dd.x, dd.y);
+              const int oi = (k & 1) + 2 * u;  // its place in the 16-lane store
+              (k < 2 ? pa : pb)[oi] = ptx::pack_bf16(pv.x, pv.y);
+              (k < 2 ? qa : qb)[oi] = ptx::pack_bf16(dd.x, dd.y);
               const float2 dm = ptx::fmul2(dd, mf);
-              ps[(c >> 1) & 3] = ptx::pack_bf16(dm.x, dm.y);
+              *reinterpret_cast<uint32_t*>(dsbuf + ((cq >> 3) + u) * kDsChunk + (32 * qd + kg + 8 * k) * 16 +
+                                           4 * qi) = ptx::pack_bf16(dm.x, dm.y);
             }
-            *reinterpret_cast<uint4*>(dsbuf + ((cq >> 3) + u) * kDsChunk + r * 16) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
           }
-          ptx::tmem_st8(lane_base + C::col_s(h) + 16 * cg, pp);
-          ptx::tmem_st8(lane_base + C::col_s(h) + 16 * cg + 8, pd);
+          ptx::tmem_st16x128_x2(lane_base + C::col_s(h) + 16 * cg, pa);
+          ptx::tmem_st16x128_x2(lane_base + half2 + C::col_s(h) + 16 * cg, pb);
+          ptx::tmem_st16x128_x2(lane_base + C::col_s(h) + 16 * cg + 8, qa);
+          ptx::tmem_st16x128_x2(lane_base + half2 + C::col_s(h) + 16 * cg + 8, qb);
           ptx::tmem_wait_st();
           ptx::fence_proxy_async_smem();
           ptx::tc_fence_before();

@@ -220,6 +220,26 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       : "memory");
 }
 
+// Warp-collective, 16 TMEM lanes from the address's lane: thread 4g + i gets
+// lanes g and g + 8 at columns 2i, 2i + 1 and, 8 columns on, 8 + 2i, 9 + 2i:
+// r = {(g, 2i), (g, 2i + 1), (g + 8, 2i), (g + 8, 2i + 1), (g, 8 + 2i),
+// (g, 9 + 2i), (g + 8, 8 + 2i), (g + 8, 9 + 2i)}.
+__device__ __forceinline__ void tmem_ld16x256_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+
+// Warp-collective, 16 TMEM lanes from the address's lane: thread 4g + i
+// writes lanes g and g + 8 at columns i and 4 + i:
+// r = {(g, i), (g + 8, i), (g, 4 + i), (g + 8, 4 + i)}.
+__device__ __forceinline__ void tmem_st16x128_x2(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
