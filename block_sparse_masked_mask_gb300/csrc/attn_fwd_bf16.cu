@@ -20,19 +20,21 @@
 //              sequence end
 //   warp 11    tcgen05 issuer of the S = Q K^T products (one thread)
 //   warps 12-15 epilogue: one thread per query row reads the item's final O
-//              from TMEM, divides by l and writes O (bf16) and LSE, while the
-//              softmax warps already work on the next item
-// The softmax warpgroups run with 160 registers a thread, the other two with
-// 96 (setmaxnreg, within the 128 x 512 the block is launched with).
+//              from TMEM once (as bf16 pairs, divided by l), releases it, and
+//              writes O and LSE while the softmax warps already work on the
+//              next item
+// The softmax warpgroups run with 160 registers a thread (144 for the dense
+// kind), the producer / issuer warpgroup with 64 (96), the epilogue with the
+// launch's 128 (setmaxnreg, within the 128 x 512 the block is launched with).
 // The two issuers work independently: an MMA issue blocks while the tensor
 // pipe's short queue is full, and with two threads one waits on its barriers
 // while the other keeps the queue fed.
-// TMEM columns: S0 [0,128), S1 [128,256) hold S of two consecutive k-tiles,
-// O0 [256, 256+D) and O1 [384, 384+D) the accumulators of alternate items, so
-// an item's epilogue overlaps the next item's products.  Each half of a row
-// writes its bf16 P over the first 32 of its own 64 S columns.  With two S
-// buffers the tensor cores compute S(j+1) and P(j-1).V while the softmax
-// works on S(j).
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384) hold S of three
+// consecutive k-tiles, O [384, 384+D) the accumulator.  Each half of a row
+// writes its bf16 P over the first 32 of its own 64 S columns, so S(j) waits
+// for P(j-3).V; the tensor cores compute S(j+1), S(j+2) and P(j-1).V while
+// the softmax works on S(j).  The next item's first P.V waits for the
+// epilogue's one read of O (a few hundred cycles), not for its stores.
 //
 // The row maximum used as the exponent reference only moves when a new tile
 // raises it by more than 2^8 (factor 256 in p); O and l are then rescaled
@@ -52,7 +54,17 @@ namespace {
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: p stays <= 256
 constexpr int kThreads = 512;
 constexpr int kWarpKLoad = 8, kWarpPV = 9, kWarpVLoad = 10, kWarpS = 11, kWarpEpi = 12;
-constexpr int kRegsSoftmax = 160, kRegsOther = 96;  // 2 x 128 x 160 + 2 x 128 x 96 = 512 x 128
+// Registers per thread: the softmax warpgroups, the producer / issuer
+// warpgroup and the epilogue warpgroup, which keeps the launch's 128 (a whole
+// row of O in bf16).  The dense kind's softmax (its bit words) fits 144 without
+// spills only if the producers get 96; the others run fastest with 160 / 64
+// (measured).
+template <bool kDense>
+struct Regs {
+  static constexpr int softmax = kDense ? 144 : 160, prod = kDense ? 96 : 64, epi = 128;
+  static_assert(2 * 128 * softmax + 128 * prod + 128 * epi == kThreads * 128, "register split");
+  static_assert(epi == 128, "the epilogue warpgroup runs with the launch's count");
+};
 
 template <int D>
 struct Cfg : TileLayout<D> {
@@ -70,9 +82,14 @@ struct Cfg : TileLayout<D> {
   static constexpr int NV = 2;                        // V ring slots
   static constexpr int NCODE = 6;                     // key-code buffers (entries in flight)
   static constexpr int OFF_Q = 0, OFF_K = NQ * TILE, OFF_V = OFF_K + NK * TILE;
-  static constexpr int NS = 2;                        // S buffers in TMEM
+  // TMEM (512 columns): NS S buffers and NO O accumulators of 128 columns.
+  // One O: the epilogue reads the item's O once into registers and releases
+  // it at once, so the next item's first P.V waits only for that read; the
+  // third S buffer keeps three k-tiles in flight (S(j) waits for P.V(j - 3)).
+  static constexpr int NO = 1;
+  static constexpr int NS = 4 - NO;
   // SFULL / PFULL / PDONE: per S buffer; XMAX: per entry parity; ODONE, OFREE,
-  // STATS: per O buffer (item parity)
+  // STATS: per item parity
   static constexpr int B_Q = 0, B_QFREE = NQ, B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NK, B_VFULL = B_KEMPTY + NK,
                        B_VEMPTY = B_VFULL + NV, B_VTMA = B_VEMPTY + NV, B_SFULL = B_VTMA + 1,
                        B_PFULL = B_SFULL + NS, B_PDONE = B_PFULL + NS, B_ODONE = B_PDONE + NS,
@@ -92,7 +109,7 @@ struct Cfg : TileLayout<D> {
   // (and its 512 TMEM columns) alone.
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024 > 116 * 1024 ? SMEM_USED + 1024 : 116 * 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t col_o(int b) { return 256u + uint32_t(b) * 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int b) { return 128u * uint32_t(NS) + uint32_t(b) * 128u; }
   __host__ __device__ static constexpr uint32_t col_s(int i) { return uint32_t(i) * 128u; }
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -268,8 +285,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (skip) {
     // nothing issued, nothing to drain
+  } else if (warp >= kWarpEpi) {
+    // ------------------------------------------------------------ epilogue
+    // One thread per query row (TMEM lane): once the softmax has posted the
+    // row's statistics and the item's last P.V is done, the row of O / l is
+    // read once into registers as bf16 pairs and the O buffer released (the
+    // next item's first P.V waits for it), then written as whole rows
+    // through a 4 KB stage, 16 rows at a time.
+    const int quarter = warp - kWarpEpi;       // TMEM lanes 32 quarter ..
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+    const float* stats = reinterpret_cast<const float*>(sbase + C::OFF_STATS);
+    uint8_t* stage = sbase + C::OFF_OSTAGE + quarter * C::OSTAGE_WARP;
+    constexpr int RB = D * 2;                  // bytes per output row
+    constexpr int CPR = RB / 16;               // 16-byte pieces per row
+    constexpr int RPI = 32 / CPR;              // rows per warp-wide store
+    for (int k = 0;; ++k) {
+      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
+      Item it;
+      const bool valid = load_item(item_ring + 8 * (k & 1), it);
+      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
+      if (!valid) break;
+      const int ob = k & 1;  // item parity: statistics buffer and barriers
+      if (!warp_wait(bar(C::B_STATS + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 18)) break;
+      const float* st = stats + ob * 3 * kTile;
+      const float lt = st[r] + st[kTile + r];  // the halves' row sums, in a fixed order
+      const float m = st[2 * kTile + r];
+      const int qn = min(kTile, it.L - it.qi0);
+      const bool has = it.e1 > it.e0;
+      if (!warp_wait(bar(C::B_ODONE + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 11)) break;
+      ptx::tc_fence_after();
+      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* obase = p.o + (size_t(it.s0 + it.qi0 + quarter * 32) * p.H + it.h) * D;
+      const size_t rstride = size_t(p.H) * D;
+      const uint32_t ocol = C::col_o(k % C::NO);
+      uint32_t pk[D / 2];  // the row as bf16 pairs
+#pragma unroll
+      for (int q32 = 0; q32 < (D + 31) / 32; ++q32) {
+        constexpr int W = D < 32 ? D : 32;   // columns per TMEM read
+        uint32_t v[32];
+        if (has) {
+          if constexpr (W == 32) ptx::tmem_ld32(lane_base + ocol + q32 * 32, v);
+          else ptx::tmem_ld16(lane_base + ocol, *reinterpret_cast<uint32_t(*)[16]>(v));
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = 0u;
+        }
+#pragma unroll
+        for (int x = 0; x < W / 2; ++x)
+          pk[q32 * 16 + x] = ptx::pack_bf16(__uint_as_float(v[2 * x]) * inv_l, __uint_as_float(v[2 * x + 1]) * inv_l);
+      }
+      // every read of the buffer is done
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(C::B_OFREE + ob));
+#pragma unroll
+      for (int half16 = 0; half16 < 2; ++half16) {
+        if ((lane >> 4) == half16) {
+          const int q = lane & 15;
+#pragma unroll
+          for (int c = 0; c < CPR; ++c)  // 16-byte piece c of the row: pairs 4c .. 4c + 3
+            *reinterpret_cast<uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 16 / RPI; ++i) {
+          const int q = i * RPI + lane / CPR, c = lane % CPR;
+          const int rr = half16 * 16 + q;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
+          if (quarter * 32 + rr < qn) *reinterpret_cast<uint4*>(obase + size_t(rr) * rstride + 8 * c) = val;
+        }
+        __syncwarp();
+      }
+      if (r < qn)
+        p.lse[size_t(it.h) * p.T + it.s0 + it.qi0 + r] =
+            lt > 0.f ? (m + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
+    }
   } else if (warp >= 8) {
-   ptx::regs_dec<kRegsOther>();
+   ptx::regs_dec<Regs<kDense>::prod>();
    if (warp == kWarpKLoad) {
     // ------------------------------------------------------------ Q, K, key codes
     int nk = 0, nq = 0, up = 0;  // K loads, Q loads, PARTIAL entries given key codes
@@ -469,9 +563,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
         if (!valid) break;
         const int n = it.e1 - it.e0;
-        const int ob = k & 1;  // this item's O buffer, free once the epilogue of item k - 2 has read it
-        if (n > 0 && k >= 2 &&
-            !wait_bar(bar(C::B_OFREE + ob), uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 14)) {
+        const int ob = k % C::NO;     // this item's O buffer, free once the epilogue of
+        const int prev = k - C::NO;   // item k - NO (its last user) has read it
+        if (n > 0 && prev >= 0 &&
+            !wait_bar(bar(C::B_OFREE + (prev & 1)), uint32_t(prev >> 1) & 1u, abort_flag, err, 14)) {
           ok = false;
           break;
         }
@@ -489,95 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // The item's last P.V: O is final once this arrives (at once for an
         // item without entries).
-        if (ok) ptx::mma_commit(bar(C::B_ODONE + ob));
+        if (ok) ptx::mma_commit(bar(C::B_ODONE + (k & 1)));
       }
       ptx::mma_commit(bar(C::B_DRAIN));
       drain_bar(bar(C::B_DRAIN), 0, err);
     }
     __syncwarp();
-   } else {
-    // ------------------------------------------------------------ epilogue
-    // One thread per query row (TMEM lane): once the softmax has posted the
-    // row's statistics and the item's last P.V is done, O / l is read from
-    // the item's O buffer and written as whole rows through a 4 KB stage, 16
-    // rows at a time (the O columns are read twice, once per 16 rows, so that
-    // no thread holds a whole row); the buffer is released after the reads.
-    const int quarter = warp - kWarpEpi;       // TMEM lanes 32 quarter ..
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
-    const float* stats = reinterpret_cast<const float*>(sbase + C::OFF_STATS);
-    uint8_t* stage = sbase + C::OFF_OSTAGE + quarter * C::OSTAGE_WARP;
-    constexpr int RB = D * 2;                  // bytes per output row
-    constexpr int CPR = RB / 16;               // 16-byte pieces per row
-    constexpr int RPI = 32 / CPR;              // rows per warp-wide store
-    for (int k = 0;; ++k) {
-      if (!warp_wait(bar(C::B_IFULL + (k & 1)), uint32_t(k >> 1) & 1u, abort_flag, err, 16)) break;
-      Item it;
-      const bool valid = load_item(item_ring + 8 * (k & 1), it);
-      ptx::mbar_arrive(bar(C::B_IEMPTY + (k & 1)));
-      if (!valid) break;
-      const int ob = k & 1;
-      if (!warp_wait(bar(C::B_STATS + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 18)) break;
-      const float* st = stats + ob * 3 * kTile;
-      const float lt = st[r] + st[kTile + r];  // the halves' row sums, in a fixed order
-      const float m = st[2 * kTile + r];
-      const int qn = min(kTile, it.L - it.qi0);
-      const bool has = it.e1 > it.e0;
-      if (!warp_wait(bar(C::B_ODONE + ob), uint32_t(k >> 1) & 1u, abort_flag, err, 11)) break;
-      ptx::tc_fence_after();
-      const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-      __nv_bfloat16* obase = p.o + (size_t(it.s0 + it.qi0 + quarter * 32) * p.H + it.h) * D;
-      const size_t rstride = size_t(p.H) * D;
-#pragma unroll 1
-      for (int half16 = 0; half16 < 2; ++half16) {
-#pragma unroll
-        for (int q32 = 0; q32 < (D + 31) / 32; ++q32) {
-          constexpr int W = D < 32 ? D : 32;   // columns per TMEM read
-          uint32_t v[32];
-          if (has) {
-            if constexpr (W == 32) ptx::tmem_ld32(lane_base + C::col_o(ob) + q32 * 32, v);
-            else ptx::tmem_ld16(lane_base + C::col_o(ob), *reinterpret_cast<uint32_t(*)[16]>(v));
-            ptx::tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = 0u;
-          }
-          if ((lane >> 4) == half16) {
-            const int q = lane & 15;
-#pragma unroll
-            for (int c4 = 0; c4 < W / 8; ++c4) {
-              const int c = q32 * (W / 8) + c4;  // 16-byte piece of the row
-              uint32_t w[4];
-#pragma unroll
-              for (int x = 0; x < 4; ++x)
-                w[x] = ptx::pack_bf16(__uint_as_float(v[8 * c4 + 2 * x]) * inv_l,
-                                      __uint_as_float(v[8 * c4 + 2 * x + 1]) * inv_l);
-              *reinterpret_cast<uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
-        if (half16 == 1) {  // every read of the buffer is done
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(C::B_OFREE + ob));
-        }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 16 / RPI; ++i) {
-          const int q = i * RPI + lane / CPR, c = lane % CPR;
-          const int rr = half16 * 16 + q;
-          const uint4 val = *reinterpret_cast<const uint4*>(stage + q * RB + ((c ^ q) & (CPR - 1)) * 16);
-          if (quarter * 32 + rr < qn) *reinterpret_cast<uint4*>(obase + size_t(rr) * rstride + 8 * c) = val;
-        }
-        __syncwarp();
-      }
-      if (r < qn)
-        p.lse[size_t(it.h) * p.T + it.s0 + it.qi0 + r] =
-            lt > 0.f ? (m + ptx::lg2(lt)) * 0.69314718055994531f : -INFINITY;
-    }
    }
   } else {
-    ptx::regs_inc<kRegsSoftmax>();
+    ptx::regs_inc<Regs<kDense>::softmax>();
     // ------------------------------------------------------------ softmax
     // Two threads per query row: warps 0-3 take score columns 0-63 of every
     // k-tile, warps 4-7 columns 64-127.  Both halves keep the same exponent
@@ -592,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kind = p.mask.kind;
     const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
     constexpr int DH = D / 2;                  // O columns this half rescales and writes
-    const uint32_t col_oh0 = C::col_o(0) + uint32_t(DH * hf);  // this half's O columns, buffer 0
+    const uint32_t col_oh = uint32_t(DH * hf);  // this half's O columns, from its buffer's first
     const float c2 = p.scale_log2;
     const float2 c22 = make_float2(c2, c2);
     float* xmax = reinterpret_cast<float*>(sbase + C::OFF_XMAX);  // [entry parity][half][row]
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int q = 0; q < DH / 16; ++q) {
               uint32_t v[16];
-              ptx::tmem_ld16(lane_base + col_oh0 + 128u * uint32_t(k & 1) + q * 16, v);
+              ptx::tmem_ld16(lane_base + C::col_o(k % C::NO) + col_oh + q * 16, v);
               ptx::tmem_wait_ld();
 #pragma unroll
               for (int c = 0; c < 16; c += 2) {
@@ -773,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v[c] = __float_as_uint(x.x);
                 v[c + 1] = __float_as_uint(x.y);
               }
-              ptx::tmem_st16(lane_base + col_oh0 + 128u * uint32_t(k & 1) + q * 16, v);
+              ptx::tmem_st16(lane_base + C::col_o(k % C::NO) + col_oh + q * 16, v);
             }
           }
           l *= alpha;
