@@ -93,8 +93,11 @@ constexpr int kItemInts = 12;
 constexpr int kDsBlock = kTile * kTile * 2;
 constexpr int kDsChunk = 2048;
 // Bound words per (sequence, head): max ||V_j||, max |K_jd| (non-negative
-// floats, so their bit patterns order like ints), two words unused.
+// floats, so their bit patterns order like ints), two words unused except
+// word 2 of the first (sequence, head): the item order's head-group size.
 constexpr int kBoundWords = 4;
+constexpr int kHeadGroupWord = 2;
+constexpr int kHeadGroupMin = 8;
 constexpr float kFixScale = 1073741824.0f;  // 2^30: the quantum is B_i / 2^30
 
 // B_i / ||dO_i|| of a (sequence, head) from its bound words.
@@ -219,11 +222,38 @@ __global__ void __launch_bounds__(kTile) bwd_mult_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ qt_seq,
                                                          const int32_t* __restrict__ qt_idx,
                                                          const int32_t* __restrict__ cu,
+                                                         const int32_t* __restrict__ korder,
+                                                         const int32_t* __restrict__ qoff,
                                                          const float* __restrict__ bounds,
                                                          const float* __restrict__ dnorm, float* __restrict__ side,
-                                                         int T, int H, int G) {
+                                                         int32_t* __restrict__ hgroup, int T, int H, int G,
+                                                         int num_sms) {
   const int g = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   if (g >= header[kHdrQtiles]) return;
+  if (g == 0 && h == 0) {
+    // The head-group size of the main kernel's item order (k-tiles longest
+    // list first inside a group of heads): a group holds at least one long
+    // item (a list of at least half the longest) per SM, or the SMs left over
+    // take short items while the long ones of the next group wait for their
+    // tickets and end late.  kHeadGroupMin heads at least (the K, V and
+    // accumulator rows in use at once stay within a few heads), doubled
+    // until the long items cover the SMs.
+    const int nt = header[kHdrQtiles];
+    const int lmax = qoff[korder[0] + 1] - qoff[korder[0]];
+    int nlong = 0;
+    for (int i0 = 0; i0 < nt; i0 += kTile) {
+      const int i = i0 + c;
+      const bool lg = i < nt && 2 * (qoff[korder[i] + 1] - qoff[korder[i]]) >= lmax;
+      const int cnt = __syncthreads_count(lg);
+      nlong += cnt;
+      if (cnt < kTile) break;  // longest first: no long list further on
+    }
+    if (c == 0) {
+      int grp = kHeadGroupMin;
+      while (grp < H && grp * nlong < num_sms) grp *= 2;
+      *hgroup = grp;
+    }
+  }
   const int b = qt_seq[g];
   const int s0 = cu[b], L = cu[b + 1] - s0;
   const int a0 = qt_idx[g] * kTile;
@@ -324,6 +354,7 @@ struct BwdParams {
   const int32_t* cu;
   MaskArgs mask;
   const float* side;        // [H][G][kBwdSideFloats]: LSE * log2 e, D, m_i of each q-tile's rows
+  const int32_t* hgroup;    // heads per group of the item order (bwd_mult_kernel writes it)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t* dqacc;           // [T, H, D] fixed point
@@ -337,18 +368,18 @@ struct BwdItem {
   int h, s0, L, i0, e0, e1, b, gbase;  // i0: first key of the tile (local); gbase: tile 0 of the sequence
 };
 
-// Items go by groups of kHeadGroup heads: inside a group, k-tiles longest list
-// first, each k-tile for every head of the group in turn.  A group keeps the
-// accumulator rows and Q / dO tiles that the CTAs touch at once to a few
-// heads (L2 locality), and the longest lists of the last group still start
-// well before the end (a purely head-major order would start the last
-// head's longest lists last and leave a tail of one list's duration).
-constexpr int kHeadGroup = 8;
-__device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t) {
+// Items go by groups of `group` heads (set per call by bwd_mult_kernel, at
+// least kHeadGroupMin): inside a group, k-tiles longest list first, each
+// k-tile for every head of the group in turn.  A group keeps the accumulator
+// rows and Q / dO tiles that the CTAs touch at once to a few heads (L2
+// locality), and the longest lists of the last group still start well
+// before the end (a purely head-major order would start the last head's
+// longest lists last and leave a tail of one list's duration).
+__device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int item, int n_t, int group) {
   BwdItem it;
-  const int grp = item / (n_t * kHeadGroup), r = item - grp * (n_t * kHeadGroup);
-  const int hg = min(kHeadGroup, p.H - grp * kHeadGroup);  // heads in this group
-  it.h = grp * kHeadGroup + r % hg;
+  const int grp = item / (n_t * group), r = item - grp * (n_t * group);
+  const int hg = min(group, p.H - grp * group);  // heads in this group
+  it.h = grp * group + r % hg;
   const int g = p.korder[r / hg];
   const int b = p.qt_seq[g];
   it.s0 = p.cu[b];
@@ -387,14 +418,15 @@ __device__ __forceinline__ bool bwd_load(const volatile int* d, BwdItem& it) {
 }
 
 // The producer takes a ticket and publishes the item in ring slot k & 1.
-__device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, int n_items, int n_t, BwdItem& it,
+__device__ __forceinline__ int bwd_publish(const BwdParams& p, int k, int lane, int n_items, int n_t, int group,
+                                           BwdItem& it,
                                            volatile int* ring, uint32_t iempty0, uint32_t ifull0,
                                            volatile uint32_t* abort_flag, int32_t* err) {
   int ticket = 0;
   if (lane == 0) ticket = take_ticket(p.sched);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);
   const bool valid = ticket < n_items;
-  if (valid) it = bwd_decode(p, ticket, n_t);
+  if (valid) it = bwd_decode(p, ticket, n_t, group);
   const int slot_i = k & 1;
   if (k >= 2 && !warp_wait(iempty0 + 8u * slot_i, uint32_t((k >> 1) - 1) & 1u, abort_flag, err, 15)) return -1;
   if (lane == 0) {
@@ -670,12 +702,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nload = 0, ntail = 0, nfix = 0, nktail = 0;
       bool tail_pending = false, ktail_pending = false, ok = true;
       BwdItem it_next;
-      int st_next = bwd_publish(p, 0, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
-                                abort_flag, err);
+      const int group = *p.hgroup;  // written by bwd_mult_kernel before this launch
+      int st_next = bwd_publish(p, 0, lane, n_items, n_t, group, it_next, item_ring, bar(C::B_IEMPTY),
+                                bar(C::B_IFULL), abort_flag, err);
       for (int k = 0; ok && st_next == 1; ++k) {
         const BwdItem it = it_next;
-        st_next = bwd_publish(p, k + 1, lane, n_items, n_t, it_next, item_ring, bar(C::B_IEMPTY), bar(C::B_IFULL),
-                              abort_flag, err);
+        st_next = bwd_publish(p, k + 1, lane, n_items, n_t, group, it_next, item_ring, bar(C::B_IEMPTY),
+                              bar(C::B_IFULL), abort_flag, err);
         if (st_next < 0) break;
         // K and V of this k-tile, once the previous item's products no longer
         // read them.  K and V rows past the sequence end are zeroed: their P
@@ -1171,8 +1204,9 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
                                            a.total_tokens, a.num_heads, G);
   e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd prep launch");
-  bwd_mult_kernel<<<tiles, kTile, 0, s>>>(a.bm.header, a.bm.qt_seq, a.bm.qt_idx, a.bm.cu, bounds, dnorm, side,
-                                          a.total_tokens, a.num_heads, G);
+  int32_t* hgroup = reinterpret_cast<int32_t*>(bounds) + kHeadGroupWord;
+  bwd_mult_kernel<<<tiles, kTile, 0, s>>>(a.bm.header, a.bm.qt_seq, a.bm.qt_idx, a.bm.cu, a.bm.korder, a.bm.qoff,
+                                          bounds, dnorm, side, hgroup, a.total_tokens, a.num_heads, G, num_sms);
   e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e, "attn_bwd multiplier launch");
 
@@ -1187,6 +1221,7 @@ attn_status launch_bwd(const BwdArgs& a, cudaStream_t s) {
   p.cu = a.bm.cu;
   p.mask = a.mask;
   p.side = side;
+  p.hgroup = hgroup;
   p.G = G;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);

@@ -270,7 +270,9 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  *   ||dout_i||                  fp32 [num_heads, total_tokens]
  *   bound words                 fp32 [batch][num_heads][4]: the largest
  *                               ||v_j|| and |k_jd| of each sequence and
- *                               head (two words unused)
+ *                               head (word 2 of the first: the call's
+ *                               work-order head-group size, int32; the
+ *                               other spare words unused)
  *   dQ accumulator              int32 [total_tokens, num_heads, head_dim],
  *                               fixed point
  * i.e. O(total_tokens * num_heads * head_dim); nothing is kept per tile pair.
