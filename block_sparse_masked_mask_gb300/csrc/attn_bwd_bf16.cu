@@ -8,6 +8,8 @@
 // the block-sparse masks, walking the transposed (k-major) lists for dK and
 // dV, and with a deterministic dQ.  Kernels:
 //   * zero: clears the per-(sequence, head) bound words;
+//   * mult: the per-row multipliers m_i, and the work order's head-group
+//     size for this call;
 //   * prep: per (q-tile, head): D = rowsum(dO * O) and ||dO_i|| of every row
 //     in fp32, the largest ||V_j|| and |K_jd| of each (sequence, head), and
 //     zeroes the q-tile's rows of the dQ accumulator;
@@ -15,7 +17,7 @@
 //     q-tiles.  Per entry it forms S^T and dP^T in TMEM, P^T and dS^T in the
 //     row warps, then dV += P^T dO and dK += dS^T Q (K, V stay in shared
 //     memory for the item) and dQ_i^T = K^T dS^T (dS kept in shared memory,
-//     never in HBM).  Four reducer warps add each dQ^T tile into the
+//     never in HBM).  Eight reducer warps add each dQ^T tile into the
 //     accumulator in HBM;
 //   * convert: dQ = scale * accumulator * quantum, rounded to bf16.
 // Five products per tile pair (S, dP, dV, dK, dQ), no per-pair HBM traffic:
@@ -40,9 +42,9 @@
 // add.  The maxima over V and K use only the sequence's own tokens, so the
 // result does not depend on what else is packed with it.
 //
-// Items are taken by groups of eight heads, longest list first inside a
-// group, so at any time the CTAs add into the accumulator rows of a few heads
-// (17 MB per head on the 32k workload).
+// Items are taken by groups of heads (eight, or more when a mask has few long
+// lists), longest list first inside a group, so at any time the CTAs add into
+// the accumulator rows of a few heads (17 MB per head on the 32k workload).
 //
 // Each entry (q-tile) runs as two units of 64 queries, one per TMEM buffer,
 // so that the tensor pipe works on one unit while the row warps work on the
@@ -51,7 +53,9 @@
 // that the tensor pipe has work from one while the other waits for a buffer.
 // Warp roles of the main kernel (896 threads): warps 0-15 the row warps (warp
 // w owns TMEM lanes, i.e. keys, 32 (w % 4) .. +31 and, in each unit, query
-// columns 16 (w / 4) .. +15; warps 0-7 also write dV and dK), warp 16 the TMA
+// columns 16 (w / 4) .. +15, read by halves of 16 lanes so that a thread
+// holds four keys at four query columns; warps 0-7 also write dV and dK),
+// warp 16 the TMA
 // producer, warps 17 and 18 the tcgen05 issuers (scores; dV, dK and dQ^T),
 // warps 20-27 the dQ reducers (warp 20 + r + 4 c owns TMEM lanes, i.e. head
 // dims, 32 r .. +31 and query columns 32 c .. +31 of each unit), warp 19
