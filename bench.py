@@ -281,13 +281,25 @@ def run_reference(args):
     return 0
 
 
-def time_loop(fn, stream, dev, min_seconds: float, batch: int = 8):
+def time_loop(fn, stream, dev, min_seconds: float, batch: int = 8, batch_ms: float = 5.0):
     """Run ``fn`` back to back for at least ``min_seconds`` of device time, in
     batches bracketed by CUDA events on ``stream``; returns the per-call device
     times (ms, one batch mean per entry), the call count and the host
-    wall-clock window of the timed calls."""
+    wall-clock window of the timed calls.  A batch is sized to about
+    ``batch_ms`` of device time (at least ``batch`` calls), so that the host's
+    time to issue the first call of a batch, which the start event sees as
+    device idle time, is a small part of it even for short calls."""
     per_call, calls = [], 0
     torch.cuda.synchronize(dev)
+    # size the batches from one untimed batch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(batch):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    est = e0.elapsed_time(e1) / batch
+    batch = max(batch, min(512, int(batch_ms / max(est, 1e-3))))
     t0 = time.time()
     while True:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
